@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark: batch-1 INT4 decode of the Qwen2.5-Coder-7B shape at KV length ~4096.
+
+One step = one decode token through the whole hot path (embedding, 28 x [RMSNorm+QKV+RoPE+
+paged append, split-K attention + combine, o_proj + residual, RMSNorm + gate/up + SiLU*mul,
+down + residual], final RMSNorm + LM head + argmax), replayed from one CUDA graph.
+
+Inputs are seeded synthetic weights of the 7B shape (INT4 group-128, bf16 scales) resident in
+HBM before timing, and a KV cache pre-filled with seeded N(0,1) bf16 values through the page
+table; timed positions cycle through [ctx - cycle, ctx) so every step attends to ~ctx tokens.
+The 4.7 GB read per step is far larger than L2 (129 MB), so no flush is needed between steps.
+
+--impl reference times the CPU oracle instead (a bounded sample of the same workload,
+scaled to ms/token).  Under torchrun every rank runs its own replica (no collective on the
+data path); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode ms/token & HBM GB/s (7B INT4, ctx 4096); TTFT pp512"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=600)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="qwen2.5-7b")
+    p.add_argument("--ctx", type=int, default=4096)
+    p.add_argument("--cycle", type=int, default=128, help="positions cycle in [ctx-cycle, ctx)")
+    p.add_argument("--layers", type=int, default=0, help="override layer count (profiling cases)")
+    p.add_argument("--vocab", type=int, default=0, help="override vocab (profiling cases)")
+    p.add_argument("--seed", type=int, default=4242)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-ttft", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--profile-steps", type=int, default=4)
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def model_cfg(args):
+    from synth import model as sm
+    cfg = sm.CONFIGS[args.config]
+    over = {"max_context": args.ctx}
+    if args.layers:
+        over["n_layers"] = args.layers
+    if args.vocab:
+        over["vocab"] = args.vocab
+    return cfg.with_(**over)
+
+
+def algorithmic_bytes(cfg, T):
+    """Bytes one decode step must move at KV length T (T cached tokens incl. the new one)."""
+    h, d, F, L, V = cfg.hidden, cfg.head_dim, cfg.mlp, cfg.n_layers, cfg.vocab
+    rq, rkv = cfg.n_q_heads * d, cfg.n_kv_heads * d
+    shapes = [(rq, h), (rkv, h), (rkv, h), (h, rq), (F, h), (F, h), (h, F)]
+    per_layer = 0
+    for N, K in shapes:
+        if cfg.weight_format == 1:
+            per_layer += N * K // 2 + N * (K // 128) * 2
+        else:
+            per_layer += N * K + N * 4
+    if cfg.qkv_bias:
+        per_layer += (rq + 2 * rkv) * 2
+    per_layer += 2 * h * 2 + (2 * d * 2 if cfg.qk_norm else 0)
+    kv_read = 2 * rkv * 2 * T
+    kv_write = 2 * rkv * 2
+    lm = V * h * (2 if (cfg.weight_format == 1 or cfg.tied_lm_head) else 1) + \
+        (V * 4 if cfg.weight_format == 2 and not cfg.tied_lm_head else 0)
+    return L * (per_layer + kv_read + kv_write) + lm + h * 2 + h * 2
+
+
+def kernel_bytes(cfg, T):
+    """Algorithmic bytes per launch of each kernel kind (for the roofline of one kernel)."""
+    h, d, F, V = cfg.hidden, cfg.head_dim, cfg.mlp, cfg.vocab
+    rq, rkv = cfg.n_q_heads * d, cfg.n_kv_heads * d
+
+    def w(N, K):
+        return N * K // 2 + N * (K // 128) * 2 if cfg.weight_format == 1 else N * K + N * 4
+
+    return {
+        "qkv": w(rq + 2 * rkv, h) + h * 4 + (rq + 2 * rkv) * 2 + 2 * rkv * 2 + rq * 4,
+        "attention": 2 * rkv * 2 * T + rq * 4 * 2,
+        "o_proj": w(h, rq) + rq * 4 + h * 4 * 2,
+        "gate_up": 2 * w(F, h) + h * 4 + F * 4,
+        "down": w(h, F) + F * 4 + h * 4 * 2,
+        "lm_head": V * h * 2 + h * 4 + V * 4,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while a region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sms, maxes, reasons = [], [], set()
+        window = [r for t, r in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for _, r in self.rows]
+        for r in window:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower() in ("active", "0x1", "1"):
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(cfg, seed, T, n_layer_steps, lm_w):
+    """Oracle ms/token for the full model from a bounded sample: a one-layer model of the
+    same shape at KV length T (timed per step) and the full LM head GEMV (timed once)."""
+    import oracle
+    from synth import model as sm
+    one = cfg.with_(n_layers=1, vocab=64, max_context=T + n_layer_steps + 1)
+    orc = oracle.OracleModel(one, seed)
+    k, v = sm.kv_fill(one, seed, 0, T)
+    orc.set_kv(0, k, v)
+    o = oracle.Oracle("f32")
+    x = np.ones(cfg.hidden, np.float32)
+    t0 = time.perf_counter()
+    if lm_w is not None:
+        o.gemv_bf16(lm_w, x)
+    lm_ms = (time.perf_counter() - t0) * 1e3
+    times = []
+    for i in range(n_layer_steps):
+        t0 = time.perf_counter()
+        orc.step(5, T + i)
+        times.append((time.perf_counter() - t0) * 1e3)
+    layer_ms = statistics.median(times)
+    total = lm_ms + cfg.n_layers * layer_ms
+    sample = (f"oracle fp32: {n_layer_steps} steps of a 1-layer {cfg.name}-shape model at KV {T} "
+              f"(median {layer_ms:.1f} ms/layer) x {cfg.n_layers} layers + one full LM-head GEMV "
+              f"({lm_ms:.1f} ms)")
+    return total, sample, times
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from synth import model as sm
+    cfg = model_cfg(args)
+    lm = sm.lm_head(cfg, args.seed)
+    lm_w = lm.get("w")
+    T = args.ctx
+    total, sample, _ = oracle_sample(cfg, args.seed, T, max(args.warmup, 1), lm_w)  # warm-up
+    total, sample, times = oracle_sample(cfg, args.seed, T, args.steps, lm_w)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(total, 3), "unit": "ms/token",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": f"{cfg.name} INT4 g128 decode, batch 1, KV {T}", "global_batch": 1,
+                   "seq_len": T, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(total, 3), "unit": "ms/token", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(total, 3), "unit": "ms/token", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    from quantized_decode_gb300 import DeviceModel, Engine
+    from synth import model as sm
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    cfg = model_cfg(args)
+    ctx, cycle = args.ctx, min(args.cycle, args.ctx - 1)
+    T0 = ctx - cycle
+
+    t_setup = time.perf_counter()
+    rec = sm.recipe(cfg, args.seed)
+    model = DeviceModel(cfg, *rec)
+    lm_w = rec[4].get("w")
+    stream = torch.cuda.Stream()
+    eng = Engine(model, stream=stream.cuda_stream)
+    setup_s = time.perf_counter() - t_setup
+
+    # ---- TTFT pp512 (prompt of seeded uniform token ids)
+    ttft_ms = None
+    if not args.no_ttft:
+        prompt = sm.prompt(cfg, args.seed, min(512, ctx - 1))
+        eng.reset()
+        eng.prefill(prompt[:8])          # warm the prefill path
+        eng.reset()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        eng.prefill(prompt)
+        ttft_ms = (time.perf_counter() - t0) * 1e3
+        eng.reset()
+
+    # ---- KV filled with seeded values through a shuffled page table
+    from tests._gpu import fill_kv
+    import synth
+    n_pages = (ctx + 15) // 16
+    fill_kv(eng, cfg, args.seed + 1, T0, page_perm=synth.permutation(args.seed, 3, n_pages))
+
+    def enqueue(n):
+        """n greedy steps, rewinding to T0 whenever the next step would pass ctx."""
+        launched = 0
+        while n > 0:
+            room = ctx - eng.seq_len()
+            if room <= 0:
+                eng.truncate(T0)
+                launched += 1
+                room = ctx - T0
+            k = min(n, room)
+            eng.decode_enqueue(k)
+            n -= k
+        return launched
+
+    eng.decode_step(7)                       # a token to feed the greedy chain
+    enqueue(args.warmup)
+    eng.sync()
+
+    # ---- timed region: graph replays, inputs resident
+    start_ev = torch.cuda.Event(enable_timing=True)
+    end_ev = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        w0 = clk.mark()
+        start_ev.record(stream)
+        extra = enqueue(args.steps)
+        end_ev.record(stream)
+        torch.cuda.synchronize()
+        w1 = clk.mark()
+        if ws > 1:
+            torch.distributed.barrier()
+    eng.sync()
+    elapsed_ms = start_ev.elapsed_time(end_ev)
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_token = elapsed_ms / args.steps
+    clocks = clk.summary(w0, w1)
+
+    # KV lengths attended during the timed steps (cycle through [T0+1, ctx])
+    mean_T = T0 + (cycle + 1) / 2.0
+    step_bytes = algorithmic_bytes(cfg, mean_T)
+    step_gbs = step_bytes / (ms_per_token * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # ---- eager launches, same kernels (graph vs eager)
+    eng.set_graph_mode(False)
+    eng.sync()
+    torch.cuda.synchronize()
+    n_eager = 20
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    enqueue(n_eager)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = s2.elapsed_time(e2) / n_eager
+    eng.set_graph_mode(True)
+
+    # ---- per-kernel breakdown (events between serialised launches)
+    names = ["qkv", "attention", "o_proj", "gate_up", "down"]
+    per = {n: [] for n in names + ["lm_head"]}
+    for _ in range(args.profile_steps):
+        if eng.seq_len() >= ctx:
+            eng.truncate(T0)
+        ms = eng.profile_step()
+        for l in range(cfg.n_layers):
+            for j, n in enumerate(names):
+                per[n].append(float(ms[5 * l + j]))
+        per["lm_head"].append(float(ms[-1]))
+    totals = {n: sum(v) / args.profile_steps for n, v in per.items()}
+    dom = max(totals, key=totals.get)
+    kb = kernel_bytes(cfg, mean_T)
+    avg_ms = statistics.mean(per[dom])
+    achieved = kb[dom] / (avg_ms * 1e-3) / 1e9
+    breakdown = {n: {"avg_us": round(1e3 * statistics.mean(v), 2),
+                     "share": round(totals[n] / sum(totals.values()), 4),
+                     "gbs": round(kb[n] / (statistics.mean(v) * 1e-3) / 1e9, 1)} for n, v in per.items()}
+
+    # ---- end to end through the C ABI: host token in (pinned H2D), host token out (D2H)
+    toks = sm.prompt(cfg, args.seed, args.e2e_steps, stream=1)
+    if eng.seq_len() + args.e2e_steps > ctx:
+        eng.truncate(max(0, ctx - args.e2e_steps - 1))
+        eng.sync()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for t in toks:
+        eng.decode_step(int(t))
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        total, sample, _ = oracle_sample(cfg, args.seed, ctx, 6, lm_w)
+        cpu = {"value": round(total, 2), "unit": "ms/token", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": sample}
+
+    tok_s = 1e3 / ms_per_token
+    line = {
+        "metric": METRIC, "value": round(ms_per_token, 4), "unit": "ms/token",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_token, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 weights, fp16 products, fp32 accumulate",
+        "data": "synthetic (seeded weights, prompts and KV fill)",
+        "config": {"workload": f"{cfg.name}-shape INT4 g128 decode, batch 1, greedy, KV {T0 + 1}..{ctx} "
+                               f"(mean {mean_T:.0f}), seeded KV through a shuffled page table",
+                   "global_batch": 1, "seq_len": ctx, "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (4.7 GB per step vs 129 MB)"},
+        "tokens_per_s": round(tok_s * ws, 2),
+        "hbm_gbs": round(step_gbs, 1),
+        "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peak,
+                          "unit": "GB/s", "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind,
+                          "frac_of_8tbs": round(step_gbs / NOMINAL_HBM_GBS, 4),
+                          "bytes_per_step": int(step_bytes)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "bytes_per_launch": int(kb[dom]), "avg_launch_us": round(avg_ms * 1e3, 2),
+                     "peak_kind": peak_kind},
+        "kernels": breakdown,
+        "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
+        "eager_ms_per_token": round(eager_ms, 4),
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 8},
+        "gpu_launches": args.steps * (5 * cfg.n_layers + 1) + extra,
+        "clocks": clocks,
+        "setup_s": round(setup_s, 1),
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

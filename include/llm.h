@@ -1,0 +1,210 @@
+/*
+ * llm.h - C ABI of the GB300 batch-1 quantized decode engine (libllm.so).
+ *
+ * The engine runs the autoregressive decode step of a dense Qwen2/Qwen3-style
+ * grouped-query-attention decoder whose seven per-layer projections (q, k, v,
+ * o, gate, up, down) hold weight-only quantized codes, on one GPU, replaying
+ * the whole step from one CUDA graph.
+ *
+ * Sources for the operation (page titles and sections):
+ *   - "How To Construct Your Personal LLM Runtime From Scratch": §3 (model
+ *     dims, GQA 7:1, 16-token bf16/fp16 KV pages, symmetric INT4 group-128
+ *     with one scale per group per output row), §4 (packed weight file that is
+ *     refused on a wrong magic or layout id), §6 (scalars live in device memory
+ *     so a captured graph stays valid as the context grows), §7 (ValueShuffle
+ *     nibble order, INT4 decode contract).
+ *   - "Bare-Metal LLM Inference on NVIDIA H100", "Architectural Blueprint" and
+ *     "Challenge 2" (one graph per step instead of ~280 eager launches).
+ *   - "FlashQwen", stages 5-8 (greedy argmax on the GPU returning one int,
+ *     single-token decode from a CUDA graph, flash-decoding split-K attention
+ *     with a combine pass, INT8 weights with one scale per output row) and the
+ *     in-chat /reset command (the KV cache persists until reset).
+ *
+ * Conventions for every call:
+ *   - Return value: LLM_OK (0) or a negative LLM_ERR_* code; nothing throws
+ *     across this boundary.  llm_status_str() names a code.
+ *   - "device" pointers are CUDA device addresses on the current device;
+ *     "host" pointers are ordinary CPU memory.
+ *   - Calls on one handle are not thread-safe; use one handle per thread.
+ */
+#ifndef QD_LLM_H
+#define QD_LLM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define LLM_OK 0
+#define LLM_ERR_ARG (-1)          /* null/misaligned pointer, unsupported shape or value     */
+#define LLM_ERR_LAYOUT (-2)       /* layout_id does not match weight_format (refused load)    */
+#define LLM_ERR_CONTEXT_FULL (-3) /* the step would write position >= max_context            */
+#define LLM_ERR_CUDA (-4)         /* a CUDA runtime call failed (allocation, launch, copy)    */
+#define LLM_ERR_TIMEOUT (-5)      /* a bounded device-side wait gave up (sticky error word)   */
+#define LLM_ERR_DEVICE (-6)       /* a device-side check failed (sticky error word)           */
+#define LLM_ERR_STATE (-7)        /* call out of order (e.g. llm_logits before any step)      */
+
+/* ---- weight formats and packed layouts -------------------------------- */
+/* INT4, symmetric, zero point 0, group 128 along K, one bfloat16 scale per
+ * (output row, group).  Codes are two's-complement nibbles in [-8, 7].       */
+#define LLM_FMT_INT4_G128 1
+/* INT8, symmetric, one fp32 scale per output row, codes in [-127, 127].      */
+#define LLM_FMT_INT8_ROW 2
+
+/* Layout 1 ("ValueShuffle", the pages' lane map): uint32 words [N][K/8],
+ * row-major and K-contiguous; logical code k = 8w + i of a row sits in word w
+ * at bit shift {0,16,4,20,8,24,12,28}[i] (even lanes in the low half-word,
+ * odd lanes in the high half-word).  Scales: bfloat16 [N][K/128] row-major.
+ * llm_pack_int4_g128() writes this layout.                                   */
+#define LLM_LAYOUT_INT4_VALUESHUFFLE 1
+/* Layout 2: int8 codes [N][K] in natural byte order, row-major; scales fp32 [N]. */
+#define LLM_LAYOUT_INT8_ROW 2
+
+/* ---- configuration ----------------------------------------------------- */
+typedef struct llm_config {
+    int32_t n_layers;   /* decoder layers L                                    */
+    int32_t hidden;     /* residual width h (multiple of 128)                  */
+    int32_t n_q_heads;  /* query heads Hq                                      */
+    int32_t n_kv_heads; /* key/value heads Hkv; Hq % Hkv == 0, Hq/Hkv <= 8      */
+    int32_t head_dim;   /* d: 64 or 128                                        */
+    int32_t mlp;        /* SwiGLU width F (multiple of 128)                    */
+    int32_t vocab;      /* V (multiple of 64)                                  */
+    float rms_eps;      /* RMSNorm epsilon                                     */
+    float rope_base;    /* RoPE base; theta_i = base^(-2i/d), pairs (i, i+d/2) */
+    int32_t qkv_bias;   /* 1: q/k/v projections add a bf16 bias                */
+    int32_t qk_norm;    /* 1: per-head RMSNorm of q and k before RoPE (Qwen3)  */
+    int32_t tied_lm_head; /* 1: the LM head is the bf16 embedding matrix       */
+    int32_t weight_format; /* LLM_FMT_*                                        */
+    int32_t layout_id;     /* LLM_LAYOUT_*; must match weight_format           */
+    int32_t max_context;   /* KV capacity in tokens (>= 1)                     */
+    int32_t page_tokens;   /* tokens per KV page; must be 16                   */
+} llm_config;
+
+/* Per-layer weights, all DEVICE pointers, 16-byte aligned, borrowed: the
+ * caller keeps them alive and unchanged until llm_destroy().
+ *   w*: packed codes in the config's layout; shapes [N][K] with
+ *       q: [Hq*d][h], k,v: [Hkv*d][h], o: [h][Hq*d], gate,up: [F][h], down: [h][F]
+ *   s*: scales in the config's layout (bf16 [N][K/128] or fp32 [N])
+ *   b*: bf16 bias [N] (only read when qkv_bias), else may be NULL
+ *   attn_norm, mlp_norm: bf16 [h]; q_norm, k_norm: bf16 [d] (only when qk_norm) */
+typedef struct llm_layer_weights {
+    const void *wq, *sq, *bq;
+    const void *wk, *sk, *bk;
+    const void *wv, *sv, *bv;
+    const void *wo, *so;
+    const void *wg, *sg;
+    const void *wu, *su;
+    const void *wd, *sd;
+    const void *attn_norm, *mlp_norm;
+    const void *q_norm, *k_norm;
+} llm_layer_weights;
+
+/* Model-level weights (DEVICE pointers, borrowed) plus a HOST array of layers
+ * that is copied during llm_create().
+ *   embed:      bf16 [V][h]
+ *   final_norm: bf16 [h]
+ *   lm_head:    bf16 [V][h] (INT4 models, untied); int8 [V][h] with lm_scale
+ *               fp32 [V] (INT8 models); ignored when tied_lm_head           */
+typedef struct llm_weights {
+    const void *embed;
+    const void *final_norm;
+    const void *lm_head;
+    const void *lm_scale;
+    const llm_layer_weights *layers;
+} llm_weights;
+
+typedef struct llm_t llm_t; /* opaque; owned by the library */
+
+/* Validate the configuration and weights, allocate the paged KV cache (one
+ * pool for K and one for V, [L][pages][Hkv][16][d] bf16, sharing one page
+ * table), the workspace and the RoPE table, and capture the decode step into
+ * one CUDA graph on `cuda_stream` (a cudaStream_t, or NULL for a stream the
+ * engine creates).  On success *out owns everything; on error *out is NULL
+ * and nothing leaks.  Errors: LLM_ERR_ARG, LLM_ERR_LAYOUT, LLM_ERR_CUDA.     */
+int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_stream,
+               llm_t **out);
+
+/* Run the prompt tokens[0..n-1] (HOST array) at positions seq_len..seq_len+n-1,
+ * filling the KV cache, and return the greedy next token in *first_token
+ * (HOST).  Blocks until done.  Errors: LLM_ERR_ARG (n <= 0, token out of range),
+ * LLM_ERR_CONTEXT_FULL, LLM_ERR_CUDA, LLM_ERR_DEVICE.                       */
+int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token);
+
+/* One decode step by graph replay.  The step consumes `forced_input` when it
+ * is >= 0 (teacher forcing), else the token the previous step emitted, writes
+ * its K/V at position seq_len, and returns the greedy argmax in *out_token
+ * (HOST).  Blocks until done.  Errors: LLM_ERR_ARG, LLM_ERR_CONTEXT_FULL
+ * (checked before any launch), LLM_ERR_STATE (no previous token), LLM_ERR_CUDA. */
+int llm_decode_step(llm_t *h, int32_t forced_input, int32_t *out_token);
+
+/* Enqueue n greedy decode steps (graph replays) on the engine's stream and
+ * return without waiting; each step feeds the previous step's argmax.  The
+ * emitted tokens stay on the device (llm_sync() then llm_last_token()).     */
+int llm_decode_enqueue(llm_t *h, int32_t n);
+
+/* Wait for enqueued work; reports a sticky device error if one was raised.  */
+int llm_sync(llm_t *h);
+
+/* Token emitted by the most recent completed step (HOST out).               */
+int llm_last_token(llm_t *h, int32_t *token);
+
+/* Copy the fp32 logits [vocab] of the most recent step to host_out.         */
+int llm_logits(llm_t *h, float *host_out, int32_t vocab);
+
+/* Number of tokens in the KV cache (the next step's position).              */
+int llm_seq_len(llm_t *h, int32_t *seq_len);
+
+/* Forget the sequence: seq_len = 0.  Keeps every allocation and the graph.  */
+int llm_reset(llm_t *h);
+
+/* Shorten the sequence to seq_len tokens (0 <= seq_len <= current length);
+ * the next step writes position seq_len.  Stream-ordered and asynchronous:
+ * it does not wait for enqueued steps.  The last emitted token stays the
+ * next input.  Errors: LLM_ERR_ARG, LLM_ERR_CUDA.                           */
+int llm_truncate(llm_t *h, int32_t seq_len);
+
+/* Per-kernel timing of one decode step ("How To Construct Your Personal LLM
+ * Runtime From Scratch", §6: the per-token ITL breakdown by region).  Runs
+ * one step with the kernels launched one by one and a CUDA event between
+ * neighbours (no launch overlap), advancing the sequence like a greedy step,
+ * and writes the duration in ms of kernel i to kernel_ms[i] (HOST, capacity
+ * cap).  Order: for each layer {qkv, attention, o_proj, gate_up, down}, then
+ * lm_head; *n_kernels = 5 * n_layers + 1.  Blocks until done.               */
+int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels);
+
+/* Free everything the handle owns (not the caller's weights).  NULL is a no-op. */
+void llm_destroy(llm_t *h);
+
+/* Static string naming a status code. */
+const char *llm_status_str(int status);
+
+/* Test and benchmark hook: DEVICE pointers to the KV pools ([L][pages][Hkv][16][d]
+ * bf16) and the page table (int32 [pages], logical page -> physical page,
+ * identity after create) so a caller can fill or shuffle them, and the number
+ * of pages.  When set_len >= 0 the sequence length becomes set_len (the caller
+ * promises positions 0..set_len-1 hold valid K/V).  Any out-param may be NULL. */
+int llm_debug_kv(llm_t *h, void **k_pool, void **v_pool, int32_t **page_table,
+                 int32_t *n_pages, int32_t set_len);
+
+/* Execution mode for llm_decode_step / llm_prefill: 1 = replay the captured
+ * graph (default), 0 = launch the same kernels one by one (eager), for timing
+ * the difference.                                                           */
+int llm_set_graph_mode(llm_t *h, int32_t use_graph);
+
+/* ---- offline packer (host memory, no GPU needed) ----------------------- */
+
+/* Pack logical INT4 codes (int8 [N][K], values in [-8, 7], K % 128 == 0) into
+ * layout LLM_LAYOUT_INT4_VALUESHUFFLE words [N][K/8].  Returns LLM_ERR_ARG on
+ * a null pointer, a bad shape or a code outside [-8, 7].                     */
+int llm_pack_int4_g128(const int8_t *codes, int64_t N, int64_t K, uint32_t *words);
+
+/* Layout LLM_LAYOUT_INT8_ROW keeps codes in natural order: this copies and
+ * checks the range [-127, 127].                                              */
+int llm_pack_int8_row(const int8_t *codes, int64_t N, int64_t K, int8_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QD_LLM_H */

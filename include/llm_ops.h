@@ -1,0 +1,59 @@
+/*
+ * llm_ops.h - single kernels of the decode step behind the C ABI (libllm.so).
+ *
+ * These run exactly the device code the engine's captured step runs, one
+ * kernel at a time, so each can be checked against the CPU oracle on its own.
+ * All array arguments are DEVICE pointers (16-byte aligned where they hold
+ * weights); `stream` is a cudaStream_t or NULL for the legacy default stream.
+ * Calls are asynchronous on `stream`; launch-time errors are returned as
+ * LLM_ERR_CUDA, argument errors as LLM_ERR_ARG (codes from llm.h).
+ */
+#ifndef QD_LLM_OPS_H
+#define QD_LLM_OPS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* y[n] = sum_k code[n][k] * scale[n][k/128] * x[k] (+ bias[n]) for n < N.
+ * INT4 group-128 dequant GEMV ("How To Construct Your Personal LLM Runtime From
+ * Scratch", §7: mask 4 bits, sign-extend bit 3, multiply by the group scale,
+ * accumulate the row in FP32).  w: layout LLM_LAYOUT_INT4_VALUESHUFFLE words
+ * [N][K/8]; s: bf16 [N][K/128]; bias: bf16 [N] or NULL; x: fp32 [K]; y: fp32 [N].
+ * N % 32 == 0, K % 256 == 0.                                               */
+int llm_op_gemv_int4(const void *w, const void *s, const void *bias, int32_t N, int32_t K,
+                     const float *x, float *y, void *stream);
+
+/* y[n] = scale[n] * sum_k code[n][k] * x[k] ("FlashQwen", stage 8: INT8 codes
+ * with one scale per output row).  w: int8 [N][K]; s: fp32 [N].
+ * N % 32 == 0, K % 128 == 0.                                               */
+int llm_op_gemv_int8(const void *w, const float *s, int32_t N, int32_t K, const float *x,
+                     float *y, void *stream);
+
+/* LM head with fused greedy argmax ("FlashQwen", stage 5): n = RMSNorm(x) with
+ * gain gamma (bf16 [K]) and eps; logits[v] = W[v] . n for v < N with W bf16
+ * [N][K] (lm_scale == NULL) or int8 [N][K] times lm_scale fp32 [N]; *token =
+ * the lowest index of the maximum logit.  N % 64 == 0, K % 256 == 0.
+ * token: int32 DEVICE pointer.                                             */
+int llm_op_lm_head_argmax(const void *w, const float *lm_scale, const void *gamma, float eps,
+                          int32_t N, int32_t K, const float *x, float *logits, int32_t *token,
+                          void *stream);
+
+/* Split-K grouped-query decode attention over a paged bf16 KV cache with the
+ * log-sum-exp combine ("FlashQwen", stage 7; GQA per "Bare-Metal LLM Inference
+ * on NVIDIA H100", "Architectural Blueprint").  For every query head h with
+ * group g = h / (Hq/Hkv): out[h] = sum_t softmax_t(q_h . K[g][t] / sqrt(d)) V[g][t]
+ * over t < T.  q: fp32 [Hq][d] (already rotated); k_pool, v_pool: bf16
+ * [pages][Hkv][16][d]; page_table: int32, logical page -> physical page;
+ * n_splits: key-range partitions per KV head (1..256, 0 = engine's choice);
+ * out: fp32 [Hq][d].  d in {64, 128}, Hq/Hkv <= 8, T >= 1.                  */
+int llm_op_attention(const float *q, const void *k_pool, const void *v_pool,
+                     const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                     int32_t n_splits, float *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QD_LLM_OPS_H */

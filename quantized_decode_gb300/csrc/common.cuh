@@ -1,0 +1,79 @@
+// common.cuh - small device helpers shared by the decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+#define QD_DEV __device__ __forceinline__
+
+namespace qd {
+
+// ---- programmatic dependent launch ---------------------------------------
+// Everything a kernel does before pdl_wait() may only touch data no earlier
+// kernel of the step writes (weights, scales, tables).  pdl_launch() lets the
+// next kernel's CTAs start their own weight prefetch while this one finishes.
+QD_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QD_DEV void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- global loads ----------------------------------------------------------
+// Weight streams are read exactly once per step: bypass L1 allocation.
+QD_DEV uint4 ld_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Prefetch a byte range of static data into L2 (no register or smem cost).
+QD_DEV void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+QD_DEV float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+QD_DEV uint16_t float_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+QD_DEV uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    // (a & b) ^ c
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+QD_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+QD_DEV half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<half2 *>(&v); }
+QD_DEV uint32_t h2_as_u32(half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// ---- warp / block reductions ---------------------------------------------
+QD_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+QD_DEV float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Sum over the LPR lanes of one row slot (slots are aligned groups of LPR lanes).
+template <int LPR>
+QD_DEV float slot_sum(float v) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace qd

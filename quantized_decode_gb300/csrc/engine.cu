@@ -1,0 +1,479 @@
+// engine.cu - the decode engine behind llm.h: validation, HBM layout, the step
+// plan, single-graph capture and the host/device handshake per step.
+//
+// One decode step = for each layer [QKV+RoPE+append] -> [split-K attention +
+// combine] -> [o_proj + residual] -> [RMSNorm + gate/up + SiLU*mul] ->
+// [down + residual], then [final RMSNorm + LM head + argmax]: 5L + 1 kernels,
+// chained with programmatic dependent launch and captured once into a CUDA
+// graph.  Position and input token live in device memory (DevState), so the
+// same graph replays at every position ("How To Construct Your Personal LLM
+// Runtime From Scratch", §6); the page for position pos is page_table[pos/16],
+// read on the device, so no host-side branch on page boundaries is needed.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/llm.h"
+#include "kernels.h"
+
+using namespace qd;
+
+struct llm_t {
+    llm_config cfg;
+    int fmt = 0;
+    std::vector<llm_layer_weights> layers;
+    llm_weights w{};
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    int device = 0;
+    LaunchCfg lc{};
+
+    uint16_t *k_pool = nullptr, *v_pool = nullptr;
+    size_t layer_kv_elems = 0;
+    int *page_table = nullptr;
+    int n_pages = 0;
+    float2 *rope_cs = nullptr;
+    DevState *st = nullptr;
+    float *x = nullptr, *raw = nullptr, *q = nullptr, *attn = nullptr, *u = nullptr, *logits = nullptr;
+    int *head_cnt = nullptr, *attn_cnt = nullptr, *lm_counter = nullptr, *lm_part_idx = nullptr;
+    float *part_o = nullptr, *part_ml = nullptr, *lm_part_val = nullptr;
+    int P = 1, lm_grid = 1;
+
+    int32_t *pinned = nullptr;  // host staging: [0] forced token, [2..3] last_token, err
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    bool use_graph = true;
+    int32_t seq_len = 0;
+    bool have_token = false;
+    bool stepped = false;
+};
+
+namespace {
+
+__global__ void k_set_state(DevState *st, int token, int pos, int clear_err) {
+    if (token >= 0) st->token = token;
+    if (pos >= 0) st->pos = pos;
+    if (clear_err) st->err = 0;
+}
+
+bool aligned16(const void *p) { return p && ((uintptr_t)p & 15) == 0; }
+
+template <typename T>
+cudaError_t dalloc(T **p, size_t count) {
+    return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T));
+}
+
+void free_all(llm_t *h) {
+    if (h->exec) cudaGraphExecDestroy(h->exec);
+    if (h->graph) cudaGraphDestroy(h->graph);
+    void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->rope_cs, h->st, h->x, h->raw, h->q,
+                    h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
+                    h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val};
+    for (void *b : bufs)
+        if (b) cudaFree(b);
+    if (h->pinned) cudaFreeHost(h->pinned);
+    if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
+}
+
+int validate(const llm_config *c, const llm_weights *w) {
+    if (!c || !w || !w->layers) return LLM_ERR_ARG;
+    if (c->weight_format == LLM_FMT_INT4_G128) {
+        if (c->layout_id != LLM_LAYOUT_INT4_VALUESHUFFLE) return LLM_ERR_LAYOUT;
+    } else if (c->weight_format == LLM_FMT_INT8_ROW) {
+        if (c->layout_id != LLM_LAYOUT_INT8_ROW) return LLM_ERR_LAYOUT;
+    } else {
+        return LLM_ERR_ARG;
+    }
+    if (c->n_layers < 1 || c->hidden < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->mlp < 1 ||
+        c->vocab < 1 || c->max_context < 1)
+        return LLM_ERR_ARG;
+    if (c->page_tokens != kPageTokens || c->vocab % 64 != 0) return LLM_ERR_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128) return LLM_ERR_ARG;
+    if (c->n_q_heads % c->n_kv_heads != 0 || c->n_q_heads / c->n_kv_heads > kMaxGqa) return LLM_ERR_ARG;
+    if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return LLM_ERR_ARG;
+    const int fmt = c->weight_format == LLM_FMT_INT4_G128 ? kFmtInt4 : kFmtInt8;
+    const int h = c->hidden, d = c->head_dim, rq = c->n_q_heads * d, rkv = c->n_kv_heads * d;
+    if (!qkv_shape_ok(fmt, rq, rkv, h, d)) return LLM_ERR_ARG;
+    if (!gemv_shape_ok(fmt, h, rq, 1) || !gemv_shape_ok(fmt, c->mlp, h, 2) ||
+        !gemv_shape_ok(fmt, h, c->mlp, 1))
+        return LLM_ERR_ARG;
+    const int lm_fmt = fmt == kFmtInt8 && !c->tied_lm_head ? kFmtInt8 : kFmtBf16;
+    if (!lm_head_shape_ok(lm_fmt, c->vocab, h)) return LLM_ERR_ARG;
+    if (!aligned16(w->embed) || !aligned16(w->final_norm)) return LLM_ERR_ARG;
+    if (!c->tied_lm_head) {
+        if (!aligned16(w->lm_head)) return LLM_ERR_ARG;
+        if (fmt == kFmtInt8 && !aligned16(w->lm_scale)) return LLM_ERR_ARG;
+    }
+    for (int l = 0; l < c->n_layers; ++l) {
+        const llm_layer_weights &L = w->layers[l];
+        const void *req[] = {L.wq, L.sq, L.wk, L.sk, L.wv, L.sv, L.wo, L.so, L.wg, L.sg,
+                             L.wu, L.su, L.wd, L.sd, L.attn_norm, L.mlp_norm};
+        for (const void *p : req)
+            if (!aligned16(p)) return LLM_ERR_ARG;
+        if (c->qkv_bias && (!L.bq || !L.bk || !L.bv)) return LLM_ERR_ARG;
+        if (c->qk_norm && (!aligned16(L.q_norm) || !aligned16(L.k_norm))) return LLM_ERR_ARG;
+    }
+    return LLM_OK;
+}
+
+// Enqueue one whole decode step (5L + 1 kernels).  With `ev`, event k is
+// recorded before kernel k and event 5L+1 after the last one.
+cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
+    const llm_config &c = h->cfg;
+    const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d;
+    cudaError_t e;
+    int k = 0;
+    auto mark = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[k++], h->stream) : cudaSuccess; };
+    for (int l = 0; l < c.n_layers; ++l) {
+        const llm_layer_weights &L = h->layers[l];
+        QkvArgs qa{};
+        qa.w[0] = L.wq; qa.w[1] = L.wk; qa.w[2] = L.wv;
+        qa.s[0] = L.sq; qa.s[1] = L.sk; qa.s[2] = L.sv;
+        if (c.qkv_bias) {
+            qa.b[0] = (const uint16_t *)L.bq;
+            qa.b[1] = (const uint16_t *)L.bk;
+            qa.b[2] = (const uint16_t *)L.bv;
+        }
+        qa.rows_q = rq; qa.rows_kv = rkv; qa.K = c.hidden; qa.d = d;
+        qa.Hq = c.n_q_heads; qa.Hkv = c.n_kv_heads;
+        qa.x = h->x;
+        qa.embed = l == 0 ? (const uint16_t *)h->w.embed : nullptr;
+        qa.x_init = h->x;
+        qa.gamma = (const uint16_t *)L.attn_norm;
+        qa.eps = c.rms_eps;
+        if (c.qk_norm) {
+            qa.q_gain = (const uint16_t *)L.q_norm;
+            qa.k_gain = (const uint16_t *)L.k_norm;
+        }
+        qa.raw = h->raw; qa.q_out = h->q; qa.head_cnt = h->head_cnt;
+        qa.k_pool = h->k_pool + (size_t)l * h->layer_kv_elems;
+        qa.v_pool = h->v_pool + (size_t)l * h->layer_kv_elems;
+        qa.page_table = h->page_table; qa.n_pages = h->n_pages;
+        qa.rope_cs = h->rope_cs; qa.st = h->st;
+        if ((e = mark()) != cudaSuccess || (e = launch_qkv(h->lc, h->fmt, qa)) != cudaSuccess) return e;
+
+        AttnArgs aa{};
+        aa.q = h->q; aa.k_pool = qa.k_pool; aa.v_pool = qa.v_pool;
+        aa.page_table = h->page_table; aa.n_pages = h->n_pages;
+        aa.st = h->st; aa.T_fixed = -1;
+        aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d; aa.P = h->P;
+        aa.part_o = h->part_o; aa.part_ml = h->part_ml; aa.counter = h->attn_cnt;
+        aa.out = h->attn; aa.err = &h->st->err;
+        if ((e = mark()) != cudaSuccess || (e = launch_attention(h->lc, aa)) != cudaSuccess) return e;
+
+        GemvArgs o{};
+        o.mode = 1; o.w = L.wo; o.s = L.so; o.N = c.hidden; o.K = rq; o.x = h->attn; o.y = h->x;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, o)) != cudaSuccess) return e;
+
+        GemvArgs gu{};
+        gu.mode = 2; gu.w = L.wg; gu.s = L.sg; gu.w2 = L.wu; gu.s2 = L.su;
+        gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
+        gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, gu)) != cudaSuccess) return e;
+
+        GemvArgs dn{};
+        dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, dn)) != cudaSuccess) return e;
+    }
+    LmHeadArgs la{};
+    const bool int8_head = h->fmt == kFmtInt8 && !c.tied_lm_head;
+    la.fmt = int8_head ? kFmtInt8 : kFmtBf16;
+    la.w = c.tied_lm_head ? h->w.embed : h->w.lm_head;
+    la.scale = int8_head ? (const float *)h->w.lm_scale : nullptr;
+    la.gamma = (const uint16_t *)h->w.final_norm;
+    la.eps = c.rms_eps; la.N = c.vocab; la.K = c.hidden; la.x = h->x; la.logits = h->logits;
+    la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
+    la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
+    if ((e = mark()) != cudaSuccess || (e = launch_lm_head(h->lc, la, h->lm_grid)) != cudaSuccess) return e;
+    return mark();
+}
+
+int run_step(llm_t *h) {
+    cudaError_t e = h->use_graph ? cudaGraphLaunch(h->exec, h->stream) : enqueue_step(h);
+    return e == cudaSuccess ? LLM_OK : LLM_ERR_CUDA;
+}
+
+int fetch_token(llm_t *h, int32_t *out) {
+    if (cudaMemcpyAsync(h->pinned + 2, &h->st->last_token, 2 * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    if (h->pinned[3] != kErrNone) return LLM_ERR_DEVICE;
+    if (out) *out = h->pinned[2];
+    return LLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *llm_status_str(int s) {
+    switch (s) {
+        case LLM_OK: return "ok";
+        case LLM_ERR_ARG: return "invalid argument";
+        case LLM_ERR_LAYOUT: return "packed layout does not match the weight format";
+        case LLM_ERR_CONTEXT_FULL: return "context full";
+        case LLM_ERR_CUDA: return "CUDA runtime error";
+        case LLM_ERR_TIMEOUT: return "device wait timed out";
+        case LLM_ERR_DEVICE: return "device-side check failed";
+        case LLM_ERR_STATE: return "call out of order";
+        default: return "unknown status";
+    }
+}
+
+int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_stream, llm_t **out) {
+    if (!out) return LLM_ERR_ARG;
+    *out = nullptr;
+    int rc = validate(cfg, weights);
+    if (rc != LLM_OK) return rc;
+    llm_t *h = new (std::nothrow) llm_t();
+    if (!h) return LLM_ERR_CUDA;
+    h->cfg = *cfg;
+    h->fmt = cfg->weight_format == LLM_FMT_INT4_G128 ? kFmtInt4 : kFmtInt8;
+    h->layers.assign(weights->layers, weights->layers + cfg->n_layers);
+    h->w = *weights;
+    h->w.layers = nullptr;
+
+    auto fail = [&](int code) {
+        free_all(h);
+        delete h;
+        return code;
+    };
+    if (cudaGetDevice(&h->device) != cudaSuccess) return fail(LLM_ERR_CUDA);
+    int n_sm = 0;
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+        return fail(LLM_ERR_CUDA);
+    if (cuda_stream) {
+        h->stream = (cudaStream_t)cuda_stream;
+    } else {
+        if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess)
+            return fail(LLM_ERR_CUDA);
+        h->own_stream = true;
+    }
+    h->lc.stream = h->stream;
+    h->lc.pdl = true;
+    h->lc.n_sm = n_sm;
+
+    const llm_config &c = h->cfg;
+    const int d = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
+    h->n_pages = (c.max_context + kPageTokens - 1) / kPageTokens;
+    h->layer_kv_elems = (size_t)h->n_pages * c.n_kv_heads * kPageTokens * d;
+    h->P = default_splits(n_sm, c.n_kv_heads, h->n_pages);
+    h->lm_grid = lm_head_grid(h->lc, c.vocab);
+    const size_t kv_elems = h->layer_kv_elems * c.n_layers;
+    const int rows_qkv = (c.n_q_heads + 2 * c.n_kv_heads) * d;
+    const int heads_qkv = c.n_q_heads + 2 * c.n_kv_heads;
+    bool ok = dalloc(&h->k_pool, kv_elems) == cudaSuccess && dalloc(&h->v_pool, kv_elems) == cudaSuccess &&
+              dalloc(&h->page_table, h->n_pages) == cudaSuccess &&
+              dalloc(&h->rope_cs, (size_t)c.max_context * (d / 2)) == cudaSuccess &&
+              dalloc(&h->st, 1) == cudaSuccess && dalloc(&h->x, c.hidden) == cudaSuccess &&
+              dalloc(&h->raw, rows_qkv) == cudaSuccess && dalloc(&h->q, c.n_q_heads * d) == cudaSuccess &&
+              dalloc(&h->attn, c.n_q_heads * d) == cudaSuccess && dalloc(&h->u, c.mlp) == cudaSuccess &&
+              dalloc(&h->logits, c.vocab) == cudaSuccess && dalloc(&h->head_cnt, heads_qkv) == cudaSuccess &&
+              dalloc(&h->attn_cnt, c.n_kv_heads) == cudaSuccess && dalloc(&h->lm_counter, 1) == cudaSuccess &&
+              dalloc(&h->lm_part_idx, h->lm_grid) == cudaSuccess &&
+              dalloc(&h->lm_part_val, h->lm_grid) == cudaSuccess &&
+              dalloc(&h->part_o, (size_t)c.n_kv_heads * h->P * G * d) == cudaSuccess &&
+              dalloc(&h->part_ml, (size_t)c.n_kv_heads * h->P * G * 2) == cudaSuccess &&
+              cudaMallocHost(reinterpret_cast<void **>(&h->pinned), 8 * sizeof(int32_t)) == cudaSuccess;
+    if (!ok) return fail(LLM_ERR_CUDA);
+
+    // Zeroed pools (slots past the sequence never hold NaN), counters at zero.
+    ok = cudaMemsetAsync(h->k_pool, 0, kv_elems * 2, h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->v_pool, 0, kv_elems * 2, h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->st, 0, sizeof(DevState), h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->head_cnt, 0, heads_qkv * sizeof(int), h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->attn_cnt, 0, c.n_kv_heads * sizeof(int), h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->lm_counter, 0, sizeof(int), h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->logits, 0, c.vocab * sizeof(float), h->stream) == cudaSuccess;
+    if (!ok) return fail(LLM_ERR_CUDA);
+
+    // Identity page table and the RoPE table: angle pos * base^(-2i/d) formed in double.
+    std::vector<int32_t> pt(h->n_pages);
+    for (int i = 0; i < h->n_pages; ++i) pt[i] = i;
+    std::vector<float2> cs((size_t)c.max_context * (d / 2));
+    for (int p = 0; p < c.max_context; ++p)
+        for (int i = 0; i < d / 2; ++i) {
+            const double theta = std::pow((double)c.rope_base, -2.0 * (double)i / (double)d);
+            const double ang = (double)p * theta;
+            cs[(size_t)p * (d / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    ok = cudaMemcpyAsync(h->page_table, pt.data(), pt.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                         h->stream) == cudaSuccess &&
+         cudaMemcpyAsync(h->rope_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                         h->stream) == cudaSuccess &&
+         cudaStreamSynchronize(h->stream) == cudaSuccess;
+    if (!ok) return fail(LLM_ERR_CUDA);
+
+    // Capture the whole step once.
+    if (cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return fail(LLM_ERR_CUDA);
+    cudaError_t ce = enqueue_step(h);
+    cudaError_t ee = cudaStreamEndCapture(h->stream, &h->graph);
+    if (ce != cudaSuccess || ee != cudaSuccess) return fail(LLM_ERR_CUDA);
+    if (cudaGraphInstantiate(&h->exec, h->graph, 0) != cudaSuccess) return fail(LLM_ERR_CUDA);
+    *out = h;
+    return LLM_OK;
+}
+
+void llm_destroy(llm_t *h) {
+    if (!h) return;
+    cudaStreamSynchronize(h->stream);
+    free_all(h);
+    delete h;
+}
+
+int llm_set_graph_mode(llm_t *h, int32_t use_graph) {
+    if (!h) return LLM_ERR_ARG;
+    h->use_graph = use_graph != 0;
+    return LLM_OK;
+}
+
+int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token) {
+    if (!h || !tokens || n <= 0) return LLM_ERR_ARG;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return LLM_ERR_ARG;
+    if ((int64_t)h->seq_len + n > h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    for (int i = 0; i < n; ++i) {
+        k_set_state<<<1, 1, 0, h->stream>>>(h->st, tokens[i], i == 0 ? h->seq_len : -1, 0);
+        if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
+        int rc = run_step(h);
+        if (rc != LLM_OK) return rc;
+    }
+    int rc = fetch_token(h, first_token);
+    if (rc != LLM_OK) return rc;
+    h->seq_len += n;
+    h->have_token = true;
+    h->stepped = true;
+    return LLM_OK;
+}
+
+int llm_decode_step(llm_t *h, int32_t forced_input, int32_t *out_token) {
+    if (!h) return LLM_ERR_ARG;
+    if (forced_input >= h->cfg.vocab) return LLM_ERR_ARG;
+    if (h->seq_len >= h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    if (forced_input < 0 && !h->have_token) return LLM_ERR_STATE;
+    if (forced_input >= 0) {
+        h->pinned[0] = forced_input;
+        if (cudaMemcpyAsync(&h->st->token, h->pinned, sizeof(int32_t), cudaMemcpyHostToDevice,
+                            h->stream) != cudaSuccess)
+            return LLM_ERR_CUDA;
+    }
+    int rc = run_step(h);
+    if (rc != LLM_OK) return rc;
+    rc = fetch_token(h, out_token);
+    if (rc != LLM_OK) return rc;
+    h->seq_len += 1;
+    h->have_token = true;
+    h->stepped = true;
+    return LLM_OK;
+}
+
+int llm_decode_enqueue(llm_t *h, int32_t n) {
+    if (!h || n < 0) return LLM_ERR_ARG;
+    if (n > 0 && !h->have_token) return LLM_ERR_STATE;
+    if ((int64_t)h->seq_len + n > h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    for (int i = 0; i < n; ++i) {
+        int rc = run_step(h);
+        if (rc != LLM_OK) return rc;
+        h->seq_len += 1;
+    }
+    if (n > 0) h->stepped = true;
+    return LLM_OK;
+}
+
+int llm_sync(llm_t *h) {
+    if (!h) return LLM_ERR_ARG;
+    return fetch_token(h, nullptr);
+}
+
+int llm_last_token(llm_t *h, int32_t *token) {
+    if (!h || !token) return LLM_ERR_ARG;
+    if (!h->stepped) return LLM_ERR_STATE;
+    return fetch_token(h, token);
+}
+
+int llm_logits(llm_t *h, float *host_out, int32_t vocab) {
+    if (!h || !host_out || vocab != h->cfg.vocab) return LLM_ERR_ARG;
+    if (!h->stepped) return LLM_ERR_STATE;
+    if (cudaMemcpyAsync(host_out, h->logits, (size_t)vocab * sizeof(float), cudaMemcpyDeviceToHost,
+                        h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    return cudaStreamSynchronize(h->stream) == cudaSuccess ? LLM_OK : LLM_ERR_CUDA;
+}
+
+int llm_seq_len(llm_t *h, int32_t *seq_len) {
+    if (!h || !seq_len) return LLM_ERR_ARG;
+    *seq_len = h->seq_len;
+    return LLM_OK;
+}
+
+int llm_reset(llm_t *h) {
+    if (!h) return LLM_ERR_ARG;
+    k_set_state<<<1, 1, 0, h->stream>>>(h->st, -1, 0, 1);
+    if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->seq_len = 0;
+    h->have_token = false;
+    h->stepped = false;
+    return LLM_OK;
+}
+
+int llm_truncate(llm_t *h, int32_t seq_len) {
+    if (!h || seq_len < 0 || seq_len > h->seq_len) return LLM_ERR_ARG;
+    k_set_state<<<1, 1, 0, h->stream>>>(h->st, -1, seq_len, 0);
+    if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
+    h->seq_len = seq_len;
+    return LLM_OK;
+}
+
+int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels) {
+    if (!h || !kernel_ms || !n_kernels) return LLM_ERR_ARG;
+    const int n = 5 * h->cfg.n_layers + 1;
+    *n_kernels = n;
+    if (cap < n) return LLM_ERR_ARG;
+    if (!h->have_token) return LLM_ERR_STATE;
+    if (h->seq_len >= h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    std::vector<cudaEvent_t> ev(n + 1, nullptr);
+    int rc = LLM_OK;
+    for (auto &e : ev)
+        if (cudaEventCreate(&e) != cudaSuccess) rc = LLM_ERR_CUDA;
+    if (rc == LLM_OK) {
+        const bool pdl = h->lc.pdl;
+        h->lc.pdl = false;
+        cudaError_t e = enqueue_step(h, ev.data());
+        h->lc.pdl = pdl;
+        if (e != cudaSuccess || cudaStreamSynchronize(h->stream) != cudaSuccess) rc = LLM_ERR_CUDA;
+    }
+    for (int i = 0; rc == LLM_OK && i < n; ++i)
+        if (cudaEventElapsedTime(&kernel_ms[i], ev[i], ev[i + 1]) != cudaSuccess) rc = LLM_ERR_CUDA;
+    for (auto &e : ev)
+        if (e) cudaEventDestroy(e);
+    if (rc != LLM_OK) return rc;
+    rc = fetch_token(h, nullptr);
+    if (rc != LLM_OK) return rc;
+    h->seq_len += 1;
+    h->stepped = true;
+    return LLM_OK;
+}
+
+int llm_debug_kv(llm_t *h, void **k_pool, void **v_pool, int32_t **page_table, int32_t *n_pages,
+                 int32_t set_len) {
+    if (!h) return LLM_ERR_ARG;
+    if (set_len > h->cfg.max_context) return LLM_ERR_ARG;
+    if (k_pool) *k_pool = h->k_pool;
+    if (v_pool) *v_pool = h->v_pool;
+    if (page_table) *page_table = h->page_table;
+    if (n_pages) *n_pages = h->n_pages;
+    if (set_len >= 0) {
+        k_set_state<<<1, 1, 0, h->stream>>>(h->st, -1, set_len, 0);
+        if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
+        if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+        h->seq_len = set_len;
+    }
+    return LLM_OK;
+}
+
+}  // extern "C"

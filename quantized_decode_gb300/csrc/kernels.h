@@ -1,0 +1,122 @@
+// kernels.h - launch interface of the decode-step kernels (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qd {
+
+constexpr int kPageTokens = 16;   // KV tokens per page (16-token pages, bf16)
+constexpr int kGroup = 128;       // INT4 quantization group along K
+constexpr int kMaxGqa = 8;        // query heads per KV head supported by the attention kernel
+
+// Device-side error word (sticky until the host clears it).
+enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3 };
+
+enum WeightFormat : int { kFmtInt4 = 1, kFmtInt8 = 2, kFmtBf16 = 3 };
+
+// Scalars of the running sequence, resident in device memory so that one
+// captured graph serves every position.
+struct DevState {
+    int32_t pos;         // position the next step writes (= tokens in the cache)
+    int32_t token;       // token the next step consumes
+    int32_t last_token;  // argmax emitted by the most recent step
+    int32_t err;         // sticky device error word (kErr*)
+};
+
+// Launch configuration shared by all kernels of one step.
+struct LaunchCfg {
+    cudaStream_t stream;
+    bool pdl;     // programmatic dependent launch attribute
+    int n_sm;     // SMs on the device
+};
+
+// RMSNorm -> Q/K/V GEMV (+bias) -> per-head (q/k RMSNorm) + RoPE -> q out,
+// K/V appended to the paged cache at the current position.
+struct QkvArgs {
+    const void *w[3];       // q, k, v codes
+    const void *s[3];       // q, k, v scales
+    const uint16_t *b[3];   // q, k, v bias (bf16) or null
+    int rows_q, rows_kv;    // Hq*d and Hkv*d
+    int K;                  // hidden
+    int d, Hq, Hkv;
+    const float *x;         // residual [K] (ignored when embed != null)
+    const uint16_t *embed;  // layer 0: bf16 embedding table [V][K]
+    float *x_init;          // layer 0: residual initialised from the embedding row
+    const uint16_t *gamma;  // attn_norm
+    float eps;
+    const uint16_t *q_gain, *k_gain;  // per-head RMSNorm gains, or null
+    float *raw;             // [rows_q + 2 rows_kv] scratch
+    float *q_out;           // [rows_q] rotated queries
+    int *head_cnt;          // [Hq + 2 Hkv] completion counters (self-resetting)
+    uint16_t *k_pool, *v_pool;  // this layer's pools [pages][Hkv][16][d]
+    const int *page_table;
+    int n_pages;
+    const float2 *rope_cs;  // [max_context][d/2] (cos, sin)
+    DevState *st;
+};
+
+// y = W x with a fused epilogue: mode 0 stores (plus optional bias), mode 1
+// adds into y (residual), mode 2 is the gate/up pair with SiLU*mul.
+struct GemvArgs {
+    int mode;
+    const void *w, *s;      // codes and scales (gate for mode 2)
+    const void *w2, *s2;    // up codes and scales (mode 2)
+    const uint16_t *bias;   // mode 0 only
+    int N, K;               // N output rows (mode 2: F hidden units)
+    const float *x;         // input activations [K]
+    const uint16_t *gamma;  // RMSNorm gain applied to x first, or null
+    float eps;
+    float *y;               // output [N]
+};
+
+// Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
+// ties).  The last CTA reduces the per-CTA maxima, writes the token into the
+// state (as the next step's input) and advances the position when `advance`.
+struct LmHeadArgs {
+    int fmt;                // kFmtBf16 or kFmtInt8
+    const void *w;          // bf16 [V][K] or int8 [V][K]
+    const float *scale;     // int8 row scales or null
+    const uint16_t *gamma;
+    float eps;
+    int N, K;
+    const float *x;
+    float *logits;          // [N]
+    float *part_val;        // [grid] per-CTA maxima
+    int *part_idx;          // [grid]
+    int *counter;           // self-resetting
+    int *token_out;         // where the argmax goes (state or user buffer)
+    DevState *st;           // non-null: last_token/token written, pos advanced
+    int advance;
+};
+
+// Split-K decode attention over the paged cache with the LSE combine.
+struct AttnArgs {
+    const float *q;                    // [Hq][d] rotated
+    const uint16_t *k_pool, *v_pool;   // this layer [pages][Hkv][16][d]
+    const int *page_table;
+    int n_pages;
+    const DevState *st;                // T = st->pos + 1 when T_fixed < 0
+    int T_fixed;
+    int Hq, Hkv, d, P;                 // P = splits per KV head
+    float *part_o;                     // [Hkv][P][G][d]
+    float *part_ml;                    // [Hkv][P][G][2]
+    int *counter;                      // [Hkv] self-resetting
+    float *out;                        // [Hq][d]
+    int *err;
+};
+
+// Each launcher returns the launch's cudaError_t.
+cudaError_t launch_qkv(const LaunchCfg &lc, int fmt, const QkvArgs &a);
+cudaError_t launch_gemv(const LaunchCfg &lc, int fmt, const GemvArgs &a);
+cudaError_t launch_lm_head(const LaunchCfg &lc, const LmHeadArgs &a, int grid);
+cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a);
+
+// Grid sizes and shape checks used by the engine when it plans buffers.
+int lm_head_grid(const LaunchCfg &lc, int N);
+int default_splits(int n_sm, int Hkv, int max_pages);
+bool gemv_shape_ok(int fmt, int N, int K, int mode);
+bool qkv_shape_ok(int fmt, int rows_q, int rows_kv, int K, int d);
+bool lm_head_shape_ok(int fmt, int N, int K);
+
+}  // namespace qd

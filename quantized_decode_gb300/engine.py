@@ -1,0 +1,183 @@
+"""Python face of the C ABI: an Engine handle and a device-resident packed model.
+
+PyTorch supplies device memory and the stream; packing runs in libllm.so's host packer and
+every step of decoding runs in libllm.so's CUDA kernels.
+"""
+import ctypes
+
+import numpy as np
+
+from . import _lib as L
+
+PROJ_FIELDS = {"q": ("wq", "sq", "bq"), "k": ("wk", "sk", "bk"), "v": ("wv", "sv", "bv"),
+               "o": ("wo", "so", None), "gate": ("wg", "sg", None), "up": ("wu", "su", None),
+               "down": ("wd", "sd", None)}
+PROJS = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def _np_ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def pack_int4(codes):
+    """Logical INT4 codes [N][K] (int8, [-8,7]) -> ValueShuffle words [N][K/8] via libllm."""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    N, K = codes.shape
+    words = np.empty((N, K // 8), dtype=np.uint32)
+    L.check(L.load().llm_pack_int4_g128(_np_ptr(codes), N, K, _np_ptr(words)), "llm_pack_int4_g128")
+    return words
+
+
+def pack_int8(codes):
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    out = np.empty_like(codes)
+    L.check(L.load().llm_pack_int8_row(_np_ptr(codes), codes.shape[0], codes.shape[1], _np_ptr(out)),
+            "llm_pack_int8_row")
+    return out
+
+
+def make_config(cfg):
+    """llm_config from any object with the model-shape attributes."""
+    fmt = int(cfg.weight_format)
+    return L.llm_config(
+        n_layers=cfg.n_layers, hidden=cfg.hidden, n_q_heads=cfg.n_q_heads,
+        n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, mlp=cfg.mlp, vocab=cfg.vocab,
+        rms_eps=cfg.rms_eps, rope_base=cfg.rope_base, qkv_bias=int(cfg.qkv_bias),
+        qk_norm=int(cfg.qk_norm), tied_lm_head=int(cfg.tied_lm_head), weight_format=fmt,
+        layout_id=L.LLM_LAYOUT_INT4_VALUESHUFFLE if fmt == L.LLM_FMT_INT4_G128 else L.LLM_LAYOUT_INT8_ROW,
+        max_context=cfg.max_context, page_tokens=16)
+
+
+class DeviceModel:
+    """Packed decoder weights resident in device memory (torch tensors) + the ABI structs.
+
+    get_proj(layer, proj) -> dict(codes [N][K] int8, scales, bias or None)
+    get_norms(layer) -> dict(attn_norm, mlp_norm, q_norm, k_norm) of bf16 bit arrays or None
+    embed: bf16 bits [V][h]; final_norm: bf16 bits [h];
+    lm_head: dict(kind='tied'|'bf16'|'int8', w | codes+scales)
+    """
+
+    def __init__(self, cfg, get_proj, get_norms, embed, final_norm, lm_head, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.device = device
+        self._t = []
+        int4 = int(cfg.weight_format) == L.LLM_FMT_INT4_G128
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            t = torch.from_numpy(a.view(np.uint8).reshape(-1)).to(device)
+            self._t.append(t)
+            return t.data_ptr()
+
+        layers = (L.llm_layer_weights * cfg.n_layers)()
+        for l in range(cfg.n_layers):
+            for proj in PROJS:
+                t = get_proj(l, proj)
+                fw, fs, fb = PROJ_FIELDS[proj]
+                w = pack_int4(t["codes"]) if int4 else pack_int8(t["codes"])
+                setattr(layers[l], fw, up(w))
+                setattr(layers[l], fs, up(np.ascontiguousarray(t["scales"])))
+                if fb and t.get("bias") is not None:
+                    setattr(layers[l], fb, up(np.ascontiguousarray(t["bias"], dtype=np.uint16)))
+            for k, v in get_norms(l).items():
+                if v is not None:
+                    setattr(layers[l], k, up(np.ascontiguousarray(v, dtype=np.uint16)))
+        self.layers = layers
+        w = L.llm_weights()
+        w.embed = up(np.ascontiguousarray(embed, dtype=np.uint16))
+        w.final_norm = up(np.ascontiguousarray(final_norm, dtype=np.uint16))
+        if lm_head["kind"] == "bf16":
+            w.lm_head = up(np.ascontiguousarray(lm_head["w"], dtype=np.uint16))
+        elif lm_head["kind"] == "int8":
+            w.lm_head = up(pack_int8(lm_head["codes"]))
+            w.lm_scale = up(np.ascontiguousarray(lm_head["scales"], dtype=np.float32))
+        w.layers = layers
+        self.weights = w
+
+    def nbytes(self):
+        return sum(t.numel() for t in self._t)
+
+
+class Engine:
+    """One decode sequence on one GPU (llm_t handle)."""
+
+    def __init__(self, model, stream=None, config=None):
+        self.lib = L.load()
+        self.model = model
+        self.cfg = config if config is not None else make_config(model.cfg)
+        self.vocab = self.cfg.vocab
+        h = ctypes.c_void_p()
+        s = None if stream is None else ctypes.c_void_p(stream)
+        L.check(self.lib.llm_create(ctypes.byref(self.cfg), ctypes.byref(model.weights), s,
+                                    ctypes.byref(h)), "llm_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            self.lib.llm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, tokens):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_prefill(self.h, toks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                     toks.size, ctypes.byref(out)), "llm_prefill")
+        return out.value
+
+    def decode_step(self, forced=-1):
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_decode_step(self.h, int(forced), ctypes.byref(out)), "llm_decode_step")
+        return out.value
+
+    def decode_enqueue(self, n):
+        L.check(self.lib.llm_decode_enqueue(self.h, int(n)), "llm_decode_enqueue")
+
+    def sync(self):
+        L.check(self.lib.llm_sync(self.h), "llm_sync")
+
+    def last_token(self):
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_last_token(self.h, ctypes.byref(out)), "llm_last_token")
+        return out.value
+
+    def logits(self):
+        out = np.empty(self.vocab, dtype=np.float32)
+        L.check(self.lib.llm_logits(self.h, _np_ptr(out), self.vocab), "llm_logits")
+        return out
+
+    def seq_len(self):
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_seq_len(self.h, ctypes.byref(out)), "llm_seq_len")
+        return out.value
+
+    def reset(self):
+        L.check(self.lib.llm_reset(self.h), "llm_reset")
+
+    def truncate(self, n):
+        L.check(self.lib.llm_truncate(self.h, int(n)), "llm_truncate")
+
+    def profile_step(self):
+        """One greedy step with per-kernel CUDA-event timing -> array of ms (5L + 1)."""
+        n_layers = self.cfg.n_layers
+        out = np.empty(5 * n_layers + 1, dtype=np.float32)
+        n = ctypes.c_int32()
+        L.check(self.lib.llm_profile_step(self.h, _np_ptr(out), out.size, ctypes.byref(n)),
+                "llm_profile_step")
+        return out[:n.value]
+
+    def set_graph_mode(self, on):
+        L.check(self.lib.llm_set_graph_mode(self.h, int(bool(on))), "llm_set_graph_mode")
+
+    def debug_kv(self, set_len=-1):
+        """-> (k_pool ptr, v_pool ptr, page_table ptr, n_pages)."""
+        k, v, pt, n = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int32()
+        L.check(self.lib.llm_debug_kv(self.h, ctypes.byref(k), ctypes.byref(v), ctypes.byref(pt),
+                                      ctypes.byref(n), int(set_len)), "llm_debug_kv")
+        return k.value, v.value, pt.value, n.value

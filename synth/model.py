@@ -165,3 +165,16 @@ def kv_fill(cfg, seed, layer, T):
 __all__ = ["ModelConfig", "CONFIGS", "PROJS", "FMT_INT4_G128", "FMT_INT8_ROW", "GROUP",
            "proj_shape", "quantized_tensor", "layer_proj", "layer_norms", "embedding",
            "final_norm", "lm_head", "prompt", "kv_fill", "bf16_to_f32"]
+
+
+def recipe(cfg, seed):
+    """Callables and arrays describing one seeded synthetic model (logical, unpacked).
+
+    Returns (get_proj(layer, proj), get_norms(layer), embed, final_norm, lm_head) in the
+    argument order a device-model builder takes.
+    """
+    return (lambda l, p: layer_proj(cfg, seed, l, p),
+            lambda l: layer_norms(cfg, seed, l),
+            embedding(cfg, seed),
+            final_norm(cfg, seed),
+            lm_head(cfg, seed))
