@@ -53,6 +53,26 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool,
                      const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
                      int32_t n_splits, float *out, void *stream);
 
+/* llm_op_attention without any device allocation.  There is no counterpart
+ * in the source pages: this serves callers that may not allocate device memory
+ * when they call in (a host framework that owns all device memory through its
+ * own pool and forbids cudaMalloc on its threads, or latency-critical paths
+ * where an allocation could lock or synchronise).  Same arguments, same kernel
+ * and same result as llm_op_attention, but the scratch (per-split partials and
+ * arrival counters) lives in a fixed 4 MiB array of device memory inside the
+ * library, which every GPU that loads the library holds until exit.
+ * Size limit: 256 + Hq * P * (d + 2) * 4 bytes <= 4 MiB, with P = n_splits (or
+ * the engine's choice when 0), and Hkv <= 63; larger requests return
+ * LLM_ERR_ARG before anything is launched.  Calls no cudaMalloc or cudaFree;
+ * the counters are reset with cudaMemsetAsync on `stream` each call.  The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make it before any
+ * stream capture.  All calls on a device share the array: calls that may run
+ * concurrently on the GPU (different streams without ordering) race.         */
+int llm_op_attention_noalloc(const float *q, const void *k_pool, const void *v_pool,
+                             const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t n_splits, float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

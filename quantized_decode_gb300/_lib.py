@@ -72,6 +72,7 @@ SIGNATURES = {
     "llm_op_gemv_int8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_op_lm_head_argmax": (i32, [vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]),
     "llm_op_attention": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "llm_op_attention_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
 }
 
 _lib = None
