@@ -331,6 +331,17 @@ def run_ours(args):
     step_gbs = step_bytes / (ms_per_token * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
+    # ---- graph replay with programmatic dependent launch (default is off)
+    eng.set_pdl(True)
+    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_pdl = 100
+    s3.record(stream)
+    enqueue(n_pdl)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    pdl_ms = s3.elapsed_time(e3) / n_pdl
+    eng.set_pdl(False)
+
     # ---- eager launches, same kernels (graph vs eager)
     eng.set_graph_mode(False)
     eng.sync()
@@ -406,6 +417,7 @@ def run_ours(args):
         "kernels": breakdown,
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
         "eager_ms_per_token": round(eager_ms, 4),
+        "graph_pdl_ms_per_token": round(pdl_ms, 4),
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps * (5 * cfg.n_layers + 1) + extra,

@@ -193,6 +193,12 @@ int llm_debug_kv(llm_t *h, void **k_pool, void **v_pool, int32_t **page_table,
  * the difference.                                                           */
 int llm_set_graph_mode(llm_t *h, int32_t use_graph);
 
+/* 1: consecutive kernels of the step are launched with programmatic dependent
+ * launch (a kernel's CTAs may start before the previous kernel ends and wait
+ * for it on the device); 0 (default): plain stream order.  Re-captures the
+ * graph; waits for enqueued work first.  Errors: LLM_ERR_ARG, LLM_ERR_CUDA.  */
+int llm_set_pdl(llm_t *h, int32_t use_pdl);
+
 /* ---- offline packer (host memory, no GPU needed) ----------------------- */
 
 /* Pack logical INT4 codes (int8 [N][K], values in [-8, 7], K % 128 == 0) into

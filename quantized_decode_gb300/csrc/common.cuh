@@ -9,6 +9,7 @@
 #include "kernels.h"
 
 #define QD_DEV __device__ __forceinline__
+#define QD_HOST_DEV_INLINE __host__ __device__ __forceinline__
 
 namespace qd {
 

@@ -39,6 +39,8 @@ struct llm_t {
     float *x = nullptr, *raw = nullptr, *q = nullptr, *attn = nullptr, *u = nullptr, *logits = nullptr;
     int *head_cnt = nullptr, *attn_cnt = nullptr, *lm_counter = nullptr, *lm_part_idx = nullptr;
     float *part_o = nullptr, *part_ml = nullptr, *lm_part_val = nullptr;
+    float *stats = nullptr;     // 4 x kStatSlots (ss, mx) pairs: attention, o_proj, gate/up, down outputs
+    uint16_t *kv_new = nullptr; // [2][Hkv][d] appended rows of the current step
     int P = 1, lm_grid = 1;
 
     int32_t *pinned = nullptr;  // host staging: [0] forced token, [2..3] last_token, err
@@ -70,7 +72,7 @@ void free_all(llm_t *h) {
     if (h->graph) cudaGraphDestroy(h->graph);
     void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->rope_cs, h->st, h->x, h->raw, h->q,
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
-                    h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val};
+                    h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -125,6 +127,8 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
     const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d;
     cudaError_t e;
     int k = 0;
+    float *st_attn = h->stats, *st_o = h->stats + 2 * kStatSlots;
+    float *st_gu = h->stats + 4 * kStatSlots, *st_down = h->stats + 6 * kStatSlots;
     auto mark = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[k++], h->stream) : cudaSuccess; };
     for (int l = 0; l < c.n_layers; ++l) {
         const llm_layer_weights &L = h->layers[l];
@@ -152,6 +156,7 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         qa.v_pool = h->v_pool + (size_t)l * h->layer_kv_elems;
         qa.page_table = h->page_table; qa.n_pages = h->n_pages;
         qa.rope_cs = h->rope_cs; qa.st = h->st;
+        qa.kv_new = h->kv_new; qa.stats_in = l == 0 ? nullptr : st_down;
         if ((e = mark()) != cudaSuccess || (e = launch_qkv(h->lc, h->fmt, qa)) != cudaSuccess) return e;
 
         AttnArgs aa{};
@@ -161,20 +166,25 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d; aa.P = h->P;
         aa.part_o = h->part_o; aa.part_ml = h->part_ml; aa.counter = h->attn_cnt;
         aa.out = h->attn; aa.err = &h->st->err;
+        aa.kv_new = h->kv_new; aa.stats_out = st_attn;
         if ((e = mark()) != cudaSuccess || (e = launch_attention(h->lc, aa)) != cudaSuccess) return e;
 
         GemvArgs o{};
         o.mode = 1; o.w = L.wo; o.s = L.so; o.N = c.hidden; o.K = rq; o.x = h->attn; o.y = h->x;
+        o.stats_in = st_attn; o.stats_out = st_o; o.stats_gamma = (const uint16_t *)L.mlp_norm;
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, o)) != cudaSuccess) return e;
 
         GemvArgs gu{};
         gu.mode = 2; gu.w = L.wg; gu.s = L.sg; gu.w2 = L.wu; gu.s2 = L.su;
         gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
         gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
+        gu.stats_in = st_o; gu.stats_out = st_gu;
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, gu)) != cudaSuccess) return e;
 
         GemvArgs dn{};
         dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
+        dn.stats_in = st_gu; dn.stats_out = st_down;
+        dn.stats_gamma = (const uint16_t *)(l + 1 < c.n_layers ? h->layers[l + 1].attn_norm : h->w.final_norm);
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, dn)) != cudaSuccess) return e;
     }
     LmHeadArgs la{};
@@ -186,8 +196,23 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
     la.eps = c.rms_eps; la.N = c.vocab; la.K = c.hidden; la.x = h->x; la.logits = h->logits;
     la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
     la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
+    la.stats_in = st_down;
     if ((e = mark()) != cudaSuccess || (e = launch_lm_head(h->lc, la, h->lm_grid)) != cudaSuccess) return e;
     return mark();
+}
+
+// (Re)capture the whole step into the graph with the current launch settings.
+int capture(llm_t *h) {
+    if (h->exec) cudaGraphExecDestroy(h->exec);
+    if (h->graph) cudaGraphDestroy(h->graph);
+    h->exec = nullptr;
+    h->graph = nullptr;
+    if (cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return LLM_ERR_CUDA;
+    cudaError_t ce = enqueue_step(h);
+    cudaError_t ee = cudaStreamEndCapture(h->stream, &h->graph);
+    if (ce != cudaSuccess || ee != cudaSuccess) return LLM_ERR_CUDA;
+    if (cudaGraphInstantiate(&h->exec, h->graph, 0) != cudaSuccess) return LLM_ERR_CUDA;
+    return LLM_OK;
 }
 
 int run_step(llm_t *h) {
@@ -253,7 +278,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
         h->own_stream = true;
     }
     h->lc.stream = h->stream;
-    h->lc.pdl = true;
+    h->lc.pdl = false;  // measured: plain stream order beats early dependent launch here
     h->lc.n_sm = n_sm;
 
     const llm_config &c = h->cfg;
@@ -277,6 +302,8 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
               dalloc(&h->lm_part_val, h->lm_grid) == cudaSuccess &&
               dalloc(&h->part_o, (size_t)c.n_kv_heads * h->P * G * d) == cudaSuccess &&
               dalloc(&h->part_ml, (size_t)c.n_kv_heads * h->P * G * 2) == cudaSuccess &&
+              dalloc(&h->stats, (size_t)8 * kStatSlots) == cudaSuccess &&
+              dalloc(&h->kv_new, (size_t)2 * c.n_kv_heads * d) == cudaSuccess &&
               cudaMallocHost(reinterpret_cast<void **>(&h->pinned), 8 * sizeof(int32_t)) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
 
@@ -287,7 +314,8 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
          cudaMemsetAsync(h->head_cnt, 0, heads_qkv * sizeof(int), h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->attn_cnt, 0, c.n_kv_heads * sizeof(int), h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->lm_counter, 0, sizeof(int), h->stream) == cudaSuccess &&
-         cudaMemsetAsync(h->logits, 0, c.vocab * sizeof(float), h->stream) == cudaSuccess;
+         cudaMemsetAsync(h->logits, 0, c.vocab * sizeof(float), h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->stats, 0, (size_t)8 * kStatSlots * sizeof(float), h->stream) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
 
     // Identity page table and the RoPE table: angle pos * base^(-2i/d) formed in double.
@@ -308,12 +336,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     if (!ok) return fail(LLM_ERR_CUDA);
 
     // Capture the whole step once.
-    if (cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
-        return fail(LLM_ERR_CUDA);
-    cudaError_t ce = enqueue_step(h);
-    cudaError_t ee = cudaStreamEndCapture(h->stream, &h->graph);
-    if (ce != cudaSuccess || ee != cudaSuccess) return fail(LLM_ERR_CUDA);
-    if (cudaGraphInstantiate(&h->exec, h->graph, 0) != cudaSuccess) return fail(LLM_ERR_CUDA);
+    if (capture(h) != LLM_OK) return fail(LLM_ERR_CUDA);
     *out = h;
     return LLM_OK;
 }
@@ -329,6 +352,13 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph) {
     if (!h) return LLM_ERR_ARG;
     h->use_graph = use_graph != 0;
     return LLM_OK;
+}
+
+int llm_set_pdl(llm_t *h, int32_t use_pdl) {
+    if (!h) return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->lc.pdl = use_pdl != 0;
+    return capture(h);
 }
 
 int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token) {

@@ -1,11 +1,10 @@
 // gemv.cuh - weight-streaming dequant dot products for the batch-1 decode GEMVs.
 //
 // Work unit: 16 bytes of one weight row (32 INT4 codes, 16 INT8 codes or 8
-// bf16 values), loaded with one 128-bit streaming load.  A warp is split into
-// 32/LPR row slots of LPR lanes; the lanes of a slot stride over the units of
-// their rows and every lane carries RT rows at once, so one shared-memory load
-// of the activations serves RT weight rows.  The LPR partial sums of a row are
-// then combined with shuffles.
+// bf16 values).  A warp is split into 32/LPR row slots of LPR lanes; the lanes
+// of a slot stride over the units of their rows and every lane carries RT rows
+// at once, so one shared-memory load of the activations serves RT weight rows.
+// The LPR partial sums of a row are then combined with shuffles.
 //
 // Activations are staged in shared memory as fp16 pairs scaled by a power of
 // two 2^-e chosen so that every |value| <= 1 (fp16 products and short fp16 sums
@@ -71,158 +70,314 @@ QD_DEV float2 ffma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
-// ---------------------------------------------------------------------------
-// Row-tile dot products.  wrow[i]: the 16-byte units of row i; xs4: staged
-// activations; U: units per row; j: this lane's index within its slot.
-// On return every lane of the slot holds the full dot product of each row
-// (in the prescaled units of the staged activations).
-// ---------------------------------------------------------------------------
+// Swizzle of staged activations (see stage_activations): the staged vector is
+// cut into blocks of one weight unit's activations (blk_bytes = 64 for INT4
+// units of 32 codes as fp16, 32 for INT8 units as fp16 and for bf16 units as
+// fp32) and the 16-byte chunks of a block are XOR-permuted by block-index bits,
+// so the 8 lanes of a row slot, which read the same chunk of 8 consecutive
+// blocks, hit distinct bank groups.
+QD_HOST_DEV_INLINE uint32_t swz_mask(uint32_t blk, int blk_bytes) {
+    return blk_bytes == 64 ? ((blk >> 1) & 3u) : ((blk >> 2) & 1u);
+}
+QD_DEV uint32_t swz_offset(uint32_t byte_off, int blk_bytes) {
+    if (blk_bytes == 0) return byte_off;
+    const uint32_t blk = byte_off / (uint32_t)blk_bytes, in = byte_off % (uint32_t)blk_bytes;
+    return blk * (uint32_t)blk_bytes + ((((in >> 4) ^ swz_mask(blk, blk_bytes))) << 4) + (in & 15u);
+}
+template <int FMT>
+constexpr int act_blk_bytes() {
+    return FMT == kFmtInt4 ? 64 : 32;
+}
 
-// INT4 group-128: unit u covers codes 32u..32u+31, group u/4; scale per (row, group).
-template <int LPR, int RT>
-QD_DEV void int4_tile_dots(const uint4 *const (&wrow)[RT], const uint16_t *const (&srow)[RT],
-                           const uint4 *__restrict__ xs4, int U, int j, float (&out)[RT]) {
+// ---------------------------------------------------------------------------
+// Weight streaming through a lane-private shared-memory ring.
+//
+// A warp owns row tiles t_first, t_first + t_stride, ... < n_tiles and, within
+// each of them, the slabs [sb_begin, sb_end) of its K part; a slab is 16
+// consecutive 16-byte units of a row (512 INT4 codes, 256 INT8 codes or 128
+// bf16 values).  A row slot is 8 lanes; lane j takes units 16 s + j and
+// 16 s + 8 + j of slab s, so each copy instruction covers 128 contiguous bytes
+// of every row.  Every lane carries RT rows (rows(tile, i): their units and,
+// for INT4, their scale rows), so one shared-memory read of the activations
+// serves RT rows.  Units past the end of a row (K not a multiple of a slab)
+// are skipped.
+//
+// Each lane copies exactly the bytes it will consume (cp.async: two 16-byte
+// units per row and step, plus for INT4 the aligned 4-byte words that hold the
+// units' scales) into its own slots of a D-stage ring, D - 1 steps ahead of the
+// arithmetic, one commit group per step; the ring flows across tile
+// boundaries, and since a lane only reads what it copied, no barrier is needed.
+// At the end of a tile the 8 partial sums of each row are combined with
+// shuffles and `epi(tile, out)` runs on every lane (all lanes of a row slot
+// hold the same sums).  `sync()` (the dependency wait and the activation
+// staging) runs on all threads once, before the first weight copy, so the
+// activation loads do not queue behind the weight stream.
+//
+// Ring layout per warp: stage s, row i, unit h, lane l -> 16-byte unit at
+// ring[((s * RT + i) * 2 + h) * 32 + l] and scale word at sring[same index].
+// ---------------------------------------------------------------------------
+constexpr int kLanesPerRow = 8;
+
+struct RowRef {
+    const uint4 *w;     // 16-byte units of the row
+    const uint16_t *s;  // INT4: bf16 scales of the row, one per 128 codes
+};
+
+QD_DEV void cp_async16(void *smem, const void *gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+QD_DEV void cp_async4(void *smem, const void *gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+QD_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+QD_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int RT, int D>
+constexpr size_t ring_bytes_per_warp() {
+    return (size_t)D * RT * 2 * 32 * (16 + 4);
+}
+
+// One 16-byte unit of a row against its staged activations (x: 4 chunks for
+// INT4 as fp16, 2 chunks for INT8 as fp16, 2 float4 for bf16), fp32 result.
+QD_DEV float int4_unit_dot(uint4 q, const uint4 (&x)[4]) {
+    half2 a = u32_as_h2(0u), b = u32_as_h2(0u);
+    a = int4_word_dot(q.x, x[0], a);
+    b = int4_word_dot(q.y, x[1], b);
+    a = int4_word_dot(q.z, x[2], a);
+    b = int4_word_dot(q.w, x[3], b);
+    const float2 f = __half22float2(__hadd2(a, b));
+    return f.x + f.y;
+}
+QD_DEV float int8_unit_dot(uint4 q, const uint4 (&x)[2]) {
+    half2 a = u32_as_h2(0u), b = u32_as_h2(0u);
+    a = int8_word_dot(q.x, x[0].x, x[0].y, a);
+    b = int8_word_dot(q.y, x[0].z, x[0].w, b);
+    a = int8_word_dot(q.z, x[1].x, x[1].y, a);
+    b = int8_word_dot(q.w, x[1].z, x[1].w, b);
+    const float2 f = __half22float2(__hadd2(a, b));
+    return f.x + f.y;
+}
+QD_DEV float bf16_unit_dot(uint4 q, const float4 (&x)[2]) {
+    float2 p = make_float2(0.f, 0.f);
+    p = ffma2(make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)), make_float2(x[0].x, x[0].y), p);
+    p = ffma2(make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)), make_float2(x[0].z, x[0].w), p);
+    p = ffma2(make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)), make_float2(x[1].x, x[1].y), p);
+    p = ffma2(make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)), make_float2(x[1].z, x[1].w), p);
+    return p.x + p.y;
+}
+
+template <int FMT, int RT, int D, class Rows, class Epi, class Sync>
+QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int t_first, int t_stride,
+                        int n_tiles, int sb_begin, int sb_end, int U, int j, const void *xs, uint4 *ring,
+                        uint32_t *sring) {
+    static_assert(D >= 2, "ring depth");
+    constexpr int XC = FMT == kFmtInt4 ? 4 : 2;  // 16-byte activation chunks per unit
+    const int lane = threadIdx.x & 31;
+    const int n_it = sb_end > sb_begin ? sb_end - sb_begin : 0;
+    const int my_tiles = t_first < n_tiles ? (n_tiles - 1 - t_first) / t_stride + 1 : 0;
+    const int F = my_tiles * n_it;
+
+    sync();
+    const uint32_t xm = swz_mask((uint32_t)j, act_blk_bytes<FMT>());  // same for both units of every slab
+
+    int lt = t_first, li = 0;  // load cursor
+    RowRef lrow[RT];
+    auto load_rows = [&](int t) {
+#pragma unroll
+        for (int i = 0; i < RT; ++i) lrow[i] = rows(t, i);
+    };
+    if (F > 0) load_rows(lt);
+    auto issue = [&](int f) {
+        const int slot = f % D;
+        const int ub = 16 * (sb_begin + li) + j;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int u = ub + 8 * h;
+            if (u < U) {
+#pragma unroll
+                for (int i = 0; i < RT; ++i) {
+                    const int idx = ((slot * RT + i) * 2 + h) * 32 + lane;
+                    cp_async16(ring + idx, lrow[i].w + u);
+                    if constexpr (FMT == kFmtInt4) {
+                        const uintptr_t a = (uintptr_t)(lrow[i].s + (u >> 2));
+                        cp_async4(sring + idx, (const void *)(a & ~(uintptr_t)3));
+                    }
+                }
+            }
+        }
+        if (++li == n_it) {
+            li = 0;
+            lt += t_stride;
+            if (lt < n_tiles) load_rows(lt);
+        }
+    };
+    for (int s = 0; s < D - 1; ++s) {
+        if (s < F) issue(s);
+        cp_async_commit();
+    }
+
     float acc[RT];
 #pragma unroll
     for (int i = 0; i < RT; ++i) acc[i] = 0.f;
-    uint4 cur[RT];
-    uint16_t scur[RT];
-    int u = j;
-    if (u < U) {
+    int ct = t_first, ci = 0;  // compute cursor
+    uint32_t shi = 0;          // bit i: row i's scales are the high halves of their aligned words
+    auto scale_parity = [&](int t) {
+        shi = 0;
+        if constexpr (FMT == kFmtInt4) {
+            // unit u's scale index is row_start + u/4; for u = 16 s + j (+8) its parity is that of row_start + j/4
 #pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            cur[i] = ld_stream(wrow[i] + u);
-            scur[i] = __ldg(srow[i] + (u >> 2));
+            for (int i = 0; i < RT; ++i)
+                shi |= (uint32_t)((((uintptr_t)(rows(t, i).s + (j >> 2))) >> 1) & 1) << i;
         }
-    }
-    for (; u < U; u += LPR) {
-        uint4 nxt[RT];
-        uint16_t snxt[RT];
-        const int un = u + LPR;
-        if (un < U) {
+    };
+    if (F > 0) scale_parity(ct);
+#pragma unroll 1
+    for (int f = 0; f < F; ++f) {
+        if (f + D - 1 < F) issue(f + D - 1);
+        cp_async_commit();
+        cp_async_wait<D - 1>();
+        const int slot = f % D;
+        const int ub = 16 * (sb_begin + ci) + j;
 #pragma unroll
-            for (int i = 0; i < RT; ++i) {
-                nxt[i] = ld_stream(wrow[i] + un);
-                snxt[i] = __ldg(srow[i] + (un >> 2));
+        for (int h = 0; h < 2; ++h) {
+            const int u = ub + 8 * h;
+            if (u < U) {
+                if constexpr (FMT == kFmtBf16) {
+                    const float4 *x4 = reinterpret_cast<const float4 *>(xs) + XC * u;
+                    float4 xr[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) xr[k] = x4[k ^ xm];
+#pragma unroll
+                    for (int i = 0; i < RT; ++i) acc[i] += bf16_unit_dot(ring[((slot * RT + i) * 2 + h) * 32 + lane], xr);
+                } else {
+                    const uint4 *x4 = reinterpret_cast<const uint4 *>(xs) + XC * u;
+                    uint4 xr[XC];
+#pragma unroll
+                    for (int k = 0; k < XC; ++k) xr[k] = x4[k ^ xm];
+#pragma unroll
+                    for (int i = 0; i < RT; ++i) {
+                        const int idx = ((slot * RT + i) * 2 + h) * 32 + lane;
+                        if constexpr (FMT == kFmtInt4) {
+                            const uint32_t sw = sring[idx];
+                            const float sc = __uint_as_float(((shi >> i) & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                            acc[i] = fmaf(int4_unit_dot(ring[idx], xr), sc, acc[i]);
+                        } else {
+                            acc[i] += int8_unit_dot(ring[idx], xr);
+                        }
+                    }
+                }
             }
         }
-        const uint4 x0 = xs4[4 * u + 0], x1 = xs4[4 * u + 1];
-        const uint4 x2 = xs4[4 * u + 2], x3 = xs4[4 * u + 3];
-#pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            half2 a = u32_as_h2(0u), b = u32_as_h2(0u);
-            a = int4_word_dot(cur[i].x, x0, a);
-            b = int4_word_dot(cur[i].y, x1, b);
-            a = int4_word_dot(cur[i].z, x2, a);
-            b = int4_word_dot(cur[i].w, x3, b);
-            acc[i] = fmaf(h2_sum(a, b), bf16_bits_to_float(scur[i]), acc[i]);
-        }
-        if (un < U) {
+        if (++ci == n_it) {
+            float out[RT];
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
-                cur[i] = nxt[i];
-                scur[i] = snxt[i];
+                out[i] = slot_sum<kLanesPerRow>(acc[i]);
+                acc[i] = 0.f;
             }
+            epi(ct, out);
+            ci = 0;
+            ct += t_stride;
+            if (ct < n_tiles) scale_parity(ct);
         }
     }
-#pragma unroll
-    for (int i = 0; i < RT; ++i) out[i] = slot_sum<LPR>(acc[i]);
+    cp_async_wait<0>();
 }
 
-// INT8 per-row: unit u covers codes 16u..16u+15; the row scale is applied by the caller.
-template <int LPR, int RT>
-QD_DEV void int8_tile_dots(const uint4 *const (&wrow)[RT], const uint4 *__restrict__ xs4, int U,
-                           int j, float (&out)[RT]) {
-    float acc[RT];
+// Sum of K-part partials for a tile shared by KS warps of one CTA (named barrier
+// per tile slot).  Every warp calls it with its partial; the warp of part 0
+// returns true with the totals in out.  red: KS * 32 * RT floats for this slot.
+template <int RT>
+QD_DEV bool ksplit_reduce(float (&out)[RT], int ks, int kp, int slot_id, float *red, int j, int row_slot,
+                          int lpr) {
+    if (ks == 1) return true;
+    const int lane = threadIdx.x & 31;
+    if (j == 0) {
 #pragma unroll
-    for (int i = 0; i < RT; ++i) acc[i] = 0.f;
-    uint4 cur[RT];
-    int u = j;
-    if (u < U) {
-#pragma unroll
-        for (int i = 0; i < RT; ++i) cur[i] = ld_stream(wrow[i] + u);
+        for (int i = 0; i < RT; ++i) red[(kp * 32 + row_slot) * RT + i] = out[i];
     }
-    for (; u < U; u += LPR) {
-        uint4 nxt[RT];
-        const int un = u + LPR;
-        if (un < U) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) nxt[i] = ld_stream(wrow[i] + un);
-        }
-        const uint4 x0 = xs4[2 * u + 0], x1 = xs4[2 * u + 1];
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + slot_id), "r"(ks * 32) : "memory");
+    bool mine = kp == 0;
+    if (mine) {
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
-            half2 a = u32_as_h2(0u), b = u32_as_h2(0u);
-            a = int8_word_dot(cur[i].x, x0.x, x0.y, a);
-            b = int8_word_dot(cur[i].y, x0.z, x0.w, b);
-            a = int8_word_dot(cur[i].z, x1.x, x1.y, a);
-            b = int8_word_dot(cur[i].w, x1.z, x1.w, b);
-            acc[i] += h2_sum(a, b);
-        }
-        if (un < U) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) cur[i] = nxt[i];
+            float v = 0.f;
+            for (int q = 0; q < ks; ++q) v += red[(q * 32 + row_slot) * RT + i];
+            out[i] = v;
         }
     }
-#pragma unroll
-    for (int i = 0; i < RT; ++i) out[i] = slot_sum<LPR>(acc[i]);
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + slot_id), "r"(ks * 32) : "memory");
+    (void)lane;
+    (void)lpr;
+    return mine;
 }
 
-// bf16 rows against fp32 activations (LM head): unit u covers values 8u..8u+7.
-template <int LPR, int RT>
-QD_DEV void bf16_tile_dots(const uint4 *const (&wrow)[RT], const float4 *__restrict__ xs,
-                           int U, int j, float (&out)[RT]) {
-    float2 acc[RT];
-#pragma unroll
-    for (int i = 0; i < RT; ++i) acc[i] = make_float2(0.f, 0.f);
-    uint4 cur[RT];
-    int u = j;
-    if (u < U) {
-#pragma unroll
-        for (int i = 0; i < RT; ++i) cur[i] = ld_stream(wrow[i] + u);
+// Units per row for a weight format: 16 bytes hold 32 INT4, 16 INT8 or 8 bf16 values.
+QD_HOST_DEV_INLINE int units_per_row(int fmt, int K) {
+    return fmt == kFmtInt4 ? K / 32 : (fmt == kFmtInt8 ? K / 16 : K / 8);
+}
+
+// Slabs (16 units) per row, the last one possibly partial.
+QD_HOST_DEV_INLINE int slabs_per_row(int fmt, int K) { return (units_per_row(fmt, K) + 15) / 16; }
+
+// ---------------------------------------------------------------------------
+// Activation statistics handed from producer to consumer.
+//
+// A kernel that writes the vector the next kernel consumes also reduces, over
+// the elements its CTA wrote, the sum of squares and max |value * gamma_next|
+// (gamma_next: the consumer's RMSNorm gain, or none) into one (ss, mx) pair per
+// CTA in a fixed array of kStatSlots pairs.  Slots of CTAs that a launch does
+// not have stay zero, which is neutral for both the sum and the max.  The
+// consumer then needs a single pass over its input.
+// ---------------------------------------------------------------------------
+// Block-wide reduction of per-thread (ss, mx) into out[2 * blockIdx.x + {0, 1}].
+QD_DEV void write_block_stats(float ss, float mx, float *out, float *red) {
+    ss = warp_sum(ss);
+    mx = warp_max(mx);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if (lane == 0) {
+        red[warp] = ss;
+        red[32 + warp] = mx;
     }
-    for (; u < U; u += LPR) {
-        uint4 nxt[RT];
-        const int un = u + LPR;
-        if (un < U) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) nxt[i] = ld_stream(wrow[i] + un);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < nw; ++w) {
+            a += red[w];
+            b = fmaxf(b, red[32 + w]);
         }
-        const float4 xa = xs[2 * u], xb = xs[2 * u + 1];
-#pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            const uint4 w = cur[i];
-            acc[i] = ffma2(make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u)),
-                           make_float2(xa.x, xa.y), acc[i]);
-            acc[i] = ffma2(make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)),
-                           make_float2(xa.z, xa.w), acc[i]);
-            acc[i] = ffma2(make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u)),
-                           make_float2(xb.x, xb.y), acc[i]);
-            acc[i] = ffma2(make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u)),
-                           make_float2(xb.z, xb.w), acc[i]);
-        }
-        if (un < U) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) cur[i] = nxt[i];
-        }
+        out[2 * blockIdx.x] = a;
+        out[2 * blockIdx.x + 1] = b;
     }
-#pragma unroll
-    for (int i = 0; i < RT; ++i) out[i] = slot_sum<LPR>(acc[i].x + acc[i].y);
 }
 
 // ---------------------------------------------------------------------------
 // Activation staging (block-wide; every thread calls).
 // src: fp32 [K] (src_bf16 == nullptr) or bf16 [K]; gamma: bf16 RMSNorm gain or
-// nullptr (no norm).  K % 4 == 0.
+// nullptr (no norm).  K % 4 == 0.  With stats_in (kStatSlots producer pairs)
+// the sum of squares and max |x*gamma| come from the producer and the input
+// is read once; otherwise they are computed here first.
 //   half_out: fp16 pairs of gamma*x*inv_rms*2^-e, max |value| < 1; returns 2^e.
 //   f32_out:  fp32 gamma*x*inv_rms (no prescale); returns 1.
-// red: shared scratch of 2*32 floats.
+// red: shared scratch of 64 floats.  Loads are issued in batches of up to 8
+// float4 per thread so that a batch costs one round trip.
+//
+// Layout: the output is cut into blocks of one weight unit's activations
+// (blk_bytes = act_blk_bytes<FMT>(); 0: plain) and the 16-byte chunks inside a
+// block are XOR-permuted by the block index, so the lanes of a row slot, which
+// read the same chunk of consecutive blocks, hit distinct bank groups.
+// swz_offset() gives the permuted byte offset.
 // ---------------------------------------------------------------------------
-template <int NT>
 QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__restrict__ src_bf16,
                                const uint16_t *__restrict__ gamma, float eps, int K,
-                               half2 *half_out, float *f32_out, float *red) {
-    const int tid = threadIdx.x;
+                               const float *__restrict__ stats_in, half2 *half_out, float *f32_out,
+                               float *red, int blk_bytes = 0) {
+    constexpr int kBatch = 8;
+    const int tid = threadIdx.x, NT = blockDim.x;
     auto load4 = [&](int i) -> float4 {
         if (src_bf16) {
             const uint2 b = *reinterpret_cast<const uint2 *>(src_bf16 + i);
@@ -237,12 +392,46 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
         return make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
     };
+    const int step = NT * 4;
+    float4 v[kBatch];
+    // first batch of the input, in flight while the statistics are reduced
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+        const int i = tid * 4 + b * step;
+        v[b] = i < K ? load4(i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float ss = 0.f, mx = 0.f;
-    for (int i = tid * 4; i < K; i += NT * 4) {
-        const float4 v = load4(i), g = gain4(i);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x * g.x), fabsf(v.y * g.y)),
-                             fmaxf(fabsf(v.z * g.z), fabsf(v.w * g.w))));
+    if (stats_in) {
+        float2 sp[(kStatSlots + 63) / 64];  // blockDim.x >= 64: every pair in one round trip
+#pragma unroll
+        for (int b = 0; b < (kStatSlots + 63) / 64; ++b) {
+            const int c = tid + b * NT;
+            sp[b] = c < kStatSlots ? __ldcg(reinterpret_cast<const float2 *>(stats_in) + c) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < (kStatSlots + 63) / 64; ++b) {
+            ss += sp[b].x;
+            mx = fmaxf(mx, sp[b].y);
+        }
+    } else {
+        for (int base = 0; base < K; base += kBatch * step) {
+            float4 w[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = base + tid * 4 + b * step;
+                w[b] = base == 0 ? v[b] : (i < K ? load4(i) : make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = base + tid * 4 + b * step;
+                if (i < K) {
+                    const float4 g = gain4(i);
+                    ss += w[b].x * w[b].x + w[b].y * w[b].y + w[b].z * w[b].z + w[b].w * w[b].w;
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(w[b].x * g.x), fabsf(w[b].y * g.y)),
+                                         fmaxf(fabsf(w[b].z * g.z), fabsf(w[b].w * g.w))));
+                }
+            }
+        }
     }
     ss = warp_sum(ss);
     mx = warp_max(mx);
@@ -253,8 +442,8 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
     }
     __syncthreads();
     if (warp == 0) {
-        float a = lane < NT / 32 ? red[lane] : 0.f;
-        float b = lane < NT / 32 ? red[32 + lane] : 0.f;
+        float a = lane < (NT + 31) / 32 ? red[lane] : 0.f;
+        float b = lane < (NT + 31) / 32 ? red[32 + lane] : 0.f;
         a = warp_sum(a);
         b = warp_max(b);
         if (lane == 0) {
@@ -272,14 +461,31 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
         pre = ldexpf(inv, -e);
         post = ldexpf(1.f, e);
     }
-    for (int i = tid * 4; i < K; i += NT * 4) {
-        const float4 v = load4(i), g = gain4(i);
-        if (half_out) {
-            half_out[i / 2] = __floats2half2_rn(g.x * (v.x * pre), g.y * (v.y * pre));
-            half_out[i / 2 + 1] = __floats2half2_rn(g.z * (v.z * pre), g.w * (v.w * pre));
-        } else {
-            *reinterpret_cast<float4 *>(f32_out + i) =
-                make_float4(g.x * (v.x * pre), g.y * (v.y * pre), g.z * (v.z * pre), g.w * (v.w * pre));
+    for (int base = 0; base < K; base += kBatch * step) {
+        if (base > 0) {
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = base + tid * 4 + b * step;
+                if (i < K) v[b] = load4(i);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = base + tid * 4 + b * step;
+            if (i < K) {
+                const float4 g = gain4(i);
+                if (half_out) {
+                    const uint32_t o = swz_offset((uint32_t)i * 2u, blk_bytes);
+                    uint2 hv;
+                    hv.x = h2_as_u32(__floats2half2_rn(g.x * (v[b].x * pre), g.y * (v[b].y * pre)));
+                    hv.y = h2_as_u32(__floats2half2_rn(g.z * (v[b].z * pre), g.w * (v[b].w * pre)));
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<char *>(half_out) + o) = hv;
+                } else {
+                    const uint32_t o = swz_offset((uint32_t)i * 4u, blk_bytes);
+                    *reinterpret_cast<float4 *>(reinterpret_cast<char *>(f32_out) + o) = make_float4(
+                        g.x * (v[b].x * pre), g.y * (v[b].y * pre), g.z * (v[b].z * pre), g.w * (v[b].w * pre));
+                }
+            }
         }
     }
     __syncthreads();

@@ -1,24 +1,44 @@
 // k_attn.cu - split-K grouped-query decode attention over the paged bf16 KV cache.
 //
-// Grid (P, Hkv): CTA (p, g) owns KV head g and a contiguous run of pages of
-// the T = pos + 1 cached tokens, and serves all G = Hq/Hkv query heads of the
-// group from one read of its K/V pages (K and V are read once per KV head,
-// not once per query head).  Pages move HBM -> shared memory with cp.async,
-// double-buffered.  Per page of 16 tokens:
-//   scores:  16 threads per token, each a d/16 slice of q (in registers) . k
-//   softmax: online (running max m, running sum l), base-2 exponentials
-//   values:  each thread owns 2 dims of the output for every head
-// The CTA's unnormalised partial (m, l, o) goes to a scratch slot; the CTA
-// that arrives last for KV head g (arrival counter, no waiting) merges the P
-// partials with the log-sum-exp weights e^(m_p - M) / sum_p e^(m_p - M) l_p.
+// Grid (P, Hkv) in clusters of kCS CTAs along x: CTA (p, g) owns KV head g and
+// a contiguous run of pages of the T = pos + 1 cached tokens, and serves all
+// G = Hq/Hkv query heads of the group from one read of its K/V pages (K and V
+// are read once per KV head, not once per query head).
+//
+// Each warp streams its own pages (the CTA's pages w, w + 8, ...) through a
+// two-slot cp.async ring in shared memory, laid out with an XOR swizzle of the
+// 16-byte chunks so that ldmatrix reads are conflict-free.  Every page except
+// the one being appended is final before the step starts, so the CTA reads the
+// position and the page table and issues its first page copies before waiting
+// for the QKV kernel; the appended row comes from the bf16 copy that kernel
+// writes (kv_new) and replaces its row in shared memory.
+//
+// Per page the scores S = Q K^T (heads x 16 tokens) and the values O += P V
+// are tensor-core contractions (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// Q and P are split into bf16 high and low parts (x = hi + lo, |lo| <= 2^-8 |x|),
+// each multiplied separately, so products carry ~16 significant bits while K
+// and V are the exact bf16 cache values.  Softmax is online, in base 2.
+//
+// Partial results merge in three levels, none of which waits on another CTA
+// outside its cluster: the 8 warps of a CTA in shared memory; the kCS CTAs of a
+// cluster through distributed shared memory; the C = P/kCS cluster results of a
+// KV head by the cluster that arrives last (arrival counter), with the
+// log-sum-exp weights e^(m_c - M) / sum_c e^(m_c - M) l_c.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch_util.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace qd {
 
 namespace {
 
-constexpr int kNT = 256;
+constexpr int kCS = 8;        // CTAs per cluster
+constexpr int kWarps = 8;
+constexpr int kNT = kWarps * 32;
+constexpr int kWRing = 2;     // page slots per warp
 constexpr float kLog2e = 1.4426950408889634f;
 
 QD_DEV void cp_async16(void *smem, const void *gmem) {
@@ -29,216 +49,317 @@ QD_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memor
 template <int N>
 QD_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int G, int D>
-__global__ void __launch_bounds__(kNT) k_attn(AttnArgs a) {
-    constexpr int TPT = 16;           // threads per token (score phase)
-    constexpr int DPT = D / TPT;      // dims per thread (8 or 4)
-    constexpr int NP = D / 2;         // dim pairs
-    constexpr int TG = kNT / NP;      // token groups in the value phase (4 or 8)
-    constexpr int TPG = 16 / TG;      // tokens per group (4 or 2)
-    constexpr int PAGE_ELEMS = kPageTokens * D;
-    constexpr int CHUNKS = PAGE_ELEMS * 2 / 16;  // 16-byte chunks per page (256 or 128)
+QD_DEV void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+QD_DEV void ldsm_x4_t(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
 
-    __shared__ __align__(16) uint16_t ks[2][PAGE_ELEMS];
-    __shared__ __align__(16) uint16_t vs[2][PAGE_ELEMS];
-    __shared__ __align__(16) float s_sc[16][8];
-    __shared__ __align__(16) float s_p[16][8];
-    __shared__ float s_alpha[8], s_m[8], s_l[8];
-    __shared__ __align__(16) float s_o[TG][G][D];
-    __shared__ float s_w[8][256];
+// d[0..3] += A(16x16, rows 0-7 from a0/a2, rows 8-15 zero) * B(16x8)
+QD_DEV void mma_bf16(float (&d)[2], float &z2, float &z3, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(z2), "+f"(z3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// Split two fp32 values into bf16 hi and lo pairs (x = hi + lo up to 2^-16 |x|).
+QD_DEV void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+template <int D>
+constexpr size_t ring_bytes() {
+    return (size_t)kWarps * kWRing * 2 * 16 * D * 2;
+}
+
+template <int G, int D>
+__global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
+    constexpr int CH = D / 8;      // 16-byte chunks per row
+    constexpr int PAGE = 16 * D;   // bf16 elements of one K (or V) page slice
+    constexpr int NKK = D / 16;    // k-steps of S = Q K^T
+    constexpr int NDT = D / 8;     // 8-wide d tiles of O
+
+    extern __shared__ __align__(128) uint16_t smem[];
+    __shared__ float s_cm[8], s_cl[8];
+    __shared__ __align__(16) float s_co[8][D];
+    __shared__ float s_fw[8][32];
     __shared__ int s_last;
 
-    const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
-    const int P = gridDim.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int g = blockIdx.y, p = blockIdx.x, P = gridDim.x;
+    const int rank = (int)cluster.block_rank();
+    const int C = P / kCS, ci = p / kCS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;
 
-    pdl_wait();
+    // ---- before the wait: only data that is final before the step
     const int T = a.T_fixed >= 0 ? a.T_fixed : a.st->pos + 1;
     const int n_pg = (T + kPageTokens - 1) / kPageTokens;
     const int cpp = (n_pg + P - 1) / P;
     const int pg0 = p * cpp;
     const int pg1 = min(n_pg, pg0 + cpp);
+    const int n = pg1 > pg0 ? pg1 - pg0 : 0;
+    const int nw = n > warp ? (n - 1 - warp) / kWarps + 1 : 0;  // this warp's pages
+    uint16_t *wring = smem + (size_t)warp * kWRing * 2 * PAGE;
 
-    const int tok = tid / TPT, part = tid % TPT;
-    const int dp = tid % NP, tg = tid / NP;
-    const float qscale = rsqrtf((float)D) * kLog2e;
-
-    float qr[G][DPT];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < DPT; ++e) qr[h][e] = __ldcg(a.q + (size_t)(g * G + h) * D + part * DPT + e) * qscale;
-
-    float2 o[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) o[h] = make_float2(0.f, 0.f);
-    if (tid < 8) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
-    }
-
-    auto issue_page = [&](int pg, int buf) {
+    auto issue = [&](int i) {
+        const int pg = pg0 + warp + i * kWarps;
         const int phys = __ldg(a.page_table + pg);
         const bool ok = phys >= 0 && phys < a.n_pages;
-        const size_t off = ((size_t)(ok ? phys : 0) * a.Hkv + g) * PAGE_ELEMS;
-        for (int c = tid; c < CHUNKS; c += kNT) {
-            cp_async16(&ks[buf][c * 8], a.k_pool + off + c * 8);
-            cp_async16(&vs[buf][c * 8], a.v_pool + off + c * 8);
+        const size_t off = ((size_t)(ok ? phys : 0) * a.Hkv + g) * PAGE;
+        uint16_t *ks = wring + (i % kWRing) * 2 * PAGE, *vs = ks + PAGE;
+#pragma unroll 4
+        for (int c = lane; c < 16 * CH; c += 32) {
+            const int r = c / CH, ch = c % CH;
+            const int sw = r * D + ((ch ^ (r & 7)) << 3);
+            cp_async16(ks + sw, a.k_pool + off + c * 8);
+            cp_async16(vs + sw, a.v_pool + off + c * 8);
         }
-        if (!ok && tid == 0) atomicCAS(a.err, kErrNone, kErrBadPage);
-        cp_async_commit();
+        if (!ok && lane == 0) atomicCAS(a.err, kErrNone, kErrBadPage);
     };
+#pragma unroll
+    for (int i = 0; i < kWRing; ++i) {
+        if (i < nw) issue(i);
+        cp_async_commit();
+    }
 
+    pdl_wait();
     pdl_launch();
-    if (pg0 < pg1) issue_page(pg0, 0);
-    __syncthreads();
-    for (int pg = pg0; pg < pg1; ++pg) {
-        const int buf = (pg - pg0) & 1;
-        if (pg + 1 < pg1) {
-            issue_page(pg + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
 
-        // ---- scores
-        {
-            float kf[DPT];
-            const uint16_t *kr = &ks[buf][tok * D + part * DPT];
-            if constexpr (DPT == 8) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(kr);
-                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    // ---- query fragments: rows = heads (gq < G), k = d; hi and lo bf16 parts
+    uint32_t qh[NKK][2], ql[NKK][2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kf[2 * e] = __uint_as_float(wv[e] << 16);
-                    kf[2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
-                }
-            } else {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(kr);
-                kf[0] = __uint_as_float(raw.x << 16);
-                kf[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                kf[2] = __uint_as_float(raw.y << 16);
-                kf[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    for (int kk = 0; kk < NKK; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int d0 = kk * 16 + hf * 8 + 2 * tq;
+            float q0 = 0.f, q1 = 0.f;
+            if (gq < G) {
+                const float2 qv = __ldcg(reinterpret_cast<const float2 *>(a.q + (size_t)(g * G + gq) * D + d0));
+                q0 = qv.x;
+                q1 = qv.y;
             }
-            float acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < DPT; ++e) s = fmaf(qr[h][e], kf[e], s);
-                acc[h] = s;
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int off = TPT / 2; off > 0; off >>= 1) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
-            }
-            const bool valid = pg * kPageTokens + tok < T;
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-                if (part == h) s_sc[tok][h] = valid ? acc[h] : -INFINITY;
+            split2(q0, q1, qh[kk][hf], ql[kk][hf]);
         }
-        __syncthreads();
+    const float sscale = rsqrtf((float)D) * kLog2e;
+    // the appended row (position T-1) is taken from kv_new when given
+    const int last_pg = n_pg - 1, new_row = (T - 1) % kPageTokens;
+    const bool patch = a.kv_new != nullptr;
 
-        // ---- online softmax update: 16 lanes per head; whole warps take part in
-        // the shuffles, lanes of heads >= G carry no data.
-        if (tid < ((16 * G + 31) / 32) * 32) {
-            const int tk = tid & 15, h = tid >> 4;
-            const bool act = h < G;
-            const float s = act ? s_sc[tk][h] : -INFINITY;
-            float pm = s;
+    float m = -INFINITY, l = 0.f;
+    float o[NDT][2];
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, off));
-            const float m_old = act ? s_m[h] : 0.f;
-            const float m_new = fmaxf(m_old, pm);
-            const float pr = act ? exp2f(s - m_new) : 0.f;
-            if (act) s_p[tk][h] = pr;
-            float ps = pr;
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-            if (act && tk == 0) {
-                const float alpha = exp2f(m_old - m_new);
-                s_alpha[h] = alpha;
-                s_l[h] = s_l[h] * alpha + ps;
-                s_m[h] = m_new;
-            }
-        }
-        __syncthreads();
+    for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = 0.f;
+    float z2 = 0.f, z3 = 0.f;  // rows 8-15 of the products (always zero)
 
-        // ---- values
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float al = s_alpha[h];
-            o[h].x *= al;
-            o[h].y *= al;
-        }
-#pragma unroll
-        for (int tt = 0; tt < TPG; ++tt) {
-            const int t = tg * TPG + tt;
-            if (pg * kPageTokens + t >= T) break;  // slots past the sequence may hold stale rows
-            const uint32_t vv = *reinterpret_cast<const uint32_t *>(&vs[buf][t * D + 2 * dp]);
-            const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float pr = s_p[t][h];
-                o[h].x = fmaf(pr, v0, o[h].x);
-                o[h].y = fmaf(pr, v1, o[h].y);
+    for (int i = 0; i < nw; ++i) {
+        cp_async_wait<kWRing - 1>();
+        __syncwarp();
+        const int pg = pg0 + warp + i * kWarps;
+        uint16_t *ks = wring + (i % kWRing) * 2 * PAGE, *vs = ks + PAGE;
+        if (pg == last_pg) {
+            const int valid = T - pg * kPageTokens;  // rows [valid, 16) lie past the sequence
+            for (int c = lane; c < (16 - valid) * CH; c += 32) {
+                const int r = valid + c / CH, ch = c % CH;
+                *reinterpret_cast<uint4 *>(vs + r * D + ((ch ^ (r & 7)) << 3)) = make_uint4(0, 0, 0, 0);
             }
+            if (patch && lane < CH) {
+                const int sw = new_row * D + ((lane ^ (new_row & 7)) << 3);
+                *reinterpret_cast<uint4 *>(ks + sw) = __ldcg(reinterpret_cast<const uint4 *>(a.kv_new + (size_t)g * D) + lane);
+                *reinterpret_cast<uint4 *>(vs + sw) =
+                    __ldcg(reinterpret_cast<const uint4 *>(a.kv_new + (size_t)(a.Hkv + g) * D) + lane);
+            }
+            __syncwarp();
         }
-        __syncthreads();
+
+        // ---- S = Q K^T for the 16 tokens of the page (two n-tiles of 8)
+        float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < NKK; ++kk) {
+            const int tok = (lane & 7) + ((lane >> 4) << 3);
+            const int ch = kk * 2 + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(ks + tok * D + ((ch ^ (tok & 7)) << 3), b0, b1, b2, b3);
+            mma_bf16(s0, z2, z3, qh[kk][0], qh[kk][1], b0, b1);
+            mma_bf16(s0, z2, z3, ql[kk][0], ql[kk][1], b0, b1);
+            mma_bf16(s1, z2, z3, qh[kk][0], qh[kk][1], b2, b3);
+            mma_bf16(s1, z2, z3, ql[kk][0], ql[kk][1], b2, b3);
+        }
+        // thread holds head gq, tokens 2tq, 2tq+1 (s0) and 8+2tq, 9+2tq (s1)
+        const int base = pg * kPageTokens;
+        float v0 = base + 2 * tq < T ? s0[0] * sscale : -INFINITY;
+        float v1 = base + 2 * tq + 1 < T ? s0[1] * sscale : -INFINITY;
+        float v2 = base + 8 + 2 * tq < T ? s1[0] * sscale : -INFINITY;
+        float v3 = base + 9 + 2 * tq < T ? s1[1] * sscale : -INFINITY;
+        float mx = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);  // finite: every processed page holds a valid token
+        const float alpha = exp2f(m - m_new);
+        const float p0 = exp2f(v0 - m_new), p1 = exp2f(v1 - m_new);
+        const float p2 = exp2f(v2 - m_new), p3 = exp2f(v3 - m_new);
+        float ps = (p0 + p1) + (p2 + p3);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l = l * alpha + ps;
+        m = m_new;
+#pragma unroll
+        for (int dt = 0; dt < NDT; ++dt) {
+            o[dt][0] *= alpha;
+            o[dt][1] *= alpha;
+        }
+        uint32_t ph0, pl0, ph2, pl2;
+        split2(p0, p1, ph0, pl0);
+        split2(p2, p3, ph2, pl2);
+
+        // ---- O += P V (16 tiles of 8 dims, two per ldmatrix)
+#pragma unroll
+        for (int dp = 0; dp < NDT / 2; ++dp) {
+            const int mi = lane >> 3, r = lane & 7;
+            const int tok = r + (mi & 1) * 8;
+            const int ch = dp * 2 + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vs + tok * D + ((ch ^ (tok & 7)) << 3), b0, b1, b2, b3);
+            mma_bf16(o[2 * dp], z2, z3, ph0, ph2, b0, b1);
+            mma_bf16(o[2 * dp], z2, z3, pl0, pl2, b0, b1);
+            mma_bf16(o[2 * dp + 1], z2, z3, ph0, ph2, b2, b3);
+            mma_bf16(o[2 * dp + 1], z2, z3, pl0, pl2, b2, b3);
+        }
+        __syncwarp();
+        if (i + kWRing < nw) issue(i + kWRing);
+        cp_async_commit();
     }
-
-    // ---- this CTA's partial: sum the token groups
-#pragma unroll
-    for (int h = 0; h < G; ++h) *reinterpret_cast<float2 *>(&s_o[tg][h][2 * dp]) = o[h];
+    cp_async_wait<0>();
     __syncthreads();
-    const size_t slot = (size_t)g * P + p;
+
+    // ---- merge the 8 warps of the CTA (the ring's shared memory is free now)
+    float *wm = reinterpret_cast<float *>(smem);  // [warps][8]
+    float *wl = wm + kWarps * 8;                   // [warps][8]
+    float *wo = wl + kWarps * 8;                   // [warps][8][D]
+    if (tq == 0) {
+        wm[warp * 8 + gq] = nw > 0 ? m : -INFINITY;
+        wl[warp * 8 + gq] = nw > 0 ? l : 0.f;
+    }
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) {
+        wo[(warp * 8 + gq) * D + dt * 8 + 2 * tq] = o[dt][0];
+        wo[(warp * 8 + gq) * D + dt * 8 + 2 * tq + 1] = o[dt][1];
+    }
+    __syncthreads();
     for (int idx = tid; idx < G * D; idx += kNT) {
-        const int h = idx / D, dd = idx % D;
-        float s = 0.f;
+        const int h = idx / D, dim = idx % D;
+        float M = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < TG; ++q) s += s_o[q][h][dd];
-        a.part_o[slot * G * D + idx] = s;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = exp2f(wm[w * 8 + h] - M);
+                num = fmaf(f, wo[(w * 8 + h) * D + dim], num);
+                den = fmaf(f, wl[w * 8 + h], den);
+            }
+        }
+        s_co[h][dim] = num;
+        if (dim == 0) {
+            s_cm[h] = M;
+            s_cl[h] = den;
+        }
     }
-    if (tid < G) {
-        a.part_ml[(slot * G + tid) * 2 + 0] = s_m[tid];
-        a.part_ml[(slot * G + tid) * 2 + 1] = s_l[tid];
+    cluster.sync();
+
+    // ---- merge the kCS CTAs of the cluster through distributed shared memory;
+    // rank r merges an equal slice of the G*D outputs into the cluster's partial
+    {
+        const int per = (G * D + kCS - 1) / kCS;
+        const int lo = rank * per, hi = min(G * D, lo + per);
+        for (int idx = lo + tid; idx < hi; idx += kNT) {
+            const int h = idx / D, dim = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < kCS; ++q) M = fmaxf(M, cluster.map_shared_rank(s_cm, q)[h]);
+            float num = 0.f, den = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int q = 0; q < kCS; ++q) {
+                    const float f = exp2f(cluster.map_shared_rank(s_cm, q)[h] - M);
+                    num = fmaf(f, cluster.map_shared_rank(&s_co[0][0], q)[h * D + dim], num);
+                    den = fmaf(f, cluster.map_shared_rank(s_cl, q)[h], den);
+                }
+            }
+            const size_t slot = (size_t)g * C + ci;
+            a.part_o[(slot * G + h) * D + dim] = num;
+            if (dim == 0) {
+                a.part_ml[(slot * G + h) * 2] = M;
+                a.part_ml[(slot * G + h) * 2 + 1] = den;
+            }
+        }
     }
     __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(a.counter + g, 1) == P - 1;
+    cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+    if (rank != 0) return;
+    if (tid == 0) s_last = atomicAdd(a.counter + g, 1) == C - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
 
-    // ---- combine the P partials of KV head g (P <= 256)
-    for (int idx = tid; idx < G * P; idx += kNT) {
-        const int h = idx / P, q = idx % P;
-        s_w[h][q] = __ldcg(a.part_ml + (((size_t)g * P + q) * G + h) * 2);
+    // ---- last cluster of KV head g: merge the C cluster partials (C <= 32)
+    if (tid < G * C) {
+        const int h = tid / C, c = tid % C;
+        s_fw[h][c] = __ldcg(a.part_ml + (((size_t)g * C + c) * G + h) * 2);
     }
     __syncthreads();
     if (tid < G) {
-        const int h = tid;
         float M = -INFINITY;
-        for (int q = 0; q < P; ++q) M = fmaxf(M, s_w[h][q]);
+        for (int c = 0; c < C; ++c) M = fmaxf(M, s_fw[tid][c]);
         float den = 0.f;
-        for (int q = 0; q < P; ++q) {
-            const float l = __ldcg(a.part_ml + (((size_t)g * P + q) * G + h) * 2 + 1);
-            const float w = s_w[h][q] == -INFINITY ? 0.f : exp2f(s_w[h][q] - M);
-            s_w[h][q] = w;
-            den += w * l;
+        for (int c = 0; c < C; ++c) {
+            const float f = s_fw[tid][c] == -INFINITY ? 0.f : exp2f(s_fw[tid][c] - M);
+            den = fmaf(f, __ldcg(a.part_ml + (((size_t)g * C + c) * G + tid) * 2 + 1), den);
+            s_fw[tid][c] = f;
         }
-        s_alpha[h] = 1.f / den;
+        s_cl[tid] = 1.f / den;
     }
     __syncthreads();
+    float mx = 0.f, ss = 0.f;
     for (int idx = tid; idx < G * D; idx += kNT) {
-        const int h = idx / D;
+        const int h = idx / D, dim = idx % D;
         float num = 0.f;
-        for (int q = 0; q < P; ++q) {
-            const float w = s_w[h][q];
-            if (w != 0.f) num = fmaf(w, __ldcg(a.part_o + ((size_t)g * P + q) * G * D + idx), num);
+        for (int c = 0; c < C; ++c)
+            num = fmaf(s_fw[h][c], __ldcg(a.part_o + (((size_t)g * C + c) * G + h) * D + dim), num);
+        const float v = num * s_cl[h];
+        a.out[(size_t)(g * G) * D + idx] = v;
+        mx = fmaxf(mx, fabsf(v));
+        ss += v * v;
+    }
+    if (a.stats_out) {
+        ss = warp_sum(ss);
+        mx = warp_max(mx);
+        if (lane == 0) {
+            s_co[0][warp] = ss;
+            s_co[1][warp] = mx;
         }
-        a.out[(size_t)(g * G) * D + idx] = num * s_alpha[h];
+        __syncthreads();
+        if (tid == 0) {
+            float a0 = 0.f, b0 = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                a0 += s_co[0][w];
+                b0 = fmaxf(b0, s_co[1][w]);
+            }
+            a.stats_out[2 * g] = a0;
+            a.stats_out[2 * g + 1] = b0;
+        }
     }
     if (tid == 0) a.counter[g] = 0;
 }
@@ -246,22 +367,25 @@ __global__ void __launch_bounds__(kNT) k_attn(AttnArgs a) {
 template <int G>
 cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
     const dim3 grid(a.P, a.Hkv);
-    if (a.d == 128) return launch_k(lc, k_attn<G, 128>, grid, dim3(kNT), 0, a);
-    if (a.d == 64) return launch_k(lc, k_attn<G, 64>, grid, dim3(kNT), 0, a);
+    if (a.d == 128) return launch_kc(lc, k_attn<G, 128>, grid, dim3(kNT), ring_bytes<128>(), kCS, a);
+    if (a.d == 64) return launch_kc(lc, k_attn<G, 64>, grid, dim3(kNT), ring_bytes<64>(), kCS, a);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+int attention_split_multiple() { return kCS; }
+
 int default_splits(int n_sm, int Hkv, int max_pages) {
-    int P = (n_sm + Hkv - 1) / Hkv;
-    if (P > max_pages) P = max_pages;
-    if (P > 256) P = 256;
-    return P < 1 ? 1 : P;
+    (void)max_pages;
+    int C = n_sm / (kCS * Hkv);
+    if (C < 1) C = 1;
+    if (C > 32) C = 32;
+    return C * kCS;
 }
 
 cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a) {
-    if (a.P < 1 || a.P > 256 || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
+    if (a.P < kCS || a.P > 256 || a.P % kCS || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
     switch (a.Hq / a.Hkv) {
         case 1: return launch_g<1>(lc, a);
         case 2: return launch_g<2>(lc, a);

@@ -1,10 +1,10 @@
 // k_gemv.cu - dequant GEMVs of the decode step with fused epilogues:
-//   mode 0: y = W x (+ bias)                     (single-kernel op)
-//   mode 1: y += W x                             (o_proj and down: residual add)
-//   mode 2: y = silu(W_gate n) * (W_up n), n = RMSNorm(x)   (fused gate/up)
-// Every CTA stages the whole input vector (RMSNorm first when a gain is given)
-// into shared memory as prescaled fp16 pairs, then its warps take row tiles
-// round-robin and stream the weight rows with 128-bit loads.
+//   mode 0: y = W x (+ bias)                                  (single-kernel op)
+//   mode 1: y += W x                                          (o_proj and down: residual add)
+//   mode 2: y = silu(W_gate n) * (W_up n), n = RMSNorm(x)      (fused gate/up)
+// One CTA per SM at most.  Warps stream row tiles through lane-private
+// shared-memory rings (gemv_stream); when a tile's K is split over ks warps of
+// the CTA, their partial sums meet in shared memory at the end of the tile.
 #include "gemv.cuh"
 #include "launch_util.cuh"
 
@@ -12,148 +12,132 @@ namespace qd {
 
 namespace {
 
-constexpr int kNT = 256;
-constexpr int kRT = 4;
+constexpr int kMaxWarps = 12;
+constexpr int kD = 3;  // ring depth
 
 QD_DEV float silu(float a) { return a / (1.f + __expf(-a)); }
 
-template <int FMT, int LPR>
-QD_DEV void rows_dot(const void *w, const void *s, int r0, int K, int U, int j, const half2 *xs,
-                     float (&out)[kRT]) {
-    const size_t row_bytes = FMT == kFmtInt4 ? (size_t)K / 2 : (size_t)K;
-    const uint4 *wrow[kRT];
-#pragma unroll
-    for (int i = 0; i < kRT; ++i)
-        wrow[i] = reinterpret_cast<const uint4 *>((const char *)w + (size_t)(r0 + i) * row_bytes);
-    if constexpr (FMT == kFmtInt4) {
-        const uint16_t *srow[kRT];
-#pragma unroll
-        for (int i = 0; i < kRT; ++i) srow[i] = (const uint16_t *)s + (size_t)(r0 + i) * (K / kGroup);
-        int4_tile_dots<LPR, kRT>(wrow, srow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-    } else {
-        int8_tile_dots<LPR, kRT>(wrow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-#pragma unroll
-        for (int i = 0; i < kRT; ++i) out[i] *= __ldg((const float *)s + r0 + i);
-    }
-}
-
-// Mode 2 tiles: a slot owns kRT/2 hidden units and computes both their gate and
-// up rows, so SiLU(gate)*up is formed in registers.
-template <int FMT, int LPR>
-QD_DEV void gateup_dot(const GemvArgs &a, int u0, int U, int j, const half2 *xs, float (&out)[kRT]) {
-    constexpr int H = kRT / 2;
-    const size_t row_bytes = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
-    const uint4 *wrow[kRT];
-#pragma unroll
-    for (int i = 0; i < H; ++i) {
-        wrow[i] = reinterpret_cast<const uint4 *>((const char *)a.w + (size_t)(u0 + i) * row_bytes);
-        wrow[H + i] = reinterpret_cast<const uint4 *>((const char *)a.w2 + (size_t)(u0 + i) * row_bytes);
-    }
-    if constexpr (FMT == kFmtInt4) {
-        const uint16_t *srow[kRT];
-#pragma unroll
-        for (int i = 0; i < H; ++i) {
-            srow[i] = (const uint16_t *)a.s + (size_t)(u0 + i) * (a.K / kGroup);
-            srow[H + i] = (const uint16_t *)a.s2 + (size_t)(u0 + i) * (a.K / kGroup);
-        }
-        int4_tile_dots<LPR, kRT>(wrow, srow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-    } else {
-        int8_tile_dots<LPR, kRT>(wrow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-#pragma unroll
-        for (int i = 0; i < H; ++i) {
-            out[i] *= __ldg((const float *)a.s + u0 + i);
-            out[H + i] *= __ldg((const float *)a.s2 + u0 + i);
-        }
-    }
-}
-
-template <int FMT, int LPR>
-__global__ void __launch_bounds__(kNT) k_gemv(GemvArgs a) {
+template <int FMT, int RT>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
+    constexpr int LPR = kLanesPerRow;
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
     constexpr int S = 32 / LPR;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slot = lane / LPR, j = lane % LPR;
-    const int U = FMT == kFmtInt4 ? a.K / 32 : a.K / 16;
-    const int rows_per_tile = a.mode == 2 ? S * (kRT / 2) : S * kRT;
-    const int n_tiles = a.N / rows_per_tile;
-    const int W = gridDim.x * (kNT / 32);
-    const size_t row_bytes = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
-
-    {   // warm L2 with this warp's first tile (weights only; safe before the wait)
-        const int t = blockIdx.x * (kNT / 32) + warp;
-        if (t < n_tiles) {
-            const char *base = (const char *)a.w + (size_t)t * rows_per_tile * row_bytes;
-            const size_t bytes = (size_t)rows_per_tile * row_bytes;
-            for (size_t off = (size_t)lane * 128; off < bytes; off += 32 * 128) prefetch_l2(base + off);
-            if (a.mode == 2) {
-                const char *b2 = (const char *)a.w2 + (size_t)t * rows_per_tile * row_bytes;
-                for (size_t off = (size_t)lane * 128; off < bytes; off += 32 * 128) prefetch_l2(b2 + off);
-            }
-        }
-    }
-
-    pdl_wait();
+    const int NW = blockDim.x >> 5, ks = a.ks, tpc = NW / ks;
+    const int kp = warp % ks, tslot = warp / ks;
+    const int NP = slabs_per_row(FMT, a.K);
+    const int U = units_per_row(FMT, a.K);
+    const int PP = (NP + ks - 1) / ks;
+    const int p_begin = kp * PP, p_end = min(NP, p_begin + PP);
+    const size_t rb = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
+    const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
-    const float post = stage_activations<kNT>(a.x, nullptr, a.gamma, a.eps, a.K, xs, nullptr, red);
-    pdl_launch();
-
-    for (int t = blockIdx.x * (kNT / 32) + warp; t < n_tiles; t += W) {
-        float out[kRT];
-        if (a.mode == 2) {
-            const int u0 = t * rows_per_tile + slot * (kRT / 2);
-            gateup_dot<FMT, LPR>(a, u0, U, j, xs, out);
-            if (j == 0) {
+    const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * RT * 2 * 32;
+    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * RT * 2 * 32 * 16) +
+                      (size_t)warp * kD * RT * 2 * 32;
+    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<RT, kD>()) +
+                  (size_t)tslot * ks * 32 * RT;
+    float post = 1.f;
+    float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
+    auto sync = [&]() {
+        pdl_wait();
+        post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, xs, nullptr, red,
+                                 act_blk_bytes<FMT>());
+        pdl_launch();
+    };
+    const int t_first = blockIdx.x * tpc + tslot, t_stride = gridDim.x * tpc;
+    if (a.mode == 2) {
+        constexpr int H = RT / 2;
+        const int TU = S * H;
+        auto rows = [&](int t, int i) -> RowRef {
+            const int u = t * TU + slot * H + (i % H);
+            const void *w = i < H ? a.w : a.w2;
+            const void *s = i < H ? a.s : a.s2;
+            return {reinterpret_cast<const uint4 *>((const char *)w + (size_t)u * rb),
+                    (const uint16_t *)s + (size_t)u * G};
+        };
+        auto epi = [&](int t, float(&out)[RT]) {
+            if (!ksplit_reduce<RT>(out, ks, kp, tslot, kred, j, slot, LPR) || j != 0) return;
 #pragma unroll
-                for (int i = 0; i < kRT / 2; ++i)
-                    a.y[u0 + i] = silu(out[i] * post) * (out[kRT / 2 + i] * post);
-            }
-        } else {
-            const int r0 = t * rows_per_tile + slot * kRT;
-            rows_dot<FMT, LPR>(a.w, a.s, r0, a.K, U, j, xs, out);
-            if (j == 0) {
-#pragma unroll
-                for (int i = 0; i < kRT; ++i) {
-                    float v = out[i] * post;
-                    if (a.mode == 1) {
-                        v += a.y[r0 + i];
-                    } else if (a.bias) {
-                        v += bf16_bits_to_float(__ldg(a.bias + r0 + i));
-                    }
-                    a.y[r0 + i] = v;
+            for (int i = 0; i < H; ++i) {
+                const int u = t * TU + slot * H + i;
+                float g = out[i] * post, up = out[H + i] * post;
+                if constexpr (FMT == kFmtInt8) {
+                    g *= __ldg((const float *)a.s + u);
+                    up *= __ldg((const float *)a.s2 + u);
                 }
+                const float yv = silu(g) * up;
+                a.y[u] = yv;
+                st_ss += yv * yv;
+                st_mx = fmaxf(st_mx, fabsf(yv));
             }
-        }
+        };
+        gemv_stream<FMT, RT, kD>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
+                                 sring);
+    } else {
+        const int TR = S * RT;
+        auto rows = [&](int t, int i) -> RowRef {
+            const int r = t * TR + slot * RT + i;
+            return {reinterpret_cast<const uint4 *>((const char *)a.w + (size_t)r * rb),
+                    (const uint16_t *)a.s + (size_t)r * G};
+        };
+        auto epi = [&](int t, float(&out)[RT]) {
+            if (!ksplit_reduce<RT>(out, ks, kp, tslot, kred, j, slot, LPR) || j != 0) return;
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const int r = t * TR + slot * RT + i;
+                float v = out[i] * post;
+                if constexpr (FMT == kFmtInt8) v *= __ldg((const float *)a.s + r);
+                if (a.mode == 1) {
+                    v += a.y[r];
+                } else if (a.bias) {
+                    v += bf16_bits_to_float(__ldg(a.bias + r));
+                }
+                a.y[r] = v;
+                st_ss += v * v;
+                st_mx = fmaxf(st_mx, fabsf(a.stats_gamma ? v * bf16_bits_to_float(__ldg(a.stats_gamma + r)) : v));
+            }
+        };
+        gemv_stream<FMT, RT, kD>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
+                                 sring);
     }
+    if (a.stats_out) write_block_stats(st_ss, st_mx, a.stats_out, red);
 }
 
+template <int FMT, int RT>
+cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
+    constexpr int LPR = kLanesPerRow;
+    const int rows_per_tile = a.mode == 2 ? (32 / LPR) * (RT / 2) : (32 / LPR) * RT;
+    const int tiles = a.N / rows_per_tile;
+    GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots, kMaxWarps);
+    a.ks = ks;
+    const size_t smem = (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)pl.nw * ring_bytes_per_warp<RT, kD>() +
+                        (size_t)pl.nw * 32 * RT * 4;
+    return launch_k(lc, k_gemv<FMT, RT>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
+}
+
+// Shape choices: K split over warps for short row counts (o_proj, down), so
+// that every SM gets enough warps; 4 rows per lane for the wide gate/up.
 template <int FMT>
 cudaError_t launch_fmt(const LaunchCfg &lc, const GemvArgs &a) {
-    const int U = FMT == kFmtInt4 ? a.K / 32 : a.K / 16;
-    const int lpr = pick_lpr(U);
-    if (!lpr) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)a.K * sizeof(__half);
-    const int rows_per_tile = a.mode == 2 ? (32 / lpr) * (kRT / 2) : (32 / lpr) * kRT;
+    const int NP = slabs_per_row(FMT, a.K);
+    if (a.mode == 2) return launch_shape<FMT, 4>(lc, a, 1);
+    int ks = 1;
+    const int rows_per_tile = 4 * 2;  // LPR 8, RT 2
     const int tiles = a.N / rows_per_tile;
-    int grid = (tiles + kNT / 32 - 1) / (kNT / 32);
-    if (grid > 2 * lc.n_sm) grid = 2 * lc.n_sm;
-    switch (lpr) {
-        case 32: return launch_k(lc, k_gemv<FMT, 32>, dim3(grid), dim3(kNT), smem, a);
-        case 16: return launch_k(lc, k_gemv<FMT, 16>, dim3(grid), dim3(kNT), smem, a);
-        case 8: return launch_k(lc, k_gemv<FMT, 8>, dim3(grid), dim3(kNT), smem, a);
-        default: return cudaErrorInvalidValue;
-    }
+    while (ks < 4 && tiles * ks < 8 * lc.n_sm && NP / (ks * 2) >= 1) ks *= 2;
+    return launch_shape<FMT, 2>(lc, a, ks);
 }
 
 }  // namespace
 
 bool gemv_shape_ok(int fmt, int N, int K, int mode) {
     if (fmt == kFmtInt4 ? (K % 256 != 0) : (K % 128 != 0)) return false;
-    const int U = fmt == kFmtInt4 ? K / 32 : K / 16;
-    const int lpr = pick_lpr(U);
-    if (!lpr) return false;
-    const int rows_per_tile = mode == 2 ? (32 / lpr) * (kRT / 2) : (32 / lpr) * kRT;
-    return N > 0 && N % rows_per_tile == 0 && (size_t)K * 2 <= 200 * 1024;
+    const int rows_per_tile = mode == 2 ? 4 * 2 : 4 * 2;
+    return N > 0 && N % rows_per_tile == 0 && (size_t)K * 2 <= 64 * 1024;
 }
 
 cudaError_t launch_gemv(const LaunchCfg &lc, int fmt, const GemvArgs &a) {

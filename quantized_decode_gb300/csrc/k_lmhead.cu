@@ -1,7 +1,7 @@
 // k_lmhead.cu - final RMSNorm -> LM-head GEMV -> logits + fused greedy argmax.
 //
-// Each CTA stages RMSNorm(x) once, streams its rows (bf16, or INT8 with a row
-// scale) and keeps the running (max, lowest index) pair; the CTA's pair goes to
+// Each CTA stages RMSNorm(x) once, streams its row tiles through the register
+// stream (bf16, or INT8 with a row scale) and keeps the running (max, lowest index) pair; the CTA's pair goes to
 // a per-CTA slot, and the CTA that arrives last (arrival counter, no waiting)
 // reduces the slots, writes the token and, inside the decode step, hands it to
 // the next step as input and advances the position.
@@ -14,8 +14,9 @@ namespace qd {
 
 namespace {
 
-constexpr int kNT = 256;
-constexpr int kRT = 4;
+constexpr int kMaxWarps = 8;
+constexpr int kRT = 4;  // rows per lane
+constexpr int kD = 3;   // ring depth
 
 QD_DEV void better(float &v, int &i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) {
@@ -24,65 +25,58 @@ QD_DEV void better(float &v, int &i, float v2, int i2) {
     }
 }
 
-template <int FMT, int LPR>
-__global__ void __launch_bounds__(kNT) k_lm_head(LmHeadArgs a) {
+constexpr int kLPR = kLanesPerRow;
+
+template <int FMT>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
-    __shared__ float s_val[kNT / 32];
-    __shared__ int s_idx[kNT / 32];
+    __shared__ float s_val[kMaxWarps];
+    __shared__ int s_idx[kMaxWarps];
     __shared__ int s_last;
-    constexpr int S = 32 / LPR;
+    constexpr int S = 32 / kLPR;
     constexpr int TR = S * kRT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slot = lane / LPR, j = lane % LPR;
-    const int U = FMT == kFmtBf16 ? a.K / 8 : a.K / 16;
-    const size_t row_bytes = FMT == kFmtBf16 ? (size_t)a.K * 2 : (size_t)a.K;
-    const int n_tiles = a.N / TR;
-    const int W = gridDim.x * (kNT / 32);
-
-    {
-        const int t = blockIdx.x * (kNT / 32) + warp;
-        if (t < n_tiles) {
-            const char *base = (const char *)a.w + (size_t)t * TR * row_bytes;
-            for (size_t off = (size_t)lane * 128; off < TR * row_bytes; off += 32 * 128) prefetch_l2(base + off);
-        }
-    }
-
-    pdl_wait();
-    float post;
-    if constexpr (FMT == kFmtBf16)
-        post = stage_activations<kNT>(a.x, nullptr, a.gamma, a.eps, a.K, nullptr,
-                                      reinterpret_cast<float *>(smem), red);
-    else
-        post = stage_activations<kNT>(a.x, nullptr, a.gamma, a.eps, a.K,
-                                      reinterpret_cast<half2 *>(smem), nullptr, red);
-    pdl_launch();
-
+    const int slot = lane / kLPR, j = lane % kLPR;
+    const int NW = blockDim.x >> 5;
+    const int gw = blockIdx.x * NW + warp, W = gridDim.x * NW;
+    const int NP = slabs_per_row(FMT, a.K);
+    const int U = units_per_row(FMT, a.K);
+    const size_t rb = FMT == kFmtBf16 ? (size_t)a.K * 2 : (size_t)a.K;
+    const size_t xbytes = ((FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2) + 15) & ~(size_t)15;
+    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * kRT * 2 * 32;
+    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * kRT * 2 * 32 * 16) +
+                      (size_t)warp * kD * kRT * 2 * 32;
+    float post = 1.f;
+    auto sync = [&]() {
+        pdl_wait();
+        if constexpr (FMT == kFmtBf16)
+            post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, nullptr,
+                                     reinterpret_cast<float *>(smem), red, act_blk_bytes<FMT>());
+        else
+            post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in,
+                                     reinterpret_cast<half2 *>(smem), nullptr, red, act_blk_bytes<FMT>());
+        pdl_launch();
+    };
+    auto rows = [&](int t, int i) -> RowRef {
+        const int r = t * TR + slot * kRT + i;
+        return {reinterpret_cast<const uint4 *>((const char *)a.w + (size_t)r * rb), nullptr};
+    };
     float best = -INFINITY;
     int bidx = INT_MAX;
-    for (int t = blockIdx.x * (kNT / 32) + warp; t < n_tiles; t += W) {
-        const int r0 = t * TR + slot * kRT;
-        const uint4 *wrow[kRT];
+    auto epi = [&](int t, float(&out)[kRT]) {
+        if (j != 0) return;
 #pragma unroll
-        for (int i = 0; i < kRT; ++i)
-            wrow[i] = reinterpret_cast<const uint4 *>((const char *)a.w + (size_t)(r0 + i) * row_bytes);
-        float out[kRT];
-        if constexpr (FMT == kFmtBf16) {
-            bf16_tile_dots<LPR, kRT>(wrow, reinterpret_cast<const float4 *>(smem), U, j, out);
-        } else {
-            int8_tile_dots<LPR, kRT>(wrow, smem, U, j, out);
-#pragma unroll
-            for (int i = 0; i < kRT; ++i) out[i] *= __ldg(a.scale + r0 + i);
+        for (int i = 0; i < kRT; ++i) {
+            const int r = t * TR + slot * kRT + i;
+            float v = out[i] * post;
+            if constexpr (FMT == kFmtInt8) v *= __ldg(a.scale + r);
+            a.logits[r] = v;
+            better(best, bidx, v, r);
         }
-        if (j == 0) {
-#pragma unroll
-            for (int i = 0; i < kRT; ++i) {
-                const float v = out[i] * post;
-                a.logits[r0 + i] = v;
-                better(best, bidx, v, r0 + i);
-            }
-        }
-    }
+    };
+    gemv_stream<FMT, kRT, kD>(rows, epi, sync, gw, W, a.N / TR, 0, NP, U, j, smem, ring, sring);
+
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -95,7 +89,7 @@ __global__ void __launch_bounds__(kNT) k_lm_head(LmHeadArgs a) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kNT / 32; ++w) better(best, bidx, s_val[w], s_idx[w]);
+        for (int w = 1; w < NW; ++w) better(best, bidx, s_val[w], s_idx[w]);
         a.part_val[blockIdx.x] = best;
         a.part_idx[blockIdx.x] = bidx;
         __threadfence();
@@ -106,7 +100,8 @@ __global__ void __launch_bounds__(kNT) k_lm_head(LmHeadArgs a) {
     __threadfence();
     best = -INFINITY;
     bidx = INT_MAX;
-    for (int c = threadIdx.x; c < (int)gridDim.x; c += kNT) better(best, bidx, __ldcg(a.part_val + c), __ldcg(a.part_idx + c));
+    for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x)
+        better(best, bidx, __ldcg(a.part_val + c), __ldcg(a.part_idx + c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -119,7 +114,7 @@ __global__ void __launch_bounds__(kNT) k_lm_head(LmHeadArgs a) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kNT / 32; ++w) better(best, bidx, s_val[w], s_idx[w]);
+        for (int w = 1; w < NW; ++w) better(best, bidx, s_val[w], s_idx[w]);
         int tok = bidx;
         if (tok < 0 || tok >= a.N) {  // every logit was NaN
             tok = 0;
@@ -137,31 +132,26 @@ __global__ void __launch_bounds__(kNT) k_lm_head(LmHeadArgs a) {
 
 template <int FMT>
 cudaError_t launch_fmt(const LaunchCfg &lc, const LmHeadArgs &a, int grid) {
-    const int U = FMT == kFmtBf16 ? a.K / 8 : a.K / 16;
-    const int lpr = pick_lpr(U);
-    const size_t smem = FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2;
-    switch (lpr) {
-        case 32: return launch_k(lc, k_lm_head<FMT, 32>, dim3(grid), dim3(kNT), smem, a);
-        case 16: return launch_k(lc, k_lm_head<FMT, 16>, dim3(grid), dim3(kNT), smem, a);
-        case 8: return launch_k(lc, k_lm_head<FMT, 8>, dim3(grid), dim3(kNT), smem, a);
-        default: return cudaErrorInvalidValue;
-    }
+    const int tiles = a.N / ((32 / kLPR) * kRT);
+    int nw = (tiles + grid - 1) / grid;
+    nw = nw < 2 ? 2 : (nw > kMaxWarps ? kMaxWarps : nw);  // >= 64 threads (statistics read)
+    const size_t smem = (((FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2) + 15) & ~(size_t)15) +
+                        (size_t)nw * ring_bytes_per_warp<kRT, kD>();
+    return launch_k(lc, k_lm_head<FMT>, dim3(grid), dim3(nw * 32), smem, a);
 }
 
 }  // namespace
 
 bool lm_head_shape_ok(int fmt, int N, int K) {
     if (fmt != kFmtBf16 && fmt != kFmtInt8) return false;
-    if (K % 256 != 0 || (size_t)K * 4 > 200 * 1024) return false;
-    const int U = fmt == kFmtBf16 ? K / 8 : K / 16;
-    const int lpr = pick_lpr(U);
-    return lpr && N > 0 && N % ((32 / lpr) * kRT) == 0;
+    if (K % 256 != 0 || (size_t)K * 4 > 64 * 1024) return false;
+    return N > 0 && N % ((32 / kLPR) * kRT) == 0;
 }
 
 int lm_head_grid(const LaunchCfg &lc, int N) {
     const int tiles = N / kRT;
-    int grid = (tiles + kNT / 32 - 1) / (kNT / 32);
-    if (grid > 2 * lc.n_sm) grid = 2 * lc.n_sm;
+    int grid = (tiles + kMaxWarps - 1) / kMaxWarps;
+    if (grid > lc.n_sm) grid = lc.n_sm;
     return grid < 1 ? 1 : grid;
 }
 

@@ -1,8 +1,8 @@
 // k_qkv.cu - fused RMSNorm -> Q/K/V dequant GEMV (+bias) -> (per-head q/k RMSNorm)
 // -> RoPE -> paged KV append, one kernel per layer of the decode step.
 //
-// Rows of the three projections are numbered q | k | v; warps take tiles of
-// TR rows round-robin.  A tile never straddles a head (TR divides d), so the
+// Rows of the three projections are numbered q | k | v; warps stream tiles of
+// TR rows (gemv_stream).  A tile never straddles a head (TR divides d), so the
 // warp that completes the last tile of a head (per-head arrival counter) runs
 // that head's epilogue: per-head RMSNorm (Qwen3), RoPE with pairs (i, i+d/2)
 // at the current position, then q to the query buffer or k/v rounded to bf16
@@ -14,8 +14,8 @@ namespace qd {
 
 namespace {
 
-constexpr int kNT = 256;
-constexpr int kRT = 4;
+constexpr int kRT = 2;  // rows per lane
+constexpr int kD = 3;   // ring depth
 
 template <int D>
 QD_DEV void head_epilogue(const QkvArgs &a, int head, int pos, int lane) {
@@ -59,109 +59,110 @@ QD_DEV void head_epilogue(const QkvArgs &a, int head, int pos, int lane) {
     }
     uint16_t *dst = (is_k ? a.k_pool : a.v_pool) +
                     (((size_t)phys * a.Hkv + g) * kPageTokens + pos % kPageTokens) * D;
+    uint16_t *cpy = a.kv_new ? a.kv_new + ((size_t)(is_k ? 0 : a.Hkv) + g) * D : nullptr;
 #pragma unroll
-    for (int m = 0; m < M; ++m) dst[lane + 32 * m] = float_to_bf16_bits(v[m]);
+    for (int m = 0; m < M; ++m) {
+        const uint16_t b = float_to_bf16_bits(v[m]);
+        dst[lane + 32 * m] = b;
+        if (cpy) cpy[lane + 32 * m] = b;
+    }
 }
 
-template <int FMT, int LPR, int D>
-__global__ void __launch_bounds__(kNT) k_qkv(QkvArgs a) {
+constexpr int kMaxWarps = 12;
+constexpr int kLPR = kLanesPerRow;
+
+template <int FMT, int DH>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
-    constexpr int S = 32 / LPR;
+    __shared__ int s_pos;
+    constexpr int S = 32 / kLPR;
     constexpr int TR = S * kRT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slot = lane / LPR, j = lane % LPR;
+    const int slot = lane / kLPR, j = lane % kLPR;
+    const int NW = blockDim.x >> 5, ks = a.ks, tpc = NW / ks;
+    const int kp = warp % ks, tslot = warp / ks;
+    const int NP = slabs_per_row(FMT, a.K);
+    const int U = units_per_row(FMT, a.K);
+    const int PP = (NP + ks - 1) / ks;
+    const int p_begin = kp * PP, p_end = min(NP, p_begin + PP);
     const int rows_total = a.rows_q + 2 * a.rows_kv;
-    const int n_tiles = rows_total / TR;
-    const int W = gridDim.x * (kNT / 32);
-    const int U = FMT == kFmtInt4 ? a.K / 32 : a.K / 16;
-    const size_t row_bytes = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
-
-    // Weights do not depend on earlier kernels: warm L2 with this warp's first tile.
-    {
-        const int t = blockIdx.x * (kNT / 32) + warp;
-        if (t < n_tiles) {
-            const int r = t * TR;
-            const int seg = r < a.rows_q ? 0 : (r < a.rows_q + a.rows_kv ? 1 : 2);
-            const int local = r - (seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv));
-            const char *base = (const char *)a.w[seg] + (size_t)local * row_bytes;
-            for (size_t off = (size_t)lane * 128; off < TR * row_bytes; off += 32 * 128)
-                prefetch_l2(base + off);
-        }
-    }
-
-    pdl_wait();
-    const int pos = a.st->pos;
-    const int token = a.st->token;
-    const uint16_t *erow = a.embed ? a.embed + (size_t)token * a.K : nullptr;
-    if (erow && blockIdx.x == 0) {
-        for (int i = threadIdx.x; i < a.K; i += kNT) a.x_init[i] = bf16_bits_to_float(erow[i]);
-    }
+    const size_t rb = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
+    const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
-    const float post = stage_activations<kNT>(a.x, erow, a.gamma, a.eps, a.K, xs, nullptr, red);
-    pdl_launch();
+    const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * kRT * 2 * 32;
+    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * kRT * 2 * 32 * 16) +
+                      (size_t)warp * kD * kRT * 2 * 32;
+    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<kRT, kD>()) +
+                  (size_t)tslot * ks * 32 * kRT;
+    float post = 1.f;
 
-    for (int t = blockIdx.x * (kNT / 32) + warp; t < n_tiles; t += W) {
+    auto segment = [&](int r, int &seg, int &local) {
+        seg = r < a.rows_q ? 0 : (r < a.rows_q + a.rows_kv ? 1 : 2);
+        local = r - (seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv));
+    };
+    auto rows = [&](int t, int i) -> RowRef {
+        int seg, local;
+        segment(t * TR, seg, local);
+        local += slot * kRT + i;
+        return {reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)local * rb),
+                (const uint16_t *)a.s[seg] + (size_t)local * G};
+    };
+    auto sync = [&]() {
+        pdl_wait();
+        const int token = a.st->token;
+        if (threadIdx.x == 0) s_pos = a.st->pos;
+        const uint16_t *erow = a.embed ? a.embed + (size_t)token * a.K : nullptr;
+        if (erow && blockIdx.x == 0)
+            for (int i = threadIdx.x; i < a.K; i += blockDim.x) a.x_init[i] = bf16_bits_to_float(erow[i]);
+        post = stage_activations(a.x, erow, a.gamma, a.eps, a.K, erow ? nullptr : a.stats_in, xs, nullptr, red,
+                                 act_blk_bytes<FMT>());
+        pdl_launch();
+    };
+    auto epi = [&](int t, float(&out)[kRT]) {
+        if (!ksplit_reduce<kRT>(out, ks, kp, tslot, kred, j, slot, kLPR)) return;
         const int tile_r = t * TR;
-        const int r0 = tile_r + slot * kRT;
-        const int seg = tile_r < a.rows_q ? 0 : (tile_r < a.rows_q + a.rows_kv ? 1 : 2);
-        const int seg0 = seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv);
-        const int local = r0 - seg0;
-        const uint4 *wrow[kRT];
-        float out[kRT];
-        if constexpr (FMT == kFmtInt4) {
-            const uint16_t *srow[kRT];
-#pragma unroll
-            for (int i = 0; i < kRT; ++i) {
-                wrow[i] = reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)(local + i) * row_bytes);
-                srow[i] = (const uint16_t *)a.s[seg] + (size_t)(local + i) * (a.K / kGroup);
-            }
-            int4_tile_dots<LPR, kRT>(wrow, srow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-        } else {
-#pragma unroll
-            for (int i = 0; i < kRT; ++i)
-                wrow[i] = reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)(local + i) * row_bytes);
-            int8_tile_dots<LPR, kRT>(wrow, reinterpret_cast<const uint4 *>(xs), U, j, out);
-#pragma unroll
-            for (int i = 0; i < kRT; ++i) out[i] *= __ldg((const float *)a.s[seg] + local + i);
-        }
+        int seg, local;
+        segment(tile_r, seg, local);
+        local += slot * kRT;
         if (j == 0) {
 #pragma unroll
             for (int i = 0; i < kRT; ++i) {
                 float v = out[i] * post;
+                if constexpr (FMT == kFmtInt8) v *= __ldg((const float *)a.s[seg] + local + i);
                 if (a.b[seg]) v += bf16_bits_to_float(__ldg(a.b[seg] + local + i));
-                a.raw[r0 + i] = v;
+                a.raw[tile_r + slot * kRT + i] = v;
             }
         }
         __threadfence();
         __syncwarp();
-        const int head = tile_r / D;
+        const int head = tile_r / DH;
         int last = 0;
-        if (lane == 0) last = (atomicAdd(&a.head_cnt[head], TR) + TR == D);
+        if (lane == 0) last = (atomicAdd(&a.head_cnt[head], TR) + TR == DH);
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence();
-            head_epilogue<D>(a, head, pos, lane);
+            head_epilogue<DH>(a, head, s_pos, lane);
             if (lane == 0) a.head_cnt[head] = 0;
         }
-    }
+    };
+    gemv_stream<FMT, kRT, kD>(rows, epi, sync, blockIdx.x * tpc + tslot, gridDim.x * tpc, rows_total / TR,
+                               p_begin, p_end, U, j, xs, ring, sring);
 }
 
-template <int FMT, int D>
-cudaError_t launch_qkv_d(const LaunchCfg &lc, const QkvArgs &a) {
-    const int U = FMT == kFmtInt4 ? a.K / 32 : a.K / 16;
-    const int lpr = pick_lpr(U);
-    const size_t smem = (size_t)a.K * sizeof(__half);
+template <int FMT, int DH>
+cudaError_t launch_qkv_d(const LaunchCfg &lc, QkvArgs a) {
     const int rows = a.rows_q + 2 * a.rows_kv;
-    const int tiles = rows / ((32 / lpr) * kRT);
-    int grid = (tiles + kNT / 32 - 1) / (kNT / 32);
-    if (grid > 2 * lc.n_sm) grid = 2 * lc.n_sm;
-    switch (lpr) {
-        case 32: return launch_k(lc, k_qkv<FMT, 32, D>, dim3(grid), dim3(kNT), smem, a);
-        case 16: return launch_k(lc, k_qkv<FMT, 16, D>, dim3(grid), dim3(kNT), smem, a);
-        case 8: return launch_k(lc, k_qkv<FMT, 8, D>, dim3(grid), dim3(kNT), smem, a);
-        default: return cudaErrorInvalidValue;
-    }
+    const int tiles = rows / ((32 / kLPR) * kRT);
+    const int NP = slabs_per_row(FMT, a.K);
+    int ks = 1;
+    while (ks < 4 && tiles * ks < 8 * lc.n_sm && NP / (ks * 2) >= 1) ks *= 2;
+    GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm, kMaxWarps);
+    a.ks = ks;
+    const size_t smem = (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)pl.nw * ring_bytes_per_warp<kRT, kD>() +
+                        (size_t)pl.nw * 32 * kRT * 4;
+    return launch_k(lc, k_qkv<FMT, DH>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
 }
 
 }  // namespace

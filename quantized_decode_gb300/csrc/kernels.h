@@ -9,6 +9,7 @@ namespace qd {
 constexpr int kPageTokens = 16;   // KV tokens per page (16-token pages, bf16)
 constexpr int kGroup = 128;       // INT4 quantization group along K
 constexpr int kMaxGqa = 8;        // query heads per KV head supported by the attention kernel
+constexpr int kStatSlots = 256;   // (sum of squares, max) pairs per producer: one per CTA, >= grid
 
 // Device-side error word (sticky until the host clears it).
 enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3 };
@@ -54,6 +55,9 @@ struct QkvArgs {
     int n_pages;
     const float2 *rope_cs;  // [max_context][d/2] (cos, sin)
     DevState *st;
+    uint16_t *kv_new;       // [2][Hkv][d] bf16 copy of the appended K and V rows
+    const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
+    int ks;                 // set by the launcher: warps per tile along K
 };
 
 // y = W x with a fused epilogue: mode 0 stores (plus optional bias), mode 1
@@ -68,6 +72,10 @@ struct GemvArgs {
     const uint16_t *gamma;  // RMSNorm gain applied to x first, or null
     float eps;
     float *y;               // output [N]
+    const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
+    float *stats_out;       // this kernel's (ss, mx) pairs for y, or null
+    const uint16_t *stats_gamma;  // gain of y's consumer norm for mx (null: none)
+    int ks;                 // set by the launcher: warps per tile along K
 };
 
 // Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
@@ -88,6 +96,7 @@ struct LmHeadArgs {
     int *token_out;         // where the argmax goes (state or user buffer)
     DevState *st;           // non-null: last_token/token written, pos advanced
     int advance;
+    const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
 };
 
 // Split-K decode attention over the paged cache with the LSE combine.
@@ -104,6 +113,8 @@ struct AttnArgs {
     int *counter;                      // [Hkv] self-resetting
     float *out;                        // [Hq][d]
     int *err;
+    const uint16_t *kv_new;            // [2][Hkv][d] appended K/V row, or null (all rows in pages)
+    float *stats_out;                  // (ss, mx) of out per KV head, or null
 };
 
 // Each launcher returns the launch's cudaError_t.
@@ -115,6 +126,7 @@ cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a);
 // Grid sizes and shape checks used by the engine when it plans buffers.
 int lm_head_grid(const LaunchCfg &lc, int N);
 int default_splits(int n_sm, int Hkv, int max_pages);
+int attention_split_multiple();  // split counts are multiples of the attention cluster size
 bool gemv_shape_ok(int fmt, int N, int K, int mode);
 bool qkv_shape_ok(int fmt, int rows_q, int rows_kv, int K, int d);
 bool lm_head_shape_ok(int fmt, int N, int K);

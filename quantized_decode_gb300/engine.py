@@ -172,6 +172,9 @@ class Engine:
                 "llm_profile_step")
         return out[:n.value]
 
+    def set_pdl(self, on):
+        L.check(self.lib.llm_set_pdl(self.h, int(bool(on))), "llm_set_pdl")
+
     def set_graph_mode(self, on):
         L.check(self.lib.llm_set_graph_mode(self.h, int(bool(on))), "llm_set_graph_mode")
 
