@@ -165,13 +165,15 @@ int llm_reset(llm_t *h);
  * next input.  Errors: LLM_ERR_ARG, LLM_ERR_CUDA.                           */
 int llm_truncate(llm_t *h, int32_t seq_len);
 
-/* Per-kernel timing of one decode step ("How To Construct Your Personal LLM
+/* Per-region timing of one decode step ("How To Construct Your Personal LLM
  * Runtime From Scratch", §6: the per-token ITL breakdown by region).  Runs
- * one step with the kernels launched one by one and a CUDA event between
- * neighbours (no launch overlap), advancing the sequence like a greedy step,
- * and writes the duration in ms of kernel i to kernel_ms[i] (HOST, capacity
- * cap).  Order: for each layer {qkv, attention, o_proj, gate_up, down}, then
- * lm_head; *n_kernels = 5 * n_layers + 1.  Blocks until done.               */
+ * one step, advancing the sequence like a greedy step, and writes the
+ * duration in ms of region i to kernel_ms[i] (HOST, capacity cap).  Order:
+ * for each layer {qkv, attention, o_proj, gate_up, down}, then lm_head;
+ * *n_kernels = 5 * n_layers + 1.  With the persistent step kernel a region is
+ * the time between phase starts as seen by CTA 0 (device clock, waits for
+ * other CTAs included); with the kernel chain it is one kernel, launched one
+ * by one with a CUDA event between neighbours.  Blocks until done.          */
 int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels);
 
 /* Free everything the handle owns (not the caller's weights).  NULL is a no-op. */
@@ -192,6 +194,14 @@ int llm_debug_kv(llm_t *h, void **k_pool, void **v_pool, int32_t **page_table,
  * graph (default), 0 = launch the same kernels one by one (eager), for timing
  * the difference.                                                           */
 int llm_set_graph_mode(llm_t *h, int32_t use_graph);
+
+/* 1: the whole step is one persistent kernel, one CTA per SM, weights
+ * streamed by TMA through a shared-memory ring, the phases of a layer ordered
+ * by device counters (available where the model's shapes fit it).  0
+ * (default): the step is a chain of 5 * n_layers + 1 kernels.  Re-captures the graph; waits for enqueued work
+ * first.  Errors: LLM_ERR_ARG (null handle, or 1 for a model outside the
+ * persistent kernel's shapes), LLM_ERR_CUDA.                                */
+int llm_set_persistent(llm_t *h, int32_t on);
 
 /* 1: consecutive kernels of the step are launched with programmatic dependent
  * launch (a kernel's CTAs may start before the previous kernel ends and wait

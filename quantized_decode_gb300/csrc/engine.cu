@@ -3,12 +3,15 @@
 //
 // One decode step = for each layer [QKV+RoPE+append] -> [split-K attention +
 // combine] -> [o_proj + residual] -> [RMSNorm + gate/up + SiLU*mul] ->
-// [down + residual], then [final RMSNorm + LM head + argmax]: 5L + 1 kernels,
-// chained with programmatic dependent launch and captured once into a CUDA
-// graph.  Position and input token live in device memory (DevState), so the
-// same graph replays at every position ("How To Construct Your Personal LLM
-// Runtime From Scratch", §6); the page for position pos is page_table[pos/16],
-// read on the device, so no host-side branch on page boundaries is needed.
+// [down + residual], then [final RMSNorm + LM head + argmax].  By default the
+// step is a chain of 5L + 1 kernels; on request (llm_set_persistent) it is one
+// persistent kernel (k_step.cu: one CTA per SM, weights streamed by TMA
+// through a shared-memory ring, phases ordered by device counters).  Either
+// form is captured once into a CUDA graph.  Position and input token live in
+// device memory (DevState), so the same graph replays at every position ("How
+// To Construct Your Personal LLM Runtime From Scratch", §6); the page for
+// position pos is page_table[pos/16], read on the device, so no host-side
+// branch on page boundaries is needed.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -17,6 +20,7 @@
 
 #include "../../include/llm.h"
 #include "kernels.h"
+#include "step.h"
 
 using namespace qd;
 
@@ -42,6 +46,15 @@ struct llm_t {
     float *stats = nullptr;     // 4 x kStatSlots (ss, mx) pairs: attention, o_proj, gate/up, down outputs
     uint16_t *kv_new = nullptr; // [2][Hkv][d] appended rows of the current step
     int P = 1, lm_grid = 1;
+
+    // persistent whole-step kernel
+    bool step_ok = false;       // the model fits the persistent kernel
+    bool persistent = false;    // the step runs as the persistent kernel
+    StepParams sp{};
+    StepLaunch sl{};
+    StepLayer *d_layers = nullptr;
+    int *step_sync = nullptr;
+    unsigned long long *prof = nullptr;
 
     int32_t *pinned = nullptr;  // host staging: [0] forced token, [2..3] last_token, err
     cudaGraph_t graph = nullptr;
@@ -72,7 +85,8 @@ void free_all(llm_t *h) {
     if (h->graph) cudaGraphDestroy(h->graph);
     void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->rope_cs, h->st, h->x, h->raw, h->q,
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
-                    h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new};
+                    h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
+                    h->d_layers, h->step_sync, h->prof};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -123,6 +137,7 @@ int validate(const llm_config *c, const llm_weights *w) {
 // Enqueue one whole decode step (5L + 1 kernels).  With `ev`, event k is
 // recorded before kernel k and event 5L+1 after the last one.
 cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
+    if (h->persistent && !ev) return launch_step(h->sl, h->sp, h->stream);
     const llm_config &c = h->cfg;
     const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d;
     cudaError_t e;
@@ -220,6 +235,92 @@ int run_step(llm_t *h) {
     return e == cudaSuccess ? LLM_OK : LLM_ERR_CUDA;
 }
 
+// Fill the persistent kernel's parameters; leaves h->step_ok false (kernel
+// chain) when the shapes are outside what it supports.
+int plan_step(llm_t *h, int n_sm) {
+    const llm_config &c = h->cfg;
+    StepParams &p = h->sp;
+    p = StepParams{};
+    p.L = c.n_layers;
+    p.h = c.hidden;
+    p.Hq = c.n_q_heads;
+    p.Hkv = c.n_kv_heads;
+    p.d = c.head_dim;
+    p.F = c.mlp;
+    p.V = c.vocab;
+    p.eps = c.rms_eps;
+    p.embed = (const uint16_t *)h->w.embed;
+    p.final_norm = (const uint16_t *)h->w.final_norm;
+    const bool int8_head = h->fmt == kFmtInt8 && !c.tied_lm_head;
+    p.lm_w = c.tied_lm_head ? h->w.embed : h->w.lm_head;
+    p.lm_scale = int8_head ? (const float *)h->w.lm_scale : nullptr;
+    p.page_table = h->page_table;
+    p.n_pages = h->n_pages;
+    p.rope_cs = h->rope_cs;
+    p.k_pool = h->k_pool;
+    p.v_pool = h->v_pool;
+    p.st = h->st;
+    p.x = h->x;
+    p.raw = h->raw;
+    p.q = h->q;
+    p.attn = h->attn;
+    p.u = h->u;
+    p.logits = h->logits;
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.lm_val = h->lm_part_val;
+    p.lm_idx = h->lm_part_idx;
+    p.wait_ns = 1000000000ull;  // 1 s: a step takes about a millisecond
+    p.inflight = 4;             // 64 KB a CTA: covers the HBM latency at the per-SM bandwidth
+    int max_smem = 0;
+    if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    h->step_ok = step_plan(p, h->fmt, int8_head ? kFmtInt8 : kFmtBf16, n_sm, max_smem, h->sl);
+    if (!h->step_ok) return LLM_OK;
+    int per_sm = 0;
+    if (step_occupancy(h->sl, &per_sm) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        h->step_ok = false;
+        return LLM_OK;
+    }
+    std::vector<StepLayer> ly(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const llm_layer_weights &L = h->layers[l];
+        StepLayer &S = ly[l];
+        S.w[0] = L.wq; S.w[1] = L.wk; S.w[2] = L.wv;
+        S.s[0] = L.sq; S.s[1] = L.sk; S.s[2] = L.sv;
+        if (c.qkv_bias) {
+            S.b[0] = (const uint16_t *)L.bq;
+            S.b[1] = (const uint16_t *)L.bk;
+            S.b[2] = (const uint16_t *)L.bv;
+        }
+        S.wo = L.wo; S.so = L.so; S.wg = L.wg; S.sg = L.sg; S.wu = L.wu; S.su = L.su; S.wd = L.wd; S.sd = L.sd;
+        S.attn_norm = (const uint16_t *)L.attn_norm;
+        S.mlp_norm = (const uint16_t *)L.mlp_norm;
+        if (c.qk_norm) {
+            S.q_norm = (const uint16_t *)L.q_norm;
+            S.k_norm = (const uint16_t *)L.k_norm;
+        }
+    }
+    const size_t n_sync = (size_t)c.n_layers * kSyncStride + 1;
+    const size_t kv_rows = (size_t)c.n_layers * h->n_pages * c.n_kv_heads * kPageTokens;
+    if (dalloc(&h->d_layers, ly.size()) != cudaSuccess || dalloc(&h->step_sync, n_sync) != cudaSuccess ||
+        dalloc(&h->prof, (size_t)5 * c.n_layers + 2) != cudaSuccess ||
+        cudaMemcpyAsync(h->d_layers, ly.data(), ly.size() * sizeof(StepLayer), cudaMemcpyHostToDevice,
+                        h->stream) != cudaSuccess ||
+        cudaMemsetAsync(h->step_sync, 0, n_sync * sizeof(int), h->stream) != cudaSuccess ||
+        cudaStreamSynchronize(h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    p.layers = h->d_layers;
+    p.sync = h->step_sync;
+    if (step_encode_kv_maps(p, kv_rows) != cudaSuccess) {
+        h->step_ok = false;
+        return LLM_OK;
+    }
+    h->persistent = false;  // opt-in (llm_set_persistent) until it outpaces the kernel chain
+    return LLM_OK;
+}
+
 int fetch_token(llm_t *h, int32_t *out) {
     if (cudaMemcpyAsync(h->pinned + 2, &h->st->last_token, 2 * sizeof(int32_t),
                         cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
@@ -287,6 +388,8 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     h->layer_kv_elems = (size_t)h->n_pages * c.n_kv_heads * kPageTokens * d;
     h->P = default_splits(n_sm, c.n_kv_heads, h->n_pages);
     h->lm_grid = lm_head_grid(h->lc, c.vocab);
+    const int P_alloc = h->P > n_sm / c.n_kv_heads ? h->P : n_sm / c.n_kv_heads + 1;
+    const int lm_alloc = h->lm_grid > n_sm ? h->lm_grid : n_sm;
     const size_t kv_elems = h->layer_kv_elems * c.n_layers;
     const int rows_qkv = (c.n_q_heads + 2 * c.n_kv_heads) * d;
     const int heads_qkv = c.n_q_heads + 2 * c.n_kv_heads;
@@ -298,10 +401,10 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
               dalloc(&h->attn, c.n_q_heads * d) == cudaSuccess && dalloc(&h->u, c.mlp) == cudaSuccess &&
               dalloc(&h->logits, c.vocab) == cudaSuccess && dalloc(&h->head_cnt, heads_qkv) == cudaSuccess &&
               dalloc(&h->attn_cnt, c.n_kv_heads) == cudaSuccess && dalloc(&h->lm_counter, 1) == cudaSuccess &&
-              dalloc(&h->lm_part_idx, h->lm_grid) == cudaSuccess &&
-              dalloc(&h->lm_part_val, h->lm_grid) == cudaSuccess &&
-              dalloc(&h->part_o, (size_t)c.n_kv_heads * h->P * G * d) == cudaSuccess &&
-              dalloc(&h->part_ml, (size_t)c.n_kv_heads * h->P * G * 2) == cudaSuccess &&
+              dalloc(&h->lm_part_idx, lm_alloc) == cudaSuccess &&
+              dalloc(&h->lm_part_val, lm_alloc) == cudaSuccess &&
+              dalloc(&h->part_o, (size_t)c.n_kv_heads * P_alloc * G * d) == cudaSuccess &&
+              dalloc(&h->part_ml, (size_t)c.n_kv_heads * P_alloc * G * 2) == cudaSuccess &&
               dalloc(&h->stats, (size_t)8 * kStatSlots) == cudaSuccess &&
               dalloc(&h->kv_new, (size_t)2 * c.n_kv_heads * d) == cudaSuccess &&
               cudaMallocHost(reinterpret_cast<void **>(&h->pinned), 8 * sizeof(int32_t)) == cudaSuccess;
@@ -335,8 +438,17 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
          cudaStreamSynchronize(h->stream) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
 
-    // Capture the whole step once.
-    if (capture(h) != LLM_OK) return fail(LLM_ERR_CUDA);
+    if (plan_step(h, n_sm) != LLM_OK) return fail(LLM_ERR_CUDA);
+
+    // Capture the whole step once (the kernel chain if the persistent kernel
+    // cannot be captured here).
+    if (capture(h) != LLM_OK) {
+        cudaGetLastError();
+        if (!h->persistent) return fail(LLM_ERR_CUDA);
+        h->persistent = false;
+        h->step_ok = false;
+        if (capture(h) != LLM_OK) return fail(LLM_ERR_CUDA);
+    }
     *out = h;
     return LLM_OK;
 }
@@ -352,6 +464,14 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph) {
     if (!h) return LLM_ERR_ARG;
     h->use_graph = use_graph != 0;
     return LLM_OK;
+}
+
+int llm_set_persistent(llm_t *h, int32_t on) {
+    if (!h) return LLM_ERR_ARG;
+    if (on && !h->step_ok) return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->persistent = on != 0;
+    return capture(h);
 }
 
 int llm_set_pdl(llm_t *h, int32_t use_pdl) {
@@ -444,6 +564,10 @@ int llm_reset(llm_t *h) {
     if (!h) return LLM_ERR_ARG;
     k_set_state<<<1, 1, 0, h->stream>>>(h->st, -1, 0, 1);
     if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
+    // a step that failed part-way leaves its counters raised
+    if (h->step_sync && cudaMemsetAsync(h->step_sync, 0, ((size_t)h->cfg.n_layers * kSyncStride + 1) * sizeof(int),
+                                        h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->seq_len = 0;
     h->have_token = false;
@@ -466,6 +590,24 @@ int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels
     if (cap < n) return LLM_ERR_ARG;
     if (!h->have_token) return LLM_ERR_STATE;
     if (h->seq_len >= h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    if (h->persistent) {
+        StepParams p = h->sp;
+        p.prof = h->prof;
+        std::vector<unsigned long long> ts((size_t)n + 1);
+        if (cudaMemsetAsync(h->prof, 0, ts.size() * sizeof(unsigned long long), h->stream) != cudaSuccess ||
+            launch_step(h->sl, p, h->stream) != cudaSuccess ||
+            cudaMemcpyAsync(ts.data(), h->prof, ts.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost,
+                            h->stream) != cudaSuccess ||
+            cudaStreamSynchronize(h->stream) != cudaSuccess)
+            return LLM_ERR_CUDA;
+        int rc = fetch_token(h, nullptr);
+        if (rc != LLM_OK) return rc;
+        for (int i = 0; i < n; ++i)
+            kernel_ms[i] = ts[i + 1] >= ts[i] ? (float)((double)(ts[i + 1] - ts[i]) * 1e-6) : 0.f;
+        h->seq_len += 1;
+        h->stepped = true;
+        return LLM_OK;
+    }
     std::vector<cudaEvent_t> ev(n + 1, nullptr);
     int rc = LLM_OK;
     for (auto &e : ev)

@@ -1,0 +1,1532 @@
+// k_step.cu - the whole decode step as one persistent kernel, one CTA per SM.
+//
+// Roles.  Warp NCW (first of the last warpgroup) is the producer: its lane 0 walks the step's
+// schedule and, for every ring item, waits until the slot is free and issues
+// TMA copies of what this CTA consumes next -- rows of a weight matrix with
+// their INT4 scales (cp.async.bulk), or K/V pages of the paged cache as
+// 128-byte-swizzled 16-row boxes (cp.async.bulk.tensor) -- completing on the
+// slot's `full` mbarrier.  It never waits for activations: weights, scales and
+// every cached K/V row except the one appended in this step are final before
+// the step starts, so the stream runs ahead across phase and layer boundaries,
+// limited only by the ring.  Warps 0..NCW-1 consume: per phase they wait for
+// the phase's input (a counter that other CTAs raise), stage the activations
+// into registers, take the phase's items in order (wait `full`, compute,
+// arrive on `empty`) and run the phase's epilogue.
+//
+// Phases per layer (each CTA owns a contiguous share of every phase's rows):
+//   QKV  RMSNorm -> Q/K/V GEMV (+bias) -> raw rows; the CTA that completes a
+//        head (per-head arrival count) applies the Qwen3 q/k norm and RoPE and
+//        writes q, or K/V rounded to bf16 into the page for position pos.
+//   ATTN CTA (g, p) of Hkv x P: split p of the cached tokens of KV head g for
+//        its G query heads (mma.sync bf16, q and p split into hi/lo parts),
+//        then the P CTAs of head g combine the P partials, each one slice of
+//        the G*d outputs (log-sum-exp weights).
+//   O    o_proj GEMV + residual.
+//   GU   RMSNorm -> gate/up GEMV -> SiLU(gate) * up.
+//   DOWN down GEMV + residual.
+// and LM: final RMSNorm -> LM head GEMV -> logits + argmax; the CTA that
+// arrives last reduces the per-CTA maxima, stores the token, advances the
+// position and zeroes the step counters for the next step.
+//
+// Dot products: a lane holds the activations of up to MU 16-byte weight units
+// (fp16, scaled per unit by a power of two so |x| < 1) and, for each row
+// assigned to its warp, multiplies them with the row's units read from the
+// ring (INT4/INT8 codes turned into exact fp16 with lop3/prmt); partial sums
+// of 8 rows are combined across the warp with one transposing shuffle tree
+// and added into the CTA's per-row results in shared memory.
+//
+// Every wait is bounded (wait_ns); a wait that runs out records kErrTimeout in
+// the device error word, and the CTA leaves at the next phase boundary after
+// its producer has seen its outstanding copies land.
+#include "gemv.cuh"
+#include "launch_util.cuh"
+#include "step.h"
+
+namespace qd {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// PTX helpers: mbarriers, TMA, timers, named barriers.
+// ---------------------------------------------------------------------------
+QD_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+QD_DEV void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+QD_DEV void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+QD_DEV void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+QD_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Same, but the thread may sleep (up to `ns`) until the phase completes
+// instead of returning at once, so waiting warps do not take issue slots.
+QD_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+// L2 policy for data read once per step (weights, cached K/V pages): evicted
+// first, so that the stream does not push the kernel's code, parameters and
+// activations out of L2.
+QD_DEV uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+QD_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+QD_DEV void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+QD_DEV uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+QD_DEV int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+QD_DEV int ld_relaxed(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Named barrier 1 over the consumer warps; returns the OR of `pred` over them.
+QD_DEV bool cbar_or(int pred, int nthreads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+QD_DEV void cbar(int nthreads) { asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory"); }
+QD_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+QD_DEV void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+QD_DEV void ldsm_x4_t(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+// d += A(16x16; rows 8-15 zero) * B(16x8), bf16 in, fp32 accumulate.
+QD_DEV void mma_bf16(float (&d)[2], float &z2, float &z3, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(z2), "+f"(z3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// x = hi + lo with both bf16 (|lo| <= 2^-8 |x|).
+QD_DEV void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+QD_DEV float silu(float a) { return a / (1.f + __expf(-a)); }
+
+// ---------------------------------------------------------------------------
+// Schedule shared by producer and consumers.
+// ---------------------------------------------------------------------------
+QD_DEV void span(int N, int c, int nc, int &r0, int &r1) {
+    r0 = (int)((long long)N * c / nc);
+    r1 = (int)((long long)N * (c + 1) / nc);
+}
+
+// Ring position: the slot and the parity of its current use.
+struct RingPos {
+    int slot = 0;
+    uint32_t par = 0;
+    QD_DEV void next(int n) {
+        if (++slot == n) {
+            slot = 0;
+            par ^= 1u;
+        }
+    }
+    QD_DEV void prev(int n) {
+        if (--slot < 0) {
+            slot = n - 1;
+            par ^= 1u;
+        }
+    }
+};
+
+// Row segments of a phase: the QKV rows are q | k | v (three matrices), every
+// other phase has one matrix.  Start of segment k = 0..3.
+QD_DEV int seg_bound(const StepParams &p, int ph, int k) {
+    const int N = p.geo[ph].N;
+    if (ph != kPhQkv) return k == 0 ? 0 : N;
+    const int b1 = p.Hq * p.d, b2 = b1 + p.Hkv * p.d;
+    return k == 0 ? 0 : (k == 1 ? b1 : (k == 2 ? b2 : N));
+}
+
+// Visit the ring items of the CTA's rows [r0, r1) of phase ph in order:
+// f(seg, local, n, j) for n rows starting at row `local` of matrix `seg`, the
+// first of them being the CTA's row j.  Producer and consumers both walk this.
+template <class Fn>
+QD_DEV void for_items(const StepParams &p, int ph, int r0, int r1, Fn &&f) {
+    const int rs = p.geo[ph].rs;
+    const int nseg = ph == kPhQkv ? 3 : 1;
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int b0 = seg_bound(p, ph, sg), b1 = seg_bound(p, ph, sg + 1);
+        const int lo = max(r0, b0), hi = min(r1, b1);
+        for (int r = lo; r < hi; r += rs) f(sg, r - b0, min(rs, hi - r), r - r0);
+    }
+}
+
+// Codes and scales of segment sg of a phase (gate/up: both matrices).
+struct SegMats {
+    const uint8_t *wa, *sa, *wb, *sb;
+};
+QD_DEV SegMats seg_mats(const StepParams &p, const StepLayer &Ly, int ph, int sg) {
+    switch (ph) {
+        case kPhQkv: return {(const uint8_t *)Ly.w[sg], (const uint8_t *)Ly.s[sg], nullptr, nullptr};
+        case kPhO: return {(const uint8_t *)Ly.wo, (const uint8_t *)Ly.so, nullptr, nullptr};
+        case kPhGu:
+            return {(const uint8_t *)Ly.wg, (const uint8_t *)Ly.sg, (const uint8_t *)Ly.wu, (const uint8_t *)Ly.su};
+        case kPhDown: return {(const uint8_t *)Ly.wd, (const uint8_t *)Ly.sd, nullptr, nullptr};
+        default: return {(const uint8_t *)p.lm_w, (const uint8_t *)p.lm_scale, nullptr, nullptr};
+    }
+}
+
+// Byte layout of a GEMV ring item of n rows starting at matrix row `local`:
+// [codes A][codes B (gate/up only)][scales A][scales B]; INT4 scale blocks are
+// the 16-byte-aligned cover of the rows' scale bytes.
+struct ItemLayout {
+    int codes_b;   // offset of the second matrix's codes
+    int sc_a, sc_b;  // offset of row `local`'s scales (INT4)
+    int sc_lo, sc_bytes;
+    uint32_t total;
+};
+QD_DEV ItemLayout gemv_layout(const StepGeo &g, int local, int n, int m) {
+    ItemLayout L{};
+    L.codes_b = n * g.row_bytes;
+    const int codes_end = m * n * g.row_bytes;
+    L.total = (uint32_t)codes_end;
+    if (g.sr) {
+        const int lo = (local * g.sr) & ~15, hi = ((local + n) * g.sr + 15) & ~15;
+        L.sc_lo = lo;
+        L.sc_bytes = hi - lo;
+        L.sc_a = codes_end + (local * g.sr - lo);
+        L.sc_b = L.sc_a + L.sc_bytes;
+        L.total += (uint32_t)(m * L.sc_bytes);
+    }
+    return L;
+}
+
+QD_DEV int pages_per_item(int d) { return kStepSlotBytes / (64 * d); }
+QD_DEV void attn_split(const StepParams &p, int c, int T, int &g, int &sp, int &pa0, int &pa1) {
+    g = c / p.P;
+    sp = c % p.P;
+    const int n_pg = (T + kPageTokens - 1) / kPageTokens;
+    pa0 = (int)((long long)n_pg * sp / p.P);
+    pa1 = (int)((long long)n_pg * (sp + 1) / p.P);
+}
+
+// Shared-memory carve-up (base aligned to 1024 bytes for the swizzled boxes).
+struct Smem {
+    uint8_t *ring;
+    uint64_t *full, *empty;
+    float *res;        // kStepResFloats; the attention phase reuses it
+    uint4 *stage;      // staged fp16 activations
+    float *post;       // per-unit scale of the staged activations
+    float *red;        // 64 floats of reduction scratch
+    int *misc;         // [0] abort, [1..32] finished heads, [33] last-CTA flag
+    StepLayer *layers; // copy of the per-layer pointer table
+};
+QD_HOST_DEV_INLINE size_t smem_bytes(int n_slots, int n_layers) {
+    return 1024 + (size_t)n_slots * kStepSlotBytes + (size_t)n_slots * 16 + (size_t)kStepResFloats * 4 +
+           kStepStageBytes + 64 * 4 + 64 * 4 + (size_t)n_layers * sizeof(StepLayer);
+}
+QD_DEV Smem carve(uint8_t *raw, int n_slots) {
+    Smem s;
+    uint8_t *b = (uint8_t *)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
+    s.ring = b;
+    b += (size_t)n_slots * kStepSlotBytes;
+    s.full = (uint64_t *)b;
+    s.empty = s.full + n_slots;
+    b += (size_t)n_slots * 16;
+    s.res = (float *)b;
+    b += kStepResFloats * 4;
+    s.stage = (uint4 *)b;
+    s.post = (float *)(b + kStepMaxStageK * 2);
+    b += kStepStageBytes;
+    s.red = (float *)b;
+    b += 64 * 4;
+    s.misc = (int *)b;
+    b += 64 * 4;
+    s.layers = (StepLayer *)b;
+    return s;
+}
+
+// Bounded wait for a device counter to reach `target` (one thread).  Returns
+// false (and records the error) when the wait runs out or another CTA failed.
+QD_DEV bool wait_counter(const StepParams &p, const int *ctr, int target) {
+    const uint64_t t0 = gtimer();
+    for (uint32_t n = 0;; ++n) {
+        if (ld_acquire(ctr) >= target) return true;
+        if (ld_relaxed(&p.st->err) != kErrNone) return false;
+        if ((n & 15) == 15 && gtimer() - t0 > p.wait_ns) {
+            atomicCAS(&p.st->err, kErrNone, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait on an mbarrier phase.  `abort` is polled so that a CTA that is
+// leaving does not sit out the full bound on every remaining item.
+QD_DEV bool wait_mbar(const StepParams &p, uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        if (mbar_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort) return false;
+        if (gtimer() - t0 > p.wait_ns) {
+            atomicCAS(&p.st->err, kErrNone, kErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Producer.
+// ---------------------------------------------------------------------------
+template <int DH>
+QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
+    volatile int *abort = s.misc;
+    const int c = blockIdx.x, nc = gridDim.x;
+    const int T = p.st->pos + 1;
+    RingPos rp, landed;
+    int issued = 0, n_landed = 0;
+    const uint64_t pol = l2_evict_first();
+    bool ok = true;
+    // Claim the next slot (warp-uniform): lane 0 waits until no more than
+    // p.inflight - 1 earlier items are still in flight (bytes on the way, not
+    // yet in shared memory) and until the consumers released the slot's
+    // previous use.  Landed items may fill the whole ring; the in-flight cap
+    // keeps the memory system's queues short, so that the latency-bound loads
+    // of the phases (activations, counters) are not stuck behind the stream.
+    auto claim = [&]() -> bool {
+        int got = 1;
+        if (lane == 0) {
+            while (got && issued - n_landed >= p.inflight) {
+                got = wait_mbar(p, s.full + landed.slot, landed.par, abort);
+                landed.next(p.n_slots);
+                ++n_landed;
+            }
+            if (got) got = wait_mbar(p, s.empty + rp.slot, rp.par ^ 1u, abort);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) ok = false;
+        return got != 0;
+    };
+    auto gemv_items = [&](const StepLayer &Ly, int ph) {
+        const StepGeo &g = p.geo[ph];
+        const int m = ph == kPhGu ? 2 : 1;
+        int r0, r1;
+        span(g.N, c, nc, r0, r1);
+        for_items(p, ph, r0, r1, [&](int sg, int local, int n, int) {
+            if (!ok || !claim()) return;
+            if (lane == 0) {
+                const SegMats M = seg_mats(p, Ly, ph, sg);
+                uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
+                uint64_t *bar = s.full + rp.slot;
+                const ItemLayout L = gemv_layout(g, local, n, m);
+                const uint32_t cb = (uint32_t)(n * g.row_bytes);
+                mbar_expect_tx(bar, L.total);
+                bulk_g2s(dst, M.wa + (size_t)local * g.row_bytes, cb, bar, pol);
+                if (m == 2) bulk_g2s(dst + cb, M.wb + (size_t)local * g.row_bytes, cb, bar, pol);
+                if (g.sr) {
+                    bulk_g2s(dst + m * cb, M.sa + L.sc_lo, (uint32_t)L.sc_bytes, bar, pol);
+                    if (m == 2) bulk_g2s(dst + m * cb + L.sc_bytes, M.sb + L.sc_lo, (uint32_t)L.sc_bytes, bar, pol);
+                }
+            }
+            rp.next(p.n_slots);
+            ++issued;
+        });
+    };
+    auto attn_items = [&](int l) {
+        if (c >= p.Hkv * p.P) return;
+        int g, sp, pa0, pa1;
+        attn_split(p, c, T, g, sp, pa0, pa1);
+        const int ppi = pages_per_item(DH);
+        for (int base = pa0; ok && base < pa1; base += 32) {
+            // lane k holds the physical page of logical page base + k
+            int phys = 0;
+            if (base + lane < pa1) {
+                phys = __ldg(p.page_table + base + lane);
+                if (phys < 0 || phys >= p.n_pages) {
+                    atomicCAS(&p.st->err, kErrNone, kErrBadPage);
+                    phys = 0;
+                }
+            }
+            const int nb = min(32, pa1 - base);
+            for (int k0 = 0; ok && k0 < nb; k0 += ppi) {
+                const int np = min(ppi, nb - k0);
+                if (!claim()) break;
+                int pg[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) pg[q] = __shfl_sync(0xffffffffu, phys, min(k0 + q, 31));
+                if (lane == 0) {
+                    uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
+                    uint64_t *bar = s.full + rp.slot;
+                    mbar_expect_tx(bar, (uint32_t)(np * 64 * DH));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (k < np) {
+                            const int y = ((l * p.n_pages + pg[k]) * p.Hkv + g) * kPageTokens;
+                            uint8_t *pgd = dst + (size_t)k * 64 * DH;
+#pragma unroll
+                            for (int hf = 0; hf < DH / 64; ++hf) {
+                                tma_2d(pgd + hf * 2048, &p.tm_k, hf * 64, y, bar, pol);
+                                tma_2d(pgd + (DH / 64 + hf) * 2048, &p.tm_v, hf * 64, y, bar, pol);
+                            }
+                        }
+                    }
+                }
+                rp.next(p.n_slots);
+                ++issued;
+            }
+        }
+    };
+    for (int l = 0; ok && l < p.L; ++l) {
+        const StepLayer &Ly = s.layers[l];
+        gemv_items(Ly, kPhQkv);
+        attn_items(l);
+        gemv_items(Ly, kPhO);
+        gemv_items(Ly, kPhGu);
+        gemv_items(Ly, kPhDown);
+    }
+    if (ok) gemv_items(s.layers[0], kPhLm);
+    // Leave only once every copy this CTA issued has landed (bounded).
+    if (lane == 0) {
+        RingPos q = rp;
+        for (int k = 0; k < min(issued, p.n_slots); ++k) {
+            q.prev(p.n_slots);
+            const uint64_t t0 = gtimer();
+            while (!mbar_try_wait(s.full + q.slot, q.par) && gtimer() - t0 < p.wait_ns) {
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Consumers: activation fragments and the row loop.
+// ---------------------------------------------------------------------------
+template <int F>
+struct Fmt {
+    static constexpr int EPU = F == kFmtInt4 ? 32 : (F == kFmtInt8 ? 16 : 8);  // values per 16-byte unit
+    static constexpr int XC = F == kFmtBf16 ? 2 : EPU / 8;  // 16-byte registers per unit (fp16, or fp32 for bf16)
+    static constexpr int SC = EPU / 8;                      // staged 16-byte fp16 chunks per unit
+};
+
+// Chunk swizzle of the staged activations (INT4: 4 chunks per unit, INT8: 2).
+template <int F>
+QD_DEV int stage_swz(int u) {
+    return Fmt<F>::SC == 4 ? ((u >> 1) & 3) : (Fmt<F>::SC == 2 ? ((u >> 2) & 1) : 0);
+}
+
+// Scale `n` values by 2^-e (e from their max |v|) into fp16 pairs; returns 2^e.
+template <int N>
+QD_DEV float to_half_scaled(const float (&v)[N], uint32_t (&h)[N / 2]) {
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    const float pre = ldexpf(1.f, -e);
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) h[i] = h2_as_u32(__floats2half2_rn(v[2 * i] * pre, v[2 * i + 1] * pre));
+    return ldexpf(1.f, e);
+}
+
+QD_DEV float4 ld_act4(const float *src32, const uint16_t *src16, int i) {
+    if (src16) {
+        const uint2 b = __ldg(reinterpret_cast<const uint2 *>(src16 + i));
+        return make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                           __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
+    }
+    return __ldcg(reinterpret_cast<const float4 *>(src32 + i));
+}
+
+// Stage a vector of K activations (fp32 src32, or bf16 src16) through shared
+// memory: optional RMSNorm with gain gamma, then per-unit power-of-two
+// scaling to fp16 (unit = the activations of one 16-byte weight unit).
+// Threads own units tid, tid + NCT, tid + 2 NCT and issue all their loads
+// at once; every consumer thread calls.
+template <int F, int NCW>
+QD_DEV void stage_smem(const StepParams &p, const Smem &s, const float *src32, const uint16_t *src16,
+                       const uint16_t *gamma, int K) {
+    using FM = Fmt<F>;
+    constexpr int NCT = NCW * 32;
+    constexpr int EPU = FM::EPU;
+    constexpr int UPT = 3;  // units per thread: U <= 3 * NCT
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int U = K / EPU;
+    float v[UPT][EPU];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < UPT; ++j) {
+        const int u = tid + j * NCT;
+#pragma unroll
+        for (int q = 0; q < EPU / 4; ++q) {
+            float4 f = u < U ? ld_act4(src32, src16, u * EPU + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j][4 * q] = f.x;
+            v[j][4 * q + 1] = f.y;
+            v[j][4 * q + 2] = f.z;
+            v[j][4 * q + 3] = f.w;
+            ss += f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w;
+        }
+    }
+    float inv = 1.f;
+    if (gamma) {
+        ss = warp_sum(ss);
+        if (lane == 0) s.red[warp] = ss;
+        cbar(NCT);
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) t += s.red[w];
+        inv = rsqrtf(t / (float)K + p.eps);
+    }
+#pragma unroll
+    for (int j = 0; j < UPT; ++j) {
+        const int u = tid + j * NCT;
+        if (u < U) {
+            if (gamma) {
+#pragma unroll
+                for (int q = 0; q < EPU / 4; ++q) {
+                    const uint2 b = __ldg(reinterpret_cast<const uint2 *>(gamma + u * EPU + 4 * q));
+                    v[j][4 * q] *= __uint_as_float(b.x << 16) * inv;
+                    v[j][4 * q + 1] *= __uint_as_float(b.x & 0xFFFF0000u) * inv;
+                    v[j][4 * q + 2] *= __uint_as_float(b.y << 16) * inv;
+                    v[j][4 * q + 3] *= __uint_as_float(b.y & 0xFFFF0000u) * inv;
+                }
+            }
+            uint32_t h[EPU / 2];
+            s.post[u] = to_half_scaled<EPU>(v[j], h);
+#pragma unroll
+            for (int k = 0; k < FM::SC; ++k)
+                s.stage[u * FM::SC + (k ^ stage_swz<F>(u))] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+        }
+    }
+    cbar(NCT);
+}
+
+// One 16-byte weight unit against its staged activations, with four independent
+// accumulation chains (one per 32-bit word) so that a unit's products overlap.
+QD_DEV float int4_unit_dot4(uint4 q, const uint4 (&x)[4]) {
+    const half2 z = u32_as_h2(0u);
+    const half2 a = int4_word_dot(q.x, x[0], z), b = int4_word_dot(q.y, x[1], z);
+    const half2 c = int4_word_dot(q.z, x[2], z), d = int4_word_dot(q.w, x[3], z);
+    const float2 f = __half22float2(__hadd2(__hadd2(a, b), __hadd2(c, d)));
+    return f.x + f.y;
+}
+QD_DEV float int8_unit_dot4(uint4 q, const uint4 (&x)[2]) {
+    const half2 z = u32_as_h2(0u);
+    const half2 a = int8_word_dot(q.x, x[0].x, x[0].y, z), b = int8_word_dot(q.y, x[0].z, x[0].w, z);
+    const half2 c = int8_word_dot(q.z, x[1].x, x[1].y, z), d = int8_word_dot(q.w, x[1].z, x[1].w, z);
+    const float2 f = __half22float2(__hadd2(__hadd2(a, b), __hadd2(c, d)));
+    return f.x + f.y;
+}
+QD_DEV float bf16_unit_dot2(uint4 q, const float4 (&x)[2]) {
+    float2 p0 = make_float2(0.f, 0.f), p1 = make_float2(0.f, 0.f);
+    p0 = ffma2(make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)), make_float2(x[0].x, x[0].y), p0);
+    p1 = ffma2(make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)), make_float2(x[0].z, x[0].w), p1);
+    p0 = ffma2(make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)), make_float2(x[1].x, x[1].y), p0);
+    p1 = ffma2(make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)), make_float2(x[1].z, x[1].w), p1);
+    return (p0.x + p0.y) + (p1.x + p1.y);
+}
+
+// Sum each of v[0..7] over the 32 lanes; lane l ends with the total of
+// v[(l >> 2) & 7] (exchange halves at xor 16, 8, 4, then plain sums at 2, 1).
+QD_DEV float transpose_sum8(float (&v)[8], int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool hi = lane & 16;
+        const float send = hi ? v[i] : v[i + 4], keep = hi ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool hi = lane & 8;
+        const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    {
+        const bool hi = lane & 4;
+        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return v[0];
+}
+
+// Walks the ring items of the CTA's rows [r0, r1) of a phase in order (the
+// same sequence as for_items): n rows from row `local` of the current
+// segment, the first being the CTA's row j.
+struct ItemCursor {
+    int ph, r, hi, b0, sg, nseg, rs, r0;
+    QD_DEV ItemCursor(const StepParams &p, int ph_, int r0_, int r1_) {
+        ph = ph_;
+        r0 = r0_;
+        rs = p.geo[ph].rs;
+        nseg = ph == kPhQkv ? 3 : 1;
+        sg = -1;
+        hi = 0;
+        r = r0_;
+        b0 = 0;
+        advance(p, r1_);
+    }
+    // move to the next segment that holds rows of [r, r1)
+    QD_DEV void advance(const StepParams &p, int r1) {
+        while (r >= hi && sg + 1 < nseg) {
+            ++sg;
+            b0 = seg_bound(p, ph, sg);
+            const int e = seg_bound(p, ph, sg + 1);
+            r = max(r, b0);
+            hi = min(r1, e);
+        }
+    }
+    QD_DEV bool more() const { return r < hi; }
+    QD_DEV void next(const StepParams &p, int r1, int &local, int &n, int &j) {
+        local = r - b0;
+        n = min(rs, hi - r);
+        j = r - r0;
+        r += n;
+        if (r >= hi) advance(p, r1);
+    }
+};
+
+// One GEMV phase's ring items for this CTA, adding the row results into
+// s.res[j * OPR + o] (j = row - r0, o = gate/up for OPR = 2).  Rows go to warp
+// group j % NG (NG = NCW / ks, a power of two), RW rows of an item per warp;
+// within a group, warp kp takes units [kp * UPW, (kp + 1) * UPW) and its lanes
+// units ub + lane + 32 i.  A lane walks its units, takes the unit's staged
+// activations once (kept in registers for the whole phase when the lane has
+// a single unit) and multiplies them with the unit of each of its RW rows in
+// straight-line code (rows past the item's end read a valid row and are
+// dropped).  Items are taken in batches of up to kBatch, so that one pass of
+// barrier waits and releases serves several items.  Partial sums of 8 rows
+// are combined across the warp with one transposing shuffle tree.
+template <int F, int OPR, int RW, int NCW>
+QD_DEV RingPos gemv_core(const StepParams &p, const Smem &s, int ph, int r0, int r1, RingPos rp) {
+    using FM = Fmt<F>;
+    constexpr int kBatch = 4;
+    volatile int *abort = s.misc;
+    const StepGeo &g = p.geo[ph];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NG = NCW / g.ks, grp = warp / g.ks, kp = warp % g.ks;
+    const int upw = (g.U + g.ks - 1) / g.ks;
+    const int ub = kp * upw, ue = min(g.U, ub + upw);
+    const int nu = ue - ub > lane ? (ue - ub - lane + 31) / 32 : 0;  // this lane's units
+    const bool one = upw <= 32;                                      // at most one unit per lane
+    const int row_bytes = g.row_bytes, sr = g.sr, n_slots = p.n_slots;
+    auto load_x = [&](int u, uint4 (&xr)[FM::XC], float &post) {
+        post = s.post[u];
+        if constexpr (F == kFmtBf16) {
+            const uint4 hv = s.stage[u];
+            const float2 a = __half22float2(u32_as_h2(hv.x)), b = __half22float2(u32_as_h2(hv.y));
+            const float2 c = __half22float2(u32_as_h2(hv.z)), d = __half22float2(u32_as_h2(hv.w));
+            xr[0] = make_uint4(__float_as_uint(a.x * post), __float_as_uint(a.y * post), __float_as_uint(b.x * post),
+                               __float_as_uint(b.y * post));
+            xr[1] = make_uint4(__float_as_uint(c.x * post), __float_as_uint(c.y * post), __float_as_uint(d.x * post),
+                               __float_as_uint(d.y * post));
+        } else {
+#pragma unroll
+            for (int k = 0; k < FM::XC; ++k) xr[k] = s.stage[u * FM::SC + (k ^ stage_swz<F>(u))];
+        }
+    };
+    uint4 x1[FM::XC];
+    float post1 = 0.f;
+    if (one && nu > 0) load_x(ub + lane, x1, post1);
+
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    int n_rows = 0, pend = 0;  // rows this warp finished; rows in acc
+    auto flush = [&]() {
+        const float t = transpose_sum8(acc, lane);
+        const int vi = (lane >> 2) & 7;
+        if ((lane & 3) == 0 && vi >= 8 - pend * OPR) {
+            const int ord = n_rows - (8 - vi + OPR - 1) / OPR;  // this value's row among the warp's rows
+            const int j = grp + ord * NG;
+            atomicAdd(s.res + j * OPR + (OPR == 2 ? (vi & 1) : 0), t);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        pend = 0;
+    };
+    // Row dot products of one item: pa[r] (and pb[r], gate/up) for rows q[r].
+    auto item_dot = [&](const uint8_t *item, int local, int n, int q0, float (&pa)[RW], float (&pb)[RW]) {
+        const ItemLayout L = gemv_layout(g, local, n, OPR);
+        int qr[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            qr[r] = min(q0 + r * NG, n - 1);
+            pa[r] = pb[r] = 0.f;
+        }
+        auto dot = [&](const uint8_t *codes, int sc_off, int q, int u, const uint4 (&xr)[FM::XC], float post) -> float {
+            const uint4 w = *reinterpret_cast<const uint4 *>(codes + q * row_bytes + u * 16);
+            if constexpr (F == kFmtInt4) {
+                const float sv = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(item + sc_off + q * sr)[u >> 2]);
+                return int4_unit_dot4(w, xr) * (sv * post);
+            } else if constexpr (F == kFmtInt8) {
+                return int8_unit_dot4(w, xr) * post;
+            } else {
+                const float4 xf[2] = {make_float4(__uint_as_float(xr[0].x), __uint_as_float(xr[0].y),
+                                                  __uint_as_float(xr[0].z), __uint_as_float(xr[0].w)),
+                                      make_float4(__uint_as_float(xr[1].x), __uint_as_float(xr[1].y),
+                                                  __uint_as_float(xr[1].z), __uint_as_float(xr[1].w))};
+                return bf16_unit_dot2(w, xf);
+            }
+        };
+        auto unit = [&](int u, const uint4 (&xr)[FM::XC], float post) {
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                pa[r] += dot(item, L.sc_a, qr[r], u, xr, post);
+                if constexpr (OPR == 2) pb[r] += dot(item + L.codes_b, L.sc_b, qr[r], u, xr, post);
+            }
+        };
+        if (one) {
+            if (nu > 0) unit(ub + lane, x1, post1);
+        } else {
+            for (int i = 0; i < nu; ++i) {
+                const int u = ub + lane + 32 * i;
+                uint4 xr[FM::XC];
+                float post;
+                load_x(u, xr, post);
+                unit(u, xr, post);
+            }
+        }
+    };
+
+    ItemCursor cur(p, ph, r0, r1);
+    while (cur.more()) {
+        const ItemCursor batch = cur;  // replayed below to revisit the batch's items
+        int nb = 0;
+        for (; nb < kBatch && cur.more(); ++nb) {
+            int l0, n0, j0;
+            cur.next(p, r1, l0, n0, j0);
+        }
+        // all lanes observe the phases (acquiring the copied bytes); the warp
+        // skips the batch together if any lane's wait ran out
+        bool ok = true;
+        {
+            RingPos q = rp;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (b < nb) {
+                    ok = wait_mbar(p, s.full + q.slot, q.par, abort) && ok;
+                    q.next(n_slots);
+                }
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        RingPos q = rp;
+        ItemCursor ic = batch;
+#pragma unroll 1
+        for (int b = 0; b < nb; ++b) {
+            int local, n, jf;
+            ic.next(p, r1, local, n, jf);
+            const int q0 = (grp - jf) & (NG - 1);
+            const int rw = ok && q0 < n ? (n - 1 - q0) / NG + 1 : 0;
+            if (rw > 0) {
+                float pa[RW], pb[RW];
+                item_dot(s.ring + (size_t)q.slot * kStepSlotBytes, local, n, q0, pa, pb);
+                if ((pend + rw) * OPR > 8) flush();
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    if (r < rw) {
+#pragma unroll
+                        for (int i = 0; i < 8 - OPR; ++i) acc[i] = acc[i + OPR];
+                        if constexpr (OPR == 2) {
+                            acc[6] = pa[r];
+                            acc[7] = pb[r];
+                        } else {
+                            acc[7] = pa[r];
+                        }
+                        ++n_rows;
+                        ++pend;
+                    }
+                }
+            }
+            q.next(n_slots);
+        }
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (b < nb) {
+                    mbar_arrive(s.empty + rp.slot);
+                    rp.next(n_slots);
+                }
+            }
+        }
+        rp = RingPos{__shfl_sync(0xffffffffu, rp.slot, 0), __shfl_sync(0xffffffffu, rp.par, 0)};
+    }
+    if (pend) flush();
+    return rp;
+}
+
+// Dispatch on the rows per warp and item chosen by the host planner.
+template <int F, int OPR, int NCW>
+QD_DEV RingPos gemv_rows(const StepParams &p, const Smem &s, int ph, int r0, int r1, RingPos rp) {
+    const int rw = p.geo[ph].rw;
+    if constexpr (OPR == 2) {
+        return rw >= 2 ? gemv_core<F, 2, 2, NCW>(p, s, ph, r0, r1, rp) : gemv_core<F, 2, 1, NCW>(p, s, ph, r0, r1, rp);
+    } else {
+        if (rw >= 4) return gemv_core<F, 1, 4, NCW>(p, s, ph, r0, r1, rp);
+        if (rw == 2) return gemv_core<F, 1, 2, NCW>(p, s, ph, r0, r1, rp);
+        return gemv_core<F, 1, 1, NCW>(p, s, ph, r0, r1, rp);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Consumers: phases.
+// ---------------------------------------------------------------------------
+template <int NCW>
+struct Ctx {
+    const StepParams &p;
+    const Smem &s;
+    int c, nc, tid, warp, lane;
+    RingPos rp;      // next ring item
+    int pos, token;
+    bool err;        // this thread saw a failed wait
+    volatile int *abort;
+    static constexpr int NCT = NCW * 32;
+
+    QD_DEV int *sync_at(int l, int k) const { return p.sync + (size_t)l * kSyncStride + k; }
+
+    // Thread 0 waits for *ctr >= target; all consumers then meet (and agree
+    // whether the CTA is leaving).
+    QD_DEV bool dep(const int *ctr, int target) {
+        if (tid == 0 && ctr && !*abort) {
+            if (!wait_counter(p, ctr, target)) *abort = 1;
+        }
+        return !cbar_or(*abort, NCT);
+    }
+    // Writes of this CTA are done: make them visible, then raise the counter.
+    QD_DEV bool signal(int *ctr, int add) {
+        __threadfence();
+        const bool fail = cbar_or(*abort, NCT);
+        if (tid == 0 && ctr) atomicAdd(ctr, add);
+        return !fail;
+    }
+    QD_DEV void stamp(int k) {
+        if (p.prof && c == 0 && tid == 0) p.prof[k] = gtimer();
+    }
+};
+
+template <int D>
+QD_DEV void head_epilogue(const StepParams &p, int l, int head, int pos, int lane) {
+    constexpr int M = D / 32;
+    float v[M];
+    const float *raw = p.raw + (size_t)head * D;
+#pragma unroll
+    for (int m = 0; m < M; ++m) v[m] = __ldcg(raw + lane + 32 * m);
+    const bool is_q = head < p.Hq;
+    const bool is_k = !is_q && head < p.Hq + p.Hkv;
+    const uint16_t *qg = p.layers[l].q_norm, *kg = p.layers[l].k_norm;
+    if ((is_q || is_k) && qg) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < M; ++m) ss += v[m] * v[m];
+        ss = warp_sum(ss);
+        const float inv = rsqrtf(ss / (float)D + p.eps);
+        const uint16_t *gm = is_q ? qg : kg;
+#pragma unroll
+        for (int m = 0; m < M; ++m) v[m] = bf16_bits_to_float(__ldg(gm + lane + 32 * m)) * (v[m] * inv);
+    }
+    if (is_q || is_k) {
+        const float2 *cs = p.rope_cs + (size_t)pos * (D / 2);
+#pragma unroll
+        for (int m = 0; m < M / 2; ++m) {
+            const float2 cv = __ldg(cs + lane + 32 * m);
+            const float x0 = v[m], x1 = v[m + M / 2];
+            v[m] = x0 * cv.x - x1 * cv.y;
+            v[m + M / 2] = x1 * cv.x + x0 * cv.y;
+        }
+    }
+    if (is_q) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) p.q[(size_t)head * D + lane + 32 * m] = v[m];
+        return;
+    }
+    const int g = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
+    int phys = __ldg(p.page_table + pos / kPageTokens);
+    if (phys < 0 || phys >= p.n_pages) {
+        if (lane == 0) atomicCAS(&p.st->err, kErrNone, kErrBadPage);
+        return;
+    }
+    uint16_t *dst = (is_k ? p.k_pool : p.v_pool) +
+                    ((((size_t)l * p.n_pages + phys) * p.Hkv + g) * kPageTokens + pos % kPageTokens) * D;
+#pragma unroll
+    for (int m = 0; m < M; ++m) dst[lane + 32 * m] = float_to_bf16_bits(v[m]);
+}
+
+template <int DH, int NCW>
+QD_DEV bool phase_attn(Ctx<NCW> &x, int l) {
+    const StepParams &p = x.p;
+    if (x.c >= p.Hkv * p.P) return true;
+    constexpr int NKK = DH / 16, NDT = DH / 8;
+    constexpr int PB = 64 * DH;  // bytes of one page's K and V boxes
+    const int G = p.Hq / p.Hkv;
+    const int T = x.pos + 1;
+    int g, sp, pa0, pa1;
+    attn_split(p, x.c, T, g, sp, pa0, pa1);
+    float *s_o = x.s.res;             // [G][DH]
+    float *s_m = s_o + 8 * DH;        // [NCW][8]
+    float *s_l = s_m + NCW * 8;       // [8]
+    for (int i = x.tid; i < 8 * DH + NCW * 8 + 8; i += x.NCT) s_o[i] = i < 8 * DH + NCW * 8 && i >= 8 * DH ? -INFINITY : 0.f;
+    if (!x.dep(x.sync_at(l, kSyncHeadsDone), p.Hq + 2 * p.Hkv)) return false;
+
+    const int lane = x.lane, warp = x.warp, gq = lane >> 2, tq = lane & 3;
+    uint32_t qh[NKK][2], ql[NKK][2];
+#pragma unroll
+    for (int kk = 0; kk < NKK; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int d0 = kk * 16 + hf * 8 + 2 * tq;
+            float q0 = 0.f, q1 = 0.f;
+            if (gq < G) {
+                const float2 qv = __ldcg(reinterpret_cast<const float2 *>(p.q + (size_t)(g * G + gq) * DH + d0));
+                q0 = qv.x;
+                q1 = qv.y;
+            }
+            split2(q0, q1, qh[kk][hf], ql[kk][hf]);
+        }
+    const float sscale = rsqrtf((float)DH) * kLog2e;
+    const int last_pg = (T - 1) / kPageTokens, new_row = (T - 1) % kPageTokens;
+    float m = -INFINITY, lsum = 0.f;
+    float o[NDT][2];
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = 0.f;
+    float z2 = 0.f, z3 = 0.f;
+    const int ppi = pages_per_item(DH);
+    for (int pa = pa0; pa < pa1; pa += ppi) {
+        const int np = min(ppi, pa1 - pa);
+        const int slot = x.rp.slot;
+        const bool have = __all_sync(0xffffffffu, wait_mbar(p, x.s.full + slot, x.rp.par, x.abort));
+        for (int k = 0; have && k < np; ++k) {
+            const int i = pa - pa0 + k;
+            if (i % NCW != warp) continue;
+            const int pg = pa + k;
+            uint8_t *kb = x.s.ring + (size_t)slot * kStepSlotBytes + (size_t)k * PB;
+            uint8_t *vb = kb + (DH / 64) * 2048;
+            auto at = [&](uint8_t *base, int tok, int ch) -> uint8_t * {  // 16-byte chunk ch of row tok
+                return base + (ch >> 3) * 2048 + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
+            };
+            if (pg == last_pg) {
+                // The appended row, written by this step's QKV phase, and zeros past the sequence.
+                int phys = __ldg(p.page_table + pg);
+                if (phys < 0 || phys >= p.n_pages) phys = 0;
+                const size_t row = ((((size_t)l * p.n_pages + phys) * p.Hkv + g) * kPageTokens + new_row) * DH;
+                if (lane < DH / 8) {
+                    *reinterpret_cast<uint4 *>(at(kb, new_row, lane)) =
+                        __ldcg(reinterpret_cast<const uint4 *>(p.k_pool + row) + lane);
+                    *reinterpret_cast<uint4 *>(at(vb, new_row, lane)) =
+                        __ldcg(reinterpret_cast<const uint4 *>(p.v_pool + row) + lane);
+                }
+                for (int cidx = lane; cidx < (kPageTokens - 1 - new_row) * (DH / 8); cidx += 32) {
+                    const int tok = new_row + 1 + cidx / (DH / 8), ch = cidx % (DH / 8);
+                    *reinterpret_cast<uint4 *>(at(vb, tok, ch)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async();
+                __syncwarp();
+            }
+            // S = Q K^T for the page's 16 tokens
+            float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < NKK; ++kk) {
+                const int tok = (lane & 7) + ((lane >> 4) << 3);
+                const int ch = kk * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(at(kb, tok, ch), b0, b1, b2, b3);
+                mma_bf16(s0, z2, z3, qh[kk][0], qh[kk][1], b0, b1);
+                mma_bf16(s0, z2, z3, ql[kk][0], ql[kk][1], b0, b1);
+                mma_bf16(s1, z2, z3, qh[kk][0], qh[kk][1], b2, b3);
+                mma_bf16(s1, z2, z3, ql[kk][0], ql[kk][1], b2, b3);
+            }
+            const int base = pg * kPageTokens;
+            const float v0 = base + 2 * tq < T ? s0[0] * sscale : -INFINITY;
+            const float v1 = base + 2 * tq + 1 < T ? s0[1] * sscale : -INFINITY;
+            const float v2 = base + 8 + 2 * tq < T ? s1[0] * sscale : -INFINITY;
+            const float v3 = base + 9 + 2 * tq < T ? s1[1] * sscale : -INFINITY;
+            float mx = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m, mx);
+            const float alpha = exp2f(m - m_new);
+            const float p0 = exp2f(v0 - m_new), p1 = exp2f(v1 - m_new);
+            const float p2 = exp2f(v2 - m_new), p3 = exp2f(v3 - m_new);
+            float ps = (p0 + p1) + (p2 + p3);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+            lsum = lsum * alpha + ps;
+            m = m_new;
+#pragma unroll
+            for (int dt = 0; dt < NDT; ++dt) {
+                o[dt][0] *= alpha;
+                o[dt][1] *= alpha;
+            }
+            uint32_t ph0, pl0, ph2, pl2;
+            split2(p0, p1, ph0, pl0);
+            split2(p2, p3, ph2, pl2);
+            // O += P V
+#pragma unroll
+            for (int dp = 0; dp < NDT / 2; ++dp) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int tok = rr + (mi & 1) * 8;
+                const int ch = dp * 2 + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(at(vb, tok, ch), b0, b1, b2, b3);
+                mma_bf16(o[2 * dp], z2, z3, ph0, ph2, b0, b1);
+                mma_bf16(o[2 * dp], z2, z3, pl0, pl2, b0, b1);
+                mma_bf16(o[2 * dp + 1], z2, z3, ph0, ph2, b2, b3);
+                mma_bf16(o[2 * dp + 1], z2, z3, pl0, pl2, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x.s.empty + slot);
+        x.rp.next(p.n_slots);
+    }
+    // ---- merge the warps: common max, then rescaled sums in shared memory
+    if (tq == 0 && gq < G) s_m[warp * 8 + gq] = m;
+    if (cbar_or(*x.abort, x.NCT)) return false;
+    if (gq < G) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, s_m[w * 8 + gq]);
+        const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+        if (f != 0.f) {
+#pragma unroll
+            for (int dt = 0; dt < NDT; ++dt) {
+                atomicAdd(s_o + gq * DH + dt * 8 + 2 * tq, o[dt][0] * f);
+                atomicAdd(s_o + gq * DH + dt * 8 + 2 * tq + 1, o[dt][1] * f);
+            }
+            if (tq == 0) atomicAdd(s_l + gq, lsum * f);
+        }
+    }
+    cbar(x.NCT);
+    const size_t slot_base = (size_t)g * p.P + sp;
+    for (int idx = x.tid; idx < G * DH; idx += x.NCT) {
+        const int h = idx / DH;
+        p.part_o[(slot_base * G + h) * DH + idx % DH] = s_o[idx];
+        if (idx % DH == 0) {
+            float M = -INFINITY;
+            for (int w = 0; w < NCW; ++w) M = fmaxf(M, s_m[w * 8 + h]);
+            p.part_ml[(slot_base * G + h) * 2] = M;
+            p.part_ml[(slot_base * G + h) * 2 + 1] = s_l[h];
+        }
+    }
+    if (!x.signal(x.sync_at(l, kSyncAttnCnt + g), 1)) return false;
+    // ---- all P partials of head g are written: combine this CTA's slice
+    if (!x.dep(x.sync_at(l, kSyncAttnCnt + g), p.P)) return false;
+    const int E = G * DH;
+    const int e0 = (int)((long long)E * sp / p.P), e1 = (int)((long long)E * (sp + 1) / p.P);
+    const int ne = e1 - e0;
+    float *w_ml = x.s.res;             // [P][G] weights, then [G] 1/den
+    float *acc = w_ml + p.P * G + 8;   // [ne] sums of the slice
+    constexpr int kPer = 4;
+    float ov[kPer];
+    int oi[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int idx = x.tid + k * x.NCT;
+        oi[k] = idx < ne * p.P ? idx : -1;
+        ov[k] = 0.f;
+        if (oi[k] >= 0) {
+            const int pp = idx / ne, e = e0 + idx % ne;
+            ov[k] = __ldcg(p.part_o + (((size_t)g * p.P + pp) * G + e / DH) * DH + e % DH);
+        }
+    }
+    for (int idx = x.tid; idx < p.P * G; idx += x.NCT) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + (size_t)g * p.P * G + idx);
+        w_ml[idx] = ml.x;                                  // m, [P][G]
+        reinterpret_cast<float *>(x.s.stage)[idx] = ml.y;  // l, [P][G]
+    }
+    for (int i = x.tid; i < ne; i += x.NCT) acc[i] = 0.f;
+    cbar(x.NCT);
+    if (x.tid < G) {
+        const int h = x.tid;
+        float M = -INFINITY;
+        for (int pp = 0; pp < p.P; ++pp) M = fmaxf(M, w_ml[pp * G + h]);
+        float den = 0.f;
+        for (int pp = 0; pp < p.P; ++pp) {
+            const float mm = w_ml[pp * G + h];
+            const float f = mm == -INFINITY ? 0.f : exp2f(mm - M);
+            den = fmaf(f, reinterpret_cast<float *>(x.s.stage)[pp * G + h], den);
+            w_ml[pp * G + h] = f;
+        }
+        w_ml[p.P * G + h] = 1.f / den;
+    }
+    cbar(x.NCT);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        if (oi[k] >= 0) {
+            const int pp = oi[k] / ne, el = oi[k] % ne, e = e0 + el;
+            atomicAdd(acc + el, w_ml[pp * G + e / DH] * ov[k]);
+        }
+    }
+    // partial counts above kPer * NCT per slice are handled by a plain loop
+    for (int idx = x.tid + kPer * x.NCT; idx < ne * p.P; idx += x.NCT) {
+        const int pp = idx / ne, el = idx % ne, e = e0 + el;
+        atomicAdd(acc + el, w_ml[pp * G + e / DH] *
+                                __ldcg(p.part_o + (((size_t)g * p.P + pp) * G + e / DH) * DH + e % DH));
+    }
+    cbar(x.NCT);
+    for (int el = x.tid; el < ne; el += x.NCT) {
+        const int e = e0 + el;
+        p.attn[(size_t)g * G * DH + e] = acc[el] * w_ml[p.P * G + e / DH];
+    }
+    return x.signal(x.sync_at(l, kSyncAttnDone), 1);
+}
+
+// One GEMV phase of a layer (QKV, o_proj, gate/up or down): wait for the
+// input, stage it, consume the phase's ring items, run the epilogue and
+// signal.  The kernel calls it from a loop that is not unrolled, so its code
+// exists once.
+template <int WF, int DH, int NCW>
+QD_DEV bool layer_gemv(Ctx<NCW> &x, int l, int ph) {
+    const StepParams &p = x.p;
+    const StepGeo &g = p.geo[ph];
+    const StepLayer *Ly = x.s.layers + l;
+    const int opr = ph == kPhGu ? 2 : 1;
+    int r0, r1;
+    span(g.N, x.c, x.nc, r0, r1);
+    for (int j = x.tid; j < opr * (r1 - r0); j += x.NCT) x.s.res[j] = 0.f;
+    const int *dep = ph == kPhQkv ? (l ? x.sync_at(l - 1, kSyncDDone) : nullptr)
+                     : ph == kPhO ? x.sync_at(l, kSyncAttnDone)
+                     : ph == kPhGu ? x.sync_at(l, kSyncODone)
+                                   : x.sync_at(l, kSyncGuDone);
+    if (!x.dep(dep, ph == kPhO ? p.Hkv * p.P : x.nc)) return false;
+    const float *src = ph == kPhO ? p.attn : (ph == kPhDown ? p.u : p.x);
+    const uint16_t *src16 = ph == kPhQkv && l == 0 ? p.embed + (size_t)x.token * p.h : nullptr;
+    const uint16_t *gamma = ph == kPhQkv ? Ly->attn_norm : (ph == kPhGu ? Ly->mlp_norm : nullptr);
+    stage_smem<WF, NCW>(p, x.s, src, src16, gamma, g.K);
+    x.rp = opr == 2 ? gemv_rows<WF, 2, NCW>(p, x.s, ph, r0, r1, x.rp) : gemv_rows<WF, 1, NCW>(p, x.s, ph, r0, r1, x.rp);
+    if (cbar_or(*x.abort, x.NCT)) return false;
+    if (ph == kPhQkv) {
+        for (int j = x.tid; j < r1 - r0; j += x.NCT) {
+            const int r = r0 + j;
+            const int sg = r < seg_bound(p, kPhQkv, 1) ? 0 : (r < seg_bound(p, kPhQkv, 2) ? 1 : 2);
+            const int local = r - seg_bound(p, kPhQkv, sg);
+            float v = x.s.res[j];
+            if (WF == kFmtInt8) v *= __ldg(reinterpret_cast<const float *>(Ly->s[sg]) + local);
+            if (Ly->b[sg]) v += bf16_bits_to_float(__ldg(Ly->b[sg] + local));
+            p.raw[r] = v;
+        }
+        __threadfence();
+        cbar(x.NCT);
+        // Per-head arrival: the CTA that completes a head runs its epilogue.
+        const int h_lo = r0 / DH, h_hi = r1 > r0 ? (r1 - 1) / DH : h_lo - 1;
+        int *fin = x.s.misc + 1;
+        if (x.tid < 32) {
+            const int h = h_lo + x.tid;
+            int done = 0;
+            if (h <= h_hi) {
+                const int n = min(r1, (h + 1) * DH) - max(r0, h * DH);
+                done = atomicAdd(x.sync_at(l, h), n) + n == DH;
+            }
+            fin[x.tid] = done;
+        }
+        cbar(x.NCT);
+        for (int t = x.warp; t <= h_hi - h_lo && t < 32; t += NCW) {
+            if (!fin[t]) continue;
+            __threadfence();
+            head_epilogue<DH>(p, l, h_lo + t, x.pos, x.lane);
+            __threadfence();
+            __syncwarp();
+            if (x.lane == 0) atomicAdd(x.sync_at(l, kSyncHeadsDone), 1);
+        }
+        return true;
+    }
+    for (int j = x.tid; j < r1 - r0; j += x.NCT) {
+        const int r = r0 + j;
+        if (ph == kPhGu) {
+            float a = x.s.res[2 * j], b = x.s.res[2 * j + 1];
+            if (WF == kFmtInt8) {
+                a *= __ldg(reinterpret_cast<const float *>(Ly->sg) + r);
+                b *= __ldg(reinterpret_cast<const float *>(Ly->su) + r);
+            }
+            p.u[r] = silu(a) * b;
+        } else {
+            float v = x.s.res[j];
+            if (WF == kFmtInt8) v *= __ldg(reinterpret_cast<const float *>(ph == kPhO ? Ly->so : Ly->sd) + r);
+            const float prev = ph == kPhO && l == 0 ? bf16_bits_to_float(__ldg(p.embed + (size_t)x.token * p.h + r))
+                                                    : __ldcg(p.x + r);
+            p.x[r] = prev + v;
+        }
+    }
+    return x.signal(x.sync_at(l, ph == kPhO ? kSyncODone : (ph == kPhGu ? kSyncGuDone : kSyncDDone)), 1);
+}
+
+template <int LMF, int NCW>
+QD_DEV void phase_lm(Ctx<NCW> &x, const StepLayer *Ly0) {
+    const StepParams &p = x.p;
+    const StepGeo &g = p.geo[kPhLm];
+    int r0, r1;
+    span(g.N, x.c, x.nc, r0, r1);
+    for (int j = x.tid; j < r1 - r0; j += x.NCT) x.s.res[j] = 0.f;
+    if (!x.dep(x.sync_at(p.L - 1, kSyncDDone), x.nc)) return;
+    stage_smem<LMF, NCW>(p, x.s, p.x, nullptr, p.final_norm, g.K);
+    x.rp = gemv_rows<LMF, 1, NCW>(p, x.s, kPhLm, r0, r1, x.rp);
+    if (cbar_or(*x.abort, x.NCT)) return;
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int j = x.tid; j < r1 - r0; j += x.NCT) {
+        const int r = r0 + j;
+        float v = x.s.res[j];
+        if (LMF == kFmtInt8) v *= __ldg(p.lm_scale + r);
+        p.logits[r] = v;
+        if (v > best || (v == best && r < bi)) {
+            best = v;
+            bi = r;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) {
+            best = ov;
+            bi = oi;
+        }
+    }
+    if (x.lane == 0) {
+        x.s.red[x.warp] = best;
+        reinterpret_cast<int *>(x.s.red)[32 + x.warp] = bi;
+    }
+    cbar(x.NCT);
+    if (x.tid == 0) {
+        for (int w = 1; w < NCW; ++w) {
+            const float ov = x.s.red[w];
+            const int oi = reinterpret_cast<int *>(x.s.red)[32 + w];
+            if (ov > best || (ov == best && oi < bi)) {
+                best = ov;
+                bi = oi;
+            }
+        }
+        p.lm_val[x.c] = best;
+        p.lm_idx[x.c] = bi;
+        __threadfence();
+        const int prev = atomicAdd(p.sync + (size_t)p.L * kSyncStride, 1);
+        x.s.misc[33] = prev == x.nc - 1;
+    }
+    cbar(x.NCT);
+    if (!x.s.misc[33]) return;
+    __threadfence();
+    // Last CTA: global argmax (lowest index on ties), state update, counters reset.
+    if (x.warp == 0) {
+        float bv = -INFINITY;
+        int bix = 0x7fffffff;
+        for (int k = x.lane; k < x.nc; k += 32) {
+            const float v = __ldcg(p.lm_val + k);
+            const int i = __ldcg(p.lm_idx + k);
+            if (v > bv || (v == bv && i < bix)) {
+                bv = v;
+                bix = i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bix, o);
+            if (ov > bv || (ov == bv && oi < bix)) {
+                bv = ov;
+                bix = oi;
+            }
+        }
+        if (x.lane == 0) {
+            p.st->last_token = bix;
+            p.st->token = bix;
+            p.st->pos = x.pos + 1;
+        }
+    }
+    for (int i = x.tid; i < p.L * kSyncStride + 1; i += x.NCT) p.sync[i] = 0;
+}
+
+// Register split.  The block is three warpgroups launched at kLaunchRegs
+// registers a thread: warpgroups 0-1 (the consumers) raise theirs to
+// kConsumerRegs and warpgroup 2 (the producer warp plus three idle warps)
+// lowers its own to kProducerRegs.  The shares add up to the launch total,
+// 256 * 224 + 128 * 56 = 384 * 168 = 64512, and each SM sub-partition holds two
+// consumer warps and one producer-group warp: 2 * 32 * 224 + 32 * 56 = 16128 of
+// its 16384 registers.
+constexpr int kLaunchRegs = 168, kConsumerRegs = 224, kProducerRegs = 56;
+static_assert(256 * kConsumerRegs + 128 * kProducerRegs <= 384 * kLaunchRegs, "register split exceeds the launch");
+
+template <int WF, int LMF, int DH, int NCW>
+__global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constant__ StepParams p) {
+    static_assert(NCW == 8, "two consumer warpgroups");
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw, p.n_slots);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < p.n_slots; ++i) {
+            mbar_init(s.full + i, 1);
+            mbar_init(s.empty + i, NCW);
+        }
+        s.misc[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    {
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.layers);
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(s.layers);
+        const int n = p.L * (int)(sizeof(StepLayer) / 8);
+        for (int i = tid; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    __syncthreads();
+    if (warp >= NCW) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+        if (warp == NCW) producer<DH>(p, s, lane);
+        return;
+    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    Ctx<NCW> x{p, s, (int)blockIdx.x, (int)gridDim.x, tid, warp, lane, RingPos{}, 0, 0, false, s.misc};
+    x.pos = p.st->pos;
+    x.token = p.st->token;
+    if (x.token < 0 || x.token >= p.V) {
+        if (tid == 0) atomicCAS(&p.st->err, kErrNone, kErrBadToken);
+        x.token = 0;
+    }
+    bool ok = true;
+#pragma unroll 1
+    for (int l = 0; ok && l < p.L; ++l) {
+#pragma unroll 1
+        for (int k = 0; ok && k < 5; ++k) {
+            x.stamp(5 * l + k);
+            if (k == 1) {
+                ok = phase_attn<DH, NCW>(x, l);
+            } else {
+                ok = layer_gemv<WF, DH, NCW>(x, l, k == 0 ? kPhQkv : (k == 2 ? kPhO : (k == 3 ? kPhGu : kPhDown)));
+            }
+        }
+    }
+    // the producer may raise `abort` at any time: decide together
+    if (!cbar_or(*x.abort, Ctx<NCW>::NCT)) {
+        x.stamp(5 * p.L);
+        phase_lm<LMF, NCW>(x, s.layers);
+        x.stamp(5 * p.L + 1);
+    }
+}
+
+constexpr int kNcw = 8;
+
+template <int WF, int LMF, int DH>
+const void *pick() {
+    return (const void *)k_step<WF, LMF, DH, kNcw>;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host: plan, tensor maps, launch.
+// ---------------------------------------------------------------------------
+bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem, StepLaunch &out) {
+    if (p.d != 64 && p.d != 128) return false;
+    if (p.Hq + 2 * p.Hkv > kSyncMaxHeads || p.Hkv > kSyncMaxKvHeads || p.Hq % p.Hkv) return false;
+    const int G = p.Hq / p.Hkv;
+    if (G > 8 || n_sm < p.Hkv) return false;
+    p.P = n_sm / p.Hkv;
+    if (p.P * G + 8 + p.d * G > kStepResFloats || p.P * G * 4 > kStepStageBytes) return false;
+    int n_slots = kStepMaxSlots;
+    while (n_slots > 2 && smem_bytes(n_slots, p.L) > (size_t)max_smem) --n_slots;
+    if (smem_bytes(n_slots, p.L) > (size_t)max_smem || n_slots < 4) return false;
+    p.n_slots = n_slots;
+    if (p.inflight < 1) p.inflight = 1;
+    if (p.inflight > n_slots) p.inflight = n_slots;
+    auto set = [&](int ph, int fmt, int N, int K, int pairs, bool norm) -> bool {
+        StepGeo &g = p.geo[ph];
+        g.fmt = fmt;
+        g.N = N;
+        g.K = K;
+        const int epu = fmt == kFmtInt4 ? 32 : (fmt == kFmtInt8 ? 16 : 8);
+        if (K % epu || (fmt == kFmtInt4 && K % kGroup)) return false;
+        g.U = K / epu;
+        g.row_bytes = g.U * 16;
+        g.sr = fmt == kFmtInt4 ? K / 64 : 0;
+        const int m = pairs ? 2 : 1;
+        if (K > kStepMaxStageK || g.U > kStepMaxStageUnits) return false;
+        // rows per item: codes plus the aligned cover of their scales
+        int rs_max = 0;
+        for (int n = 1; n <= 64; ++n) {
+            const int sc = g.sr ? ((n * g.sr + 15) / 16 + 1) * 16 : 0;
+            if (m * (n * g.row_bytes + sc) <= kStepSlotBytes) rs_max = n;
+        }
+        if (rs_max == 0) return false;
+        // K split (ks warps per row, NG = 8 / ks row groups) and rows per item
+        // (n, so rw = ceil(n / NG) rows per warp): a warp spends about
+        // iters * (rw * m + 1/4) unit products per item (iters = its lanes'
+        // unit count; the quarter is the activation load) plus a fixed
+        // overhead; take the most bytes per cost.
+        double best = -1.0;
+        g.ks = 0;
+        for (int ks = 1; ks <= kNcw; ks *= 2) {
+            const int NG = kNcw / ks;
+            const int upw = (g.U + ks - 1) / ks, iters = (upw + 31) / 32;
+            for (int n = 1; n <= rs_max; ++n) {
+                const int rw = (n + NG - 1) / NG;
+                if (rw != 1 && rw != 2 && !(rw == 4 && m == 1)) continue;
+                const double cost = iters * (rw * m + 0.25) + 1.0;
+                const double score = (double)n * g.row_bytes * m / cost;
+                if (score > best + 1e-9) {
+                    best = score;
+                    g.ks = ks;
+                    g.rw = rw;
+                    g.rs = n;
+                }
+            }
+        }
+        if (!g.ks) return false;
+        (void)norm;
+        // per-CTA rows must fit the result buffer
+        const long long rows = ((long long)N + n_sm - 1) / n_sm;
+        if (rows * m > kStepResFloats) return false;
+        return true;
+    };
+    const int rq = p.Hq * p.d, rkv = p.Hkv * p.d;
+    if (!set(kPhQkv, weight_fmt, rq + 2 * rkv, p.h, 0, true)) return false;
+    if (!set(kPhO, weight_fmt, p.h, rq, 0, false)) return false;
+    if (!set(kPhGu, weight_fmt, p.F, p.h, 1, true)) return false;
+    if (!set(kPhDown, weight_fmt, p.h, p.F, 0, false)) return false;
+    if (!set(kPhLm, lm_fmt, p.V, p.h, 0, true)) return false;
+    // INT4 scale covers may read up to 15 bytes past a row's scales: every
+    // matrix's scale array must end on a 16-byte boundary.
+    if (weight_fmt == kFmtInt4) {
+        const int Ns[] = {rq, rkv, p.h, p.F};
+        const int Ks[] = {p.h, p.h, rq, p.h};
+        for (int i = 0; i < 4; ++i)
+            if (((long long)Ns[i] * (Ks[i] / 64)) % 16) return false;
+        if (((long long)p.h * (p.F / 64)) % 16) return false;
+    }
+    const void *k = nullptr;
+    if (weight_fmt == kFmtInt4 && lm_fmt == kFmtBf16) k = p.d == 128 ? pick<kFmtInt4, kFmtBf16, 128>() : pick<kFmtInt4, kFmtBf16, 64>();
+    else if (weight_fmt == kFmtInt8 && lm_fmt == kFmtBf16) k = p.d == 128 ? pick<kFmtInt8, kFmtBf16, 128>() : pick<kFmtInt8, kFmtBf16, 64>();
+    else if (weight_fmt == kFmtInt8 && lm_fmt == kFmtInt8) k = p.d == 128 ? pick<kFmtInt8, kFmtInt8, 128>() : pick<kFmtInt8, kFmtInt8, 64>();
+    if (!k) return false;
+    out.kernel = k;
+    out.grid = n_sm;
+    out.block = (kNcw + 4) * 32;
+    out.smem = smem_bytes(n_slots, p.L);
+    return true;
+}
+
+cudaError_t step_encode_kv_maps(StepParams &p, size_t total_rows) {
+    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = (EncodeFn)fn;
+    }
+    if (total_rows >= (1ull << 31)) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)total_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d * 2};
+    const cuuint32_t box[2] = {64, kPageTokens};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap *maps[2] = {&p.tm_k, &p.tm_v};
+    void *bases[2] = {p.k_pool, p.v_pool};
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = encode(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, bases[i], dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t step_occupancy(const StepLaunch &sl, int *blocks_per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(sl.kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(sl.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sl.kernel, sl.block, sl.smem);
+    return e;
+}
+
+cudaError_t launch_step(const StepLaunch &sl, const StepParams &p, cudaStream_t stream) {
+    {
+        static std::mutex mu;
+        static std::map<std::pair<const void *, int>, size_t> configured;
+        int dev = 0;
+        cudaError_t ge = cudaGetDevice(&dev);
+        if (ge != cudaSuccess) return ge;
+        std::lock_guard<std::mutex> lock(mu);
+        auto key = std::make_pair(sl.kernel, dev);
+        auto it = configured.find(key);
+        if (it == configured.end() || it->second < sl.smem) {
+            // the whole L1/shared array as shared memory, so that one CTA with
+            // its ring fits on every SM (the cooperative launch checks this)
+            cudaError_t e = cudaFuncSetAttribute(sl.kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                 (int)cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(sl.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.smem);
+            if (e != cudaSuccess) return e;
+            configured[key] = sl.smem;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sl.grid);
+    cfg.blockDim = dim3(sl.block);
+    cfg.dynamicSmemBytes = sl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {(void *)&p};
+    return cudaLaunchKernelExC(&cfg, sl.kernel, args);
+}
+
+}  // namespace qd

@@ -1,0 +1,103 @@
+// step.h - the persistent decode-step kernel: parameters shared by the host
+// planner (engine.cu) and the kernel (k_step.cu).
+//
+// One launch runs the whole decode step: for every layer the phases
+//   QKV  RMSNorm -> Q/K/V GEMV (+bias) -> per-head q/k norm + RoPE -> KV append
+//   ATTN split-K GQA attention over the paged cache + log-sum-exp combine
+//   O    o_proj GEMV + residual
+//   GU   RMSNorm -> gate/up GEMV -> SiLU * mul
+//   DOWN down GEMV + residual
+// and then LM (final RMSNorm -> LM head GEMV -> argmax).  One CTA per SM; a
+// phase waits for the phase it depends on through counters in device memory.
+#pragma once
+
+#include <cuda.h>
+
+#include "kernels.h"
+
+namespace qd {
+
+constexpr int kStepSlotBytes = 20480;     // one ring item (1024-byte multiple: swizzled boxes)
+constexpr int kStepResFloats = 2048;      // per-CTA row results of one phase
+constexpr int kStepMaxStageK = 18944;     // activations staged as fp16: K * 2 bytes ...
+constexpr int kStepMaxStageUnits = 768;   // ... then one fp32 scale per 16-byte weight unit
+constexpr int kStepStageBytes = kStepMaxStageK * 2 + kStepMaxStageUnits * 4;
+constexpr int kStepMaxSlots = 8;
+
+enum StepPhase : int { kPhQkv = 0, kPhAttn = 1, kPhO = 2, kPhGu = 3, kPhDown = 4, kPhLm = 5, kPhCount = 6 };
+
+// Step counters, per layer (zeroed by the last CTA of the step, so every step
+// starts from zero).
+constexpr int kSyncStride = 128;
+constexpr int kSyncHeadsDone = 96;   // [0, Hq + 2 Hkv): rows arrived per head; 96: heads finished
+constexpr int kSyncAttnCnt = 100;    // [100, 100 + Hkv): attention partials written per KV head
+constexpr int kSyncAttnDone = 120;   // attention CTAs that wrote their combined slice
+constexpr int kSyncODone = 121;      // CTAs past the o_proj epilogue
+constexpr int kSyncGuDone = 122;
+constexpr int kSyncDDone = 123;
+constexpr int kSyncMaxHeads = 96;
+constexpr int kSyncMaxKvHeads = 16;
+
+// Device error codes beyond kErr* of kernels.h.
+constexpr int kErrTimeout = 16;
+
+struct StepLayer {
+    const void *w[3], *s[3];     // q, k, v codes and scales
+    const uint16_t *b[3];        // q, k, v bias (bf16) or null
+    const void *wo, *so, *wg, *sg, *wu, *su, *wd, *sd;
+    const uint16_t *attn_norm, *mlp_norm, *q_norm, *k_norm;
+};
+
+// One GEMV phase as the CTAs split it.
+struct StepGeo {
+    int fmt;        // kFmtInt4 / kFmtInt8 / kFmtBf16
+    int N, K;       // output rows (GU: gate/up pairs) and inputs
+    int U;          // 16-byte units per row
+    int row_bytes;  // U * 16
+    int sr;         // INT4: bf16 scale bytes per row (K / 64); else 0
+    int rs;         // rows (GU: pairs) per ring item
+    int ks;         // consumer warps sharing one row (K split)
+    int rw;         // rows (GU: pairs) of an item per warp: 1, 2 or 4
+};
+
+struct StepParams {
+    CUtensorMap tm_k, tm_v;      // KV pools as 2-D [rows][d] bf16, 128-byte swizzled 16-row boxes
+    StepGeo geo[kPhCount];
+    const StepLayer *layers;     // [L], device memory
+    int L, h, Hq, Hkv, d, F, V;
+    float eps;
+    const uint16_t *embed, *final_norm;
+    const void *lm_w;
+    const float *lm_scale;       // INT8 LM head row scales or null
+    const int *page_table;
+    int n_pages;
+    const float2 *rope_cs;
+    uint16_t *k_pool, *v_pool;   // all layers [L][pages][Hkv][16][d]
+    DevState *st;
+    float *x, *raw, *q, *attn, *u, *logits;
+    float *part_o, *part_ml;     // attention partials [Hkv][P][G][d], [Hkv][P][G][2]
+    float *lm_val;
+    int *lm_idx;
+    int *sync;                   // [L][kSyncStride] + 1 (LM arrival)
+    int P;                       // attention splits per KV head (Hkv * P CTAs take part)
+    int n_slots;                 // ring items
+    int inflight;                // ring items a CTA may have in flight at once
+    unsigned long long *prof;    // null, or 5 L + 2 phase timestamps (CTA 0)
+    unsigned long long wait_ns;  // bound on every wait
+};
+
+// Host side (k_step.cu).
+struct StepLaunch {
+    const void *kernel = nullptr;
+    int grid = 0, block = 0;
+    size_t smem = 0;
+};
+// Chooses the instantiation and the launch shape; false if the model is outside
+// what the persistent kernel supports (the engine then runs the kernel chain).
+bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem, StepLaunch &out);
+cudaError_t step_encode_kv_maps(StepParams &p, size_t total_rows);
+cudaError_t launch_step(const StepLaunch &sl, const StepParams &p, cudaStream_t stream);
+// CTAs of the step kernel that fit on one SM (the launch needs >= 1).
+cudaError_t step_occupancy(const StepLaunch &sl, int *blocks_per_sm);
+
+}  // namespace qd

@@ -164,7 +164,8 @@ class Engine:
         L.check(self.lib.llm_truncate(self.h, int(n)), "llm_truncate")
 
     def profile_step(self):
-        """One greedy step with per-kernel CUDA-event timing -> array of ms (5L + 1)."""
+        """One greedy step timed per region (qkv, attention, o_proj, gate_up, down per layer, then
+        lm_head) -> array of ms (5L + 1)."""
         n_layers = self.cfg.n_layers
         out = np.empty(5 * n_layers + 1, dtype=np.float32)
         n = ctypes.c_int32()
@@ -174,6 +175,10 @@ class Engine:
 
     def set_pdl(self, on):
         L.check(self.lib.llm_set_pdl(self.h, int(bool(on))), "llm_set_pdl")
+
+    def set_persistent(self, on):
+        """True: the step is the persistent whole-step kernel; False: the kernel chain."""
+        L.check(self.lib.llm_set_persistent(self.h, int(bool(on))), "llm_set_persistent")
 
     def set_graph_mode(self, on):
         L.check(self.lib.llm_set_graph_mode(self.h, int(bool(on))), "llm_set_graph_mode")
