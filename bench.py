@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-ttft", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--profile-steps", type=int, default=4)
+    p.add_argument("--step", default="chain", choices=["chain", "persistent"],
+                   help="decode step as a kernel chain or as one persistent kernel")
     return p.parse_args()
 
 
@@ -241,7 +243,7 @@ def run_reference(args):
 
 def run_ours(args):
     import torch
-    from quantized_decode_gb300 import DeviceModel, Engine
+    from quantized_decode_gb300 import DeviceModel, Engine, LLMError
     from synth import model as sm
 
     ws, rank, local = dist_env()
@@ -262,6 +264,8 @@ def run_ours(args):
     lm_w = rec[4].get("w")
     stream = torch.cuda.Stream()
     eng = Engine(model, stream=stream.cuda_stream)
+    if args.step == "persistent":
+        eng.set_persistent(True)
     setup_s = time.perf_counter() - t_setup
 
     # ---- TTFT pp512 (prompt of seeded uniform token ids)
@@ -330,6 +334,21 @@ def run_ours(args):
     step_bytes = algorithmic_bytes(cfg, mean_T)
     step_gbs = step_bytes / (ms_per_token * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
+
+    # ---- the other step form (persistent kernel vs kernel chain), same cache and greedy chain
+    other_ms = None
+    try:
+        eng.set_persistent(args.step != "persistent")
+        s4, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        enqueue(10)
+        s4.record(stream)
+        enqueue(100)
+        e4.record(stream)
+        torch.cuda.synchronize()
+        other_ms = s4.elapsed_time(e4) / 100
+    except LLMError:
+        pass
+    eng.set_persistent(args.step == "persistent")
 
     # ---- graph replay with programmatic dependent launch (default is off)
     eng.set_pdl(True)
@@ -418,6 +437,8 @@ def run_ours(args):
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
         "eager_ms_per_token": round(eager_ms, 4),
         "graph_pdl_ms_per_token": round(pdl_ms, 4),
+        ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
+            None if other_ms is None else round(other_ms, 4),
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps * (5 * cfg.n_layers + 1) + extra,

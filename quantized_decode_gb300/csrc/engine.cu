@@ -271,7 +271,7 @@ int plan_step(llm_t *h, int n_sm) {
     p.lm_val = h->lm_part_val;
     p.lm_idx = h->lm_part_idx;
     p.wait_ns = 1000000000ull;  // 1 s: a step takes about a millisecond
-    p.inflight = 4;             // 64 KB a CTA: covers the HBM latency at the per-SM bandwidth
+    p.inflight = kStepMaxSlots; // ring items in flight: enough bytes to cover the HBM latency
     int max_smem = 0;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
         return LLM_ERR_CUDA;

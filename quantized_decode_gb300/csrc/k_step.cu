@@ -204,17 +204,21 @@ QD_DEV int seg_bound(const StepParams &p, int ph, int k) {
     return k == 0 ? 0 : (k == 1 ? b1 : (k == 2 ? b2 : N));
 }
 
-// Visit the ring items of the CTA's rows [r0, r1) of phase ph in order:
-// f(seg, local, n, j) for n rows starting at row `local` of matrix `seg`, the
-// first of them being the CTA's row j.  Producer and consumers both walk this.
+// GEMV ring items of the CTA's rows [r0, r1) of phase ph, in order: blocks
+// of up to kStepLines consecutive rows of one segment (gate/up: 2 consecutive
+// pairs, lines = gate, gate, up, up), each cut into nt K-tiles.
+// f(sg, local, nl, j, t): nl rows (pairs) from row `local` of segment sg, the
+// first being the CTA's row j, K-tile t.  Producer and consumers walk this.
 template <class Fn>
 QD_DEV void for_items(const StepParams &p, int ph, int r0, int r1, Fn &&f) {
-    const int rs = p.geo[ph].rs;
+    const int nt = p.geo[ph].nt;
+    const int rpb = ph == kPhGu ? kStepLines / 2 : kStepLines;
     const int nseg = ph == kPhQkv ? 3 : 1;
     for (int sg = 0; sg < nseg; ++sg) {
         const int b0 = seg_bound(p, ph, sg), b1 = seg_bound(p, ph, sg + 1);
         const int lo = max(r0, b0), hi = min(r1, b1);
-        for (int r = lo; r < hi; r += rs) f(sg, r - b0, min(rs, hi - r), r - r0);
+        for (int r = lo; r < hi; r += rpb)
+            for (int t = 0; t < nt; ++t) f(sg, r - b0, min(rpb, hi - r), r - r0, t);
     }
 }
 
@@ -233,29 +237,26 @@ QD_DEV SegMats seg_mats(const StepParams &p, const StepLayer &Ly, int ph, int sg
     }
 }
 
-// Byte layout of a GEMV ring item of n rows starting at matrix row `local`:
-// [codes A][codes B (gate/up only)][scales A][scales B]; INT4 scale blocks are
-// the 16-byte-aligned cover of the rows' scale bytes.
-struct ItemLayout {
-    int codes_b;   // offset of the second matrix's codes
-    int sc_a, sc_b;  // offset of row `local`'s scales (INT4)
-    int sc_lo, sc_bytes;
-    uint32_t total;
-};
-QD_DEV ItemLayout gemv_layout(const StepGeo &g, int local, int n, int m) {
-    ItemLayout L{};
-    L.codes_b = n * g.row_bytes;
-    const int codes_end = m * n * g.row_bytes;
-    L.total = (uint32_t)codes_end;
-    if (g.sr) {
-        const int lo = (local * g.sr) & ~15, hi = ((local + n) * g.sr + 15) & ~15;
-        L.sc_lo = lo;
-        L.sc_bytes = hi - lo;
-        L.sc_a = codes_end + (local * g.sr - lo);
-        L.sc_b = L.sc_a + L.sc_bytes;
-        L.total += (uint32_t)(m * L.sc_bytes);
+// Line i of an item: the matrix row it holds (gate/up: lines 0, 1 gate rows,
+// 2, 3 up rows of the same two pairs) and whether it exists (nl rows/pairs).
+QD_DEV bool item_line(int ph, int local, int nl, int i, int &row, bool &second) {
+    if (ph == kPhGu) {
+        second = i >= 2;
+        row = local + (i & 1);
+        return (i & 1) < nl;
     }
-    return L;
+    second = false;
+    row = local + i;
+    return i < nl;
+}
+// Bytes of K-tile t of a row, and (INT4) the 16-byte cover of its scales.
+QD_DEV int tile_bytes(const StepGeo &g, int t) { return min(g.tk, g.row_bytes - t * g.tk); }
+QD_DEV void tile_scale_cover(const StepGeo &g, int row, int t, int &lo, int &len, int &delta) {
+    const int start = row * g.sr + t * (g.tk / 32);
+    const int end = start + tile_bytes(g, t) / 32;
+    lo = start & ~15;
+    len = ((end + 15) & ~15) - lo;
+    delta = start - lo;
 }
 
 QD_DEV int pages_per_item(int d) { return kStepSlotBytes / (64 * d); }
@@ -272,8 +273,8 @@ struct Smem {
     uint8_t *ring;
     uint64_t *full, *empty;
     float *res;        // kStepResFloats; the attention phase reuses it
-    uint4 *stage;      // staged fp16 activations
-    float *post;       // per-unit scale of the staged activations
+    uint4 *stage;      // staged activations (mma B fragments)
+    float *corr;       // per-block offset corrections of the staged activations
     float *red;        // 64 floats of reduction scratch
     int *misc;         // [0] abort, [1..32] finished heads, [33] last-CTA flag
     StepLayer *layers; // copy of the per-layer pointer table
@@ -293,7 +294,7 @@ QD_DEV Smem carve(uint8_t *raw, int n_slots) {
     s.res = (float *)b;
     b += kStepResFloats * 4;
     s.stage = (uint4 *)b;
-    s.post = (float *)(b + kStepMaxStageK * 2);
+    s.corr = (float *)(b + kStepMaxStageK * 2);
     b += kStepStageBytes;
     s.red = (float *)b;
     b += 64 * 4;
@@ -341,6 +342,9 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
     volatile int *abort = s.misc;
     const int c = blockIdx.x, nc = gridDim.x;
     const int T = p.st->pos + 1;
+    // Kernel parameters used per item live in registers: every PTX statement
+    // below clobbers memory, which would otherwise reload them each time.
+    const int n_slots = p.n_slots, inflight = p.inflight;
     RingPos rp, landed;
     int issued = 0, n_landed = 0;
     const uint64_t pol = l2_evict_first();
@@ -354,9 +358,9 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
     auto claim = [&]() -> bool {
         int got = 1;
         if (lane == 0) {
-            while (got && issued - n_landed >= p.inflight) {
+            while (got && issued - n_landed >= inflight) {
                 got = wait_mbar(p, s.full + landed.slot, landed.par, abort);
-                landed.next(p.n_slots);
+                landed.next(n_slots);
                 ++n_landed;
             }
             if (got) got = wait_mbar(p, s.empty + rp.slot, rp.par ^ 1u, abort);
@@ -366,27 +370,43 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
         return got != 0;
     };
     auto gemv_items = [&](const StepLayer &Ly, int ph) {
-        const StepGeo &g = p.geo[ph];
-        const int m = ph == kPhGu ? 2 : 1;
+        const StepGeo g = p.geo[ph];
         int r0, r1;
         span(g.N, c, nc, r0, r1);
-        for_items(p, ph, r0, r1, [&](int sg, int local, int n, int) {
+        int msg = -1;
+        SegMats M{};
+        for_items(p, ph, r0, r1, [&](int sg, int local, int nl, int, int t) {
             if (!ok || !claim()) return;
-            if (lane == 0) {
-                const SegMats M = seg_mats(p, Ly, ph, sg);
-                uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
-                uint64_t *bar = s.full + rp.slot;
-                const ItemLayout L = gemv_layout(g, local, n, m);
-                const uint32_t cb = (uint32_t)(n * g.row_bytes);
-                mbar_expect_tx(bar, L.total);
-                bulk_g2s(dst, M.wa + (size_t)local * g.row_bytes, cb, bar, pol);
-                if (m == 2) bulk_g2s(dst + cb, M.wb + (size_t)local * g.row_bytes, cb, bar, pol);
-                if (g.sr) {
-                    bulk_g2s(dst + m * cb, M.sa + L.sc_lo, (uint32_t)L.sc_bytes, bar, pol);
-                    if (m == 2) bulk_g2s(dst + m * cb + L.sc_bytes, M.sb + L.sc_lo, (uint32_t)L.sc_bytes, bar, pol);
-                }
+            // lanes 0-3 copy the codes of line `lane`, lanes 4-7 its INT4 scales
+            if (sg != msg) {
+                M = seg_mats(p, Ly, ph, sg);
+                msg = sg;
             }
-            rp.next(p.n_slots);
+            uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
+            uint64_t *bar = s.full + rp.slot;
+            const int tb = tile_bytes(g, t);
+            uint32_t bytes = 0;
+            const int i = lane & 3;
+            int row;
+            bool second;
+            const bool valid = lane < 8 && item_line(ph, local, nl, i, row, second);
+            int lo = 0, len = 0, delta = 0;
+            if (valid && g.sr) tile_scale_cover(g, row, t, lo, len, delta);
+            if (valid) bytes = lane < 4 ? (uint32_t)tb : (uint32_t)len;
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+            if (lane == 0) mbar_expect_tx(bar, bytes);
+            __syncwarp();
+            if (valid) {
+                const uint8_t *w = second ? M.wb : M.wa;
+                const uint8_t *sc = second ? M.sb : M.sa;
+                if (lane < 4)
+                    bulk_g2s(dst + i * kStepLineStride, w + (size_t)row * g.row_bytes + (size_t)t * g.tk, (uint32_t)tb, bar,
+                             pol);
+                else if (len)
+                    bulk_g2s(dst + kStepLines * kStepLineStride + i * kStepScaleLine, sc + lo, (uint32_t)len, bar, pol);
+            }
+            rp.next(n_slots);
             ++issued;
         });
     };
@@ -429,7 +449,7 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
                         }
                     }
                 }
-                rp.next(p.n_slots);
+                rp.next(n_slots);
                 ++issued;
             }
         }
@@ -446,8 +466,8 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
     // Leave only once every copy this CTA issued has landed (bounded).
     if (lane == 0) {
         RingPos q = rp;
-        for (int k = 0; k < min(issued, p.n_slots); ++k) {
-            q.prev(p.n_slots);
+        for (int k = 0; k < min(issued, n_slots); ++k) {
+            q.prev(n_slots);
             const uint64_t t0 = gtimer();
             while (!mbar_try_wait(s.full + q.slot, q.par) && gtimer() - t0 < p.wait_ns) {
             }
@@ -456,33 +476,35 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// Consumers: activation fragments and the row loop.
+// Consumers: GEMV through mma.sync.
+//
+// An item (4 row-lines x one K-tile) is owned by one warp.  Its 16 mma rows
+// are the 4 lines x 4 K-parts of the tile (part p = blocks [p S, p S + S),
+// S = ceil(blocks / 4)); mma row m = part * 4 + line, so thread (gq, tq) feeds
+// line gq & 3 of parts gq >> 2 (A rows gq) and 2 + (gq >> 2) (A rows gq + 8),
+// and B column n holds the activations of part n.  The k order inside a block
+// is permuted the same way on both sides (thread tq takes the block's word /
+// quad tq), which leaves every dot product unchanged.  D[m][part(m)] is the
+// useful output: thread (gq, 0) holds line gq & 3 of part gq >> 2, thread
+// (gq, 1) of part 2 + (gq >> 2); two shuffles sum the parts of a line.
+//
+// Dequantization folds the code offset into the fp32 accumulator: INT4
+// nibbles n = c + 8 become fp16 1024 + n (low pairs) or 1024 + 16 n (high
+// pairs, met by activations pre-divided by 16), INT8 bytes c + 128 become
+// fp16 1024 + c + 128; the exact per-block sum of activation x offset
+// (`corr`) is subtracted in fp32.
 // ---------------------------------------------------------------------------
-template <int F>
-struct Fmt {
-    static constexpr int EPU = F == kFmtInt4 ? 32 : (F == kFmtInt8 ? 16 : 8);  // values per 16-byte unit
-    static constexpr int XC = F == kFmtBf16 ? 2 : EPU / 8;  // 16-byte registers per unit (fp16, or fp32 for bf16)
-    static constexpr int SC = EPU / 8;                      // staged 16-byte fp16 chunks per unit
-};
-
-// Chunk swizzle of the staged activations (INT4: 4 chunks per unit, INT8: 2).
-template <int F>
-QD_DEV int stage_swz(int u) {
-    return Fmt<F>::SC == 4 ? ((u >> 1) & 3) : (Fmt<F>::SC == 2 ? ((u >> 2) & 1) : 0);
+QD_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-// Scale `n` values by 2^-e (e from their max |v|) into fp16 pairs; returns 2^e.
-template <int N>
-QD_DEV float to_half_scaled(const float (&v)[N], uint32_t (&h)[N / 2]) {
-    float mx = 0.f;
-#pragma unroll
-    for (int i = 0; i < N; ++i) mx = fmaxf(mx, fabsf(v[i]));
-    int e = 0;
-    if (mx > 0.f) frexpf(mx, &e);
-    const float pre = ldexpf(1.f, -e);
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) h[i] = h2_as_u32(__floats2half2_rn(v[2 * i] * pre, v[2 * i + 1] * pre));
-    return ldexpf(1.f, e);
+QD_DEV void mma_bf16x4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 QD_DEV float4 ld_act4(const float *src32, const uint16_t *src16, int i) {
@@ -494,337 +516,232 @@ QD_DEV float4 ld_act4(const float *src32, const uint16_t *src16, int i) {
     return __ldcg(reinterpret_cast<const float4 *>(src32 + i));
 }
 
-// Stage a vector of K activations (fp32 src32, or bf16 src16) through shared
-// memory: optional RMSNorm with gain gamma, then per-unit power-of-two
-// scaling to fp16 (unit = the activations of one 16-byte weight unit).
-// Threads own units tid, tid + NCT, tid + 2 NCT and issue all their loads
-// at once; every consumer thread calls.
-template <int F, int NCW>
-QD_DEV void stage_smem(const StepParams &p, const Smem &s, const float *src32, const uint16_t *src16,
-                       const uint16_t *gamma, int K) {
-    using FM = Fmt<F>;
-    constexpr int NCT = NCW * 32;
-    constexpr int EPU = FM::EPU;
-    constexpr int UPT = 3;  // units per thread: U <= 3 * NCT
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int U = K / EPU;
-    float v[UPT][EPU];
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-        const int u = tid + j * NCT;
-#pragma unroll
-        for (int q = 0; q < EPU / 4; ++q) {
-            float4 f = u < U ? ld_act4(src32, src16, u * EPU + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[j][4 * q] = f.x;
-            v[j][4 * q + 1] = f.y;
-            v[j][4 * q + 2] = f.z;
-            v[j][4 * q + 3] = f.w;
-            ss += f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w;
-        }
+// Values per staged chunk: INT4 8 (one 32-bit word of codes), INT8 4, bf16 4.
+template <int F>
+constexpr int chunk_elems() {
+    return F == kFmtInt4 ? 8 : 4;
+}
+// INT4 staging slot of chunk c (unit u = c / 4, word t = c % 4, group g =
+// u / 4): units of odd groups are swapped pairwise so that the four parts of a
+// step, whose groups alternate in parity when S is odd, read different banks.
+QD_DEV int int4_chunk_slot(int c) {
+    const int u = c >> 2, g = u >> 2;
+    return ((u ^ (g & 1)) << 2) | (c & 3);
+}
+
+// Write chunk c of the (normalized) activations in B-fragment form and return
+// its offset sum for the block correction.
+template <int F>
+QD_DEV float emit_chunk(const Smem &s, int c, const float (&v)[chunk_elems<F>()]) {
+    if constexpr (F == kFmtInt4) {
+        // positions 2, 3, 6, 7 face the high-nibble pairs (x 16): store them / 16
+        const half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2] * 0.0625f, v[3] * 0.0625f);
+        const half2 h2 = __floats2half2_rn(v[4], v[5]), h3 = __floats2half2_rn(v[6] * 0.0625f, v[7] * 0.0625f);
+        s.stage[int4_chunk_slot(c)] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1), f2 = __half22float2(h2), f3 = __half22float2(h3);
+        return 1032.f * ((f0.x + f0.y) + (f2.x + f2.y)) + 1152.f * ((f1.x + f1.y) + (f3.x + f3.y));
+    } else if constexpr (F == kFmtInt8) {
+        const half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+        reinterpret_cast<uint2 *>(s.stage)[c] = make_uint2(h2_as_u32(h0), h2_as_u32(h1));
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+        return 1152.f * ((f0.x + f0.y) + (f1.x + f1.y));
+    } else {
+        uint32_t hi[2], lo[2];
+        split2(v[0], v[1], hi[0], lo[0]);
+        split2(v[2], v[3], hi[1], lo[1]);
+        s.stage[c] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+        return 0.f;
     }
-    float inv = 1.f;
+}
+
+// Stage K activations (fp32 src32, or bf16 src16) for the mma GEMV: optional
+// RMSNorm with gain gamma, then B-fragment chunks and per-block corrections
+// (s.corr[b]: INT4 per 128-code group, INT8 per 16-code block).  Every
+// consumer thread calls; ends with a barrier.
+template <int F, int NCW>
+QD_DEV void stage_mma(const StepParams &p, const Smem &s, const float *src32, const uint16_t *src16,
+                      const uint16_t *gamma, int K) {
+    constexpr int NCT = NCW * 32;
+    constexpr int CE = chunk_elems<F>();
+    constexpr int CPB = F == kFmtInt4 ? 16 : 4;  // chunks per correction block
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NC = K / CE;
+    auto load = [&](int c, float (&v)[CE]) {
+#pragma unroll
+        for (int q = 0; q < CE / 4; ++q) {
+            const float4 f = ld_act4(src32, src16, c * CE + 4 * q);
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+    };
+    // chunk sums -> one correction per block (CPB consecutive lanes)
+    auto emit = [&](int c, bool ok, const float (&v)[CE]) {
+        float e = ok ? emit_chunk<F>(s, c, v) : 0.f;
+        if constexpr (F != kFmtBf16) {
+#pragma unroll
+            for (int o = CPB / 2; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            if (ok && (c % CPB) == 0) s.corr[c / CPB] = e;
+        }
+    };
     if (gamma) {
+        // normalized vectors are at most 4096 long: keep them in registers across the reduction
+        constexpr int CPT = 4096 / CE / NCT;
+        float v[CPT][CE];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int c = tid + k * NCT;
+            if (c < NC) {
+                load(c, v[k]);
+#pragma unroll
+                for (int e = 0; e < CE; ++e) ss += v[k][e] * v[k][e];
+            }
+        }
         ss = warp_sum(ss);
         if (lane == 0) s.red[warp] = ss;
         cbar(NCT);
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) t += s.red[w];
-        inv = rsqrtf(t / (float)K + p.eps);
-    }
+        const float inv = rsqrtf(t / (float)K + p.eps);
 #pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-        const int u = tid + j * NCT;
-        if (u < U) {
-            if (gamma) {
+        for (int k = 0; k < CPT; ++k) {
+            const int c = tid + k * NCT;
+            const bool ok = c < NC;
+            if (ok) {
 #pragma unroll
-                for (int q = 0; q < EPU / 4; ++q) {
-                    const uint2 b = __ldg(reinterpret_cast<const uint2 *>(gamma + u * EPU + 4 * q));
-                    v[j][4 * q] *= __uint_as_float(b.x << 16) * inv;
-                    v[j][4 * q + 1] *= __uint_as_float(b.x & 0xFFFF0000u) * inv;
-                    v[j][4 * q + 2] *= __uint_as_float(b.y << 16) * inv;
-                    v[j][4 * q + 3] *= __uint_as_float(b.y & 0xFFFF0000u) * inv;
+                for (int q = 0; q < CE / 4; ++q) {
+                    const uint2 b = __ldg(reinterpret_cast<const uint2 *>(gamma + c * CE + 4 * q));
+                    v[k][4 * q] *= __uint_as_float(b.x << 16) * inv;
+                    v[k][4 * q + 1] *= __uint_as_float(b.x & 0xFFFF0000u) * inv;
+                    v[k][4 * q + 2] *= __uint_as_float(b.y << 16) * inv;
+                    v[k][4 * q + 3] *= __uint_as_float(b.y & 0xFFFF0000u) * inv;
                 }
             }
-            uint32_t h[EPU / 2];
-            s.post[u] = to_half_scaled<EPU>(v[j], h);
-#pragma unroll
-            for (int k = 0; k < FM::SC; ++k)
-                s.stage[u * FM::SC + (k ^ stage_swz<F>(u))] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+            emit(c, ok, v[k]);
+        }
+    } else {
+        for (int base = 0; base < NC; base += NCT) {
+            const int c = base + tid;
+            const bool ok = c < NC;
+            float v[CE];
+            if (ok) load(c, v);
+            emit(c, ok, v);
         }
     }
     cbar(NCT);
 }
 
-// One 16-byte weight unit against its staged activations, with four independent
-// accumulation chains (one per 32-bit word) so that a unit's products overlap.
-QD_DEV float int4_unit_dot4(uint4 q, const uint4 (&x)[4]) {
-    const half2 z = u32_as_h2(0u);
-    const half2 a = int4_word_dot(q.x, x[0], z), b = int4_word_dot(q.y, x[1], z);
-    const half2 c = int4_word_dot(q.z, x[2], z), d = int4_word_dot(q.w, x[3], z);
-    const float2 f = __half22float2(__hadd2(__hadd2(a, b), __hadd2(c, d)));
-    return f.x + f.y;
-}
-QD_DEV float int8_unit_dot4(uint4 q, const uint4 (&x)[2]) {
-    const half2 z = u32_as_h2(0u);
-    const half2 a = int8_word_dot(q.x, x[0].x, x[0].y, z), b = int8_word_dot(q.y, x[0].z, x[0].w, z);
-    const half2 c = int8_word_dot(q.z, x[1].x, x[1].y, z), d = int8_word_dot(q.w, x[1].z, x[1].w, z);
-    const float2 f = __half22float2(__hadd2(__hadd2(a, b), __hadd2(c, d)));
-    return f.x + f.y;
-}
-QD_DEV float bf16_unit_dot2(uint4 q, const float4 (&x)[2]) {
-    float2 p0 = make_float2(0.f, 0.f), p1 = make_float2(0.f, 0.f);
-    p0 = ffma2(make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)), make_float2(x[0].x, x[0].y), p0);
-    p1 = ffma2(make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)), make_float2(x[0].z, x[0].w), p1);
-    p0 = ffma2(make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)), make_float2(x[1].x, x[1].y), p0);
-    p1 = ffma2(make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)), make_float2(x[1].z, x[1].w), p1);
-    return (p0.x + p0.y) + (p1.x + p1.y);
-}
-
-// Sum each of v[0..7] over the 32 lanes; lane l ends with the total of
-// v[(l >> 2) & 7] (exchange halves at xor 16, 8, 4, then plain sums at 2, 1).
-QD_DEV float transpose_sum8(float (&v)[8], int lane) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool hi = lane & 16;
-        const float send = hi ? v[i] : v[i + 4], keep = hi ? v[i + 4] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool hi = lane & 8;
-        const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    {
-        const bool hi = lane & 4;
-        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    return v[0];
-}
-
-// Walks the ring items of the CTA's rows [r0, r1) of a phase in order (the
-// same sequence as for_items): n rows from row `local` of the current
-// segment, the first being the CTA's row j.
-struct ItemCursor {
-    int ph, r, hi, b0, sg, nseg, rs, r0;
-    QD_DEV ItemCursor(const StepParams &p, int ph_, int r0_, int r1_) {
-        ph = ph_;
-        r0 = r0_;
-        rs = p.geo[ph].rs;
-        nseg = ph == kPhQkv ? 3 : 1;
-        sg = -1;
-        hi = 0;
-        r = r0_;
-        b0 = 0;
-        advance(p, r1_);
-    }
-    // move to the next segment that holds rows of [r, r1)
-    QD_DEV void advance(const StepParams &p, int r1) {
-        while (r >= hi && sg + 1 < nseg) {
-            ++sg;
-            b0 = seg_bound(p, ph, sg);
-            const int e = seg_bound(p, ph, sg + 1);
-            r = max(r, b0);
-            hi = min(r1, e);
-        }
-    }
-    QD_DEV bool more() const { return r < hi; }
-    QD_DEV void next(const StepParams &p, int r1, int &local, int &n, int &j) {
-        local = r - b0;
-        n = min(rs, hi - r);
-        j = r - r0;
-        r += n;
-        if (r >= hi) advance(p, r1);
-    }
-};
-
-// One GEMV phase's ring items for this CTA, adding the row results into
-// s.res[j * OPR + o] (j = row - r0, o = gate/up for OPR = 2).  Rows go to warp
-// group j % NG (NG = NCW / ks, a power of two), RW rows of an item per warp;
-// within a group, warp kp takes units [kp * UPW, (kp + 1) * UPW) and its lanes
-// units ub + lane + 32 i.  A lane walks its units, takes the unit's staged
-// activations once (kept in registers for the whole phase when the lane has
-// a single unit) and multiplies them with the unit of each of its RW rows in
-// straight-line code (rows past the item's end read a valid row and are
-// dropped).  Items are taken in batches of up to kBatch, so that one pass of
-// barrier waits and releases serves several items.  Partial sums of 8 rows
-// are combined across the warp with one transposing shuffle tree.
-template <int F, int OPR, int RW, int NCW>
-QD_DEV RingPos gemv_core(const StepParams &p, const Smem &s, int ph, int r0, int r1, RingPos rp) {
-    using FM = Fmt<F>;
-    constexpr int kBatch = 4;
+// The warp-owned GEMV items of one phase: adds each item's line totals into
+// s.res[j * opr + o] (j = row - r0; o = 0 gate / 1 up for gate/up).  Items go
+// to the consumer warps round-robin; a warp only waits for and releases its
+// own items.  Returns the ring position after the phase.
+template <int F, int NCW>
+QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int r1, RingPos rp) {
     volatile int *abort = s.misc;
-    const StepGeo &g = p.geo[ph];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NG = NCW / g.ks, grp = warp / g.ks, kp = warp % g.ks;
-    const int upw = (g.U + g.ks - 1) / g.ks;
-    const int ub = kp * upw, ue = min(g.U, ub + upw);
-    const int nu = ue - ub > lane ? (ue - ub - lane + 31) / 32 : 0;  // this lane's units
-    const bool one = upw <= 32;                                      // at most one unit per lane
-    const int row_bytes = g.row_bytes, sr = g.sr, n_slots = p.n_slots;
-    auto load_x = [&](int u, uint4 (&xr)[FM::XC], float &post) {
-        post = s.post[u];
-        if constexpr (F == kFmtBf16) {
-            const uint4 hv = s.stage[u];
-            const float2 a = __half22float2(u32_as_h2(hv.x)), b = __half22float2(u32_as_h2(hv.y));
-            const float2 c = __half22float2(u32_as_h2(hv.z)), d = __half22float2(u32_as_h2(hv.w));
-            xr[0] = make_uint4(__float_as_uint(a.x * post), __float_as_uint(a.y * post), __float_as_uint(b.x * post),
-                               __float_as_uint(b.y * post));
-            xr[1] = make_uint4(__float_as_uint(c.x * post), __float_as_uint(c.y * post), __float_as_uint(d.x * post),
-                               __float_as_uint(d.y * post));
-        } else {
-#pragma unroll
-            for (int k = 0; k < FM::XC; ++k) xr[k] = s.stage[u * FM::SC + (k ^ stage_swz<F>(u))];
-        }
-    };
-    uint4 x1[FM::XC];
-    float post1 = 0.f;
-    if (one && nu > 0) load_x(ub + lane, x1, post1);
-
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    int n_rows = 0, pend = 0;  // rows this warp finished; rows in acc
-    auto flush = [&]() {
-        const float t = transpose_sum8(acc, lane);
-        const int vi = (lane >> 2) & 7;
-        if ((lane & 3) == 0 && vi >= 8 - pend * OPR) {
-            const int ord = n_rows - (8 - vi + OPR - 1) / OPR;  // this value's row among the warp's rows
-            const int j = grp + ord * NG;
-            atomicAdd(s.res + j * OPR + (OPR == 2 ? (vi & 1) : 0), t);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        pend = 0;
-    };
-    // Row dot products of one item: pa[r] (and pb[r], gate/up) for rows q[r].
-    auto item_dot = [&](const uint8_t *item, int local, int n, int q0, float (&pa)[RW], float (&pb)[RW]) {
-        const ItemLayout L = gemv_layout(g, local, n, OPR);
-        int qr[RW];
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            qr[r] = min(q0 + r * NG, n - 1);
-            pa[r] = pb[r] = 0.f;
-        }
-        auto dot = [&](const uint8_t *codes, int sc_off, int q, int u, const uint4 (&xr)[FM::XC], float post) -> float {
-            const uint4 w = *reinterpret_cast<const uint4 *>(codes + q * row_bytes + u * 16);
+    const StepGeo g = p.geo[ph];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+    const int line = gq & 3, pa = gq >> 2, pb = 2 + (gq >> 2);
+    const int xpart = gq < 4 ? gq : 0;  // B column gq = part gq (columns 4-7 unused)
+    const int n_slots = p.n_slots, bb = g.bb;
+    const int bpt = g.tk / bb;          // blocks in a full tile
+    int k = 0;
+    for_items(p, ph, r0, r1, [&](int, int local, int nl, int jf, int t) {
+        const RingPos q = rp;
+        rp.next(n_slots);
+        if ((k++ % NCW) != warp) return;
+        const bool have = __all_sync(0xffffffffu, wait_mbar(p, s.full + q.slot, q.par, abort));
+        const uint8_t *item = s.ring + (size_t)q.slot * kStepSlotBytes;
+        const uint8_t *ln = item + line * kStepLineStride;
+        int row;
+        bool second;
+        const bool lvalid = item_line(ph, local, nl, line, row, second);
+        const int nb = tile_bytes(g, t) / bb;  // blocks in this tile
+        const int S = (nb + 3) >> 2;
+        const int b0 = t * bpt;                // first block of the tile in the row
+        const int mypart = tq == 0 ? pa : pb;
+        float acc = 0.f;
+        if (have) {
             if constexpr (F == kFmtInt4) {
-                const float sv = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(item + sc_off + q * sr)[u >> 2]);
-                return int4_unit_dot4(w, xr) * (sv * post);
-            } else if constexpr (F == kFmtInt8) {
-                return int8_unit_dot4(w, xr) * post;
-            } else {
-                const float4 xf[2] = {make_float4(__uint_as_float(xr[0].x), __uint_as_float(xr[0].y),
-                                                  __uint_as_float(xr[0].z), __uint_as_float(xr[0].w)),
-                                      make_float4(__uint_as_float(xr[1].x), __uint_as_float(xr[1].y),
-                                                  __uint_as_float(xr[1].z), __uint_as_float(xr[1].w))};
-                return bf16_unit_dot2(w, xf);
-            }
-        };
-        auto unit = [&](int u, const uint4 (&xr)[FM::XC], float post) {
+                int lo, len, delta;
+                tile_scale_cover(g, row, t, lo, len, delta);
+                const uint16_t *scl = reinterpret_cast<const uint16_t *>(item + kStepLines * kStepLineStride +
+                                                                         line * kStepScaleLine + delta);
+#pragma unroll 2
+                for (int st = 0; st < S; ++st) {
+                    const int ba = min(pa * S + st, nb - 1), bq = min(pb * S + st, nb - 1);
+                    const int bx = xpart * S + st;
+                    const bool xok = bx < nb;
+                    const int gx = b0 + min(bx, nb - 1);
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                pa[r] += dot(item, L.sc_a, qr[r], u, xr, post);
-                if constexpr (OPR == 2) pb[r] += dot(item + L.codes_b, L.sc_b, qr[r], u, xr, post);
-            }
-        };
-        if (one) {
-            if (nu > 0) unit(ub + lane, x1, post1);
-        } else {
-            for (int i = 0; i < nu; ++i) {
-                const int u = ub + lane + 32 * i;
-                uint4 xr[FM::XC];
-                float post;
-                load_x(u, xr, post);
-                unit(u, xr, post);
-            }
-        }
-    };
-
-    ItemCursor cur(p, ph, r0, r1);
-    while (cur.more()) {
-        const ItemCursor batch = cur;  // replayed below to revisit the batch's items
-        int nb = 0;
-        for (; nb < kBatch && cur.more(); ++nb) {
-            int l0, n0, j0;
-            cur.next(p, r1, l0, n0, j0);
-        }
-        // all lanes observe the phases (acquiring the copied bytes); the warp
-        // skips the batch together if any lane's wait ran out
-        bool ok = true;
-        {
-            RingPos q = rp;
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                if (b < nb) {
-                    ok = wait_mbar(p, s.full + q.slot, q.par, abort) && ok;
-                    q.next(n_slots);
-                }
-            }
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        RingPos q = rp;
-        ItemCursor ic = batch;
-#pragma unroll 1
-        for (int b = 0; b < nb; ++b) {
-            int local, n, jf;
-            ic.next(p, r1, local, n, jf);
-            const int q0 = (grp - jf) & (NG - 1);
-            const int rw = ok && q0 < n ? (n - 1 - q0) / NG + 1 : 0;
-            if (rw > 0) {
-                float pa[RW], pb[RW];
-                item_dot(s.ring + (size_t)q.slot * kStepSlotBytes, local, n, q0, pa, pb);
-                if ((pend + rw) * OPR > 8) flush();
-#pragma unroll
-                for (int r = 0; r < RW; ++r) {
-                    if (r < rw) {
-#pragma unroll
-                        for (int i = 0; i < 8 - OPR; ++i) acc[i] = acc[i + OPR];
-                        if constexpr (OPR == 2) {
-                            acc[6] = pa[r];
-                            acc[7] = pb[r];
-                        } else {
-                            acc[7] = pa[r];
-                        }
-                        ++n_rows;
-                        ++pend;
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(ln + ba * 64 + j * 16 + tq * 4);
+                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(ln + bq * 64 + j * 16 + tq * 4);
+                        uint4 xv = s.stage[int4_chunk_slot((gx * 4 + j) * 4 + tq)];
+                        if (!xok) xv = make_uint4(0, 0, 0, 0);
+                        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                        mma_f16(d, lop3_and_xor(wa, 0x000F000Fu, 0x64086408u), lop3_and_xor(wb, 0x000F000Fu, 0x64086408u),
+                                lop3_and_xor(wa, 0x00F000F0u, 0x64806480u), lop3_and_xor(wb, 0x00F000F0u, 0x64806480u),
+                                xv.x, xv.y);
+                        mma_f16(d, lop3_and_xor(wa8, 0x000F000Fu, 0x64086408u), lop3_and_xor(wb8, 0x000F000Fu, 0x64086408u),
+                                lop3_and_xor(wa8, 0x00F000F0u, 0x64806480u), lop3_and_xor(wb8, 0x00F000F0u, 0x64806480u),
+                                xv.z, xv.w);
+                    }
+                    const int bm = mypart * S + st;  // this thread's block (unclamped)
+                    const float v = tq == 0 ? (pa ? d[1] : d[0]) : (pb == 3 ? d[3] : d[2]);
+                    if (tq < 2 && bm < nb) {
+                        const float sv = bf16_bits_to_float(scl[bm]);
+                        acc = fmaf(v - s.corr[b0 + bm], sv, acc);
                     }
                 }
+            } else if constexpr (F == kFmtInt8) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f}, cor = 0.f;
+#pragma unroll 4
+                for (int st = 0; st < S; ++st) {
+                    const int ba = min(pa * S + st, nb - 1), bq = min(pb * S + st, nb - 1);
+                    const int bx = xpart * S + st;
+                    uint2 xv = reinterpret_cast<const uint2 *>(s.stage)[(b0 + min(bx, nb - 1)) * 4 + tq];
+                    if (bx >= nb) xv = make_uint2(0, 0);
+                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(ln + ba * 16 + tq * 4) ^ 0x80808080u;
+                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(ln + bq * 16 + tq * 4) ^ 0x80808080u;
+                    mma_f16(d, prmt(wa, 0x64646464u, 0x4140u), prmt(wb, 0x64646464u, 0x4140u),
+                            prmt(wa, 0x64646464u, 0x4342u), prmt(wb, 0x64646464u, 0x4342u), xv.x, xv.y);
+                    const int bm = mypart * S + st;
+                    if (bm < nb) cor += s.corr[b0 + bm];
+                }
+                const float v = tq == 0 ? (pa ? d[1] : d[0]) : (pb == 3 ? d[3] : d[2]);
+                if (tq < 2) acc = v - cor;
+            } else {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int st = 0; st < S; ++st) {
+                    const int ba = min(pa * S + st, nb - 1), bq = min(pb * S + st, nb - 1);
+                    const int bx = xpart * S + st;
+                    uint4 xv = s.stage[(b0 + min(bx, nb - 1)) * 4 + tq];
+                    if (bx >= nb) xv = make_uint4(0, 0, 0, 0);
+                    const uint2 wa = *reinterpret_cast<const uint2 *>(ln + ba * 32 + tq * 8);
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(ln + bq * 32 + tq * 8);
+                    mma_bf16x4(d, wa.x, wb.x, wa.y, wb.y, xv.x, xv.y);
+                    mma_bf16x4(d, wa.x, wb.x, wa.y, wb.y, xv.z, xv.w);
+                }
+                const float v = tq == 0 ? (pa ? d[1] : d[0]) : (pb == 3 ? d[3] : d[2]);
+                if (tq < 2) acc = v;
             }
-            q.next(n_slots);
+        }
+        // line total: parts 0/1 (gq, gq + 4) and the tq 0/1 halves
+        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (have && tq == 0 && gq < 4 && lvalid) {
+            const int j = jf + (ph == kPhGu ? (line & 1) : line);
+            atomicAdd(s.res + (ph == kPhGu ? 2 * j + (second ? 1 : 0) : j), acc);
         }
         __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                if (b < nb) {
-                    mbar_arrive(s.empty + rp.slot);
-                    rp.next(n_slots);
-                }
-            }
-        }
-        rp = RingPos{__shfl_sync(0xffffffffu, rp.slot, 0), __shfl_sync(0xffffffffu, rp.par, 0)};
-    }
-    if (pend) flush();
+        if (lane == 0) mbar_arrive(s.empty + q.slot);
+    });
     return rp;
-}
-
-// Dispatch on the rows per warp and item chosen by the host planner.
-template <int F, int OPR, int NCW>
-QD_DEV RingPos gemv_rows(const StepParams &p, const Smem &s, int ph, int r0, int r1, RingPos rp) {
-    const int rw = p.geo[ph].rw;
-    if constexpr (OPR == 2) {
-        return rw >= 2 ? gemv_core<F, 2, 2, NCW>(p, s, ph, r0, r1, rp) : gemv_core<F, 2, 1, NCW>(p, s, ph, r0, r1, rp);
-    } else {
-        if (rw >= 4) return gemv_core<F, 1, 4, NCW>(p, s, ph, r0, r1, rp);
-        if (rw == 2) return gemv_core<F, 1, 2, NCW>(p, s, ph, r0, r1, rp);
-        return gemv_core<F, 1, 1, NCW>(p, s, ph, r0, r1, rp);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -949,13 +866,15 @@ QD_DEV bool phase_attn(Ctx<NCW> &x, int l) {
     for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = 0.f;
     float z2 = 0.f, z3 = 0.f;
     const int ppi = pages_per_item(DH);
+    int item = 0;
     for (int pa = pa0; pa < pa1; pa += ppi) {
         const int np = min(ppi, pa1 - pa);
         const int slot = x.rp.slot;
-        const bool have = __all_sync(0xffffffffu, wait_mbar(p, x.s.full + slot, x.rp.par, x.abort));
+        const uint32_t par = x.rp.par;
+        x.rp.next(p.n_slots);
+        if ((item++ % NCW) != warp) continue;  // each item belongs to one warp
+        const bool have = __all_sync(0xffffffffu, wait_mbar(p, x.s.full + slot, par, x.abort));
         for (int k = 0; have && k < np; ++k) {
-            const int i = pa - pa0 + k;
-            if (i % NCW != warp) continue;
             const int pg = pa + k;
             uint8_t *kb = x.s.ring + (size_t)slot * kStepSlotBytes + (size_t)k * PB;
             uint8_t *vb = kb + (DH / 64) * 2048;
@@ -1034,7 +953,6 @@ QD_DEV bool phase_attn(Ctx<NCW> &x, int l) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(x.s.empty + slot);
-        x.rp.next(p.n_slots);
     }
     // ---- merge the warps: common max, then rescaled sums in shared memory
     if (tq == 0 && gq < G) s_m[warp * 8 + gq] = m;
@@ -1149,8 +1067,8 @@ QD_DEV bool layer_gemv(Ctx<NCW> &x, int l, int ph) {
     const float *src = ph == kPhO ? p.attn : (ph == kPhDown ? p.u : p.x);
     const uint16_t *src16 = ph == kPhQkv && l == 0 ? p.embed + (size_t)x.token * p.h : nullptr;
     const uint16_t *gamma = ph == kPhQkv ? Ly->attn_norm : (ph == kPhGu ? Ly->mlp_norm : nullptr);
-    stage_smem<WF, NCW>(p, x.s, src, src16, gamma, g.K);
-    x.rp = opr == 2 ? gemv_rows<WF, 2, NCW>(p, x.s, ph, r0, r1, x.rp) : gemv_rows<WF, 1, NCW>(p, x.s, ph, r0, r1, x.rp);
+    stage_mma<WF, NCW>(p, x.s, src, src16, gamma, g.K);
+    x.rp = gemv_mma<WF, NCW>(p, x.s, ph, r0, r1, x.rp);
     if (cbar_or(*x.abort, x.NCT)) return false;
     if (ph == kPhQkv) {
         for (int j = x.tid; j < r1 - r0; j += x.NCT) {
@@ -1215,8 +1133,8 @@ QD_DEV void phase_lm(Ctx<NCW> &x, const StepLayer *Ly0) {
     span(g.N, x.c, x.nc, r0, r1);
     for (int j = x.tid; j < r1 - r0; j += x.NCT) x.s.res[j] = 0.f;
     if (!x.dep(x.sync_at(p.L - 1, kSyncDDone), x.nc)) return;
-    stage_smem<LMF, NCW>(p, x.s, p.x, nullptr, p.final_norm, g.K);
-    x.rp = gemv_rows<LMF, 1, NCW>(p, x.s, kPhLm, r0, r1, x.rp);
+    stage_mma<LMF, NCW>(p, x.s, p.x, nullptr, p.final_norm, g.K);
+    x.rp = gemv_mma<LMF, NCW>(p, x.s, kPhLm, r0, r1, x.rp);
     if (cbar_or(*x.abort, x.NCT)) return;
     float best = -INFINITY;
     int bi = 0x7fffffff;
@@ -1311,7 +1229,7 @@ __global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < p.n_slots; ++i) {
             mbar_init(s.full + i, 1);
-            mbar_init(s.empty + i, NCW);
+            mbar_init(s.empty + i, 1);  // each item is released by the one warp that owns it
         }
         s.misc[0] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1376,6 +1294,7 @@ bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem
     if (G > 8 || n_sm < p.Hkv) return false;
     p.P = n_sm / p.Hkv;
     if (p.P * G + 8 + p.d * G > kStepResFloats || p.P * G * 4 > kStepStageBytes) return false;
+    if (n_sm % p.Hkv) return false;  // every CTA takes part in attention
     int n_slots = kStepMaxSlots;
     while (n_slots > 2 && smem_bytes(n_slots, p.L) > (size_t)max_smem) --n_slots;
     if (smem_bytes(n_slots, p.L) > (size_t)max_smem || n_slots < 4) return false;
@@ -1387,48 +1306,22 @@ bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem
         g.fmt = fmt;
         g.N = N;
         g.K = K;
-        const int epu = fmt == kFmtInt4 ? 32 : (fmt == kFmtInt8 ? 16 : 8);
-        if (K % epu || (fmt == kFmtInt4 && K % kGroup)) return false;
-        g.U = K / epu;
-        g.row_bytes = g.U * 16;
-        g.sr = fmt == kFmtInt4 ? K / 64 : 0;
-        const int m = pairs ? 2 : 1;
-        if (K > kStepMaxStageK || g.U > kStepMaxStageUnits) return false;
-        // rows per item: codes plus the aligned cover of their scales
-        int rs_max = 0;
-        for (int n = 1; n <= 64; ++n) {
-            const int sc = g.sr ? ((n * g.sr + 15) / 16 + 1) * 16 : 0;
-            if (m * (n * g.row_bytes + sc) <= kStepSlotBytes) rs_max = n;
-        }
-        if (rs_max == 0) return false;
-        // K split (ks warps per row, NG = 8 / ks row groups) and rows per item
-        // (n, so rw = ceil(n / NG) rows per warp): a warp spends about
-        // iters * (rw * m + 1/4) unit products per item (iters = its lanes'
-        // unit count; the quarter is the activation load) plus a fixed
-        // overhead; take the most bytes per cost.
-        double best = -1.0;
-        g.ks = 0;
-        for (int ks = 1; ks <= kNcw; ks *= 2) {
-            const int NG = kNcw / ks;
-            const int upw = (g.U + ks - 1) / ks, iters = (upw + 31) / 32;
-            for (int n = 1; n <= rs_max; ++n) {
-                const int rw = (n + NG - 1) / NG;
-                if (rw != 1 && rw != 2 && !(rw == 4 && m == 1)) continue;
-                const double cost = iters * (rw * m + 0.25) + 1.0;
-                const double score = (double)n * g.row_bytes * m / cost;
-                if (score > best + 1e-9) {
-                    best = score;
-                    g.ks = ks;
-                    g.rw = rw;
-                    g.rs = n;
-                }
-            }
-        }
-        if (!g.ks) return false;
         (void)norm;
+        // mma blocks: INT4 one 128-code group (64 bytes), INT8 16 codes, bf16 16 values
+        if (fmt == kFmtInt4 ? K % kGroup : K % 16) return false;
+        if (K > kStepMaxStageK || (norm && K > 4096)) return false;
+        if (fmt == kFmtBf16 && K * 4 > kStepMaxStageK * 2) return false;  // hi + lo pairs
+        if (fmt == kFmtInt8 && K / 16 > 768) return false;                 // corrections per block
+        g.row_bytes = fmt == kFmtInt4 ? K / 2 : (fmt == kFmtInt8 ? K : 2 * K);
+        g.sr = fmt == kFmtInt4 ? K / 64 : 0;
+        g.bb = fmt == kFmtInt4 ? 64 : (fmt == kFmtInt8 ? 16 : 32);
+        g.tk = g.row_bytes < kStepTileBytes ? g.row_bytes : kStepTileBytes / g.bb * g.bb;
+        g.nt = (g.row_bytes + g.tk - 1) / g.tk;
+        const int sc = g.sr ? kStepLines * kStepScaleLine : 0;
+        if (kStepLines * kStepLineStride + sc > kStepSlotBytes) return false;
         // per-CTA rows must fit the result buffer
         const long long rows = ((long long)N + n_sm - 1) / n_sm;
-        if (rows * m > kStepResFloats) return false;
+        if (rows * (pairs ? 2 : 1) > kStepResFloats) return false;
         return true;
     };
     const int rq = p.Hq * p.d, rkv = p.Hkv * p.d;

@@ -17,12 +17,20 @@
 
 namespace qd {
 
-constexpr int kStepSlotBytes = 20480;     // one ring item (1024-byte multiple: swizzled boxes)
+constexpr int kStepSlotBytes = 8192;      // one ring item (1024-byte multiple: swizzled boxes)
 constexpr int kStepResFloats = 2048;      // per-CTA row results of one phase
-constexpr int kStepMaxStageK = 18944;     // activations staged as fp16: K * 2 bytes ...
-constexpr int kStepMaxStageUnits = 768;   // ... then one fp32 scale per 16-byte weight unit
-constexpr int kStepStageBytes = kStepMaxStageK * 2 + kStepMaxStageUnits * 4;
-constexpr int kStepMaxSlots = 8;
+constexpr int kStepMaxSlots = 20;
+// A GEMV ring item is kStepLines row-lines of one K-tile of up to
+// kStepTileBytes bytes a row, each line at a padded shared-memory stride, then
+// (INT4) the 16-byte-aligned cover of each line's scales.
+constexpr int kStepLines = 4;
+constexpr int kStepTileBytes = 1792;
+constexpr int kStepLineStride = kStepTileBytes + 16;
+constexpr int kStepScaleLine = 96;
+// Staged activations: fp16 (INT4/INT8 weights) or bf16 hi/lo pairs (bf16
+// weights) laid out as mma B fragments, then one fp32 correction per block.
+constexpr int kStepMaxStageK = 18944;
+constexpr int kStepStageBytes = kStepMaxStageK * 2 + 768 * 4;
 
 enum StepPhase : int { kPhQkv = 0, kPhAttn = 1, kPhO = 2, kPhGu = 3, kPhDown = 4, kPhLm = 5, kPhCount = 6 };
 
@@ -52,12 +60,11 @@ struct StepLayer {
 struct StepGeo {
     int fmt;        // kFmtInt4 / kFmtInt8 / kFmtBf16
     int N, K;       // output rows (GU: gate/up pairs) and inputs
-    int U;          // 16-byte units per row
-    int row_bytes;  // U * 16
+    int row_bytes;  // bytes of one weight row
     int sr;         // INT4: bf16 scale bytes per row (K / 64); else 0
-    int rs;         // rows (GU: pairs) per ring item
-    int ks;         // consumer warps sharing one row (K split)
-    int rw;         // rows (GU: pairs) of an item per warp: 1, 2 or 4
+    int tk;         // bytes of one row in a K-tile (<= kStepTileBytes)
+    int nt;         // K-tiles per row
+    int bb;         // bytes of one mma block of a row: INT4 64 (128 codes), INT8 16, bf16 32
 };
 
 struct StepParams {
