@@ -128,8 +128,12 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
 
 /* Run the prompt tokens[0..n-1] (HOST array) at positions seq_len..seq_len+n-1,
  * filling the KV cache, and return the greedy next token in *first_token
- * (HOST).  Blocks until done.  Errors: LLM_ERR_ARG (n <= 0, token out of range),
- * LLM_ERR_CONTEXT_FULL, LLM_ERR_CUDA, LLM_ERR_DEVICE.                       */
+ * (HOST).  Blocks until done.  Prompts of 2 or more tokens run as one batch
+ * on the tensor cores (llm_set_prefill_batched); the first such call
+ * allocates the batch workspace (up to 1024 rows of activations plus one fp16
+ * copy of the largest weight matrix, 2 * mlp * hidden * 2 bytes).  Errors:
+ * LLM_ERR_ARG (n <= 0, token out of range), LLM_ERR_CONTEXT_FULL,
+ * LLM_ERR_CUDA, LLM_ERR_DEVICE.                                             */
 int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token);
 
 /* One decode step by graph replay.  The step consumes `forced_input` when it
@@ -202,6 +206,18 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph);
  * first.  Errors: LLM_ERR_ARG (null handle, or 1 for a model outside the
  * persistent kernel's shapes), LLM_ERR_CUDA.                                */
 int llm_set_persistent(llm_t *h, int32_t on);
+
+/* Prefill mode for prompts of 2 or more tokens.  1 (default where the model's
+ * shapes allow it): the prompt runs as a batch -- per layer RMSNorm, weight
+ * matrices dequantized to fp16 and multiplied on the tcgen05 tensor cores
+ * (fp32 accumulate), causal attention over the paged cache, and the LM head on
+ * the last row only ("Bare-Metal LLM Inference on NVIDIA H100": prefill is a
+ * compute-bound GEMM phase).  0: the prompt is fed through the decode step one
+ * token at a time.  Both give the same cache and first token within the
+ * acceptance tolerance.  Errors: LLM_ERR_ARG (null handle, or 1 for a model
+ * whose shapes the batched path does not take: (Hq + 2 Hkv) d and hidden must
+ * be multiples of 128, mlp of 64).                                          */
+int llm_set_prefill_batched(llm_t *h, int32_t on);
 
 /* 1: consecutive kernels of the step are launched with programmatic dependent
  * launch (a kernel's CTAs may start before the previous kernel ends and wait

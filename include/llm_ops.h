@@ -74,6 +74,24 @@ int llm_op_attention_noalloc(const float *q, const void *k_pool, const void *v_p
                              const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv,
                              int32_t d, int32_t n_splits, float *out, void *stream);
 
+/* Weight dequantization for the batched prefill ("Bare-Metal LLM Inference on
+ * NVIDIA H100", prefill path: dequantized tiles feed the tensor cores):
+ * out[n][k] = fp16(code[n][k] * scale).  fmt 1 = INT4 group-128 (w: layout
+ * LLM_LAYOUT_INT4_VALUESHUFFLE words [N][K/8], s: bf16 [N][K/128]; every INT4
+ * weight is exact in fp16 while its scale is at least 2^-14), fmt 2 = INT8 per
+ * row (w: int8 [N][K], s: fp32 [N]; rounded to nearest fp16).  out: fp16
+ * [N][K], 16-byte aligned.  K % 128 == 0 (INT4) or K % 8 == 0 (INT8).       */
+int llm_op_dequant_f16(int32_t fmt, const void *w, const void *s, int32_t N, int32_t K, void *out,
+                       void *stream);
+
+/* C[m][n] = sum_k A[m][k] * B[n][k] on the tcgen05 tensor cores: fp16 operands
+ * staged by TMA, fp32 accumulation in tensor memory (the prefill GEMM).  A: fp16
+ * [M][K], B: fp16 [N][K], both row-major and 16-byte aligned; C: fp32 [M][N].
+ * M >= 1, N % 128 == 0, K % 64 == 0.  A wait inside the kernel that runs out
+ * (1 s; only a stalled GPU) leaves C undefined.                               */
+int llm_op_gemm_f16(const void *A, const void *B, int32_t M, int32_t N, int32_t K, float *C,
+                    void *stream);
+
 #ifdef __cplusplus
 }
 #endif

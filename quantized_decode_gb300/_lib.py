@@ -68,6 +68,7 @@ SIGNATURES = {
     "llm_set_graph_mode": (i32, [vp, i32]),
     "llm_set_pdl": (i32, [vp, i32]),
     "llm_set_persistent": (i32, [vp, i32]),
+    "llm_set_prefill_batched": (i32, [vp, i32]),
     "llm_pack_int4_g128": (i32, [vp, i64, i64, vp]),
     "llm_pack_int8_row": (i32, [vp, i64, i64, vp]),
     "llm_op_gemv_int4": (i32, [vp, vp, vp, i32, i32, vp, vp, vp]),
@@ -75,6 +76,8 @@ SIGNATURES = {
     "llm_op_lm_head_argmax": (i32, [vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]),
     "llm_op_attention": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
     "llm_op_attention_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "llm_op_dequant_f16": (i32, [i32, vp, vp, i32, i32, vp, vp]),
+    "llm_op_gemm_f16": (i32, [vp, vp, i32, i32, i32, vp, vp]),
 }
 
 _lib = None

@@ -12,6 +12,7 @@
 // To Construct Your Personal LLM Runtime From Scratch", §6); the page for
 // position pos is page_table[pos/16], read on the device, so no host-side
 // branch on page boundaries is needed.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -20,6 +21,7 @@
 
 #include "../../include/llm.h"
 #include "kernels.h"
+#include "prefill.h"
 #include "step.h"
 
 using namespace qd;
@@ -56,6 +58,16 @@ struct llm_t {
     int *step_sync = nullptr;
     unsigned long long *prof = nullptr;
 
+    // batched prefill (tcgen05 GEMMs); buffers allocated by the first call
+    bool pf_ok = false;         // the model's shapes fit the GEMM path
+    bool pf_batched = true;     // llm_set_prefill_batched
+    bool pf_ready = false;
+    int pf_rows = 0;            // prompt rows per chunk
+    float *pf_x = nullptr, *pf_raw = nullptr;
+    uint16_t *pf_a = nullptr, *pf_u = nullptr, *pf_qh = nullptr, *pf_ql = nullptr, *pf_w = nullptr;
+    int *pf_tok = nullptr;
+    CUtensorMap pf_map_ah{}, pf_map_aq{}, pf_map_u{}, pf_map_wqkv{}, pf_map_wo{}, pf_map_wgu{}, pf_map_wd{};
+
     int32_t *pinned = nullptr;  // host staging: [0] forced token, [2..3] last_token, err
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -86,7 +98,8 @@ void free_all(llm_t *h) {
     void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->rope_cs, h->st, h->x, h->raw, h->q,
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
-                    h->d_layers, h->step_sync, h->prof};
+                    h->d_layers, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
+                    h->pf_qh, h->pf_ql, h->pf_w, h->pf_tok};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -331,6 +344,148 @@ int fetch_token(llm_t *h, int32_t *out) {
     return LLM_OK;
 }
 
+// ---- batched prefill -------------------------------------------------------------
+// Rows of a prompt chunk go through the layers as GEMMs: RMSNorm -> fp16 rows,
+// each weight matrix dequantized to an fp16 scratch copy, tcgen05 GEMM with a
+// fused epilogue (QKV store, o_proj/down residual add, gate/up SiLU * mul),
+// causal flash attention over the paged cache.  The last row of the prompt
+// then runs the decode step's LM head (+ argmax), which also advances the
+// device state.
+constexpr int kPrefillChunk = 1024;
+
+bool prefill_shapes_ok(const llm_config &c) {
+    const int d = c.head_dim, rq = c.n_q_heads * d, nq = (c.n_q_heads + 2 * c.n_kv_heads) * d;
+    return nq % kTcBN == 0 && c.hidden % kTcBN == 0 && c.mlp % 64 == 0 && c.hidden % kTcBK == 0 &&
+           rq % kTcBK == 0 && c.mlp % kTcBK == 0;
+}
+
+int prefill_alloc(llm_t *h) {
+    if (h->pf_ready) return LLM_OK;
+    const llm_config &c = h->cfg;
+    const int d = c.head_dim, rq = c.n_q_heads * d, nq = (c.n_q_heads + 2 * c.n_kv_heads) * d;
+    const int R = ((c.max_context < kPrefillChunk ? c.max_context : kPrefillChunk) + kTcBM - 1) / kTcBM * kTcBM;
+    h->pf_rows = R;
+    const size_t wmax = std::max(std::max((size_t)nq * c.hidden, (size_t)c.hidden * rq),
+                                 std::max((size_t)2 * c.mlp * c.hidden, (size_t)c.hidden * c.mlp));
+    const size_t arow = (size_t)std::max(c.hidden, rq);
+    bool ok = dalloc(&h->pf_x, (size_t)R * c.hidden) == cudaSuccess &&
+              dalloc(&h->pf_raw, (size_t)R * nq) == cudaSuccess && dalloc(&h->pf_a, (size_t)R * arow) == cudaSuccess &&
+              dalloc(&h->pf_u, (size_t)R * c.mlp) == cudaSuccess && dalloc(&h->pf_qh, (size_t)R * rq) == cudaSuccess &&
+              dalloc(&h->pf_ql, (size_t)R * rq) == cudaSuccess && dalloc(&h->pf_w, wmax) == cudaSuccess &&
+              dalloc(&h->pf_tok, (size_t)R) == cudaSuccess;
+    if (!ok) return LLM_ERR_CUDA;
+    // rows past a chunk's end are read by the GEMMs (their outputs are dropped): keep them finite
+    ok = cudaMemsetAsync(h->pf_a, 0, (size_t)R * arow * 2, h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->pf_u, 0, (size_t)R * c.mlp * 2, h->stream) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_ah, h->pf_a, R, c.hidden) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_aq, h->pf_a, R, rq) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_u, h->pf_u, R, c.mlp) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_wqkv, h->pf_w, nq, c.hidden) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_wo, h->pf_w, c.hidden, rq) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_wgu, h->pf_w, (uint64_t)2 * c.mlp, c.hidden) == cudaSuccess &&
+         tc_operand_map(&h->pf_map_wd, h->pf_w, c.hidden, c.mlp) == cudaSuccess;
+    if (!ok) return LLM_ERR_CUDA;
+    h->pf_ready = true;
+    return LLM_OK;
+}
+
+// One chunk of m prompt rows at positions pos0 .. pos0 + m - 1 (tokens already
+// on the device in pf_tok).  Leaves the residual rows in pf_x.
+cudaError_t prefill_chunk(llm_t *h, int m, int pos0) {
+    const llm_config &c = h->cfg;
+    const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d, nq = rq + 2 * rkv;
+    cudaStream_t st = h->stream;
+    const int n_sm = h->lc.n_sm;
+    int *err = &h->st->err;
+    cudaError_t e;
+    auto gemm = [&](const CUtensorMap &am, const CUtensorMap &bm, int N, int K, int mode, float *cc, int ldc,
+                    uint16_t *hh, int ldh) {
+        TcGemmArgs g{};
+        g.M = m; g.N = N; g.K = K; g.mode = mode; g.c = cc; g.ldc = ldc; g.h = hh; g.ldh = ldh;
+        g.err = err; g.wait_ns = 1000000000ull;
+        return launch_tc_gemm(st, am, bm, g);
+    };
+    auto dequant = [&](const void *w, const void *sc, const void *w2, const void *s2, int N, int K, uint16_t *out) {
+        DequantArgs q{};
+        q.fmt = h->fmt; q.w = w; q.s = sc; q.w2 = w2; q.s2 = s2; q.N = N; q.K = K; q.out = out;
+        return launch_dequant(st, n_sm, q);
+    };
+    if ((e = launch_embed_rows(st, (const uint16_t *)h->w.embed, h->pf_tok, m, c.hidden, h->pf_x)) != cudaSuccess)
+        return e;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const llm_layer_weights &L = h->layers[l];
+        uint16_t *kp = h->k_pool + (size_t)l * h->layer_kv_elems, *vp = h->v_pool + (size_t)l * h->layer_kv_elems;
+        if ((e = launch_rmsnorm_rows(st, h->pf_x, (const uint16_t *)L.attn_norm, c.rms_eps, m, c.hidden, h->pf_a)) ||
+            (e = dequant(L.wq, L.sq, nullptr, nullptr, rq, c.hidden, h->pf_w)) ||
+            (e = dequant(L.wk, L.sk, nullptr, nullptr, rkv, c.hidden, h->pf_w + (size_t)rq * c.hidden)) ||
+            (e = dequant(L.wv, L.sv, nullptr, nullptr, rkv, c.hidden, h->pf_w + (size_t)(rq + rkv) * c.hidden)) ||
+            (e = gemm(h->pf_map_ah, h->pf_map_wqkv, nq, c.hidden, kEpiStore, h->pf_raw, nq, nullptr, 0)))
+            return e;
+        QkvRowsArgs qa{};
+        qa.raw = h->pf_raw;
+        if (c.qkv_bias) {
+            qa.bq = (const uint16_t *)L.bq;
+            qa.bk = (const uint16_t *)L.bk;
+            qa.bv = (const uint16_t *)L.bv;
+        }
+        if (c.qk_norm) {
+            qa.q_gain = (const uint16_t *)L.q_norm;
+            qa.k_gain = (const uint16_t *)L.k_norm;
+        }
+        qa.eps = c.rms_eps; qa.n = m; qa.pos0 = pos0; qa.Hq = c.n_q_heads; qa.Hkv = c.n_kv_heads; qa.d = d;
+        qa.rope_cs = h->rope_cs; qa.k_pool = kp; qa.v_pool = vp; qa.page_table = h->page_table;
+        qa.n_pages = h->n_pages; qa.q_hi = h->pf_qh; qa.q_lo = h->pf_ql; qa.err = err;
+        AttnRowsArgs aa{};
+        aa.q_hi = h->pf_qh; aa.q_lo = h->pf_ql; aa.k_pool = kp; aa.v_pool = vp; aa.page_table = h->page_table;
+        aa.n_pages = h->n_pages; aa.n = m; aa.pos0 = pos0; aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d;
+        aa.out = h->pf_a; aa.err = err;
+        if ((e = launch_qkv_rows(st, qa)) || (e = launch_attn_rows(st, aa)) ||
+            (e = dequant(L.wo, L.so, nullptr, nullptr, c.hidden, rq, h->pf_w)) ||
+            (e = gemm(h->pf_map_aq, h->pf_map_wo, c.hidden, rq, kEpiAdd, h->pf_x, c.hidden, nullptr, 0)) ||
+            (e = launch_rmsnorm_rows(st, h->pf_x, (const uint16_t *)L.mlp_norm, c.rms_eps, m, c.hidden, h->pf_a)) ||
+            (e = dequant(L.wg, L.sg, L.wu, L.su, c.mlp, c.hidden, h->pf_w)) ||
+            (e = gemm(h->pf_map_ah, h->pf_map_wgu, 2 * c.mlp, c.hidden, kEpiSwiGlu, nullptr, 0, h->pf_u, c.mlp)) ||
+            (e = dequant(L.wd, L.sd, nullptr, nullptr, c.hidden, c.mlp, h->pf_w)) ||
+            (e = gemm(h->pf_map_u, h->pf_map_wd, c.hidden, c.mlp, kEpiAdd, h->pf_x, c.hidden, nullptr, 0)))
+            return e;
+    }
+    return cudaSuccess;
+}
+
+int prefill_batched(llm_t *h, const int32_t *tokens, int n, int32_t *first_token) {
+    int rc = prefill_alloc(h);
+    if (rc != LLM_OK) return rc;
+    const llm_config &c = h->cfg;
+    int last_rows = 0;
+    for (int off = 0; off < n; off += h->pf_rows) {
+        const int m = n - off < h->pf_rows ? n - off : h->pf_rows;
+        if (cudaMemcpyAsync(h->pf_tok, tokens + off, (size_t)m * sizeof(int32_t), cudaMemcpyHostToDevice,
+                            h->stream) != cudaSuccess ||
+            prefill_chunk(h, m, h->seq_len + off) != cudaSuccess)
+            return LLM_ERR_CUDA;
+        last_rows = m;
+    }
+    // the last prompt row -> final RMSNorm -> LM head + argmax; the state moves to seq_len + n
+    k_set_state<<<1, 1, 0, h->stream>>>(h->st, -1, h->seq_len + n - 1, 0);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(h->x, h->pf_x + (size_t)(last_rows - 1) * c.hidden, (size_t)c.hidden * sizeof(float),
+                        cudaMemcpyDeviceToDevice, h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    LmHeadArgs la{};
+    const bool int8_head = h->fmt == kFmtInt8 && !c.tied_lm_head;
+    la.fmt = int8_head ? kFmtInt8 : kFmtBf16;
+    la.w = c.tied_lm_head ? h->w.embed : h->w.lm_head;
+    la.scale = int8_head ? (const float *)h->w.lm_scale : nullptr;
+    la.gamma = (const uint16_t *)h->w.final_norm;
+    la.eps = c.rms_eps; la.N = c.vocab; la.K = c.hidden; la.x = h->x; la.logits = h->logits;
+    la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
+    la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
+    LaunchCfg lc = h->lc;
+    lc.pdl = false;
+    if (launch_lm_head(lc, la, h->lm_grid) != cudaSuccess) return LLM_ERR_CUDA;
+    return fetch_token(h, first_token);
+}
+
 }  // namespace
 
 extern "C" {
@@ -439,6 +594,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     if (!ok) return fail(LLM_ERR_CUDA);
 
     if (plan_step(h, n_sm) != LLM_OK) return fail(LLM_ERR_CUDA);
+    h->pf_ok = prefill_shapes_ok(c);
 
     // Capture the whole step once (the kernel chain if the persistent kernel
     // cannot be captured here).
@@ -474,6 +630,13 @@ int llm_set_persistent(llm_t *h, int32_t on) {
     return capture(h);
 }
 
+int llm_set_prefill_batched(llm_t *h, int32_t on) {
+    if (!h) return LLM_ERR_ARG;
+    if (on && !h->pf_ok) return LLM_ERR_ARG;
+    h->pf_batched = on != 0;
+    return LLM_OK;
+}
+
 int llm_set_pdl(llm_t *h, int32_t use_pdl) {
     if (!h) return LLM_ERR_ARG;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
@@ -486,6 +649,14 @@ int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token
     for (int i = 0; i < n; ++i)
         if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return LLM_ERR_ARG;
     if ((int64_t)h->seq_len + n > h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    if (h->pf_ok && h->pf_batched && n >= 2) {
+        int rc = prefill_batched(h, tokens, n, first_token);
+        if (rc != LLM_OK) return rc;
+        h->seq_len += n;
+        h->have_token = true;
+        h->stepped = true;
+        return LLM_OK;
+    }
     for (int i = 0; i < n; ++i) {
         k_set_state<<<1, 1, 0, h->stream>>>(h->st, tokens[i], i == 0 ? h->seq_len : -1, 0);
         if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;

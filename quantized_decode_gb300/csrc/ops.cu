@@ -5,6 +5,7 @@
 #include "../../include/llm.h"
 #include "../../include/llm_ops.h"
 #include "kernels.h"
+#include "prefill.h"
 
 using namespace qd;
 
@@ -103,6 +104,28 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, con
     cudaError_t e = launch_attention(lc, a);
     cudaError_t f = cudaFreeAsync(scratch, lc.stream);
     return status(e != cudaSuccess ? e : f);
+}
+
+int llm_op_dequant_f16(int32_t fmt, const void *w, const void *s, int32_t N, int32_t K, void *out,
+                       void *stream) {
+    if (!a16(w) || !s || !a16(out) || N <= 0 || K <= 0) return LLM_ERR_ARG;
+    if (fmt == LLM_FMT_INT4_G128 ? K % 128 != 0 : (fmt != LLM_FMT_INT8_ROW || K % 8 != 0)) return LLM_ERR_ARG;
+    DequantArgs a{};
+    a.fmt = fmt == LLM_FMT_INT4_G128 ? kFmtInt4 : kFmtInt8;
+    a.w = w; a.s = s; a.N = N; a.K = K; a.out = (uint16_t *)out;
+    LaunchCfg lc = op_cfg(stream);
+    return status(launch_dequant(lc.stream, lc.n_sm, a));
+}
+
+int llm_op_gemm_f16(const void *A, const void *B, int32_t M, int32_t N, int32_t K, float *C, void *stream) {
+    if (!a16(A) || !a16(B) || !a16(C) || M <= 0 || N <= 0 || K <= 0 || N % kTcBN || K % kTcBK) return LLM_ERR_ARG;
+    CUtensorMap am, bm;
+    if (tc_operand_map(&am, A, (uint64_t)M, (uint64_t)K) != cudaSuccess ||
+        tc_operand_map(&bm, B, (uint64_t)N, (uint64_t)K) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    TcGemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.mode = kEpiStore; a.c = C; a.ldc = N; a.wait_ns = 1000000000ull;
+    return status(launch_tc_gemm((cudaStream_t)stream, am, bm, a));
 }
 
 }  // extern "C"

@@ -180,6 +180,10 @@ class Engine:
         """True: the step is the persistent whole-step kernel; False: the kernel chain."""
         L.check(self.lib.llm_set_persistent(self.h, int(bool(on))), "llm_set_persistent")
 
+    def set_prefill_batched(self, on):
+        """True: prompts run as one batch on the tensor cores; False: token by token."""
+        L.check(self.lib.llm_set_prefill_batched(self.h, int(bool(on))), "llm_set_prefill_batched")
+
     def set_graph_mode(self, on):
         L.check(self.lib.llm_set_graph_mode(self.h, int(bool(on))), "llm_set_graph_mode")
 
