@@ -55,6 +55,7 @@ struct llm_t {
     StepParams sp{};
     StepLaunch sl{};
     StepLayer *d_layers = nullptr;
+    CUtensorMap *d_maps = nullptr;  // [n_layers][kMapCount] weight boxes of the persistent kernel
     int *step_sync = nullptr;
     unsigned long long *prof = nullptr;
 
@@ -98,7 +99,7 @@ void free_all(llm_t *h) {
     void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->rope_cs, h->st, h->x, h->raw, h->q,
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
-                    h->d_layers, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
+                    h->d_layers, h->d_maps, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
                     h->pf_qh, h->pf_ql, h->pf_w, h->pf_tok};
     for (void *b : bufs)
         if (b) cudaFree(b);
@@ -297,9 +298,24 @@ int plan_step(llm_t *h, int n_sm) {
         return LLM_OK;
     }
     std::vector<StepLayer> ly(c.n_layers);
+    std::vector<CUtensorMap> maps((size_t)c.n_layers * kMapCount);
+    if (dalloc(&h->d_maps, maps.size()) != cudaSuccess) return LLM_ERR_CUDA;
+    const int rq = c.n_q_heads * c.head_dim, rkv = c.n_kv_heads * c.head_dim;
     for (int l = 0; l < c.n_layers; ++l) {
         const llm_layer_weights &L = h->layers[l];
         StepLayer &S = ly[l];
+        CUtensorMap *m = maps.data() + (size_t)l * kMapCount;
+        if (step_encode_weight_map(m + kMapQ, L.wq, rq, p.geo[kPhQkv], kStepLines) != cudaSuccess ||
+            step_encode_weight_map(m + kMapK, L.wk, rkv, p.geo[kPhQkv], kStepLines) != cudaSuccess ||
+            step_encode_weight_map(m + kMapV, L.wv, rkv, p.geo[kPhQkv], kStepLines) != cudaSuccess ||
+            step_encode_weight_map(m + kMapO, L.wo, c.hidden, p.geo[kPhO], kStepLines) != cudaSuccess ||
+            step_encode_weight_map(m + kMapGate, L.wg, c.mlp, p.geo[kPhGu], kStepLines / 2) != cudaSuccess ||
+            step_encode_weight_map(m + kMapUp, L.wu, c.mlp, p.geo[kPhGu], kStepLines / 2) != cudaSuccess ||
+            step_encode_weight_map(m + kMapDown, L.wd, c.hidden, p.geo[kPhDown], kStepLines) != cudaSuccess) {
+            h->step_ok = false;
+            return LLM_OK;
+        }
+        S.tm = h->d_maps + (size_t)l * kMapCount;
         S.w[0] = L.wq; S.w[1] = L.wk; S.w[2] = L.wv;
         S.s[0] = L.sq; S.s[1] = L.sk; S.s[2] = L.sv;
         if (c.qkv_bias) {
@@ -321,12 +337,15 @@ int plan_step(llm_t *h, int n_sm) {
         dalloc(&h->prof, (size_t)5 * c.n_layers + 2) != cudaSuccess ||
         cudaMemcpyAsync(h->d_layers, ly.data(), ly.size() * sizeof(StepLayer), cudaMemcpyHostToDevice,
                         h->stream) != cudaSuccess ||
+        cudaMemcpyAsync(h->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                        h->stream) != cudaSuccess ||
         cudaMemsetAsync(h->step_sync, 0, n_sync * sizeof(int), h->stream) != cudaSuccess ||
         cudaStreamSynchronize(h->stream) != cudaSuccess)
         return LLM_ERR_CUDA;
     p.layers = h->d_layers;
     p.sync = h->step_sync;
-    if (step_encode_kv_maps(p, kv_rows) != cudaSuccess) {
+    if (step_encode_kv_maps(p, kv_rows) != cudaSuccess ||
+        step_encode_weight_map(&p.tm_lm, p.lm_w, c.vocab, p.geo[kPhLm], kStepLines) != cudaSuccess) {
         h->step_ok = false;
         return LLM_OK;
     }

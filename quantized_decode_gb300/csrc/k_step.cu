@@ -1,17 +1,19 @@
 // k_step.cu - the whole decode step as one persistent kernel, one CTA per SM.
 //
-// Roles.  Warp NCW (first of the last warpgroup) is the producer: its lane 0 walks the step's
-// schedule and, for every ring item, waits until the slot is free and issues
-// TMA copies of what this CTA consumes next -- rows of a weight matrix with
-// their INT4 scales (cp.async.bulk), or K/V pages of the paged cache as
-// 128-byte-swizzled 16-row boxes (cp.async.bulk.tensor) -- completing on the
-// slot's `full` mbarrier.  It never waits for activations: weights, scales and
-// every cached K/V row except the one appended in this step are final before
-// the step starts, so the stream runs ahead across phase and layer boundaries,
-// limited only by the ring.  Warps 0..NCW-1 consume: per phase they wait for
-// the phase's input (a counter that other CTAs raise), stage the activations
-// into registers, take the phase's items in order (wait `full`, compute,
-// arrive on `empty`) and run the phase's epilogue.
+// Roles.  Warps NCW .. NCW + kStepProducers - 1 produce: lane 0 of each walks
+// the step's schedule and takes every kStepProducers-th ring item; for an
+// item it waits until the slot is free and issues the TMA copies of what this
+// CTA consumes next -- a 3-D box of 4 weight rows x one K-tile (128-byte
+// swizzle) plus the cover of the rows' INT4 scales (cp.async.bulk), or K/V
+// pages of the paged cache as 128-byte-swizzled 16-row boxes -- completing on
+// the slot's `full` mbarrier.  Producers never wait for activations: weights,
+// scales and every cached K/V row except the one appended in this step are
+// final before the step starts, so the stream runs ahead across phase and
+// layer boundaries, limited only by the ring.  Warps 0..NCW-1 consume: per
+// phase they wait for the phase's input (a counter that other CTAs raise),
+// stage the activations, take the phase's items (item k belongs to warp
+// k % NCW: wait `full`, compute, arrive on `empty`) and run the phase's
+// epilogue.
 //
 // Phases per layer (each CTA owns a contiguous share of every phase's rows):
 //   QKV  RMSNorm -> Q/K/V GEMV (+bias) -> raw rows; the CTA that completes a
@@ -107,6 +109,13 @@ QD_DEV void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *ba
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
         "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+QD_DEV void tma_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 QD_DEV uint64_t gtimer() {
@@ -237,6 +246,29 @@ QD_DEV SegMats seg_mats(const StepParams &p, const StepLayer &Ly, int ph, int sg
     }
 }
 
+// Tensor maps of segment sg of a phase (gate/up: gate, up).
+QD_DEV void seg_maps(const StepParams &p, const StepLayer &Ly, int ph, int sg, const CUtensorMap *&a,
+                     const CUtensorMap *&b) {
+    b = nullptr;
+    switch (ph) {
+        case kPhQkv: a = Ly.tm + kMapQ + sg; break;
+        case kPhO: a = Ly.tm + kMapO; break;
+        case kPhGu:
+            a = Ly.tm + kMapGate;
+            b = Ly.tm + kMapUp;
+            break;
+        case kPhDown: a = Ly.tm + kMapDown; break;
+        default: a = &p.tm_lm; break;
+    }
+}
+
+// Byte o of line i of an item's codes (ch = 128-byte chunks per line in the
+// box): the 128-byte swizzle permutes the 16-byte units of each segment.
+QD_DEV const uint8_t *code_at(const uint8_t *item, int line, int ch, int o) {
+    const int seg = line * ch + (o >> 7);
+    return item + (seg << 7) + ((((o >> 4) & 7) ^ (seg & 7)) << 4) + (o & 15);
+}
+
 // Line i of an item: the matrix row it holds (gate/up: lines 0, 1 gate rows,
 // 2, 3 up rows of the same two pairs) and whether it exists (nl rows/pairs).
 QD_DEV bool item_line(int ph, int local, int nl, int i, int &row, bool &second) {
@@ -251,13 +283,6 @@ QD_DEV bool item_line(int ph, int local, int nl, int i, int &row, bool &second) 
 }
 // Bytes of K-tile t of a row, and (INT4) the 16-byte cover of its scales.
 QD_DEV int tile_bytes(const StepGeo &g, int t) { return min(g.tk, g.row_bytes - t * g.tk); }
-QD_DEV void tile_scale_cover(const StepGeo &g, int row, int t, int &lo, int &len, int &delta) {
-    const int start = row * g.sr + t * (g.tk / 32);
-    const int end = start + tile_bytes(g, t) / 32;
-    lo = start & ~15;
-    len = ((end + 15) & ~15) - lo;
-    delta = start - lo;
-}
 
 QD_DEV int pages_per_item(int d) { return kStepSlotBytes / (64 * d); }
 QD_DEV void attn_split(const StepParams &p, int c, int T, int &g, int &sp, int &pa0, int &pa1) {
@@ -338,76 +363,66 @@ QD_DEV bool wait_mbar(const StepParams &p, uint64_t *bar, uint32_t parity, volat
 // Producer.
 // ---------------------------------------------------------------------------
 template <int DH>
-QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
+QD_DEV void producer(const StepParams &p, const Smem &s, int pw) {
+    // kStepProducers threads (lane 0 of each producer warp) share the copies:
+    // producer pw issues the items k with k % kStepProducers == pw of the
+    // schedule, so the issue latency of one item overlaps the others'.
     volatile int *abort = s.misc;
     const int c = blockIdx.x, nc = gridDim.x;
     const int T = p.st->pos + 1;
     // Kernel parameters used per item live in registers: every PTX statement
     // below clobbers memory, which would otherwise reload them each time.
-    const int n_slots = p.n_slots, inflight = p.inflight;
-    RingPos rp, landed;
-    int issued = 0, n_landed = 0;
+    const int n_slots = p.n_slots;
+    RingPos rp;          // slot of the current item of the schedule
+    int k_item = 0;
     const uint64_t pol = l2_evict_first();
     bool ok = true;
-    // Claim the next slot (warp-uniform): lane 0 waits until no more than
-    // p.inflight - 1 earlier items are still in flight (bytes on the way, not
-    // yet in shared memory) and until the consumers released the slot's
-    // previous use.  Landed items may fill the whole ring; the in-flight cap
-    // keeps the memory system's queues short, so that the latency-bound loads
-    // of the phases (activations, counters) are not stuck behind the stream.
+    // Take the schedule's next item: false when it belongs to another
+    // producer (or after an abort); else wait until the consumers released
+    // the slot's previous use.
     auto claim = [&]() -> bool {
-        int got = 1;
-        if (lane == 0) {
-            while (got && issued - n_landed >= inflight) {
-                got = wait_mbar(p, s.full + landed.slot, landed.par, abort);
-                landed.next(n_slots);
-                ++n_landed;
-            }
-            if (got) got = wait_mbar(p, s.empty + rp.slot, rp.par ^ 1u, abort);
+        const bool mine = (k_item++ % kStepProducers) == pw;
+        if (mine && ok && !wait_mbar(p, s.empty + rp.slot, rp.par ^ 1u, abort)) ok = false;
+        if (!mine || !ok) {
+            rp.next(n_slots);
+            return false;
         }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) ok = false;
-        return got != 0;
+        return true;
     };
     auto gemv_items = [&](const StepLayer &Ly, int ph) {
         const StepGeo g = p.geo[ph];
+        const int ch = g.tk >> 7;
         int r0, r1;
         span(g.N, c, nc, r0, r1);
         int msg = -1;
         SegMats M{};
+        const CUtensorMap *ma = nullptr, *mb = nullptr;
         for_items(p, ph, r0, r1, [&](int sg, int local, int nl, int, int t) {
-            if (!ok || !claim()) return;
-            // lanes 0-3 copy the codes of line `lane`, lanes 4-7 its INT4 scales
+            if (!claim()) return;
             if (sg != msg) {
                 M = seg_mats(p, Ly, ph, sg);
+                seg_maps(p, Ly, ph, sg, ma, mb);
                 msg = sg;
             }
             uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
             uint64_t *bar = s.full + rp.slot;
-            const int tb = tile_bytes(g, t);
-            uint32_t bytes = 0;
-            const int i = lane & 3;
-            int row;
-            bool second;
-            const bool valid = lane < 8 && item_line(ph, local, nl, i, row, second);
-            int lo = 0, len = 0, delta = 0;
-            if (valid && g.sr) tile_scale_cover(g, row, t, lo, len, delta);
-            if (valid) bytes = lane < 4 ? (uint32_t)tb : (uint32_t)len;
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-            if (lane == 0) mbar_expect_tx(bar, bytes);
-            __syncwarp();
-            if (valid) {
-                const uint8_t *w = second ? M.wb : M.wa;
-                const uint8_t *sc = second ? M.sb : M.sa;
-                if (lane < 4)
-                    bulk_g2s(dst + i * kStepLineStride, w + (size_t)row * g.row_bytes + (size_t)t * g.tk, (uint32_t)tb, bar,
-                             pol);
-                else if (len)
-                    bulk_g2s(dst + kStepLines * kStepLineStride + i * kStepScaleLine, sc + lo, (uint32_t)len, bar, pol);
+            // codes: one box of 4 rows (gate/up: 2 gate rows, then 2 up rows);
+            // INT4 scales: the 16-byte cover of the rows' whole scale rows
+            const int lo = (local * g.sr) & ~15, hi = ((local + nl) * g.sr + 15) & ~15;
+            const uint32_t cover = g.sr ? (uint32_t)(hi - lo) : 0u;
+            mbar_expect_tx(bar, (uint32_t)(kStepLines * ch * 128) + (mb ? 2u : 1u) * cover);
+            if (mb) {
+                tma_3d(dst, ma, 0, t * ch, local, bar, pol);
+                tma_3d(dst + kStepUpOff, mb, 0, t * ch, local, bar, pol);
+                if (cover) {
+                    bulk_g2s(dst + kStepGuScaleOff, M.sa + lo, cover, bar, pol);
+                    bulk_g2s(dst + kStepGuScaleOff + kStepGuScaleSpan, M.sb + lo, cover, bar, pol);
+                }
+            } else {
+                tma_3d(dst, ma, 0, t * ch, local, bar, pol);
+                if (cover) bulk_g2s(dst + kStepScaleOff, M.sa + lo, cover, bar, pol);
             }
             rp.next(n_slots);
-            ++issued;
         });
     };
     auto attn_items = [&](int l) {
@@ -415,43 +430,27 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
         int g, sp, pa0, pa1;
         attn_split(p, c, T, g, sp, pa0, pa1);
         const int ppi = pages_per_item(DH);
-        for (int base = pa0; ok && base < pa1; base += 32) {
-            // lane k holds the physical page of logical page base + k
-            int phys = 0;
-            if (base + lane < pa1) {
-                phys = __ldg(p.page_table + base + lane);
+        for (int k0 = pa0; k0 < pa1; k0 += ppi) {
+            const int np = min(ppi, pa1 - k0);
+            if (!claim()) continue;
+            uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
+            uint64_t *bar = s.full + rp.slot;
+            mbar_expect_tx(bar, (uint32_t)(np * 64 * DH));
+            for (int k = 0; k < np; ++k) {
+                int phys = __ldg(p.page_table + k0 + k);
                 if (phys < 0 || phys >= p.n_pages) {
                     atomicCAS(&p.st->err, kErrNone, kErrBadPage);
                     phys = 0;
                 }
-            }
-            const int nb = min(32, pa1 - base);
-            for (int k0 = 0; ok && k0 < nb; k0 += ppi) {
-                const int np = min(ppi, nb - k0);
-                if (!claim()) break;
-                int pg[4];
+                const int y = ((l * p.n_pages + phys) * p.Hkv + g) * kPageTokens;
+                uint8_t *pgd = dst + (size_t)k * 64 * DH;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) pg[q] = __shfl_sync(0xffffffffu, phys, min(k0 + q, 31));
-                if (lane == 0) {
-                    uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
-                    uint64_t *bar = s.full + rp.slot;
-                    mbar_expect_tx(bar, (uint32_t)(np * 64 * DH));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (k < np) {
-                            const int y = ((l * p.n_pages + pg[k]) * p.Hkv + g) * kPageTokens;
-                            uint8_t *pgd = dst + (size_t)k * 64 * DH;
-#pragma unroll
-                            for (int hf = 0; hf < DH / 64; ++hf) {
-                                tma_2d(pgd + hf * 2048, &p.tm_k, hf * 64, y, bar, pol);
-                                tma_2d(pgd + (DH / 64 + hf) * 2048, &p.tm_v, hf * 64, y, bar, pol);
-                            }
-                        }
-                    }
+                for (int hf = 0; hf < DH / 64; ++hf) {
+                    tma_2d(pgd + hf * 2048, &p.tm_k, hf * 64, y, bar, pol);
+                    tma_2d(pgd + (DH / 64 + hf) * 2048, &p.tm_v, hf * 64, y, bar, pol);
                 }
-                rp.next(n_slots);
-                ++issued;
             }
+            rp.next(n_slots);
         }
     };
     for (int l = 0; ok && l < p.L; ++l) {
@@ -463,13 +462,16 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int lane) {
         gemv_items(Ly, kPhDown);
     }
     if (ok) gemv_items(s.layers[0], kPhLm);
-    // Leave only once every copy this CTA issued has landed (bounded).
-    if (lane == 0) {
-        RingPos q = rp;
-        for (int k = 0; k < min(issued, n_slots); ++k) {
-            q.prev(n_slots);
-            const uint64_t t0 = gtimer();
-            while (!mbar_try_wait(s.full + q.slot, q.par) && gtimer() - t0 < p.wait_ns) {
+    // Producer 0 leaves only once the last use of every slot has landed
+    // (bounded): consumers that gave up early must not leave copies in flight
+    // into a CTA that has exited.  Every producer walked the same schedule,
+    // so k_item is the CTA's item count.
+    if (pw == 0) {
+        const uint64_t t0 = gtimer();
+        for (int sl = 0; sl < n_slots && sl < k_item; ++sl) {
+            const int last = (k_item - 1 - sl) / n_slots * n_slots + sl;  // last item in slot sl
+            const uint32_t par = (uint32_t)(last / n_slots) & 1u;
+            while (!mbar_try_wait(s.full + sl, par) && gtimer() - t0 < p.wait_ns) {
             }
         }
     }
@@ -587,7 +589,7 @@ QD_DEV void stage_mma(const StepParams &p, const Smem &s, const float *src32, co
     };
     if (gamma) {
         // normalized vectors are at most 4096 long: keep them in registers across the reduction
-        constexpr int CPT = 4096 / CE / NCT;
+        constexpr int CPT = (4096 / CE + NCT - 1) / NCT;
         float v[CPT][CE];
         float ss = 0.f;
 #pragma unroll
@@ -647,6 +649,7 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
     const int xpart = gq < 4 ? gq : 0;  // B column gq = part gq (columns 4-7 unused)
     const int n_slots = p.n_slots, bb = g.bb;
     const int bpt = g.tk / bb;          // blocks in a full tile
+    const int ch = g.tk >> 7;           // 128-byte chunks of a line in the item
     int k = 0;
     for_items(p, ph, r0, r1, [&](int, int local, int nl, int jf, int t) {
         const RingPos q = rp;
@@ -654,7 +657,10 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
         if ((k++ % NCW) != warp) return;
         const bool have = __all_sync(0xffffffffu, wait_mbar(p, s.full + q.slot, q.par, abort));
         const uint8_t *item = s.ring + (size_t)q.slot * kStepSlotBytes;
-        const uint8_t *ln = item + line * kStepLineStride;
+        // this thread's line inside its box (gate/up: lines 2, 3 are the up box)
+        const bool upbox = ph == kPhGu && line >= 2;
+        const uint8_t *box = item + (upbox ? kStepUpOff : 0);
+        const int bl = upbox ? line - 2 : line;
         int row;
         bool second;
         const bool lvalid = item_line(ph, local, nl, line, row, second);
@@ -665,10 +671,12 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
         float acc = 0.f;
         if (have) {
             if constexpr (F == kFmtInt4) {
-                int lo, len, delta;
-                tile_scale_cover(g, row, t, lo, len, delta);
-                const uint16_t *scl = reinterpret_cast<const uint16_t *>(item + kStepLines * kStepLineStride +
-                                                                         line * kStepScaleLine + delta);
+                // this line's scales of the tile: its row within the cover, then the tile's groups
+                const int first = ph == kPhGu ? (line & 1) : line;
+                const uint8_t *cov =
+                    item + (ph == kPhGu ? kStepGuScaleOff + (line >= 2 ? kStepGuScaleSpan : 0) : kStepScaleOff);
+                const uint16_t *scl = reinterpret_cast<const uint16_t *>(
+                                          cov + (local * g.sr - ((local * g.sr) & ~15)) + first * g.sr) + b0;
 #pragma unroll 2
                 for (int st = 0; st < S; ++st) {
                     const int ba = min(pa * S + st, nb - 1), bq = min(pb * S + st, nb - 1);
@@ -678,8 +686,8 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(ln + ba * 64 + j * 16 + tq * 4);
-                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(ln + bq * 64 + j * 16 + tq * 4);
+                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(code_at(box, bl, ch, ba * 64 + j * 16 + tq * 4));
+                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(code_at(box, bl, ch, bq * 64 + j * 16 + tq * 4));
                         uint4 xv = s.stage[int4_chunk_slot((gx * 4 + j) * 4 + tq)];
                         if (!xok) xv = make_uint4(0, 0, 0, 0);
                         const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
@@ -692,10 +700,7 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
                     }
                     const int bm = mypart * S + st;  // this thread's block (unclamped)
                     const float v = tq == 0 ? (pa ? d[1] : d[0]) : (pb == 3 ? d[3] : d[2]);
-                    if (tq < 2 && bm < nb) {
-                        const float sv = bf16_bits_to_float(scl[bm]);
-                        acc = fmaf(v - s.corr[b0 + bm], sv, acc);
-                    }
+                    if (tq < 2 && bm < nb) acc = fmaf(v - s.corr[b0 + bm], bf16_bits_to_float(scl[bm]), acc);
                 }
             } else if constexpr (F == kFmtInt8) {
                 float d[4] = {0.f, 0.f, 0.f, 0.f}, cor = 0.f;
@@ -705,8 +710,8 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
                     const int bx = xpart * S + st;
                     uint2 xv = reinterpret_cast<const uint2 *>(s.stage)[(b0 + min(bx, nb - 1)) * 4 + tq];
                     if (bx >= nb) xv = make_uint2(0, 0);
-                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(ln + ba * 16 + tq * 4) ^ 0x80808080u;
-                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(ln + bq * 16 + tq * 4) ^ 0x80808080u;
+                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(code_at(box, bl, ch, ba * 16 + tq * 4)) ^ 0x80808080u;
+                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(code_at(box, bl, ch, bq * 16 + tq * 4)) ^ 0x80808080u;
                     mma_f16(d, prmt(wa, 0x64646464u, 0x4140u), prmt(wb, 0x64646464u, 0x4140u),
                             prmt(wa, 0x64646464u, 0x4342u), prmt(wb, 0x64646464u, 0x4342u), xv.x, xv.y);
                     const int bm = mypart * S + st;
@@ -722,8 +727,8 @@ QD_DEV RingPos gemv_mma(const StepParams &p, const Smem &s, int ph, int r0, int 
                     const int bx = xpart * S + st;
                     uint4 xv = s.stage[(b0 + min(bx, nb - 1)) * 4 + tq];
                     if (bx >= nb) xv = make_uint4(0, 0, 0, 0);
-                    const uint2 wa = *reinterpret_cast<const uint2 *>(ln + ba * 32 + tq * 8);
-                    const uint2 wb = *reinterpret_cast<const uint2 *>(ln + bq * 32 + tq * 8);
+                    const uint2 wa = *reinterpret_cast<const uint2 *>(code_at(box, bl, ch, ba * 32 + tq * 8));
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(code_at(box, bl, ch, bq * 32 + tq * 8));
                     mma_bf16x4(d, wa.x, wb.x, wa.y, wb.y, xv.x, xv.y);
                     mma_bf16x4(d, wa.x, wb.x, wa.y, wb.y, xv.z, xv.w);
                 }
@@ -1210,19 +1215,17 @@ QD_DEV void phase_lm(Ctx<NCW> &x, const StepLayer *Ly0) {
     for (int i = x.tid; i < p.L * kSyncStride + 1; i += x.NCT) p.sync[i] = 0;
 }
 
-// Register split.  The block is three warpgroups launched at kLaunchRegs
-// registers a thread: warpgroups 0-1 (the consumers) raise theirs to
-// kConsumerRegs and warpgroup 2 (the producer warp plus three idle warps)
-// lowers its own to kProducerRegs.  The shares add up to the launch total,
-// 256 * 224 + 128 * 56 = 384 * 168 = 64512, and each SM sub-partition holds two
-// consumer warps and one producer-group warp: 2 * 32 * 224 + 32 * 56 = 16128 of
-// its 16384 registers.
-constexpr int kLaunchRegs = 168, kConsumerRegs = 224, kProducerRegs = 56;
-static_assert(256 * kConsumerRegs + 128 * kProducerRegs <= 384 * kLaunchRegs, "register split exceeds the launch");
-
+// Register split.  The block is 16 warps launched at 128 registers a thread
+// (the SM's whole register file): warpgroups 0-2 (the NCW = 12 consumers)
+// raise theirs to kConsumerRegs and warpgroup 3 (the producers) lowers its
+// own to kProducerRegs; 384 * 152 + 128 * 56 = 65536.  Each SM sub-partition
+// runs three consumer warps beside one producer.
+constexpr int kLaunchRegs = 128, kConsumerRegs = 152, kProducerRegs = 56;
 template <int WF, int LMF, int DH, int NCW>
 __global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constant__ StepParams p) {
-    static_assert(NCW == 8, "two consumer warpgroups");
+    static_assert(NCW == 12 && kStepProducers == 4, "three consumer warpgroups, one producer warpgroup");
+    static_assert(NCW * 32 * kConsumerRegs + kStepProducers * 32 * kProducerRegs <= (NCW + 4) * 32 * kLaunchRegs,
+                  "register split");
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p.n_slots);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1243,7 +1246,7 @@ __global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constan
     __syncthreads();
     if (warp >= NCW) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-        if (warp == NCW) producer<DH>(p, s, lane);
+        if (lane == 0) producer<DH>(p, s, warp - NCW);
         return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
@@ -1275,7 +1278,7 @@ __global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constan
     }
 }
 
-constexpr int kNcw = 8;
+constexpr int kNcw = 12;
 
 template <int WF, int LMF, int DH>
 const void *pick() {
@@ -1317,8 +1320,10 @@ bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem
         g.bb = fmt == kFmtInt4 ? 64 : (fmt == kFmtInt8 ? 16 : 32);
         g.tk = g.row_bytes < kStepTileBytes ? g.row_bytes : kStepTileBytes / g.bb * g.bb;
         g.nt = (g.row_bytes + g.tk - 1) / g.tk;
-        const int sc = g.sr ? kStepLines * kStepScaleLine : 0;
-        if (kStepLines * kStepLineStride + sc > kStepSlotBytes) return false;
+        // codes: 3-D boxes of 128-byte chunks; INT4 scales: covers of whole scale rows
+        if (g.row_bytes % 128 || g.tk % 128) return false;
+        const int cover_rows = pairs ? kStepLines / 2 : kStepLines;
+        if (g.sr && cover_rows * g.sr + 16 > (pairs ? kStepGuScaleSpan : kStepSlotBytes - kStepScaleOff)) return false;
         // per-CTA rows must fit the result buffer
         const long long rows = ((long long)N + n_sm - 1) / n_sm;
         if (rows * (pairs ? 2 : 1) > kStepResFloats) return false;
@@ -1349,6 +1354,29 @@ bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem
     out.block = (kNcw + 4) * 32;
     out.smem = smem_bytes(n_slots, p.L);
     return true;
+}
+
+cudaError_t step_encode_weight_map(CUtensorMap *map, const void *w, int N, const StepGeo &g, int lines) {
+    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = (EncodeFn)fn;
+    }
+    if (!w || ((uintptr_t)w & 15) || g.row_bytes % 128 || g.tk % 128 || N < 1) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)(g.row_bytes / 128), (cuuint64_t)N};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)g.row_bytes};
+    const cuuint32_t box[3] = {128, (cuuint32_t)(g.tk / 128), (cuuint32_t)lines};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t step_encode_kv_maps(StepParams &p, size_t total_rows) {

@@ -17,16 +17,25 @@
 
 namespace qd {
 
-constexpr int kStepSlotBytes = 8192;      // one ring item (1024-byte multiple: swizzled boxes)
+constexpr int kStepSlotBytes = 9216;      // one ring item (1024-byte multiple: swizzled boxes)
 constexpr int kStepResFloats = 2048;      // per-CTA row results of one phase
 constexpr int kStepMaxSlots = 20;
+constexpr int kStepProducers = 4;           // copy-issuing threads per CTA (one per producer warp)
 // A GEMV ring item is kStepLines row-lines of one K-tile of up to
-// kStepTileBytes bytes a row, each line at a padded shared-memory stride, then
-// (INT4) the 16-byte-aligned cover of each line's scales.
+// kStepTileBytes bytes a row, loaded by one 3-D TMA box per matrix (rows x
+// 128-byte chunks x 128 bytes, 128-byte swizzle: line i, chunk c sits in
+// 128-byte segment i * chunks + c of the box with its 16-byte units
+// XOR-permuted by the segment index), then (INT4) the 16-byte-aligned cover
+// of the lines' whole scale rows at kStepScaleOff.  Gate/up items hold two
+// boxes of two rows, the gate box at 0 and the up box at kStepUpOff (each box
+// starts on a 1024-byte boundary), and two covers at kStepGuScaleOff and
+// kStepGuScaleOff + kStepGuScaleSpan.
 constexpr int kStepLines = 4;
 constexpr int kStepTileBytes = 1792;
-constexpr int kStepLineStride = kStepTileBytes + 16;
-constexpr int kStepScaleLine = 96;
+constexpr int kStepScaleOff = kStepLines * kStepTileBytes;
+constexpr int kStepUpOff = 4096;
+constexpr int kStepGuScaleOff = kStepUpOff + 2 * kStepTileBytes;
+constexpr int kStepGuScaleSpan = 768;
 // Staged activations: fp16 (INT4/INT8 weights) or bf16 hi/lo pairs (bf16
 // weights) laid out as mma B fragments, then one fp32 correction per block.
 constexpr int kStepMaxStageK = 18944;
@@ -49,7 +58,11 @@ constexpr int kSyncMaxKvHeads = 16;
 // Device error codes beyond kErr* of kernels.h.
 constexpr int kErrTimeout = 16;
 
+// Weight tensor maps of a layer (3-D codes boxes, see above).
+enum StepMap : int { kMapQ = 0, kMapK = 1, kMapV = 2, kMapO = 3, kMapGate = 4, kMapUp = 5, kMapDown = 6, kMapCount = 7 };
+
 struct StepLayer {
+    const CUtensorMap *tm;       // [kMapCount] in device memory
     const void *w[3], *s[3];     // q, k, v codes and scales
     const uint16_t *b[3];        // q, k, v bias (bf16) or null
     const void *wo, *so, *wg, *sg, *wu, *su, *wd, *sd;
@@ -69,6 +82,7 @@ struct StepGeo {
 
 struct StepParams {
     CUtensorMap tm_k, tm_v;      // KV pools as 2-D [rows][d] bf16, 128-byte swizzled 16-row boxes
+    CUtensorMap tm_lm;           // LM head codes (3-D box like the layer weights)
     StepGeo geo[kPhCount];
     const StepLayer *layers;     // [L], device memory
     int L, h, Hq, Hkv, d, F, V;
@@ -103,6 +117,9 @@ struct StepLaunch {
 // what the persistent kernel supports (the engine then runs the kernel chain).
 bool step_plan(StepParams &p, int weight_fmt, int lm_fmt, int n_sm, int max_smem, StepLaunch &out);
 cudaError_t step_encode_kv_maps(StepParams &p, size_t total_rows);
+// 3-D box map of a weight matrix [N][row_bytes] for phase geometry g (box:
+// 128 bytes x g.tk / 128 chunks x `lines` rows); row_bytes % 128 == 0.
+cudaError_t step_encode_weight_map(CUtensorMap *map, const void *w, int N, const StepGeo &g, int lines);
 cudaError_t launch_step(const StepLaunch &sl, const StepParams &p, cudaStream_t stream);
 // CTAs of the step kernel that fit on one SM (the launch needs >= 1).
 cudaError_t step_occupancy(const StepLaunch &sl, int *blocks_per_sm);

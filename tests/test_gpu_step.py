@@ -122,3 +122,23 @@ def test_full_width_two_layers_vs_oracle(name, T0):
             tok = int(np.argmax(ref))
     finally:
         eng.close()
+
+
+def test_full_width_steps_do_not_stall():
+    """Every wait in the kernel is bounded by 1 s; a step that finishes only through such a
+    timeout (a wait on the wrong barrier phase) is still correct but takes ~1 s.  Twenty steps
+    of the 2-layer 7B shape take well under a millisecond each."""
+    import time
+    from quantized_decode_gb300 import Engine
+    cfg = sm.CONFIGS["qwen2.5-7b"].with_(n_layers=2)
+    eng = Engine(device_model(cfg, SEED))
+    try:
+        eng.set_persistent(True)
+        fill_kv(eng, cfg, 11, 3000)
+        eng.decode_step(7)
+        t0 = time.perf_counter()
+        for _ in range(20):
+            eng.decode_step()
+        assert time.perf_counter() - t0 < 0.5
+    finally:
+        eng.close()
