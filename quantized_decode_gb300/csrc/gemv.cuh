@@ -110,8 +110,8 @@ constexpr int act_blk_bytes() {
 // At the end of a tile the 8 partial sums of each row are combined with
 // shuffles and `epi(tile, out)` runs on every lane (all lanes of a row slot
 // hold the same sums).  `sync()` (the dependency wait and the activation
-// staging) runs on all threads once, before the first weight copy, so the
-// activation loads do not queue behind the weight stream.
+// staging) runs on all threads once, after the ring's first D - 1 steps of
+// weight copies are on their way.
 //
 // Ring layout per warp: stage s, row i, unit h, lane l -> 16-byte unit at
 // ring[((s * RT + i) * 2 + h) * 32 + l] and scale word at sring[same index].
@@ -180,7 +180,6 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
     const int my_tiles = t_first < n_tiles ? (n_tiles - 1 - t_first) / t_stride + 1 : 0;
     const int F = my_tiles * n_it;
 
-    sync();
     const uint32_t xm = swz_mask((uint32_t)j, act_blk_bytes<FMT>());  // same for both units of every slab
 
     int lt = t_first, li = 0;  // load cursor
@@ -214,10 +213,14 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
             if (lt < n_tiles) load_rows(lt);
         }
     };
+    // The first D - 1 steps of weights go out before the dependency wait:
+    // nothing an earlier kernel writes is read by them, so under programmatic
+    // dependent launch they overlap the previous kernel's tail.
     for (int s = 0; s < D - 1; ++s) {
         if (s < F) issue(s);
         cp_async_commit();
     }
+    sync();
 
     float acc[RT];
 #pragma unroll

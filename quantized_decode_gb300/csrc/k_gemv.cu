@@ -13,7 +13,10 @@ namespace qd {
 namespace {
 
 constexpr int kMaxWarps = 12;
-constexpr int kD = 3;  // ring depth
+// Ring depth: copies D - 1 steps ahead of the arithmetic.  Deeper rings keep
+// more weight bytes in flight per SM (HBM latency under load is ~2-3 us).
+template <int RT>
+constexpr int kDepth = RT >= 4 ? 4 : 5;
 
 QD_DEV float silu(float a) { return a / (1.f + __expf(-a)); }
 
@@ -35,10 +38,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
     const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
-    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * RT * 2 * 32;
-    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * RT * 2 * 32 * 16) +
-                      (size_t)warp * kD * RT * 2 * 32;
-    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<RT, kD>()) +
+    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kDepth<RT> * RT * 2 * 32;
+    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kDepth<RT> * RT * 2 * 32 * 16) +
+                      (size_t)warp * kDepth<RT> * RT * 2 * 32;
+    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<RT, kDepth<RT>>()) +
                   (size_t)tslot * ks * 32 * RT;
     float post = 1.f;
     float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                 st_mx = fmaxf(st_mx, fabsf(yv));
             }
         };
-        gemv_stream<FMT, RT, kD>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
+        gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
                                  sring);
     } else {
         const int TR = S * RT;
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                 st_mx = fmaxf(st_mx, fabsf(a.stats_gamma ? v * bf16_bits_to_float(__ldg(a.stats_gamma + r)) : v));
             }
         };
-        gemv_stream<FMT, RT, kD>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
+        gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
                                  sring);
     }
     if (a.stats_out) write_block_stats(st_ss, st_mx, a.stats_out, red);
@@ -112,10 +115,13 @@ cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
     constexpr int LPR = kLanesPerRow;
     const int rows_per_tile = a.mode == 2 ? (32 / LPR) * (RT / 2) : (32 / LPR) * RT;
     const int tiles = a.N / rows_per_tile;
-    GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots, kMaxWarps);
+    const size_t fixed = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    const size_t per_warp = ring_bytes_per_warp<RT, kDepth<RT>>() + (size_t)32 * RT * 4;
+    const int fit = (int)((kMaxSmemOptin - fixed) / per_warp);  // warps whose rings fit in shared memory
+    GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots,
+                            (fit < kMaxWarps ? fit : kMaxWarps) / ks * ks);
     a.ks = ks;
-    const size_t smem = (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)pl.nw * ring_bytes_per_warp<RT, kD>() +
-                        (size_t)pl.nw * 32 * RT * 4;
+    const size_t smem = fixed + (size_t)pl.nw * per_warp;
     return launch_k(lc, k_gemv<FMT, RT>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
 }
 

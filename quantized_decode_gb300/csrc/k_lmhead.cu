@@ -16,7 +16,7 @@ namespace {
 
 constexpr int kMaxWarps = 8;
 constexpr int kRT = 4;  // rows per lane
-constexpr int kD = 3;   // ring depth
+constexpr int kD = 4;   // ring depth (copies 3 steps ahead)
 
 QD_DEV void better(float &v, int &i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) {

@@ -15,7 +15,7 @@ namespace qd {
 namespace {
 
 constexpr int kRT = 2;  // rows per lane
-constexpr int kD = 3;   // ring depth
+constexpr int kD = 5;   // ring depth (copies 4 steps ahead)
 
 template <int D>
 QD_DEV void head_epilogue(const QkvArgs &a, int head, int pos, int lane) {

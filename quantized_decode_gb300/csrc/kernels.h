@@ -10,6 +10,7 @@ constexpr int kPageTokens = 16;   // KV tokens per page (16-token pages, bf16)
 constexpr int kGroup = 128;       // INT4 quantization group along K
 constexpr int kMaxGqa = 8;        // query heads per KV head supported by the attention kernel
 constexpr int kStatSlots = 256;   // (sum of squares, max) pairs per producer: one per CTA, >= grid
+constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in to (sm_103a)
 
 // Device-side error word (sticky until the host clears it).
 enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3 };
