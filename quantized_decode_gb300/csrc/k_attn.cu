@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     extern __shared__ __align__(128) uint16_t smem[];
     __shared__ float s_cm[8], s_cl[8];
     __shared__ __align__(16) float s_co[8][D];
-    __shared__ float s_fw[8][32];
+    __shared__ float s_fw[8][32], s_fl[8][32];
     __shared__ int s_last;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -317,7 +317,9 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     // ---- last cluster of KV head g: merge the C cluster partials (C <= 32)
     if (tid < G * C) {
         const int h = tid / C, c = tid % C;
-        s_fw[h][c] = __ldcg(a.part_ml + (((size_t)g * C + c) * G + h) * 2);
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + ((size_t)g * C + c) * G + h);
+        s_fw[h][c] = ml.x;
+        s_fl[h][c] = ml.y;
     }
     __syncthreads();
     if (tid < G) {
@@ -326,22 +328,39 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
         float den = 0.f;
         for (int c = 0; c < C; ++c) {
             const float f = s_fw[tid][c] == -INFINITY ? 0.f : exp2f(s_fw[tid][c] - M);
-            den = fmaf(f, __ldcg(a.part_ml + (((size_t)g * C + c) * G + tid) * 2 + 1), den);
+            den = fmaf(f, s_fl[tid][c], den);
             s_fw[tid][c] = f;
         }
         s_cl[tid] = 1.f / den;
     }
     __syncthreads();
     float mx = 0.f, ss = 0.f;
-    for (int idx = tid; idx < G * D; idx += kNT) {
-        const int h = idx / D, dim = idx % D;
-        float num = 0.f;
-        for (int c = 0; c < C; ++c)
-            num = fmaf(s_fw[h][c], __ldcg(a.part_o + (((size_t)g * C + c) * G + h) * D + dim), num);
-        const float v = num * s_cl[h];
-        a.out[(size_t)(g * G) * D + idx] = v;
-        mx = fmaxf(mx, fabsf(v));
-        ss += v * v;
+    // every output of the thread at once, the cluster partials four at a time:
+    // the L2 reads of a batch are in flight together
+    constexpr int kPer = (G * D + kNT - 1) / kNT;
+    float num[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) num[r] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < C; ++c) {
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const int idx = tid + r * kNT;
+            if (idx < G * D) {
+                const int h = idx / D, dim = idx % D;
+                num[r] = fmaf(s_fw[h][c], __ldcg(a.part_o + (((size_t)g * C + c) * G + h) * D + dim), num[r]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int idx = tid + r * kNT;
+        if (idx < G * D) {
+            const float v = num[r] * s_cl[idx / D];
+            a.out[(size_t)(g * G) * D + idx] = v;
+            mx = fmaxf(mx, fabsf(v));
+            ss += v * v;
+        }
     }
     if (a.stats_out) {
         ss = warp_sum(ss);
