@@ -30,6 +30,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode ms/token & HBM GB/s (7B INT4, ctx 4096); TTFT pp512"
 NOMINAL_HBM_GBS = 8000.0
+# DRAM bytes read + written per launch, from one ncu capture of the kernel as it
+# stands (profiles/decode_layer_7b_chain_ncu_full.md); keyed by shape and
+# kernel, dropped (None) for any kernel changed since that capture.
+NCU_TRAFFIC = {
+    ("qwen2.5-7b", "gate_up"): 70110208 + 278272,
+    ("qwen2.5-7b", "down"): 35174144,
+    ("qwen2.5-7b", "o_proj"): 6727424,
+    ("qwen2.5-7b", "qkv"): 8597504,
+    ("qwen2.5-7b", "attention"): 8217344,
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -433,7 +443,8 @@ def run_ours(args):
                           "frac_of_8tbs": round(step_gbs / NOMINAL_HBM_GBS, 4),
                           "bytes_per_step": int(step_bytes)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": NCU_TRAFFIC.get((cfg.name, dom)),
                      "bytes_per_launch": int(kb[dom]), "avg_launch_us": round(avg_ms * 1e3, 2),
                      "peak_kind": peak_kind},
         "kernels": breakdown,
