@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-ttft", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-kv-sweep", action="store_true",
+                   help="skip the ms/token sweep over KV lengths (512, 2048; 8192-32768 long context)")
     p.add_argument("--profile-steps", type=int, default=4)
     p.add_argument("--step", default="chain", choices=["chain", "persistent"],
                    help="decode step as a kernel chain or as one persistent kernel")
@@ -348,6 +350,40 @@ def run_ours(args):
     step_gbs = step_bytes / (ms_per_token * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
+    # ---- ms/token at other KV lengths of the same cache (the workload's 512 / 2048 / 4096 sweep)
+    def timed_at(e, L, n=64):
+        e.debug_kv(set_len=L)        # K/V rows below L hold the seeded fill (or earlier steps)
+        e.decode_enqueue(4)
+        e.debug_kv(set_len=L)
+        s5, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s5.record(stream)
+        e.decode_enqueue(n)
+        e5.record(stream)
+        torch.cuda.synchronize()
+        e.sync()
+        return round(s5.elapsed_time(e5) / n, 4)
+
+    kv_sweep = None
+    if not args.no_kv_sweep and ws == 1 and ctx >= 2048 + 64:
+        kv_sweep = {str(L): timed_at(eng, L) for L in (512, 2048) if L + 64 <= ctx}
+        kv_sweep[str(ctx)] = round(ms_per_token, 4)
+        eng.debug_kv(set_len=T0)
+
+    # ---- long-context decode: the same weights with a 32K cache pre-filled with seeded K/V
+    # through a shuffled page table; 64 greedy steps at 8192, 16384 and 32768 tokens
+    long_ctx = None
+    if not args.no_kv_sweep and ws == 1 and args.layers == 0 and args.vocab == 0:
+        lmax = 32768
+        cfg_l = cfg.with_(max_context=lmax + 128)
+        eng_l = Engine(DeviceModel(cfg_l, *rec), stream=stream.cuda_stream)
+        try:
+            fill_kv(eng_l, cfg_l, args.seed + 2, lmax,
+                    page_perm=synth.permutation(args.seed, 4, (cfg_l.max_context + 15) // 16))
+            eng_l.decode_step(7)
+            long_ctx = {str(L): timed_at(eng_l, L) for L in (8192, 16384, 32768)}
+        finally:
+            eng_l.close()
+
     # ---- the other step form (persistent kernel vs kernel chain), same cache and greedy chain
     other_ms = None
     try:
@@ -449,6 +485,8 @@ def run_ours(args):
                      "peak_kind": peak_kind},
         "kernels": breakdown,
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
+        "kv_sweep_ms_per_token": kv_sweep,
+        "long_context_ms_per_token": long_ctx,
         "eager_ms_per_token": round(eager_ms, 4),
         "graph_no_pdl_ms_per_token": round(no_pdl_ms, 4),
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
