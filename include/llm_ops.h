@@ -92,6 +92,16 @@ int llm_op_dequant_f16(int32_t fmt, const void *w, const void *s, int32_t N, int
 int llm_op_gemm_f16(const void *A, const void *B, int32_t M, int32_t N, int32_t K, float *C,
                     void *stream);
 
+/* C[m][n] = sum_k A[m][k] * W[n][k] on the tcgen05 tensor cores with the
+ * weights dequantized inside the kernel (the prefill GEMM as the engine runs
+ * it): W is fmt 1 = INT4 group-128 (w: LLM_LAYOUT_INT4_VALUESHUFFLE words
+ * [N][K/8], s: bf16 [N][K/128]) or fmt 2 = INT8 per row (w: int8 [N][K],
+ * s: fp32 [N]); each code tile is converted to fp16 in shared memory (exact
+ * for INT4, one rounding for INT8) and never written back.  A: fp16 [M][K],
+ * C: fp32 [M][N], 16-byte aligned.  M >= 1, N % 128 == 0, K % 128 == 0.      */
+int llm_op_gemm_quant(int32_t fmt, const void *A, const void *w, const void *s, int32_t M, int32_t N,
+                      int32_t K, float *C, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,6 +78,7 @@ SIGNATURES = {
     "llm_op_attention_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
     "llm_op_dequant_f16": (i32, [i32, vp, vp, i32, i32, vp, vp]),
     "llm_op_gemm_f16": (i32, [vp, vp, i32, i32, i32, vp, vp]),
+    "llm_op_gemm_quant": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, vp]),
 }
 
 _lib = None

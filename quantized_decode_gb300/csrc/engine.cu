@@ -65,9 +65,10 @@ struct llm_t {
     bool pf_ready = false;
     int pf_rows = 0;            // prompt rows per chunk
     float *pf_x = nullptr, *pf_raw = nullptr;
-    uint16_t *pf_a = nullptr, *pf_u = nullptr, *pf_qh = nullptr, *pf_ql = nullptr, *pf_w = nullptr;
+    uint16_t *pf_a = nullptr, *pf_u = nullptr, *pf_qh = nullptr, *pf_ql = nullptr;
     int *pf_tok = nullptr;
-    CUtensorMap pf_map_ah{}, pf_map_aq{}, pf_map_u{}, pf_map_wqkv{}, pf_map_wo{}, pf_map_wgu{}, pf_map_wd{};
+    CUtensorMap pf_map_ah{}, pf_map_aq{}, pf_map_u{};
+    std::vector<CUtensorMap> pf_wmaps;  // per layer: q, k, v, o, gate, up, down code tiles
 
     int32_t *pinned = nullptr;  // host staging: [0] forced token, [2..3] last_token, err
     cudaGraph_t graph = nullptr;
@@ -100,7 +101,7 @@ void free_all(llm_t *h) {
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
                     h->d_layers, h->d_maps, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
-                    h->pf_qh, h->pf_ql, h->pf_w, h->pf_tok};
+                    h->pf_qh, h->pf_ql, h->pf_tok};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -365,7 +366,7 @@ int fetch_token(llm_t *h, int32_t *out) {
 
 // ---- batched prefill -------------------------------------------------------------
 // Rows of a prompt chunk go through the layers as GEMMs: RMSNorm -> fp16 rows,
-// each weight matrix dequantized to an fp16 scratch copy, tcgen05 GEMM with a
+// tcgen05 GEMMs that dequantize each weight code tile in shared memory, with a
 // fused epilogue (QKV store, o_proj/down residual add, gate/up SiLU * mul),
 // causal flash attention over the paged cache.  The last row of the prompt
 // then runs the decode step's LM head (+ argmax), which also advances the
@@ -374,8 +375,10 @@ constexpr int kPrefillChunk = 1024;
 
 bool prefill_shapes_ok(const llm_config &c) {
     const int d = c.head_dim, rq = c.n_q_heads * d, nq = (c.n_q_heads + 2 * c.n_kv_heads) * d;
-    return nq % kTcBN == 0 && c.hidden % kTcBN == 0 && c.mlp % 64 == 0 && c.hidden % kTcBK == 0 &&
-           rq % kTcBK == 0 && c.mlp % kTcBK == 0;
+    const int rkv = c.n_kv_heads * d;
+    // every 128-row weight tile lies in one matrix (q, k, v stacked); K % 128 for the code tiles
+    return rq % kTcBN == 0 && rkv % kTcBN == 0 && nq % kTcBN == 0 && c.hidden % kTcBN == 0 && c.mlp % 64 == 0 &&
+           c.hidden % 128 == 0 && rq % 128 == 0 && c.mlp % 128 == 0;
 }
 
 int prefill_alloc(llm_t *h) {
@@ -384,26 +387,34 @@ int prefill_alloc(llm_t *h) {
     const int d = c.head_dim, rq = c.n_q_heads * d, nq = (c.n_q_heads + 2 * c.n_kv_heads) * d;
     const int R = ((c.max_context < kPrefillChunk ? c.max_context : kPrefillChunk) + kTcBM - 1) / kTcBM * kTcBM;
     h->pf_rows = R;
-    const size_t wmax = std::max(std::max((size_t)nq * c.hidden, (size_t)c.hidden * rq),
-                                 std::max((size_t)2 * c.mlp * c.hidden, (size_t)c.hidden * c.mlp));
     const size_t arow = (size_t)std::max(c.hidden, rq);
     bool ok = dalloc(&h->pf_x, (size_t)R * c.hidden) == cudaSuccess &&
               dalloc(&h->pf_raw, (size_t)R * nq) == cudaSuccess && dalloc(&h->pf_a, (size_t)R * arow) == cudaSuccess &&
               dalloc(&h->pf_u, (size_t)R * c.mlp) == cudaSuccess && dalloc(&h->pf_qh, (size_t)R * rq) == cudaSuccess &&
-              dalloc(&h->pf_ql, (size_t)R * rq) == cudaSuccess && dalloc(&h->pf_w, wmax) == cudaSuccess &&
-              dalloc(&h->pf_tok, (size_t)R) == cudaSuccess;
+              dalloc(&h->pf_ql, (size_t)R * rq) == cudaSuccess && dalloc(&h->pf_tok, (size_t)R) == cudaSuccess;
     if (!ok) return LLM_ERR_CUDA;
     // rows past a chunk's end are read by the GEMMs (their outputs are dropped): keep them finite
     ok = cudaMemsetAsync(h->pf_a, 0, (size_t)R * arow * 2, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->pf_u, 0, (size_t)R * c.mlp * 2, h->stream) == cudaSuccess &&
          tc_operand_map(&h->pf_map_ah, h->pf_a, R, c.hidden) == cudaSuccess &&
          tc_operand_map(&h->pf_map_aq, h->pf_a, R, rq) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_u, h->pf_u, R, c.mlp) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_wqkv, h->pf_w, nq, c.hidden) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_wo, h->pf_w, c.hidden, rq) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_wgu, h->pf_w, (uint64_t)2 * c.mlp, c.hidden) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_wd, h->pf_w, c.hidden, c.mlp) == cudaSuccess;
+         tc_operand_map(&h->pf_map_u, h->pf_u, R, c.mlp) == cudaSuccess;
     if (!ok) return LLM_ERR_CUDA;
+    // code-tile maps of every weight matrix (the GEMMs dequantize in shared memory)
+    const int rkv = c.n_kv_heads * d;
+    h->pf_wmaps.assign((size_t)c.n_layers * 7, CUtensorMap{});
+    for (int l = 0; l < c.n_layers; ++l) {
+        const llm_layer_weights &L = h->layers[l];
+        CUtensorMap *m = h->pf_wmaps.data() + (size_t)l * 7;
+        ok = tc_weight_map(m + 0, L.wq, h->fmt, rq, c.hidden, kTcBN) == cudaSuccess &&
+             tc_weight_map(m + 1, L.wk, h->fmt, rkv, c.hidden, kTcBN) == cudaSuccess &&
+             tc_weight_map(m + 2, L.wv, h->fmt, rkv, c.hidden, kTcBN) == cudaSuccess &&
+             tc_weight_map(m + 3, L.wo, h->fmt, c.hidden, rq, kTcBN) == cudaSuccess &&
+             tc_weight_map(m + 4, L.wg, h->fmt, c.mlp, c.hidden, kTcBN / 2) == cudaSuccess &&
+             tc_weight_map(m + 5, L.wu, h->fmt, c.mlp, c.hidden, kTcBN / 2) == cudaSuccess &&
+             tc_weight_map(m + 6, L.wd, h->fmt, c.hidden, c.mlp, kTcBN) == cudaSuccess;
+        if (!ok) return LLM_ERR_CUDA;
+    }
     h->pf_ready = true;
     return LLM_OK;
 }
@@ -414,31 +425,39 @@ cudaError_t prefill_chunk(llm_t *h, int m, int pos0) {
     const llm_config &c = h->cfg;
     const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d, nq = rq + 2 * rkv;
     cudaStream_t st = h->stream;
-    const int n_sm = h->lc.n_sm;
     int *err = &h->st->err;
     cudaError_t e;
-    auto gemm = [&](const CUtensorMap &am, const CUtensorMap &bm, int N, int K, int mode, float *cc, int ldc,
-                    uint16_t *hh, int ldh) {
+    // A (fp16 rows) x the weight codes of up to three stacked matrices, or an interleaved pair
+    auto gemm = [&](const CUtensorMap &am, const CUtensorMap *w0, const CUtensorMap *w1, const CUtensorMap *w2,
+                    TcQuantB qb, int N, int K, int mode, float *cc, int ldc, uint16_t *hh, int ldh) {
+        const CUtensorMap wm[3] = {*w0, w1 ? *w1 : *w0, w2 ? *w2 : *w0};
+        qb.fmt = h->fmt;
         TcGemmArgs g{};
         g.M = m; g.N = N; g.K = K; g.mode = mode; g.c = cc; g.ldc = ldc; g.h = hh; g.ldh = ldh;
         g.err = err; g.wait_ns = 1000000000ull;
-        return launch_tc_gemm(st, am, bm, g);
+        return launch_tc_gemm_q(st, am, wm, qb, g);
     };
-    auto dequant = [&](const void *w, const void *sc, const void *w2, const void *s2, int N, int K, uint16_t *out) {
-        DequantArgs q{};
-        q.fmt = h->fmt; q.w = w; q.s = sc; q.w2 = w2; q.s2 = s2; q.N = N; q.K = K; q.out = out;
-        return launch_dequant(st, n_sm, q);
+    auto one = [](const void *scale, int rows) {
+        TcQuantB q{};
+        q.n_seg = 1; q.seg_rows[0] = rows; q.scale[0] = scale;
+        return q;
     };
     if ((e = launch_embed_rows(st, (const uint16_t *)h->w.embed, h->pf_tok, m, c.hidden, h->pf_x)) != cudaSuccess)
         return e;
     for (int l = 0; l < c.n_layers; ++l) {
         const llm_layer_weights &L = h->layers[l];
         uint16_t *kp = h->k_pool + (size_t)l * h->layer_kv_elems, *vp = h->v_pool + (size_t)l * h->layer_kv_elems;
+        const CUtensorMap *wm = h->pf_wmaps.data() + (size_t)l * 7;
+        TcQuantB qkv{};
+        qkv.n_seg = 3;
+        qkv.seg_rows[0] = rq; qkv.seg_rows[1] = rkv; qkv.seg_rows[2] = rkv;
+        qkv.scale[0] = L.sq; qkv.scale[1] = L.sk; qkv.scale[2] = L.sv;
+        TcQuantB gu{};
+        gu.interleave = 1;
+        gu.seg_rows[0] = gu.seg_rows[1] = c.mlp;
+        gu.scale[0] = L.sg; gu.scale[1] = L.su;
         if ((e = launch_rmsnorm_rows(st, h->pf_x, (const uint16_t *)L.attn_norm, c.rms_eps, m, c.hidden, h->pf_a)) ||
-            (e = dequant(L.wq, L.sq, nullptr, nullptr, rq, c.hidden, h->pf_w)) ||
-            (e = dequant(L.wk, L.sk, nullptr, nullptr, rkv, c.hidden, h->pf_w + (size_t)rq * c.hidden)) ||
-            (e = dequant(L.wv, L.sv, nullptr, nullptr, rkv, c.hidden, h->pf_w + (size_t)(rq + rkv) * c.hidden)) ||
-            (e = gemm(h->pf_map_ah, h->pf_map_wqkv, nq, c.hidden, kEpiStore, h->pf_raw, nq, nullptr, 0)))
+            (e = gemm(h->pf_map_ah, wm + 0, wm + 1, wm + 2, qkv, nq, c.hidden, kEpiStore, h->pf_raw, nq, nullptr, 0)))
             return e;
         QkvRowsArgs qa{};
         qa.raw = h->pf_raw;
@@ -459,13 +478,13 @@ cudaError_t prefill_chunk(llm_t *h, int m, int pos0) {
         aa.n_pages = h->n_pages; aa.n = m; aa.pos0 = pos0; aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d;
         aa.out = h->pf_a; aa.err = err;
         if ((e = launch_qkv_rows(st, qa)) || (e = launch_attn_rows(st, aa)) ||
-            (e = dequant(L.wo, L.so, nullptr, nullptr, c.hidden, rq, h->pf_w)) ||
-            (e = gemm(h->pf_map_aq, h->pf_map_wo, c.hidden, rq, kEpiAdd, h->pf_x, c.hidden, nullptr, 0)) ||
+            (e = gemm(h->pf_map_aq, wm + 3, nullptr, nullptr, one(L.so, c.hidden), c.hidden, rq, kEpiAdd, h->pf_x,
+                      c.hidden, nullptr, 0)) ||
             (e = launch_rmsnorm_rows(st, h->pf_x, (const uint16_t *)L.mlp_norm, c.rms_eps, m, c.hidden, h->pf_a)) ||
-            (e = dequant(L.wg, L.sg, L.wu, L.su, c.mlp, c.hidden, h->pf_w)) ||
-            (e = gemm(h->pf_map_ah, h->pf_map_wgu, 2 * c.mlp, c.hidden, kEpiSwiGlu, nullptr, 0, h->pf_u, c.mlp)) ||
-            (e = dequant(L.wd, L.sd, nullptr, nullptr, c.hidden, c.mlp, h->pf_w)) ||
-            (e = gemm(h->pf_map_u, h->pf_map_wd, c.hidden, c.mlp, kEpiAdd, h->pf_x, c.hidden, nullptr, 0)))
+            (e = gemm(h->pf_map_ah, wm + 4, wm + 5, nullptr, gu, 2 * c.mlp, c.hidden, kEpiSwiGlu, nullptr, 0,
+                      h->pf_u, c.mlp)) ||
+            (e = gemm(h->pf_map_u, wm + 6, nullptr, nullptr, one(L.sd, c.hidden), c.hidden, c.mlp, kEpiAdd, h->pf_x,
+                      c.hidden, nullptr, 0)))
             return e;
     }
     return cudaSuccess;

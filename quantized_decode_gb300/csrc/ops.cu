@@ -128,4 +128,21 @@ int llm_op_gemm_f16(const void *A, const void *B, int32_t M, int32_t N, int32_t 
     return status(launch_tc_gemm((cudaStream_t)stream, am, bm, a));
 }
 
+int llm_op_gemm_quant(int32_t fmt, const void *A, const void *w, const void *s, int32_t M, int32_t N, int32_t K,
+                      float *C, void *stream) {
+    if (!a16(A) || !a16(w) || !s || !a16(C) || M <= 0 || N <= 0 || K <= 0 || N % kTcBN || K % 128) return LLM_ERR_ARG;
+    if (fmt != LLM_FMT_INT4_G128 && fmt != LLM_FMT_INT8_ROW) return LLM_ERR_ARG;
+    const int f = fmt == LLM_FMT_INT4_G128 ? kFmtInt4 : kFmtInt8;
+    CUtensorMap am, wm[3];
+    if (tc_operand_map(&am, A, (uint64_t)M, (uint64_t)K) != cudaSuccess ||
+        tc_weight_map(&wm[0], w, f, (uint64_t)N, (uint64_t)K, kTcBN) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    wm[1] = wm[2] = wm[0];
+    TcQuantB b{};
+    b.fmt = f; b.interleave = 0; b.n_seg = 1; b.seg_rows[0] = N; b.scale[0] = s;
+    TcGemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.mode = kEpiStore; a.c = C; a.ldc = N; a.wait_ns = 1000000000ull;
+    return status(launch_tc_gemm_q((cudaStream_t)stream, am, wm, b, a));
+}
+
 }  // extern "C"

@@ -41,6 +41,23 @@ cudaError_t tc_operand_map(CUtensorMap *map, const void *base, uint64_t rows, ui
 cudaError_t launch_tc_gemm(cudaStream_t stream, const CUtensorMap &a_map, const CUtensorMap &b_map,
                            const TcGemmArgs &a);
 
+// ---- the same GEMM with quantized weights dequantized inside the kernel -------
+// B = the weight codes: up to three stacked matrices (QKV: seg_rows = q, k, v
+// rows, each a multiple of 128), or (interleave) a gate/up pair of seg_rows[0]
+// rows each, whose 128-row tiles hold 64 gate rows then the matching 64 up rows.
+struct TcQuantB {
+    int fmt;                 // kFmtInt4 (bf16 group scales) / kFmtInt8 (fp32 row scales)
+    int interleave;
+    int n_seg;
+    int seg_rows[3];
+    const void *scale[3];
+};
+// Tensor map of a code matrix [rows][K] (INT4: K/2 bytes a row) for tiles of
+// box_rows (128, or 64 for an interleaved pair) x 64 codes.
+cudaError_t tc_weight_map(CUtensorMap *map, const void *codes, int fmt, uint64_t rows, uint64_t K, int box_rows);
+cudaError_t launch_tc_gemm_q(cudaStream_t stream, const CUtensorMap &a_map, const CUtensorMap (&w_maps)[3],
+                             const TcQuantB &b, const TcGemmArgs &a);
+
 // ---- weight dequantization to fp16 rows ----------------------------------------
 // out[r][k] = code[src(r)][k] * scale (INT4: bf16 group scale; INT8: fp32 row
 // scale), fp16.  With `interleave` (gate/up pair, w2/s2 = up matrix) output

@@ -78,6 +78,9 @@ QD_DEV void tmem_alloc(uint32_t *slot, uint32_t ncols) {
 QD_DEV void tmem_free(uint32_t base, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
 }
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / tensor core) accesses.
+QD_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 QD_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 QD_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

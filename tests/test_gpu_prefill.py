@@ -85,6 +85,36 @@ def test_gemm_f16_vs_float64(lib, M, N, K):
     assert np.all(err <= 1e-5 * absacc + 1e-30), float(np.max(err / absacc))
 
 
+@pytest.mark.parametrize("fmt,M,N,K", [(1, 1, 128, 128), (1, 130, 256, 384), (1, 512, 4608, 3584),
+                                       (1, 77, 3584, 18944), (2, 200, 384, 4096), (2, 64, 256, 12288)])
+def test_gemm_quant_vs_float64(lib, fmt, M, N, K):
+    """In-kernel dequantization: C against a float64 matmul of A and the oracle's dequantized
+    weights (INT4: the exact products; INT8: the weights as fp16 after one rounding)."""
+    import quantized_decode_gb300 as qd
+    a = _f16(41, M * 7 + K, M, K, 1.0)
+    if fmt == 1:
+        codes, scales = sm.quantized_tensor(sm.FMT_INT4_G128, 42, N + K, N, K)
+        w = to_dev(qd.pack_int4(codes))
+        sc = (scales.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        wref = oracle.unpack_int4(oracle.pack_int4(codes), K).astype(np.float64) * np.repeat(sc, 128, axis=1)
+    else:
+        codes, scales = sm.quantized_tensor(sm.FMT_INT8_ROW, 43, N + K, N, K)
+        w = to_dev(np.ascontiguousarray(codes, np.int8))
+        wref = (codes.astype(np.float32) * scales.astype(np.float32)[:, None]).astype(np.float16).astype(np.float64)
+    s = to_dev(scales)
+    ad = to_dev(a)
+    c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    assert lib.llm_op_gemm_quant(fmt, ad.data_ptr(), w.data_ptr(), s.data_ptr(), M, N, K, c.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    got = c.cpu().numpy().astype(np.float64)
+    rows = np.arange(M) if M * N * K <= 2 ** 31 else np.arange(0, M, 5)
+    a64 = a.astype(np.float64)[rows]
+    ref = a64 @ wref.T
+    absacc = np.abs(a64) @ np.abs(wref).T
+    err = np.abs(got[rows] - ref)
+    assert np.all(err <= 1e-5 * absacc + 1e-30), float(np.max(err / absacc))
+
+
 def test_gemm_f16_rejects_bad_shapes(lib):
     a = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
     b = torch.zeros((100, 64), dtype=torch.float16, device="cuda")
