@@ -579,7 +579,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     const int d = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
     h->n_pages = (c.max_context + kPageTokens - 1) / kPageTokens;
     h->layer_kv_elems = (size_t)h->n_pages * c.n_kv_heads * kPageTokens * d;
-    h->P = default_splits(n_sm, c.n_kv_heads, h->n_pages);
+    h->P = default_splits(n_sm, c.n_q_heads, c.n_kv_heads, d, h->n_pages);
     h->lm_grid = lm_head_grid(h->lc, c.vocab);
     const int P_alloc = h->P > n_sm / c.n_kv_heads ? h->P : n_sm / c.n_kv_heads + 1;
     const int lm_alloc = h->lm_grid > n_sm ? h->lm_grid : n_sm;

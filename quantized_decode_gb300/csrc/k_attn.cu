@@ -391,13 +391,64 @@ cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
     return cudaErrorInvalidValue;
 }
 
+// Clusters of the kernel that the device holds at once (0 if the query fails).
+template <int G, int D>
+int max_clusters_gd(int Hkv) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;  // (device, Hkv) -> clusters
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, Hkv});
+    if (it != cache.end()) return it->second;
+    const size_t smem = ring_bytes<D>();
+    if (cudaFuncSetAttribute(k_attn<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCS, Hkv);
+    cfg.blockDim = dim3(kNT);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCS;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_attn<G, D>, &cfg) != cudaSuccess) return 0;
+    cache[{dev, Hkv}] = n;
+    return n;
+}
+template <int G>
+int max_clusters_g(int Hkv, int d) {
+    return d == 128 ? max_clusters_gd<G, 128>(Hkv) : max_clusters_gd<G, 64>(Hkv);
+}
+
 }  // namespace
 
 int attention_split_multiple() { return kCS; }
 
-int default_splits(int n_sm, int Hkv, int max_pages) {
+int default_splits(int n_sm, int Hq, int Hkv, int d, int max_pages) {
     (void)max_pages;
     int C = n_sm / (kCS * Hkv);
+    // every cluster of the grid resident at once: a cluster that has to wait
+    // for a free GPC slot starts a second wave and delays the whole step
+    static const int kMaxG = 8;
+    int mc = 0;
+    if (Hkv >= 1 && Hq % Hkv == 0 && Hq / Hkv <= kMaxG && (d == 64 || d == 128)) {
+        switch (Hq / Hkv) {
+            case 1: mc = max_clusters_g<1>(Hkv, d); break;
+            case 2: mc = max_clusters_g<2>(Hkv, d); break;
+            case 3: mc = max_clusters_g<3>(Hkv, d); break;
+            case 4: mc = max_clusters_g<4>(Hkv, d); break;
+            case 5: mc = max_clusters_g<5>(Hkv, d); break;
+            case 6: mc = max_clusters_g<6>(Hkv, d); break;
+            case 7: mc = max_clusters_g<7>(Hkv, d); break;
+            default: mc = max_clusters_g<8>(Hkv, d); break;
+        }
+    }
+    if (mc > 0 && C * Hkv > mc) C = mc / Hkv;
     if (C < 1) C = 1;
     if (C > 32) C = 32;
     return C * kCS;

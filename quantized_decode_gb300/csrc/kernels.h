@@ -126,7 +126,9 @@ cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a);
 
 // Grid sizes and shape checks used by the engine when it plans buffers.
 int lm_head_grid(const LaunchCfg &lc, int N);
-int default_splits(int n_sm, int Hkv, int max_pages);
+// Splits per KV head: as many 8-CTA clusters as fill the SMs and are resident
+// at once on this device (cudaOccupancyMaxActiveClusters).
+int default_splits(int n_sm, int Hq, int Hkv, int d, int max_pages);
 int attention_split_multiple();  // split counts are multiples of the attention cluster size
 bool gemv_shape_ok(int fmt, int N, int K, int mode);
 bool qkv_shape_ok(int fmt, int rows_q, int rows_kv, int K, int d);

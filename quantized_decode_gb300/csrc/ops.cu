@@ -81,7 +81,7 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, con
     LaunchCfg lc = op_cfg(stream);
     const int n_pg = (T + kPageTokens - 1) / kPageTokens;
     const int cs = attention_split_multiple();
-    const int P = n_splits ? (n_splits + cs - 1) / cs * cs : default_splits(lc.n_sm, Hkv, n_pg);
+    const int P = n_splits ? (n_splits + cs - 1) / cs * cs : default_splits(lc.n_sm, Hq, Hkv, d, n_pg);
     if (P > 256) return LLM_ERR_ARG;
     const int G = Hq / Hkv;
     const size_t o_bytes = (size_t)Hkv * P * G * d * 4, ml_bytes = (size_t)Hkv * P * G * 2 * 4;
