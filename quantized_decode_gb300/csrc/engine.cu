@@ -47,7 +47,7 @@ struct llm_t {
     float *part_o = nullptr, *part_ml = nullptr, *lm_part_val = nullptr;
     float *stats = nullptr;     // 4 x kStatSlots (ss, mx) pairs: attention, o_proj, gate/up, down outputs
     uint16_t *kv_new = nullptr; // [2][Hkv][d] appended rows of the current step
-    int P = 1, lm_grid = 1;
+    int P = 1, attn_cs = 8, lm_grid = 1;
 
     // persistent whole-step kernel
     bool step_ok = false;       // the model fits the persistent kernel
@@ -193,7 +193,7 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         aa.q = h->q; aa.k_pool = qa.k_pool; aa.v_pool = qa.v_pool;
         aa.page_table = h->page_table; aa.n_pages = h->n_pages;
         aa.st = h->st; aa.T_fixed = -1;
-        aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d; aa.P = h->P;
+        aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d; aa.P = h->P; aa.cs = h->attn_cs;
         aa.part_o = h->part_o; aa.part_ml = h->part_ml; aa.counter = h->attn_cnt;
         aa.out = h->attn; aa.err = &h->st->err;
         aa.kv_new = h->kv_new; aa.stats_out = st_attn;
@@ -579,7 +579,9 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     const int d = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
     h->n_pages = (c.max_context + kPageTokens - 1) / kPageTokens;
     h->layer_kv_elems = (size_t)h->n_pages * c.n_kv_heads * kPageTokens * d;
-    h->P = default_splits(n_sm, c.n_q_heads, c.n_kv_heads, d, h->n_pages);
+    const AttnPlan ap = plan_attention(n_sm, c.n_q_heads, c.n_kv_heads, d, h->n_pages);
+    h->P = ap.P;
+    h->attn_cs = ap.cs;
     h->lm_grid = lm_head_grid(h->lc, c.vocab);
     const int P_alloc = h->P > n_sm / c.n_kv_heads ? h->P : n_sm / c.n_kv_heads + 1;
     const int lm_alloc = h->lm_grid > n_sm ? h->lm_grid : n_sm;

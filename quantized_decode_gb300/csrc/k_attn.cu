@@ -1,6 +1,7 @@
 // k_attn.cu - split-K grouped-query decode attention over the paged bf16 KV cache.
 //
-// Grid (P, Hkv) in clusters of kCS CTAs along x: CTA (p, g) owns KV head g and
+// Grid (P, Hkv) in clusters of CS CTAs along x (CS = 8, or 16 where the device
+// holds one such cluster per KV head): CTA (p, g) owns KV head g and
 // a contiguous run of pages of the T = pos + 1 cached tokens, and serves all
 // G = Hq/Hkv query heads of the group from one read of its K/V pages (K and V
 // are read once per KV head, not once per query head).
@@ -20,10 +21,12 @@
 // and V are the exact bf16 cache values.  Softmax is online, in base 2.
 //
 // Partial results merge in three levels, none of which waits on another CTA
-// outside its cluster: the 8 warps of a CTA in shared memory; the kCS CTAs of a
-// cluster through distributed shared memory; the C = P/kCS cluster results of a
+// outside its cluster: the 8 warps of a CTA in shared memory; the CS CTAs of a
+// cluster through distributed shared memory; the C = P/CS cluster results of a
 // KV head by the cluster that arrives last (arrival counter), with the
-// log-sum-exp weights e^(m_c - M) / sum_c e^(m_c - M) l_c.
+// log-sum-exp weights e^(m_c - M) / sum_c e^(m_c - M) l_c.  With one cluster
+// per KV head (C = 1) the second level writes the output and the third is
+// skipped.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -35,7 +38,8 @@ namespace qd {
 
 namespace {
 
-constexpr int kCS = 8;        // CTAs per cluster
+constexpr int kCS = 8;        // CTAs per cluster (portable size)
+constexpr int kCSWide = 16;   // one cluster per KV head (non-portable size)
 constexpr int kWarps = 8;
 constexpr int kNT = kWarps * 32;
 constexpr int kWRing = 2;     // page slots per warp
@@ -83,7 +87,7 @@ constexpr size_t ring_bytes() {
     return (size_t)kWarps * kWRing * 2 * 16 * D * 2;
 }
 
-template <int G, int D>
+template <int G, int D, int CS>
 __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     constexpr int CH = D / 8;      // 16-byte chunks per row
     constexpr int PAGE = 16 * D;   // bf16 elements of one K (or V) page slice
@@ -94,12 +98,13 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     __shared__ float s_cm[8], s_cl[8];
     __shared__ __align__(16) float s_co[8][D];
     __shared__ float s_fw[8][32], s_fl[8][32];
+    __shared__ float s_st[2][kWarps];
     __shared__ int s_last;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int g = blockIdx.y, p = blockIdx.x, P = gridDim.x;
     const int rank = (int)cluster.block_rank();
-    const int C = P / kCS, ci = p / kCS;
+    const int C = P / CS, ci = p / CS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
 
@@ -279,24 +284,34 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     }
     cluster.sync();
 
-    // ---- merge the kCS CTAs of the cluster through distributed shared memory;
-    // rank r merges an equal slice of the G*D outputs into the cluster's partial
+    // ---- merge the CS CTAs of the cluster through distributed shared memory;
+    // rank r merges an equal slice of the G*D outputs into the cluster's partial,
+    // or, with one cluster per KV head, into the final output
+    const bool direct = C == 1 && a.out != nullptr;
+    float st_ss = 0.f, st_mx = 0.f;
     {
-        const int per = (G * D + kCS - 1) / kCS;
+        const int per = (G * D + CS - 1) / CS;
         const int lo = rank * per, hi = min(G * D, lo + per);
         for (int idx = lo + tid; idx < hi; idx += kNT) {
             const int h = idx / D, dim = idx % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < kCS; ++q) M = fmaxf(M, cluster.map_shared_rank(s_cm, q)[h]);
+            for (int q = 0; q < CS; ++q) M = fmaxf(M, cluster.map_shared_rank(s_cm, q)[h]);
             float num = 0.f, den = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
-                for (int q = 0; q < kCS; ++q) {
+                for (int q = 0; q < CS; ++q) {
                     const float f = exp2f(cluster.map_shared_rank(s_cm, q)[h] - M);
                     num = fmaf(f, cluster.map_shared_rank(&s_co[0][0], q)[h * D + dim], num);
                     den = fmaf(f, cluster.map_shared_rank(s_cl, q)[h], den);
                 }
+            }
+            if (direct) {  // den > 0: the cluster holds every token
+                const float v = num * (1.f / den);
+                a.out[(size_t)(g * G) * D + idx] = v;
+                st_ss += v * v;
+                st_mx = fmaxf(st_mx, fabsf(v));
+                continue;
             }
             const size_t slot = (size_t)g * C + ci;
             a.part_o[(slot * G + h) * D + dim] = num;
@@ -305,6 +320,28 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
                 a.part_ml[(slot * G + h) * 2 + 1] = den;
             }
         }
+    }
+    if (direct) {
+        if (a.stats_out) {  // one (ss, mx) slot per CTA: g * CS + rank
+            st_ss = warp_sum(st_ss);
+            st_mx = warp_max(st_mx);
+            if (lane == 0) {
+                s_st[0][warp] = st_ss;
+                s_st[1][warp] = st_mx;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                float a0 = 0.f, b0 = 0.f;
+                for (int w = 0; w < kWarps; ++w) {
+                    a0 += s_st[0][w];
+                    b0 = fmaxf(b0, s_st[1][w]);
+                }
+                a.stats_out[2 * (g * CS + rank)] = a0;
+                a.stats_out[2 * (g * CS + rank) + 1] = b0;
+            }
+        }
+        cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+        return;
     }
     __threadfence();
     cluster.sync();  // no CTA leaves while a peer may still read its shared memory
@@ -383,17 +420,38 @@ __global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
     if (tid == 0) a.counter[g] = 0;
 }
 
+// Clusters above the portable size need the kernel's opt-in (once).
+template <typename K>
+bool allow_wide(K kernel) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, bool> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair((const void *)kernel, dev);
+    auto it = done.find(key);
+    if (it != done.end()) return it->second;
+    const bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    done[key] = ok;
+    return ok;
+}
+
 template <int G>
 cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
     const dim3 grid(a.P, a.Hkv);
-    if (a.d == 128) return launch_kc(lc, k_attn<G, 128>, grid, dim3(kNT), ring_bytes<128>(), kCS, a);
-    if (a.d == 64) return launch_kc(lc, k_attn<G, 64>, grid, dim3(kNT), ring_bytes<64>(), kCS, a);
+    if (a.cs == kCSWide && a.d == 128) {
+        if (!allow_wide(k_attn<G, 128, kCSWide>)) return cudaErrorInvalidValue;
+        return launch_kc(lc, k_attn<G, 128, kCSWide>, grid, dim3(kNT), ring_bytes<128>(), kCSWide, a);
+    }
+    if (a.cs != 0 && a.cs != kCS) return cudaErrorInvalidValue;
+    if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCS>, grid, dim3(kNT), ring_bytes<128>(), kCS, a);
+    if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCS>, grid, dim3(kNT), ring_bytes<64>(), kCS, a);
     return cudaErrorInvalidValue;
 }
 
 // Clusters of the kernel that the device holds at once (0 if the query fails).
-template <int G, int D>
-int max_clusters_gd(int Hkv) {
+template <int G, int D, int CS>
+int max_clusters_gdc(int Hkv) {
     static std::mutex mu;
     static std::map<std::pair<int, int>, int> cache;  // (device, Hkv) -> clusters
     int dev = 0;
@@ -402,28 +460,48 @@ int max_clusters_gd(int Hkv) {
     auto it = cache.find({dev, Hkv});
     if (it != cache.end()) return it->second;
     const size_t smem = ring_bytes<D>();
-    if (cudaFuncSetAttribute(k_attn<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (CS > kCS && !allow_wide(k_attn<G, D, CS>)) return 0;
+    if (cudaFuncSetAttribute(k_attn<G, D, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCS, Hkv);
+    cfg.gridDim = dim3(CS, Hkv);
     cfg.blockDim = dim3(kNT);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kCS;
+    at[0].val.clusterDim.x = CS;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_attn<G, D>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_attn<G, D, CS>, &cfg) != cudaSuccess) n = 0;
     cache[{dev, Hkv}] = n;
     return n;
 }
 template <int G>
-int max_clusters_g(int Hkv, int d) {
-    return d == 128 ? max_clusters_gd<G, 128>(Hkv) : max_clusters_gd<G, 64>(Hkv);
+int max_clusters_g(int Hkv, int d, int cs) {
+    if (cs == kCSWide) return d == 128 ? max_clusters_gdc<G, 128, kCSWide>(Hkv) : 0;
+    return d == 128 ? max_clusters_gdc<G, 128, kCS>(Hkv) : max_clusters_gdc<G, 64, kCS>(Hkv);
 }
+// Clusters of cs CTAs that the device holds at once (0 if unknown).
+int max_clusters(int Hq, int Hkv, int d, int cs) {
+    if (Hkv < 1 || Hq % Hkv || Hq / Hkv > kMaxGqa || (d != 64 && d != 128)) return 0;
+    switch (Hq / Hkv) {
+        case 1: return max_clusters_g<1>(Hkv, d, cs);
+        case 2: return max_clusters_g<2>(Hkv, d, cs);
+        case 3: return max_clusters_g<3>(Hkv, d, cs);
+        case 4: return max_clusters_g<4>(Hkv, d, cs);
+        case 5: return max_clusters_g<5>(Hkv, d, cs);
+        case 6: return max_clusters_g<6>(Hkv, d, cs);
+        case 7: return max_clusters_g<7>(Hkv, d, cs);
+        default: return max_clusters_g<8>(Hkv, d, cs);
+    }
+}
+
+// Contexts up to this many pages take one 16-CTA cluster per KV head when it fits.
+constexpr int kWideMaxPages = 512;
 
 }  // namespace
 
@@ -434,28 +512,27 @@ int default_splits(int n_sm, int Hq, int Hkv, int d, int max_pages) {
     int C = n_sm / (kCS * Hkv);
     // every cluster of the grid resident at once: a cluster that has to wait
     // for a free GPC slot starts a second wave and delays the whole step
-    static const int kMaxG = 8;
-    int mc = 0;
-    if (Hkv >= 1 && Hq % Hkv == 0 && Hq / Hkv <= kMaxG && (d == 64 || d == 128)) {
-        switch (Hq / Hkv) {
-            case 1: mc = max_clusters_g<1>(Hkv, d); break;
-            case 2: mc = max_clusters_g<2>(Hkv, d); break;
-            case 3: mc = max_clusters_g<3>(Hkv, d); break;
-            case 4: mc = max_clusters_g<4>(Hkv, d); break;
-            case 5: mc = max_clusters_g<5>(Hkv, d); break;
-            case 6: mc = max_clusters_g<6>(Hkv, d); break;
-            case 7: mc = max_clusters_g<7>(Hkv, d); break;
-            default: mc = max_clusters_g<8>(Hkv, d); break;
-        }
-    }
+    const int mc = max_clusters(Hq, Hkv, d, kCS);
     if (mc > 0 && C * Hkv > mc) C = mc / Hkv;
     if (C < 1) C = 1;
     if (C > 32) C = 32;
     return C * kCS;
 }
 
+AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages) {
+    // One 16-CTA cluster per KV head: its merge through distributed shared
+    // memory gives the final output, with no cross-cluster combine (an atomic
+    // arrival and L2 round trips on the step's critical path).  Longer caches
+    // keep more, smaller clusters for more SMs streaming K/V.
+    if (d == 128 && max_pages <= kWideMaxPages && n_sm >= kCSWide * Hkv &&
+        max_clusters(Hq, Hkv, d, kCSWide) >= Hkv)
+        return {kCSWide, kCSWide};
+    return {default_splits(n_sm, Hq, Hkv, d, max_pages), kCS};
+}
+
 cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a) {
-    if (a.P < kCS || a.P > 256 || a.P % kCS || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
+    const int cs = a.cs == kCSWide ? kCSWide : kCS;
+    if (a.P < cs || a.P > 256 || a.P % cs || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
     switch (a.Hq / a.Hkv) {
         case 1: return launch_g<1>(lc, a);
         case 2: return launch_g<2>(lc, a);

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     float post = 1.f;
     float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
     auto sync = [&]() {
+        prefetch_gain_l1(a.gamma, a.K);
         pdl_wait();
         post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, xs, nullptr, red,
                                  act_blk_bytes<FMT>());

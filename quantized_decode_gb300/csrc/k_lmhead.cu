@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
                       (size_t)warp * kD * kRT * 2 * 32;
     float post = 1.f;
     auto sync = [&]() {
+        prefetch_gain_l1(a.gamma, a.K);
         pdl_wait();
         if constexpr (FMT == kFmtBf16)
             post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, nullptr,

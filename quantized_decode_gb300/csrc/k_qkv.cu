@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
                 (const uint16_t *)a.s[seg] + (size_t)local * G};
     };
     auto sync = [&]() {
+        prefetch_gain_l1(a.gamma, a.K);
         pdl_wait();
         const int token = a.st->token;
         if (threadIdx.x == 0) s_pos = a.st->pos;

@@ -115,7 +115,9 @@ struct AttnArgs {
     float *out;                        // [Hq][d]
     int *err;
     const uint16_t *kv_new;            // [2][Hkv][d] appended K/V row, or null (all rows in pages)
-    float *stats_out;                  // (ss, mx) of out per KV head, or null
+    int cs;                            // CTAs per cluster: 8 (0 = 8) or 16 (d = 128 only)
+    float *stats_out;                  // (ss, mx) pairs of out, or null: slot g per KV head, or with
+                                       // one 16-CTA cluster per head slot 16 g + rank (others untouched)
 };
 
 // Each launcher returns the launch's cudaError_t.
@@ -129,6 +131,11 @@ int lm_head_grid(const LaunchCfg &lc, int N);
 // Splits per KV head: as many 8-CTA clusters as fill the SMs and are resident
 // at once on this device (cudaOccupancyMaxActiveClusters).
 int default_splits(int n_sm, int Hq, int Hkv, int d, int max_pages);
+// The engine's attention shape: P splits per KV head in clusters of cs CTAs.
+struct AttnPlan {
+    int P, cs;
+};
+AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages);
 int attention_split_multiple();  // split counts are multiples of the attention cluster size
 bool gemv_shape_ok(int fmt, int N, int K, int mode);
 bool qkv_shape_ok(int fmt, int rows_q, int rows_kv, int K, int d);
