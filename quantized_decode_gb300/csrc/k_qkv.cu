@@ -2,11 +2,14 @@
 // -> RoPE -> paged KV append, one kernel per layer of the decode step.
 //
 // Rows of the three projections are numbered q | k | v; warps stream tiles of
-// TR rows (gemv_stream).  A tile never straddles a head (TR divides d), so the
-// warp that completes the last tile of a head (per-head arrival counter) runs
-// that head's epilogue: per-head RMSNorm (Qwen3), RoPE with pairs (i, i+d/2)
-// at the current position, then q to the query buffer or k/v rounded to bf16
-// into slot pos % 16 of page page_table[pos / 16].
+// TR rows (gemv_stream).  A tile never straddles a head (TR divides d).
+// Without per-head q/k norms, a lane's two rows are the RoPE pair (p, p + d/2)
+// of one head (a tile holds pairs p0 .. p0 + 3), so the tile's epilogue
+// rotates them at the current position and writes q to the query buffer or
+// k/v rounded to bf16 into slot pos % 16 of page page_table[pos / 16] at once.
+// With the norms (Qwen3) a head's RMS needs all its rows: tiles hold 8
+// consecutive rows, and the warp that completes the last tile of a head
+// (per-head arrival counter) runs that head's epilogue: RMSNorm, RoPE, write.
 #include "gemv.cuh"
 #include "launch_util.cuh"
 
@@ -14,7 +17,7 @@ namespace qd {
 
 namespace {
 
-constexpr int kRT = 2;  // rows per lane
+constexpr int kRT = 2;  // rows per lane (a RoPE pair in the pair tiling)
 constexpr int kD = 5;   // ring depth (copies 4 steps ahead)
 
 template <int D>
@@ -68,6 +71,50 @@ QD_DEV void head_epilogue(const QkvArgs &a, int head, int pos, int lane) {
     }
 }
 
+// Rows (p, p + D/2) of head `head` (global row r0 = head * D + p): scale, bias,
+// RoPE for q and k at position pos, then q out or the bf16 K/V append.
+template <int FMT, int D>
+QD_DEV void pair_epilogue(const QkvArgs &a, int head, int p, int r0, const float (&out)[2], float post, int pos,
+                          int phys) {
+    const int seg = head < a.Hq ? 0 : (head < a.Hq + a.Hkv ? 1 : 2);
+    const int base = seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv);
+    const int l0 = r0 - base, l1 = l0 + D / 2;
+    float v0 = out[0] * post, v1 = out[1] * post;
+    if constexpr (FMT == kFmtInt8) {
+        v0 *= __ldg((const float *)a.s[seg] + l0);
+        v1 *= __ldg((const float *)a.s[seg] + l1);
+    }
+    if (a.b[seg]) {
+        v0 += bf16_bits_to_float(__ldg(a.b[seg] + l0));
+        v1 += bf16_bits_to_float(__ldg(a.b[seg] + l1));
+    }
+    if (seg < 2) {
+        const float2 c = __ldg(a.rope_cs + (size_t)pos * (D / 2) + p);
+        const float x0 = v0, x1 = v1;
+        v0 = x0 * c.x - x1 * c.y;
+        v1 = x1 * c.x + x0 * c.y;
+    }
+    if (seg == 0) {
+        a.q_out[(size_t)head * D + p] = v0;
+        a.q_out[(size_t)head * D + p + D / 2] = v1;
+        return;
+    }
+    const int g = head - a.Hq - (seg == 2 ? a.Hkv : 0);
+    if (phys < 0 || phys >= a.n_pages) {
+        atomicCAS(&a.st->err, kErrNone, kErrBadPage);
+        return;
+    }
+    uint16_t *dst = (seg == 1 ? a.k_pool : a.v_pool) + (((size_t)phys * a.Hkv + g) * kPageTokens + pos % kPageTokens) * D;
+    const uint16_t b0 = float_to_bf16_bits(v0), b1 = float_to_bf16_bits(v1);
+    dst[p] = b0;
+    dst[p + D / 2] = b1;
+    if (a.kv_new) {
+        uint16_t *cpy = a.kv_new + ((size_t)(seg == 1 ? 0 : a.Hkv) + g) * D;
+        cpy[p] = b0;
+        cpy[p + D / 2] = b1;
+    }
+}
+
 constexpr int kMaxWarps = 12;
 constexpr int kLPR = kLanesPerRow;
 
@@ -75,7 +122,6 @@ template <int FMT, int DH>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
-    __shared__ int s_pos;
     constexpr int S = 32 / kLPR;
     constexpr int TR = S * kRT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,32 +143,45 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<kRT, kD>()) +
                   (size_t)tslot * ks * 32 * kRT;
     float post = 1.f;
+    int pos = 0, phys = -1;
+    // pair mode: tile t = pairs (t % TPH) * S .. + S - 1 of head t / TPH
+    const bool pairs = a.q_gain == nullptr;
+    constexpr int TPH = DH / TR;
 
     auto segment = [&](int r, int &seg, int &local) {
         seg = r < a.rows_q ? 0 : (r < a.rows_q + a.rows_kv ? 1 : 2);
         local = r - (seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv));
     };
+    // global row of row i of this lane's slot in tile t
+    auto row_of = [&](int t, int i) -> int {
+        if (pairs) return (t / TPH) * DH + (t % TPH) * S + slot + i * (DH / 2);
+        return t * TR + slot * kRT + i;
+    };
     auto rows = [&](int t, int i) -> RowRef {
         int seg, local;
-        segment(t * TR, seg, local);
-        local += slot * kRT + i;
+        segment(row_of(t, i), seg, local);
         return {reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)local * rb),
                 (const uint16_t *)a.s[seg] + (size_t)local * G};
     };
     auto sync = [&]() {
         prefetch_gain_l1(a.gamma, a.K);
         pdl_wait();
-        const int token = a.st->token;
-        if (threadIdx.x == 0) s_pos = a.st->pos;
-        const uint16_t *erow = a.embed ? a.embed + (size_t)token * a.K : nullptr;
+        pos = __ldcg(&a.st->pos);  // consumed after the staging: no stall before its loads
+        const uint16_t *erow = a.embed ? a.embed + (size_t)__ldcg(&a.st->token) * a.K : nullptr;
         if (erow && blockIdx.x == 0)
             for (int i = threadIdx.x; i < a.K; i += blockDim.x) a.x_init[i] = bf16_bits_to_float(erow[i]);
         post = stage_activations(a.x, erow, a.gamma, a.eps, a.K, erow ? nullptr : a.stats_in, xs, nullptr, red,
                                  act_blk_bytes<FMT>());
+        phys = __ldg(a.page_table + pos / kPageTokens);  // used by the k/v tiles' epilogues
         pdl_launch();
     };
     auto epi = [&](int t, float(&out)[kRT]) {
         if (!ksplit_reduce<kRT>(out, ks, kp, tslot, kred, j, slot, kLPR)) return;
+        if (pairs) {
+            if (j != 0) return;
+            pair_epilogue<FMT, DH>(a, t / TPH, (t % TPH) * S + slot, row_of(t, 0), out, post, pos, phys);
+            return;
+        }
         const int tile_r = t * TR;
         int seg, local;
         segment(tile_r, seg, local);
@@ -144,7 +203,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence();
-            head_epilogue<DH>(a, head, s_pos, lane);
+            head_epilogue<DH>(a, head, pos, lane);
             if (lane == 0) a.head_cnt[head] = 0;
         }
     };
