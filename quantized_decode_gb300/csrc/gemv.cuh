@@ -103,10 +103,13 @@ constexpr int act_blk_bytes() {
 // are skipped.
 //
 // Each lane copies exactly the bytes it will consume (cp.async: two 16-byte
-// units per row and step, plus for INT4 the aligned 4-byte words that hold the
-// units' scales) into its own slots of a D-stage ring, D - 1 steps ahead of the
-// arithmetic, one commit group per step; the ring flows across tile
-// boundaries, and since a lane only reads what it copied, no barrier is needed.
+// units per row and step) into its own slots of a D-stage ring, D - 1 steps
+// ahead of the arithmetic, one commit group per step; the ring flows across
+// tile boundaries, and since a lane only reads what its row slot copied, no
+// barrier is needed beyond the warp's own.  For INT4 the 16 units of a row's
+// slab share 4 bf16 group scales (8 bytes, two aligned words: the row's scales
+// start 4-byte aligned as groups per row are even), which lanes 0 and 1 of the
+// row slot copy once per step.
 // At the end of a tile the 8 partial sums of each row are combined with
 // shuffles and `epi(tile, out)` runs on every lane (all lanes of a row slot
 // hold the same sums).  `sync()` (the dependency wait and the activation
@@ -114,7 +117,8 @@ constexpr int act_blk_bytes() {
 // weight copies are on their way.
 //
 // Ring layout per warp: stage s, row i, unit h, lane l -> 16-byte unit at
-// ring[((s * RT + i) * 2 + h) * 32 + l] and scale word at sring[same index].
+// ring[((s * RT + i) * 2 + h) * 32 + l]; row slot r's scale word w (groups
+// 4 slab + 2w, +1) at sring[((s * RT + i) * 4 + r) * 2 + w].
 // ---------------------------------------------------------------------------
 constexpr int kLanesPerRow = 8;
 
@@ -136,8 +140,24 @@ template <int N>
 QD_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int RT, int D>
+constexpr size_t code_ring_bytes_per_warp() {
+    return (size_t)D * RT * 2 * 32 * 16;
+}
+template <int RT, int D>
+constexpr size_t scale_ring_words_per_warp() {
+    return (size_t)D * RT * 8;
+}
+template <int RT, int D>
 constexpr size_t ring_bytes_per_warp() {
-    return (size_t)D * RT * 2 * 32 * (16 + 4);
+    return code_ring_bytes_per_warp<RT, D>() + scale_ring_words_per_warp<RT, D>() * 4;
+}
+// Warp `warp`'s code and scale rings in a block of NW warps' rings at `base`
+// (all code rings first, 16-byte aligned, then all scale rings).
+template <int RT, int D>
+QD_DEV void warp_rings(void *base, int NW, int warp, uint4 *&ring, uint32_t *&sring) {
+    ring = reinterpret_cast<uint4 *>(base) + (size_t)warp * (code_ring_bytes_per_warp<RT, D>() / 16);
+    sring = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(base) + (size_t)NW * code_ring_bytes_per_warp<RT, D>()) +
+            (size_t)warp * scale_ring_words_per_warp<RT, D>();
 }
 
 // One 16-byte unit of a row against its staged activations (x: 4 chunks for
@@ -189,22 +209,25 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
         for (int i = 0; i < RT; ++i) lrow[i] = rows(t, i);
     };
     if (F > 0) load_rows(lt);
+    const int rslot = lane / kLanesPerRow;
     auto issue = [&](int f) {
         const int slot = f % D;
-        const int ub = 16 * (sb_begin + li) + j;
+        const int sb = sb_begin + li;
+        const int ub = 16 * sb + j;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int u = ub + 8 * h;
             if (u < U) {
 #pragma unroll
-                for (int i = 0; i < RT; ++i) {
-                    const int idx = ((slot * RT + i) * 2 + h) * 32 + lane;
-                    cp_async16(ring + idx, lrow[i].w + u);
-                    if constexpr (FMT == kFmtInt4) {
-                        const uintptr_t a = (uintptr_t)(lrow[i].s + (u >> 2));
-                        cp_async4(sring + idx, (const void *)(a & ~(uintptr_t)3));
-                    }
-                }
+                for (int i = 0; i < RT; ++i) cp_async16(ring + ((slot * RT + i) * 2 + h) * 32 + lane, lrow[i].w + u);
+            }
+        }
+        if constexpr (FMT == kFmtInt4) {
+            // lane j < 2 of the slot: word j of the slab's 4 group scales (groups per row: U / 4, even)
+            if (j < 2 && 4 * sb + 2 * j < (U >> 2)) {
+#pragma unroll
+                for (int i = 0; i < RT; ++i)
+                    cp_async4(sring + ((slot * RT + i) * 4 + rslot) * 2 + j, lrow[i].s + 4 * sb + 2 * j);
             }
         }
         if (++li == n_it) {
@@ -226,22 +249,17 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
 #pragma unroll
     for (int i = 0; i < RT; ++i) acc[i] = 0.f;
     int ct = t_first, ci = 0;  // compute cursor
-    uint32_t shi = 0;          // bit i: row i's scales are the high halves of their aligned words
-    auto scale_parity = [&](int t) {
-        shi = 0;
-        if constexpr (FMT == kFmtInt4) {
-            // unit u's scale index is row_start + u/4; for u = 16 s + j (+8) its parity is that of row_start + j/4
-#pragma unroll
-            for (int i = 0; i < RT; ++i)
-                shi |= (uint32_t)((((uintptr_t)(rows(t, i).s + (j >> 2))) >> 1) & 1) << i;
-        }
-    };
-    if (F > 0) scale_parity(ct);
+    const bool shi = (j >> 2) != 0;  // the unit's group scale is the high half of its word
 #pragma unroll 1
     for (int f = 0; f < F; ++f) {
+        // the scale words are shared by the lanes of a row slot: every lane is
+        // past its reads of the stage before it is refilled (here), and sees the
+        // copying lanes' words once they completed (after the wait)
+        if constexpr (FMT == kFmtInt4) __syncwarp();
         if (f + D - 1 < F) issue(f + D - 1);
         cp_async_commit();
         cp_async_wait<D - 1>();
+        if constexpr (FMT == kFmtInt4) __syncwarp();
         const int slot = f % D;
         const int ub = 16 * (sb_begin + ci) + j;
 #pragma unroll
@@ -264,8 +282,8 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
                     for (int i = 0; i < RT; ++i) {
                         const int idx = ((slot * RT + i) * 2 + h) * 32 + lane;
                         if constexpr (FMT == kFmtInt4) {
-                            const uint32_t sw = sring[idx];
-                            const float sc = __uint_as_float(((shi >> i) & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                            const uint32_t sw = sring[((slot * RT + i) * 4 + rslot) * 2 + h];
+                            const float sc = __uint_as_float(shi ? (sw & 0xFFFF0000u) : (sw << 16));
                             acc[i] = fmaf(int4_unit_dot(ring[idx], xr), sc, acc[i]);
                         } else {
                             acc[i] += int8_unit_dot(ring[idx], xr);
@@ -284,7 +302,6 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
             epi(ct, out);
             ci = 0;
             ct += t_stride;
-            if (ct < n_tiles) scale_parity(ct);
         }
     }
     cp_async_wait<0>();

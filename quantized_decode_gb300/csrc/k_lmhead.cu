@@ -44,9 +44,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
     const int U = units_per_row(FMT, a.K);
     const size_t rb = FMT == kFmtBf16 ? (size_t)a.K * 2 : (size_t)a.K;
     const size_t xbytes = ((FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2) + 15) & ~(size_t)15;
-    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * kRT * 2 * 32;
-    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * kRT * 2 * 32 * 16) +
-                      (size_t)warp * kD * kRT * 2 * 32;
+    uint4 *ring;
+    uint32_t *sring;
+    warp_rings<kRT, kD>((char *)smem + xbytes, NW, warp, ring, sring);
     float post = 1.f;
     auto sync = [&]() {
         prefetch_gain_l1(a.gamma, a.K);

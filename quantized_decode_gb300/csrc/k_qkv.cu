@@ -137,9 +137,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
     const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
-    uint4 *ring = reinterpret_cast<uint4 *>((char *)smem + xbytes) + (size_t)warp * kD * kRT * 2 * 32;
-    uint32_t *sring = reinterpret_cast<uint32_t *>((char *)smem + xbytes + (size_t)NW * kD * kRT * 2 * 32 * 16) +
-                      (size_t)warp * kD * kRT * 2 * 32;
+    uint4 *ring;
+    uint32_t *sring;
+    warp_rings<kRT, kD>((char *)smem + xbytes, NW, warp, ring, sring);
     float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<kRT, kD>()) +
                   (size_t)tslot * ks * 32 * kRT;
     float post = 1.f;
