@@ -12,7 +12,7 @@ namespace qd {
 
 namespace {
 
-constexpr int kMaxWarps = 12;
+constexpr int kMaxWarps = 16;  // 512 threads at <= 128 registers
 // Ring depth: copies D - 1 steps ahead of the arithmetic.  Deeper rings keep
 // more weight bytes in flight per SM (HBM latency under load is ~2-3 us).
 template <int RT>

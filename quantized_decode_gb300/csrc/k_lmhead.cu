@@ -14,9 +14,9 @@ namespace qd {
 
 namespace {
 
-constexpr int kMaxWarps = 8;
+constexpr int kMaxWarps = 16;
 constexpr int kRT = 4;  // rows per lane
-constexpr int kD = 4;   // ring depth (copies 3 steps ahead)
+constexpr int kD = 3;   // ring depth (copies 2 steps ahead; measured: more warps beat deeper rings)
 
 QD_DEV void better(float &v, int &i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) {
