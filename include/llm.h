@@ -226,6 +226,20 @@ int llm_set_prefill_batched(llm_t *h, int32_t on);
  * Errors: LLM_ERR_ARG, LLM_ERR_CUDA.                                         */
 int llm_set_pdl(llm_t *h, int32_t use_pdl);
 
+/* 1 (where the model fits it: head_dim 128, no per-head q/k norms, one 16-CTA
+ * cluster per KV head resident at once, context up to 8K tokens): the QKV
+ * projection and the attention of a layer run as one kernel -- the
+ * cluster of a KV head computes the group's projection rows, exchanges them
+ * through distributed shared memory and attends over its pages, whose copies
+ * started before the projection.  The step is then 4 * n_layers + 1 kernels;
+ * llm_profile_step reports the fused kernel in each layer's QKV entry and 0 in
+ * its attention entry.  0 (default; the fused kernel measured slower at the 7B
+ * shape): separate QKV and attention kernels.  Results agree
+ * within rounding (the projection's K parts are summed in another order).
+ * Re-captures the graph; waits for enqueued work first.  Errors: LLM_ERR_ARG
+ * (null handle, or 1 for a model outside the fused kernel), LLM_ERR_CUDA.    */
+int llm_set_fused_attention(llm_t *h, int32_t on);
+
 /* ---- offline packer (host memory, no GPU needed) ----------------------- */
 
 /* Pack logical INT4 codes (int8 [N][K], values in [-8, 7], K % 128 == 0) into

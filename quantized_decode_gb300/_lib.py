@@ -67,6 +67,7 @@ SIGNATURES = {
                            ctypes.POINTER(i32), i32]),
     "llm_set_graph_mode": (i32, [vp, i32]),
     "llm_set_pdl": (i32, [vp, i32]),
+    "llm_set_fused_attention": (i32, [vp, i32]),
     "llm_set_persistent": (i32, [vp, i32]),
     "llm_set_prefill_batched": (i32, [vp, i32]),
     "llm_pack_int4_g128": (i32, [vp, i64, i64, vp]),

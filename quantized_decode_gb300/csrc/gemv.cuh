@@ -127,17 +127,6 @@ struct RowRef {
     const uint16_t *s;  // INT4: bf16 scales of the row, one per 128 codes
 };
 
-QD_DEV void cp_async16(void *smem, const void *gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-QD_DEV void cp_async4(void *smem, const void *gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-QD_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-QD_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int RT, int D>
 constexpr size_t code_ring_bytes_per_warp() {

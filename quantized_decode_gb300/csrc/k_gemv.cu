@@ -45,14 +45,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                   (size_t)tslot * ks * 32 * RT;
     float post = 1.f;
     float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
+    const int t_first = blockIdx.x * tpc + tslot, t_stride = gridDim.x * tpc;
+    // Modes 0 and 1: the epilogue inputs of the lane's first tile, loaded before
+    // the dependency wait -- row scales, bias and the next norm's gain are
+    // static; the residual y (mode 1) was last written two or more kernels
+    // earlier, which under programmatic dependent launch has completed before
+    // this kernel's CTAs are launched (each kernel signals its dependents only
+    // after its own wait, i.e. after its predecessor completed).
+    float pre_mul[RT], pre_add[RT], pre_g[RT];
     auto sync = [&]() {
         prefetch_gain_l1(a.gamma, a.K);
+        if (a.mode != 2 && j == 0 && kp == 0 && t_first < a.N / (S * RT)) {
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const int r = t_first * S * RT + slot * RT + i;
+                pre_mul[i] = FMT == kFmtInt8 ? __ldg((const float *)a.s + r) : 1.f;
+                pre_add[i] = a.mode == 1 ? __ldcg(a.y + r) : (a.bias ? bf16_bits_to_float(__ldg(a.bias + r)) : 0.f);
+                pre_g[i] = a.stats_gamma ? bf16_bits_to_float(__ldg(a.stats_gamma + r)) : 1.f;
+            }
+        }
         pdl_wait();
         post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, xs, nullptr, red,
                                  act_blk_bytes<FMT>());
         pdl_launch();
     };
-    const int t_first = blockIdx.x * tpc + tslot, t_stride = gridDim.x * tpc;
     if (a.mode == 2) {
         constexpr int H = RT / 2;
         const int TU = S * H;
@@ -90,19 +106,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
         };
         auto epi = [&](int t, float(&out)[RT]) {
             if (!ksplit_reduce<RT>(out, ks, kp, tslot, kred, j, slot, LPR) || j != 0) return;
+            const bool first = t == t_first;
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
                 const int r = t * TR + slot * RT + i;
                 float v = out[i] * post;
-                if constexpr (FMT == kFmtInt8) v *= __ldg((const float *)a.s + r);
-                if (a.mode == 1) {
-                    v += a.y[r];
+                if constexpr (FMT == kFmtInt8) v *= first ? pre_mul[i] : __ldg((const float *)a.s + r);
+                if (first) {
+                    v += pre_add[i];
+                } else if (a.mode == 1) {
+                    v += __ldcg(a.y + r);
                 } else if (a.bias) {
                     v += bf16_bits_to_float(__ldg(a.bias + r));
                 }
                 a.y[r] = v;
                 st_ss += v * v;
-                st_mx = fmaxf(st_mx, fabsf(a.stats_gamma ? v * bf16_bits_to_float(__ldg(a.stats_gamma + r)) : v));
+                const float gn = first ? pre_g[i] : (a.stats_gamma ? bf16_bits_to_float(__ldg(a.stats_gamma + r)) : 1.f);
+                st_mx = fmaxf(st_mx, fabsf(v * gn));
             }
         };
         gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,

@@ -71,28 +71,42 @@ QD_DEV void head_epilogue(const QkvArgs &a, int head, int pos, int lane) {
     }
 }
 
-// Rows (p, p + D/2) of head `head` (global row r0 = head * D + p): scale, bias,
-// RoPE for q and k at position pos, then q out or the bf16 K/V append.
+// The static inputs of a RoPE pair's epilogue: bias, INT8 row scales and the
+// (cos, sin) of pair p at position pos.  Loaded before the dependency wait for
+// a warp's first tiles, so that the epilogue does not wait on them.
+struct PairConst {
+    float b0, b1, s0, s1;
+    float2 cs;
+};
 template <int FMT, int D>
-QD_DEV void pair_epilogue(const QkvArgs &a, int head, int p, int r0, const float (&out)[2], float post, int pos,
-                          int phys) {
+QD_DEV PairConst pair_const(const QkvArgs &a, int head, int p, int r0, int pos) {
     const int seg = head < a.Hq ? 0 : (head < a.Hq + a.Hkv ? 1 : 2);
     const int base = seg == 0 ? 0 : (seg == 1 ? a.rows_q : a.rows_q + a.rows_kv);
     const int l0 = r0 - base, l1 = l0 + D / 2;
-    float v0 = out[0] * post, v1 = out[1] * post;
+    PairConst c{0.f, 0.f, 1.f, 1.f, make_float2(1.f, 0.f)};
     if constexpr (FMT == kFmtInt8) {
-        v0 *= __ldg((const float *)a.s[seg] + l0);
-        v1 *= __ldg((const float *)a.s[seg] + l1);
+        c.s0 = __ldg((const float *)a.s[seg] + l0);
+        c.s1 = __ldg((const float *)a.s[seg] + l1);
     }
     if (a.b[seg]) {
-        v0 += bf16_bits_to_float(__ldg(a.b[seg] + l0));
-        v1 += bf16_bits_to_float(__ldg(a.b[seg] + l1));
+        c.b0 = bf16_bits_to_float(__ldg(a.b[seg] + l0));
+        c.b1 = bf16_bits_to_float(__ldg(a.b[seg] + l1));
     }
+    if (seg < 2) c.cs = __ldg(a.rope_cs + (size_t)pos * (D / 2) + p);
+    return c;
+}
+
+// Rows (p, p + D/2) of head `head` (global row r0 = head * D + p): scale, bias,
+// RoPE for q and k at position pos, then q out or the bf16 K/V append.
+template <int FMT, int D>
+QD_DEV void pair_epilogue(const QkvArgs &a, int head, int p, const float (&out)[2], float post, int pos,
+                          int phys, const PairConst &c) {
+    const int seg = head < a.Hq ? 0 : (head < a.Hq + a.Hkv ? 1 : 2);
+    float v0 = out[0] * post * c.s0 + c.b0, v1 = out[1] * post * c.s1 + c.b1;
     if (seg < 2) {
-        const float2 c = __ldg(a.rope_cs + (size_t)pos * (D / 2) + p);
         const float x0 = v0, x1 = v1;
-        v0 = x0 * c.x - x1 * c.y;
-        v1 = x1 * c.x + x0 * c.y;
+        v0 = x0 * c.cs.x - x1 * c.cs.y;
+        v1 = x1 * c.cs.x + x0 * c.cs.y;
     }
     if (seg == 0) {
         a.q_out[(size_t)head * D + p] = v0;
@@ -144,6 +158,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
                   (size_t)tslot * ks * 32 * kRT;
     float post = 1.f;
     int pos = 0, phys = -1;
+    PairConst pc[2];  // the lane's first two tiles (pair mode; j == 0 lanes of the reducing warp)
     // pair mode: tile t = pairs (t % TPH) * S .. + S - 1 of head t / TPH
     const bool pairs = a.q_gain == nullptr;
     constexpr int TPH = DH / TR;
@@ -163,10 +178,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
         return {reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)local * rb),
                 (const uint16_t *)a.s[seg] + (size_t)local * G};
     };
+    const int t_first = blockIdx.x * tpc + tslot, t_stride = gridDim.x * tpc, n_tiles = rows_total / TR;
     auto sync = [&]() {
         prefetch_gain_l1(a.gamma, a.K);
+        // static data and the position (final: the step's first kernel starts after the last step)
+        pos = __ldcg(&a.st->pos);
+        if (pairs && j == 0 && kp == 0) {
+            const int t0 = t_first, t1 = t_first + t_stride;
+            if (t0 < n_tiles) pc[0] = pair_const<FMT, DH>(a, t0 / TPH, (t0 % TPH) * S + slot, row_of(t0, 0), pos);
+            if (t1 < n_tiles) pc[1] = pair_const<FMT, DH>(a, t1 / TPH, (t1 % TPH) * S + slot, row_of(t1, 0), pos);
+        }
         pdl_wait();
-        pos = __ldcg(&a.st->pos);  // consumed after the staging: no stall before its loads
         const uint16_t *erow = a.embed ? a.embed + (size_t)__ldcg(&a.st->token) * a.K : nullptr;
         if (erow && blockIdx.x == 0)
             for (int i = threadIdx.x; i < a.K; i += blockDim.x) a.x_init[i] = bf16_bits_to_float(erow[i]);
@@ -179,7 +201,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
         if (!ksplit_reduce<kRT>(out, ks, kp, tslot, kred, j, slot, kLPR)) return;
         if (pairs) {
             if (j != 0) return;
-            pair_epilogue<FMT, DH>(a, t / TPH, (t % TPH) * S + slot, row_of(t, 0), out, post, pos, phys);
+            const int k = (t - t_first) / t_stride;
+            const PairConst c = k == 0   ? pc[0]
+                                : k == 1 ? pc[1]
+                                         : pair_const<FMT, DH>(a, t / TPH, (t % TPH) * S + slot, row_of(t, 0), pos);
+            pair_epilogue<FMT, DH>(a, t / TPH, (t % TPH) * S + slot, out, post, pos, phys, c);
             return;
         }
         const int tile_r = t * TR;
@@ -207,8 +233,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
             if (lane == 0) a.head_cnt[head] = 0;
         }
     };
-    gemv_stream<FMT, kRT, kD>(rows, epi, sync, blockIdx.x * tpc + tslot, gridDim.x * tpc, rows_total / TR,
-                               p_begin, p_end, U, j, xs, ring, sring);
+    gemv_stream<FMT, kRT, kD>(rows, epi, sync, t_first, t_stride, n_tiles, p_begin, p_end, U, j, xs, ring, sring);
 }
 
 template <int FMT, int DH>

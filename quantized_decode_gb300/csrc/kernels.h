@@ -136,6 +136,13 @@ struct AttnPlan {
     int P, cs;
 };
 AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages);
+
+// QKV projection + attention of a layer in one kernel (one 16-CTA cluster per
+// KV head; models without q/k norms, d = 128).  `at` as for launch_attention
+// with P = cs = 16 and out set; qa as for launch_qkv (q_out, raw, head_cnt and
+// kv_new unused).
+bool qkv_attn_fusable(int fmt, int Hq, int Hkv, int d, int K, bool qk_norm, const AttnPlan &plan);
+cudaError_t launch_qkv_attn(const LaunchCfg &lc, int fmt, const QkvArgs &qa, const AttnArgs &at);
 int attention_split_multiple();  // split counts are multiples of the attention cluster size
 bool gemv_shape_ok(int fmt, int N, int K, int mode);
 bool qkv_shape_ok(int fmt, int rows_q, int rows_kv, int K, int d);

@@ -65,6 +65,22 @@ cudaError_t launch_kc(const LaunchCfg &lc, void (*kernel)(KArgs...), dim3 grid, 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Clusters above the portable size (8) need the kernel's opt-in (once per kernel and device).
+template <typename K>
+bool allow_wide(K kernel) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, bool> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair((const void *)kernel, dev);
+    auto it = done.find(key);
+    if (it != done.end()) return it->second;
+    const bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    done[key] = ok;
+    return ok;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(const LaunchCfg &lc, void (*kernel)(KArgs...), dim3 grid, dim3 block,
                      size_t smem, Args &&...args) {

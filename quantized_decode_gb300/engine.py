@@ -176,6 +176,10 @@ class Engine:
     def set_pdl(self, on):
         L.check(self.lib.llm_set_pdl(self.h, int(bool(on))), "llm_set_pdl")
 
+    def set_fused_attention(self, on):
+        """True: QKV projection and attention of a layer in one kernel (where the model fits it)."""
+        L.check(self.lib.llm_set_fused_attention(self.h, int(bool(on))), "llm_set_fused_attention")
+
     def set_persistent(self, on):
         """True: the step is the persistent whole-step kernel; False: the kernel chain."""
         L.check(self.lib.llm_set_persistent(self.h, int(bool(on))), "llm_set_persistent")
