@@ -34,11 +34,11 @@ NOMINAL_HBM_GBS = 8000.0
 # stands (profiles/decode_layer_7b_chain_ncu_full.md); keyed by shape and
 # kernel, dropped (None) for any kernel changed since that capture.
 NCU_TRAFFIC = {
-    ("qwen2.5-7b", "gate_up"): 70110208 + 278272,
-    ("qwen2.5-7b", "down"): 35174144,
-    ("qwen2.5-7b", "o_proj"): 6727424,
-    ("qwen2.5-7b", "qkv"): 8597504,
-    ("qwen2.5-7b", "attention"): 8217344,
+    ("qwen2.5-7b", "gate_up"): 70110208 + 305664,
+    ("qwen2.5-7b", "down"): 35177984,
+    ("qwen2.5-7b", "o_proj"): 6731264,
+    ("qwen2.5-7b", "qkv"): 8602112,
+    ("qwen2.5-7b", "attention"): 8219136,
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -57,6 +57,10 @@ def parse():
     p.add_argument("--seed", type=int, default=4242)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-ttft", action="store_true")
+    p.add_argument("--ttft-only", action="store_true",
+                   help="time the pp512 prefill only and print {'ttft_ms': ...} (profiling case)")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the persistent / no-PDL / fused / eager comparisons (profiling case)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-kv-sweep", action="store_true",
                    help="skip the ms/token sweep over KV lengths (512, 2048; 8192-32768 long context)")
@@ -295,6 +299,11 @@ def run_ours(args):
             runs.append((time.perf_counter() - t0) * 1e3)
         ttft_ms = float(np.median(runs))
         eng.reset()
+    if args.ttft_only:
+        if rank == 0:
+            print(json.dumps({"ttft_ms": None if ttft_ms is None else round(ttft_ms, 2)}))
+        eng.close()
+        return
 
     # ---- KV filled with seeded values through a shuffled page table
     from tests._gpu import fill_kv
@@ -384,59 +393,61 @@ def run_ours(args):
         finally:
             eng_l.close()
 
-    # ---- the other step form (persistent kernel vs kernel chain), same cache and greedy chain
-    other_ms = None
-    try:
-        eng.set_persistent(args.step != "persistent")
-        s4, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        enqueue(10)
-        s4.record(stream)
-        enqueue(100)
-        e4.record(stream)
-        torch.cuda.synchronize()
-        other_ms = s4.elapsed_time(e4) / 100
-    except LLMError:
-        pass
-    eng.set_persistent(args.step == "persistent")
+    other_ms = no_pdl_ms = fused_ms = eager_ms = None
+    if not args.no_variants:
+        # ---- the other step form (persistent kernel vs kernel chain), same cache and greedy chain
+        other_ms = None
+        try:
+            eng.set_persistent(args.step != "persistent")
+            s4, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            enqueue(10)
+            s4.record(stream)
+            enqueue(100)
+            e4.record(stream)
+            torch.cuda.synchronize()
+            other_ms = s4.elapsed_time(e4) / 100
+        except LLMError:
+            pass
+        eng.set_persistent(args.step == "persistent")
 
-    # ---- graph replay without programmatic dependent launch (the default uses it)
-    eng.set_pdl(False)
-    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_pdl = 100
-    s3.record(stream)
-    enqueue(n_pdl)
-    e3.record(stream)
-    torch.cuda.synchronize()
-    no_pdl_ms = s3.elapsed_time(e3) / n_pdl
-    eng.set_pdl(True)
-
-    # ---- graph replay with the fused QKV + attention kernel (opt-in, where the model fits it)
-    fused_ms = None
-    try:
-        eng.set_fused_attention(True)
-        enqueue(3)
-        s6, e6 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s6.record(stream)
+        # ---- graph replay without programmatic dependent launch (the default uses it)
+        eng.set_pdl(False)
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_pdl = 100
+        s3.record(stream)
         enqueue(n_pdl)
-        e6.record(stream)
+        e3.record(stream)
         torch.cuda.synchronize()
-        fused_ms = round(s6.elapsed_time(e6) / n_pdl, 4)
-        eng.set_fused_attention(False)
-    except LLMError:
-        pass
+        no_pdl_ms = s3.elapsed_time(e3) / n_pdl
+        eng.set_pdl(True)
 
-    # ---- eager launches, same kernels (graph vs eager)
-    eng.set_graph_mode(False)
-    eng.sync()
-    torch.cuda.synchronize()
-    n_eager = 20
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    enqueue(n_eager)
-    e2.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = s2.elapsed_time(e2) / n_eager
-    eng.set_graph_mode(True)
+        # ---- graph replay with the fused QKV + attention kernel (opt-in, where the model fits it)
+        fused_ms = None
+        try:
+            eng.set_fused_attention(True)
+            enqueue(3)
+            s6, e6 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s6.record(stream)
+            enqueue(n_pdl)
+            e6.record(stream)
+            torch.cuda.synchronize()
+            fused_ms = round(s6.elapsed_time(e6) / n_pdl, 4)
+            eng.set_fused_attention(False)
+        except LLMError:
+            pass
+
+        # ---- eager launches, same kernels (graph vs eager)
+        eng.set_graph_mode(False)
+        eng.sync()
+        torch.cuda.synchronize()
+        n_eager = 20
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        enqueue(n_eager)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = s2.elapsed_time(e2) / n_eager
+        eng.set_graph_mode(True)
 
     # ---- per-kernel breakdown (events between serialised launches)
     names = ["qkv", "attention", "o_proj", "gate_up", "down"]
@@ -505,8 +516,8 @@ def run_ours(args):
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
         "kv_sweep_ms_per_token": kv_sweep,
         "long_context_ms_per_token": long_ctx,
-        "eager_ms_per_token": round(eager_ms, 4),
-        "graph_no_pdl_ms_per_token": round(no_pdl_ms, 4),
+        "eager_ms_per_token": None if eager_ms is None else round(eager_ms, 4),
+        "graph_no_pdl_ms_per_token": None if no_pdl_ms is None else round(no_pdl_ms, 4),
         "fused_qkv_attention_ms_per_token": fused_ms,
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
             None if other_ms is None else round(other_ms, 4),
