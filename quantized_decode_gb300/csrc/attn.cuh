@@ -307,6 +307,10 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
         }
     }
     if (direct) {
+        // this CTA's reads of its peers' shared memory are done: arrive now and
+        // wait only before leaving (no CTA leaves while a peer may still read its
+        // shared memory), so the statistics overlap the barrier
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
         if (a.stats_out) {  // one (ss, mx) slot per CTA: g * CS + rank
             st_ss = warp_sum(st_ss);
             st_mx = warp_max(st_mx);
@@ -325,7 +329,7 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
                 a.stats_out[2 * (g * CS + rank) + 1] = b0;
             }
         }
-        cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
         return;
     }
     __threadfence();
