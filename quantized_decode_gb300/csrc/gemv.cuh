@@ -372,6 +372,9 @@ QD_DEV void write_block_stats(float ss, float mx, float *out, float *red) {
 // is read once; otherwise they are computed here first.
 //   half_out: fp16 pairs of gamma*x*inv_rms*2^-e, max |value| < 1; returns 2^e.
 //   f32_out:  fp32 gamma*x*inv_rms (no prescale); returns 1.
+// gamma_s: the gain's shared-memory copy from gain_copy_async() (completed by
+// this thread before the call), used from the conversion pass on (or null: the
+// gain is read from global memory).
 // red: shared scratch of 64 floats.  Loads are issued in batches of up to 8
 // float4 per thread so that a batch costs one round trip.
 //
@@ -383,20 +386,22 @@ QD_DEV void write_block_stats(float ss, float mx, float *out, float *red) {
 // ---------------------------------------------------------------------------
 constexpr int kStageBatch = 8;  // float4 loads per thread and staging pass
 
-// The RMSNorm gains of the first staging pass are static: fetch the thread's
-// lines into L1 before the dependency wait, so that the staging waits on the
-// input's round trip only (a prefetch holds no register).
-QD_DEV void prefetch_gain_l1(const uint16_t *__restrict__ gamma, int K) {
-    if (!gamma) return;
-    const int step = blockDim.x * 4;
-    for (int i = threadIdx.x * 4; i < K && i < kStageBatch * step; i += step)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(gamma + i));
+// The RMSNorm gain is static: the block copies it into shared memory (gs, K
+// bf16, 16-byte aligned, K % 8 == 0) as the first cp.async group of every
+// thread, before the weight ring's first steps, so that the staging waits on
+// the input's round trip only.  The caller then waits with
+// cp_async_wait<ring steps issued since>() (every group but the ring's) before
+// the staging, whose block barriers publish the copy.
+QD_DEV void gain_copy_async(const uint16_t *__restrict__ gamma, int K, uint16_t *gs) {
+    if (gamma)
+        for (int i = threadIdx.x * 8; i < K; i += blockDim.x * 8) cp_async16(gs + i, gamma + i);
+    cp_async_commit();
 }
 
 QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__restrict__ src_bf16,
                                const uint16_t *__restrict__ gamma, float eps, int K,
                                const float *__restrict__ stats_in, half2 *half_out, float *f32_out,
-                               float *red, int blk_bytes = 0) {
+                               float *red, int blk_bytes = 0, const uint16_t *gamma_s = nullptr) {
     constexpr int kBatch = kStageBatch;
     const int tid = threadIdx.x, NT = blockDim.x;
     auto load4 = [&](int i) -> float4 {
@@ -407,9 +412,11 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
         }
         return __ldcg(reinterpret_cast<const float4 *>(src + i));
     };
+    bool gs_ok = false;  // the gain's shared-memory copy is visible (after the first barrier)
     auto gain4 = [&](int i) -> float4 {
         if (!gamma) return make_float4(1.f, 1.f, 1.f, 1.f);
-        const uint2 g = __ldg(reinterpret_cast<const uint2 *>(gamma + i));
+        const uint2 g = gs_ok ? *reinterpret_cast<const uint2 *>(gamma_s + i)
+                              : __ldg(reinterpret_cast<const uint2 *>(gamma + i));
         return make_float4(__uint_as_float(g.x << 16), __uint_as_float(g.x & 0xFFFF0000u),
                            __uint_as_float(g.y << 16), __uint_as_float(g.y & 0xFFFF0000u));
     };
@@ -473,6 +480,7 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
         }
     }
     __syncthreads();
+    gs_ok = gamma && gamma_s;
     const float inv = gamma ? rsqrtf(red[0] / (float)K + eps) : 1.f;
     float post = 1.f, pre = inv;
     if (half_out) {

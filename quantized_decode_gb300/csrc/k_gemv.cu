@@ -38,10 +38,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
     const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    uint16_t *gs = reinterpret_cast<uint16_t *>((char *)smem + xbytes);  // the gain (when a.gamma)
+    const size_t gbytes = a.gamma ? xbytes : 0;
     uint4 *ring;
     uint32_t *sring;
-    warp_rings<RT, kDepth<RT>>((char *)smem + xbytes, NW, warp, ring, sring);
-    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<RT, kDepth<RT>>()) +
+    warp_rings<RT, kDepth<RT>>((char *)smem + xbytes + gbytes, NW, warp, ring, sring);
+    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + gbytes +
+                                            (size_t)NW * ring_bytes_per_warp<RT, kDepth<RT>>()) +
                   (size_t)tslot * ks * 32 * RT;
     float post = 1.f;
     float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     // after its own wait, i.e. after its predecessor completed).
     float pre_mul[RT], pre_add[RT], pre_g[RT];
     auto sync = [&]() {
-        prefetch_gain_l1(a.gamma, a.K);
+        cp_async_wait<kDepth<RT> - 1>();  // the gain (the ring's first steps stay in flight)
         if (a.mode != 2 && j == 0 && kp == 0 && t_first < a.N / (S * RT)) {
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
@@ -66,9 +69,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
         }
         pdl_wait();
         post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, xs, nullptr, red,
-                                 act_blk_bytes<FMT>());
+                                 act_blk_bytes<FMT>(), a.gamma ? gs : nullptr);
         pdl_launch();
     };
+    gain_copy_async(a.gamma, a.K, gs);
     if (a.mode == 2) {
         constexpr int H = RT / 2;
         const int TU = S * H;
@@ -136,7 +140,7 @@ cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
     constexpr int LPR = kLanesPerRow;
     const int rows_per_tile = a.mode == 2 ? (32 / LPR) * (RT / 2) : (32 / LPR) * RT;
     const int tiles = a.N / rows_per_tile;
-    const size_t fixed = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    const size_t fixed = (((size_t)a.K * 2 + 15) & ~(size_t)15) * (a.gamma ? 2 : 1);  // activations (+ gain)
     const size_t per_warp = ring_bytes_per_warp<RT, kDepth<RT>>() + (size_t)32 * RT * 4;
     const int fit = (int)((kMaxSmemOptin - fixed) / per_warp);  // warps whose rings fit in shared memory
     GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots,

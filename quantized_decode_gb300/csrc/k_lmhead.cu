@@ -44,19 +44,21 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
     const int U = units_per_row(FMT, a.K);
     const size_t rb = FMT == kFmtBf16 ? (size_t)a.K * 2 : (size_t)a.K;
     const size_t xbytes = ((FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2) + 15) & ~(size_t)15;
+    const size_t gbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    uint16_t *gs = reinterpret_cast<uint16_t *>((char *)smem + xbytes);  // the final norm's gain
     uint4 *ring;
     uint32_t *sring;
-    warp_rings<kRT, kD>((char *)smem + xbytes, NW, warp, ring, sring);
+    warp_rings<kRT, kD>((char *)smem + xbytes + gbytes, NW, warp, ring, sring);
     float post = 1.f;
     auto sync = [&]() {
-        prefetch_gain_l1(a.gamma, a.K);
+        cp_async_wait<kD - 1>();  // the gain (the ring's first steps stay in flight)
         pdl_wait();
         if constexpr (FMT == kFmtBf16)
             post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, nullptr,
-                                     reinterpret_cast<float *>(smem), red, act_blk_bytes<FMT>());
+                                     reinterpret_cast<float *>(smem), red, act_blk_bytes<FMT>(), gs);
         else
             post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in,
-                                     reinterpret_cast<half2 *>(smem), nullptr, red, act_blk_bytes<FMT>());
+                                     reinterpret_cast<half2 *>(smem), nullptr, red, act_blk_bytes<FMT>(), gs);
         pdl_launch();
     };
     auto rows = [&](int t, int i) -> RowRef {
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
             better(best, bidx, v, r);
         }
     };
+    gain_copy_async(a.gamma, a.K, gs);
     gemv_stream<FMT, kRT, kD>(rows, epi, sync, gw, W, a.N / TR, 0, NP, U, j, smem, ring, sring);
 
 #pragma unroll
@@ -137,7 +140,8 @@ cudaError_t launch_fmt(const LaunchCfg &lc, const LmHeadArgs &a, int grid) {
     int nw = (tiles + grid - 1) / grid;
     nw = nw < 2 ? 2 : (nw > kMaxWarps ? kMaxWarps : nw);  // >= 64 threads (statistics read)
     const size_t smem = (((FMT == kFmtBf16 ? (size_t)a.K * 4 : (size_t)a.K * 2) + 15) & ~(size_t)15) +
-                        (size_t)nw * ring_bytes_per_warp<kRT, kD>();
+                        (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)nw * ring_bytes_per_warp<kRT, kD>();
+    if (smem > kMaxSmemOptin - 1024) return cudaErrorInvalidValue;
     return launch_k(lc, k_lm_head<FMT>, dim3(grid), dim3(nw * 32), smem, a);
 }
 

@@ -151,10 +151,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
     const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    uint16_t *gs = reinterpret_cast<uint16_t *>((char *)smem + xbytes);  // the attention norm's gain
     uint4 *ring;
     uint32_t *sring;
-    warp_rings<kRT, kD>((char *)smem + xbytes, NW, warp, ring, sring);
-    float *kred = reinterpret_cast<float *>((char *)smem + xbytes + (size_t)NW * ring_bytes_per_warp<kRT, kD>()) +
+    warp_rings<kRT, kD>((char *)smem + 2 * xbytes, NW, warp, ring, sring);
+    float *kred = reinterpret_cast<float *>((char *)smem + 2 * xbytes + (size_t)NW * ring_bytes_per_warp<kRT, kD>()) +
                   (size_t)tslot * ks * 32 * kRT;
     float post = 1.f;
     int pos = 0, phys = -1;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     };
     const int t_first = blockIdx.x * tpc + tslot, t_stride = gridDim.x * tpc, n_tiles = rows_total / TR;
     auto sync = [&]() {
-        prefetch_gain_l1(a.gamma, a.K);
+        cp_async_wait<kD - 1>();  // the gain (the ring's first steps stay in flight)
         // static data and the position (final: the step's first kernel starts after the last step)
         pos = __ldcg(&a.st->pos);
         if (pairs && j == 0 && kp == 0) {
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
         if (erow && blockIdx.x == 0)
             for (int i = threadIdx.x; i < a.K; i += blockDim.x) a.x_init[i] = bf16_bits_to_float(erow[i]);
         post = stage_activations(a.x, erow, a.gamma, a.eps, a.K, erow ? nullptr : a.stats_in, xs, nullptr, red,
-                                 act_blk_bytes<FMT>());
+                                 act_blk_bytes<FMT>(), gs);
         phys = __ldg(a.page_table + pos / kPageTokens);  // used by the k/v tiles' epilogues
         pdl_launch();
     };
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
             if (lane == 0) a.head_cnt[head] = 0;
         }
     };
+    gain_copy_async(a.gamma, a.K, gs);
     gemv_stream<FMT, kRT, kD>(rows, epi, sync, t_first, t_stride, n_tiles, p_begin, p_end, U, j, xs, ring, sring);
 }
 
@@ -245,7 +247,7 @@ cudaError_t launch_qkv_d(const LaunchCfg &lc, QkvArgs a) {
     while (ks < 4 && tiles * ks < 8 * lc.n_sm && NP / (ks * 2) >= 1) ks *= 2;
     GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm, kMaxWarps);
     a.ks = ks;
-    const size_t smem = (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)pl.nw * ring_bytes_per_warp<kRT, kD>() +
+    const size_t smem = 2 * (((size_t)a.K * 2 + 15) & ~(size_t)15) + (size_t)pl.nw * ring_bytes_per_warp<kRT, kD>() +
                         (size_t)pl.nw * 32 * kRT * 4;
     return launch_k(lc, k_qkv<FMT, DH>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
 }

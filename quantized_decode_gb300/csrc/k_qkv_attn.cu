@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kNT, 1) k_qkv_attn(QkvArgs qa, AttnArgs at) {
                     (const uint16_t *)qa.s[seg] + (size_t)r * Gs};
         };
         auto sync = [&]() {
-            prefetch_gain_l1(qa.gamma, qa.K);
             // the tiles' epilogue constants, static data read before the wait (the
             // position is final too: the step's first kernel starts after the last step)
             pos = __ldcg(&qa.st->pos);
