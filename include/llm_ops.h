@@ -46,10 +46,11 @@ int llm_op_lm_head_argmax(const void *w, const float *lm_scale, const void *gamm
  * on NVIDIA H100", "Architectural Blueprint").  For every query head h with
  * group g = h / (Hq/Hkv): out[h] = sum_t softmax_t(q_h . K[g][t] / sqrt(d)) V[g][t]
  * over t < T.  q: fp32 [Hq][d] (already rotated); k_pool, v_pool: bf16
- * [pages][Hkv][16][d]; page_table: int32, logical page -> physical page;
- * n_splits: key-range partitions per KV head (1..256, rounded up to a multiple
- * of 8, the CTAs of one cluster; 0 = engine's choice);
- * out: fp32 [Hq][d].  d in {64, 128}, Hq/Hkv <= 8, T >= 1.                  */
+ * [pages][Hkv][16][d]; page_table: int32, logical page -> physical page
+ * (entries below (2^31 - 1) / (16 Hkv); one outside [0, that bound) reads page
+ * 0 and is an error of the call); n_splits: key-range partitions per KV head
+ * (1..256, rounded up to a multiple of 8, the CTAs of one cluster; 0 = the
+ * engine's choice); out: fp32 [Hq][d].  d in {64, 128}, Hq/Hkv <= 8, T >= 1.  */
 int llm_op_attention(const float *q, const void *k_pool, const void *v_pool,
                      const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
                      int32_t n_splits, float *out, void *stream);

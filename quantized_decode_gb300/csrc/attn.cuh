@@ -6,6 +6,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace qd {
 
@@ -53,7 +54,24 @@ template <int D>
 constexpr size_t ring_bytes() {
     return (size_t)kWarps * kWRing * 2 * 16 * D * 2;
 }
+// Dynamic shared memory to request for the ring: its base is rounded up to
+// 1024 bytes (the 128-byte swizzle atom of the TMA page boxes).
+template <int D>
+constexpr size_t ring_alloc_bytes() {
+    return ring_bytes<D>() + 1024;
+}
+QD_DEV uint16_t *align_ring(uint16_t *p) {
+    return reinterpret_cast<uint16_t *>(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
 
+// A K (or V) page slice in shared memory: 16 rows x D bf16 as D / 64 TMA boxes
+// of 16 rows x 128 bytes, each with the 128-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ (r & 7) of its 128-byte line), so that the 8 rows an
+// ldmatrix reads at one chunk hit distinct banks.  Element offset of (row r,
+// 16-byte chunk ch of the D-element row).
+QD_DEV int page_off(int r, int ch) { return (ch >> 3) * (16 * 64) + r * 64 + (((ch & 7) ^ (r & 7)) << 3); }
+
+constexpr uint64_t kPageWaitNs = 1000000000ull;  // bound on a page's arrival
 // Where a CTA finds its inputs once they exist: the group's G query rows
 // (D floats each, RoPE applied) and the appended K and V rows (bf16, D each;
 // null when every row is in the pages already).
@@ -81,6 +99,7 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
     __shared__ float s_fw[8][32], s_fl[8][32];
     __shared__ float s_st[2][kWarps];
     __shared__ int s_last;
+    __shared__ uint64_t s_pbar[kWarps][kWRing];  // page slot arrivals (TMA transaction bytes)
 
     cg::cluster_group cluster = cg::this_cluster();
     const int g = blockIdx.y, p = blockIdx.x, P = gridDim.x;
@@ -97,29 +116,37 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
     const int pg1 = min(n_pg, pg0 + cpp);
     const int n = pg1 > pg0 ? pg1 - pg0 : 0;
     const int nw = n > warp ? (n - 1 - warp) / kWarps + 1 : 0;  // this warp's pages
-    uint16_t *wring = smem + (size_t)warp * kWRing * 2 * PAGE;
+    uint16_t *wring = smem + (size_t)warp * kWRing * 2 * PAGE;  // 1024-byte aligned: smem is, slots are 8 KB
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < kWRing; ++j) ptx::mbar_init(&s_pbar[warp][j], 1);
+        ptx::mbar_fence_init();
+    }
+    __syncwarp();
 
+    // page i of this warp into slot i % kWRing: lane 0 issues the K and V boxes
+    // (TMA), the slot's barrier counts their bytes
     auto issue = [&](int i) {
+        if (lane != 0) return;
         const int pg = pg0 + warp + i * kWarps;
         const int phys = __ldg(a.page_table + pg);
         const bool ok = phys >= 0 && phys < a.n_pages;
-        const size_t off = ((size_t)(ok ? phys : 0) * a.Hkv + g) * PAGE;
+        if (!ok) atomicCAS(a.err, kErrNone, kErrBadPage);
+        const int row = ((ok ? phys : 0) * a.Hkv + g) * kPageTokens;
         uint16_t *ks = wring + (i % kWRing) * 2 * PAGE, *vs = ks + PAGE;
-#pragma unroll 4
-        for (int c = lane; c < 16 * CH; c += 32) {
-            const int r = c / CH, ch = c % CH;
-            const int sw = r * D + ((ch ^ (r & 7)) << 3);
-            cp_async16(ks + sw, a.k_pool + off + c * 8);
-            cp_async16(vs + sw, a.v_pool + off + c * 8);
+        uint64_t *bar = &s_pbar[warp][i % kWRing];
+        ptx::fence_proxy_async_smem();  // the warp's earlier accesses of the slot come before the copy's writes
+        ptx::mbar_expect_tx(bar, (uint32_t)(2 * PAGE * 2));
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+            ptx::tma_load_2d(ks + b * 16 * 64, &a.k_map, b * 64, row, bar);
+            ptx::tma_load_2d(vs + b * 16 * 64, &a.v_map, b * 64, row, bar);
         }
-        if (!ok && lane == 0) atomicCAS(a.err, kErrNone, kErrBadPage);
     };
     auto issue_pages = [&]() {
 #pragma unroll
-        for (int i = 0; i < kWRing; ++i) {
+        for (int i = 0; i < kWRing; ++i)
             if (i < nw) issue(i);
-            cp_async_commit();
-        }
     };
     if (!LATE) issue_pages();
 
@@ -152,19 +179,23 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
     for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = 0.f;
     float z2 = 0.f, z3 = 0.f;  // rows 8-15 of the products (always zero)
 
+    int stop = nw;  // pages consumed; < nw only if a page's arrival wait ran out
     for (int i = 0; i < nw; ++i) {
-        cp_async_wait<kWRing - 1>();
-        __syncwarp();
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&s_pbar[warp][i % kWRing], (i / kWRing) & 1u, kPageWaitNs))) {
+            if (lane == 0) atomicCAS(a.err, kErrNone, kErrTimeout);
+            stop = i;
+            break;
+        }
         const int pg = pg0 + warp + i * kWarps;
         uint16_t *ks = wring + (i % kWRing) * 2 * PAGE, *vs = ks + PAGE;
         if (pg == last_pg) {
             const int valid = T - pg * kPageTokens;  // rows [valid, 16) lie past the sequence
             for (int c = lane; c < (16 - valid) * CH; c += 32) {
                 const int r = valid + c / CH, ch = c % CH;
-                *reinterpret_cast<uint4 *>(vs + r * D + ((ch ^ (r & 7)) << 3)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(vs + page_off(r, ch)) = make_uint4(0, 0, 0, 0);
             }
             if (patch && lane < CH) {
-                const int sw = new_row * D + ((lane ^ (new_row & 7)) << 3);
+                const int sw = page_off(new_row, lane);
                 const uint4 *kn = reinterpret_cast<const uint4 *>(in.k_new) + lane;
                 const uint4 *vn = reinterpret_cast<const uint4 *>(in.v_new) + lane;
                 *reinterpret_cast<uint4 *>(ks + sw) = QS ? *kn : __ldcg(kn);
@@ -180,7 +211,7 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
             const int tok = (lane & 7) + ((lane >> 4) << 3);
             const int ch = kk * 2 + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(ks + tok * D + ((ch ^ (tok & 7)) << 3), b0, b1, b2, b3);
+            ldsm_x4(ks + page_off(tok, ch), b0, b1, b2, b3);
             mma_bf16(s0, z2, z3, qh[kk][0], qh[kk][1], b0, b1);
             mma_bf16(s0, z2, z3, ql[kk][0], ql[kk][1], b0, b1);
             mma_bf16(s1, z2, z3, qh[kk][0], qh[kk][1], b2, b3);
@@ -220,7 +251,7 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
             const int tok = r + (mi & 1) * 8;
             const int ch = dp * 2 + (mi >> 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vs + tok * D + ((ch ^ (tok & 7)) << 3), b0, b1, b2, b3);
+            ldsm_x4_t(vs + page_off(tok, ch), b0, b1, b2, b3);
             mma_bf16(o[2 * dp], z2, z3, ph0, ph2, b0, b1);
             mma_bf16(o[2 * dp], z2, z3, pl0, pl2, b0, b1);
             mma_bf16(o[2 * dp + 1], z2, z3, ph0, ph2, b2, b3);
@@ -228,9 +259,10 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
         }
         __syncwarp();
         if (i + kWRing < nw) issue(i + kWRing);
-        cp_async_commit();
     }
-    cp_async_wait<0>();
+    // after a wait ran out: the pages still in flight land before the slots are reused
+    for (int i = stop; i < nw && i < stop + kWRing; ++i)
+        ptx::mbar_wait(&s_pbar[warp][i % kWRing], (i / kWRing) & 1u, kPageWaitNs);
     __syncthreads();
 
     // ---- merge the 8 warps of the CTA (the ring's shared memory is free now)

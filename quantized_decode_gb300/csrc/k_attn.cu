@@ -37,8 +37,9 @@ namespace {
 using namespace attn;
 
 template <int G, int D, int CS>
-__global__ void __launch_bounds__(kNT, 1) k_attn(AttnArgs a) {
-    extern __shared__ __align__(128) uint16_t smem[];
+__global__ void __launch_bounds__(kNT, 1) k_attn(const __grid_constant__ AttnArgs a) {
+    extern __shared__ __align__(128) uint16_t smem_raw[];
+    uint16_t *smem = align_ring(smem_raw);
     const int g = blockIdx.y;
     attn_cta<G, D, CS, false, false>(a, smem, [&](auto &&) {
         pdl_wait();
@@ -54,11 +55,11 @@ cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
     const dim3 grid(a.P, a.Hkv);
     if (a.cs == kCSWide && a.d == 128) {
         if (!allow_wide(k_attn<G, 128, kCSWide>)) return cudaErrorInvalidValue;
-        return launch_kc(lc, k_attn<G, 128, kCSWide>, grid, dim3(kNT), ring_bytes<128>(), kCSWide, a);
+        return launch_kc(lc, k_attn<G, 128, kCSWide>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCSWide, a);
     }
     if (a.cs != 0 && a.cs != kCS) return cudaErrorInvalidValue;
-    if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCS>, grid, dim3(kNT), ring_bytes<128>(), kCS, a);
-    if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCS>, grid, dim3(kNT), ring_bytes<64>(), kCS, a);
+    if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCS>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCS, a);
+    if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCS>, grid, dim3(kNT), ring_alloc_bytes<64>(), kCS, a);
     return cudaErrorInvalidValue;
 }
 
@@ -72,7 +73,7 @@ int max_clusters_gdc(int Hkv) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find({dev, Hkv});
     if (it != cache.end()) return it->second;
-    const size_t smem = ring_bytes<D>();
+    const size_t smem = ring_alloc_bytes<D>();
     if (CS > kCS && !allow_wide(k_attn<G, D, CS>)) return 0;
     if (cudaFuncSetAttribute(k_attn<G, D, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -143,9 +144,44 @@ AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages) {
     return {default_splits(n_sm, Hq, Hkv, d, max_pages), kCS};
 }
 
-cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a) {
-    const int cs = a.cs == kCSWide ? kCSWide : kCS;
-    if (a.P < cs || a.P > 256 || a.P % cs || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
+cudaError_t attention_pool_maps(AttnArgs &a) {
+    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn enc = []() -> EncodeFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeFn>(p);
+        return nullptr;
+    }();
+    if (!enc) return cudaErrorNotSupported;
+    if (!a.k_pool || !a.v_pool || ((uintptr_t)a.k_pool & 15) || ((uintptr_t)a.v_pool & 15) || a.n_pages < 1 ||
+        a.Hkv < 1 || (a.d != 64 && a.d != 128))
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.d, (cuuint64_t)a.n_pages * a.Hkv * kPageTokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.d * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kPageTokens};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap *maps[2] = {&a.k_map, &a.v_map};
+    const uint16_t *pools[2] = {a.k_pool, a.v_pool};
+    for (int i = 0; i < 2; ++i) {
+        const CUresult r = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(pools[i]), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &args) {
+    const int cs = args.cs == kCSWide ? kCSWide : kCS;
+    if (args.P < cs || args.P > 256 || args.P % cs || args.Hkv < 1 || args.Hq % args.Hkv) return cudaErrorInvalidValue;
+    AttnArgs a = args;
+    const cudaError_t me = attention_pool_maps(a);
+    if (me != cudaSuccess) return me;
     switch (a.Hq / a.Hkv) {
         case 1: return launch_g<1>(lc, a);
         case 2: return launch_g<2>(lc, a);

@@ -61,15 +61,16 @@ QD_HOST_DEV_INLINE FusedLayout fused_layout(int G, int K) {
     o += (size_t)G * kD128 * 4;
     L.kv = o;
     o += (size_t)2 * kD128 * 2;
-    L.total = o;
+    L.total = o + 1024;  // alignment slack of the base
     return L;
 }
 
 template <int FMT, int G>
-__global__ void __launch_bounds__(kNT, 1) k_qkv_attn(QkvArgs qa, AttnArgs at) {
+__global__ void __launch_bounds__(kNT, 1) k_qkv_attn(QkvArgs qa, const __grid_constant__ AttnArgs at) {
     constexpr int D = kD128;
     constexpr int NT = G + 2;  // tiles per CTA
-    extern __shared__ __align__(128) uint16_t smem[];
+    extern __shared__ __align__(128) uint16_t smem_raw[];
+    uint16_t *smem = align_ring(smem_raw);  // the page ring's TMA boxes want 1024-byte alignment
     __shared__ float red[64];
     cg::cluster_group cluster = cg::this_cluster();
     const int g = blockIdx.y, rank = (int)cluster.block_rank();
@@ -230,8 +231,12 @@ bool qkv_attn_fusable(int fmt, int Hq, int Hkv, int d, int K, bool qk_norm, cons
     return fused_layout(Hq / Hkv, K).total <= kMaxSmemOptin - 8 * 1024;
 }
 
-cudaError_t launch_qkv_attn(const LaunchCfg &lc, int fmt, const QkvArgs &qa, const AttnArgs &at) {
-    if (at.P != kCSWide || at.cs != kCSWide || at.d != kD128 || qa.q_gain || !at.out) return cudaErrorInvalidValue;
+cudaError_t launch_qkv_attn(const LaunchCfg &lc, int fmt, const QkvArgs &qa, const AttnArgs &args) {
+    if (args.P != kCSWide || args.cs != kCSWide || args.d != kD128 || qa.q_gain || !args.out)
+        return cudaErrorInvalidValue;
+    AttnArgs at = args;
+    const cudaError_t me = attention_pool_maps(at);
+    if (me != cudaSuccess) return me;
     if (fmt == kFmtInt4) return launch_f<kFmtInt4>(lc, qa, at);
     if (fmt == kFmtInt8) return launch_f<kFmtInt8>(lc, qa, at);
     return cudaErrorInvalidValue;

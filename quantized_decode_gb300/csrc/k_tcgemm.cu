@@ -19,7 +19,7 @@
 #include "launch_util.cuh"
 #include "prefill.h"
 #include "ptx.cuh"
-#include "step.h"  // kErrTimeout
+#include "kernels.h"
 
 namespace qd {
 

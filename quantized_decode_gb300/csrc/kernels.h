@@ -1,6 +1,7 @@
 // kernels.h - launch interface of the decode-step kernels (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,7 +14,7 @@ constexpr int kStatSlots = 256;   // (sum of squares, max) pairs per producer: o
 constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in to (sm_103a)
 
 // Device-side error word (sticky until the host clears it).
-enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3 };
+enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3, kErrTimeout = 16 };
 
 enum WeightFormat : int { kFmtInt4 = 1, kFmtInt8 = 2, kFmtBf16 = 3 };
 
@@ -116,6 +117,8 @@ struct AttnArgs {
     int *err;
     const uint16_t *kv_new;            // [2][Hkv][d] appended K/V row, or null (all rows in pages)
     int cs;                            // CTAs per cluster: 8 (0 = 8) or 16 (d = 128 only)
+    CUtensorMap k_map, v_map;          // set by the launcher: the pools as 2-D tensors
+                                       // [pages * Hkv * 16][d] for TMA page loads
     float *stats_out;                  // (ss, mx) pairs of out, or null: slot g per KV head, or with
                                        // one 16-CTA cluster per head slot 16 g + rank (others untouched)
 };
@@ -125,6 +128,8 @@ cudaError_t launch_qkv(const LaunchCfg &lc, int fmt, const QkvArgs &a);
 cudaError_t launch_gemv(const LaunchCfg &lc, int fmt, const GemvArgs &a);
 cudaError_t launch_lm_head(const LaunchCfg &lc, const LmHeadArgs &a, int grid);
 cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &a);
+// The TMA maps of a's pools (boxes of 64 columns x 16 rows, 128-byte swizzle).
+cudaError_t attention_pool_maps(AttnArgs &a);
 
 // Grid sizes and shape checks used by the engine when it plans buffers.
 int lm_head_grid(const LaunchCfg &lc, int N);

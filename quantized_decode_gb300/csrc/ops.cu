@@ -11,6 +11,12 @@ using namespace qd;
 
 namespace {
 
+// The pools' extent is not an argument of the ops: pages are bounded only so
+// that every row index (page * Hkv * 16) stays an int32 TMA coordinate; a
+// table entry past the bound is flagged as a bad page.
+inline int op_max_pages(int Hkv) { return (int)(((1u << 31) - 1) / (unsigned)(Hkv * kPageTokens)); }
+
+
 LaunchCfg op_cfg(void *stream) {
     LaunchCfg lc{};
     lc.stream = (cudaStream_t)stream;
@@ -93,7 +99,7 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, con
     if (cudaMemsetAsync(scratch, 0, cnt_bytes, lc.stream) != cudaSuccess) return LLM_ERR_CUDA;
     AttnArgs a{};
     a.q = q; a.k_pool = (const uint16_t *)k_pool; a.v_pool = (const uint16_t *)v_pool;
-    a.page_table = page_table; a.n_pages = 1 << 30;
+    a.page_table = page_table; a.n_pages = op_max_pages(Hkv);
     a.st = nullptr; a.T_fixed = T;
     a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.P = P;
     a.counter = (int *)scratch;

@@ -27,6 +27,12 @@ using namespace qd;
 
 namespace {
 
+// The pools' extent is not an argument of the ops: pages are bounded only so
+// that every row index (page * Hkv * 16) stays an int32 TMA coordinate; a
+// table entry past the bound is flagged as a bad page.
+inline int op_max_pages(int Hkv) { return (int)(((1u << 31) - 1) / (unsigned)(Hkv * kPageTokens)); }
+
+
 constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB per device
 constexpr size_t kCounterBytes = 256;              // arrival counters + error word, zeroed per call
 constexpr int kMaxDevices = 64;
@@ -87,7 +93,7 @@ extern "C" int llm_op_attention_noalloc(const float *q, const void *k_pool, cons
     a.k_pool = (const uint16_t *)k_pool;
     a.v_pool = (const uint16_t *)v_pool;
     a.page_table = page_table;
-    a.n_pages = 1 << 30;
+    a.n_pages = op_max_pages(Hkv);
     a.st = nullptr;
     a.T_fixed = T;
     a.Hq = Hq;

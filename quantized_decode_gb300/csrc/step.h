@@ -55,8 +55,6 @@ constexpr int kSyncDDone = 123;
 constexpr int kSyncMaxHeads = 96;
 constexpr int kSyncMaxKvHeads = 16;
 
-// Device error codes beyond kErr* of kernels.h.
-constexpr int kErrTimeout = 16;
 
 // Weight tensor maps of a layer (3-D codes boxes, see above).
 enum StepMap : int { kMapQ = 0, kMapK = 1, kMapV = 2, kMapO = 3, kMapGate = 4, kMapUp = 5, kMapDown = 6, kMapCount = 7 };
