@@ -393,8 +393,19 @@ def run_ours(args):
         finally:
             eng_l.close()
 
-    other_ms = no_pdl_ms = fused_ms = eager_ms = None
+    other_ms = no_pdl_ms = fused_ms = eager_ms = sampling_ms = None
     if not args.no_variants:
+        # ---- graph replay with top-k / top-p sampling (Qwen's recommended 0.6 / 20 / 0.95) instead of argmax
+        eng.set_sampling(0.6, 20, 0.95, args.seed)
+        enqueue(3)
+        s7, e7 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s7.record(stream)
+        enqueue(100)
+        e7.record(stream)
+        torch.cuda.synchronize()
+        sampling_ms = round(s7.elapsed_time(e7) / 100, 4)
+        eng.set_sampling(0.0)
+
         # ---- the other step form (persistent kernel vs kernel chain), same cache and greedy chain
         other_ms = None
         try:
@@ -519,6 +530,7 @@ def run_ours(args):
         "eager_ms_per_token": None if eager_ms is None else round(eager_ms, 4),
         "graph_no_pdl_ms_per_token": None if no_pdl_ms is None else round(no_pdl_ms, 4),
         "fused_qkv_attention_ms_per_token": fused_ms,
+        "sampling_ms_per_token": sampling_ms,
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
             None if other_ms is None else round(other_ms, 4),
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,

@@ -240,6 +240,23 @@ int llm_set_pdl(llm_t *h, int32_t use_pdl);
  * (null handle, or 1 for a model outside the fused kernel), LLM_ERR_CUDA.    */
 int llm_set_fused_attention(llm_t *h, int32_t on);
 
+/* How each step (and the batched prefill) picks the next token.  temperature
+ * <= 0 (default): greedy argmax, lowest index on ties ("FlashQwen", "Stage 5 -
+ * GPU argmax for greedy").  Otherwise sampling on the GPU ("FlashQwen" run
+ * options --temperature / --top-k / --top-p, Qwen's recommended 0.6 / 20 /
+ * 0.95; naive Qwen engine, "Sampler"): the top_k largest logits (lowest index
+ * on ties), weights exp((l - l_max) / temperature), the smallest prefix of
+ * them in decreasing order whose weight reaches top_p of their sum, and the
+ * first token of that prefix whose running weight exceeds u times the
+ * prefix's weight, with u uniform in [0, 1) from SplitMix64 started at
+ * mix(seed), draw number = the position whose logits are sampled (so a step
+ * at a given position draws the same u after llm_reset or llm_truncate).
+ * One extra kernel after the LM head; llm_profile_step counts it in the LM
+ * head's entry.  1 <= top_k <= min(vocab, 1024), 0 < top_p <= 1.  Not with
+ * the persistent step.  Re-captures the graph; waits for enqueued work first.
+ * Errors: LLM_ERR_ARG, LLM_ERR_CUDA.                                          */
+int llm_set_sampling(llm_t *h, float temperature, int32_t top_k, float top_p, uint64_t seed);
+
 /* ---- offline packer (host memory, no GPU needed) ----------------------- */
 
 /* Pack logical INT4 codes (int8 [N][K], values in [-8, 7], K % 128 == 0) into

@@ -41,6 +41,13 @@ int llm_op_lm_head_argmax(const void *w, const float *lm_scale, const void *gamm
                           int32_t N, int32_t K, const float *x, float *logits, int32_t *token,
                           void *stream);
 
+/* The decode step's sampler on given logits (see llm_set_sampling in llm.h):
+ * logits fp32 [V] and token (one int32) are device pointers; the draw uses
+ * counter as its number.  temperature > 0, 1 <= top_k <= min(V, 1024),
+ * 0 < top_p <= 1; otherwise LLM_ERR_ARG.                                     */
+int llm_op_sample(const float *logits, int32_t V, float temperature, int32_t top_k, float top_p,
+                  uint64_t seed, uint64_t counter, int32_t *token, void *stream);
+
 /* Split-K grouped-query decode attention over a paged bf16 KV cache with the
  * log-sum-exp combine ("FlashQwen", stage 7; GQA per "Bare-Metal LLM Inference
  * on NVIDIA H100", "Architectural Blueprint").  For every query head h with

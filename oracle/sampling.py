@@ -52,8 +52,9 @@ def sample(logits, temperature, top_k, top_p, seed, counter):
         tok = int(np.flatnonzero(logits == m)[0])
         return tok, [tok], np.inf
     k = min(int(top_k), V)
-    order = sorted(range(V), key=lambda i: (-float(logits[i]), i))[:k]
-    l = np.array([float(logits[i]) for i in order], dtype=np.float64)
+    # decreasing value, ties by increasing index (lexsort orders by its last key first)
+    order = [int(i) for i in np.lexsort((np.arange(V), -logits.astype(np.float64)))[:k]]
+    l = logits[order].astype(np.float64)
     w = np.exp((l - l[0]) / float(temperature))
     cum = np.zeros(k)
     acc = 0.0

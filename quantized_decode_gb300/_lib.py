@@ -68,6 +68,8 @@ SIGNATURES = {
     "llm_set_graph_mode": (i32, [vp, i32]),
     "llm_set_pdl": (i32, [vp, i32]),
     "llm_set_fused_attention": (i32, [vp, i32]),
+    "llm_set_sampling": (i32, [vp, f32, i32, f32, ctypes.c_uint64]),
+    "llm_op_sample": (i32, [vp, i32, f32, i32, f32, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
     "llm_set_persistent": (i32, [vp, i32]),
     "llm_set_prefill_batched": (i32, [vp, i32]),
     "llm_pack_int4_g128": (i32, [vp, i64, i64, vp]),

@@ -48,6 +48,12 @@ struct llm_t {
     float *stats = nullptr;     // 4 x kStatSlots (ss, mx) pairs: attention, o_proj, gate/up, down outputs
     uint16_t *kv_new = nullptr; // [2][Hkv][d] appended rows of the current step
     int P = 1, attn_cs = 8, lm_grid = 1;
+    // llm_set_sampling: temperature / top-k / top-p instead of the greedy argmax
+    bool sampling = false;
+    float samp_t = 0.f, samp_p = 1.f;
+    int samp_k = 1;
+    uint64_t samp_seed = 0;
+    int *samp_scratch = nullptr;  // the LM head's unused argmax while sampling
     bool fused_ok = false;      // the model fits the fused QKV + attention kernel
     bool fused = false;         // llm_set_fused_attention
 
@@ -103,7 +109,7 @@ void free_all(llm_t *h) {
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
                     h->d_layers, h->d_maps, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
-                    h->pf_qh, h->pf_ql, h->pf_tok};
+                    h->pf_qh, h->pf_ql, h->pf_tok, h->samp_scratch};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -149,6 +155,16 @@ int validate(const llm_config *c, const llm_weights *w) {
         if (c->qk_norm && (!aligned16(L.q_norm) || !aligned16(L.k_norm))) return LLM_ERR_ARG;
     }
     return LLM_OK;
+}
+
+// The sampler after the LM head: the token into the state (the next step's
+// input), the position advanced; the draw's counter is the sampled position.
+SampleArgs sampler_args(const llm_t *h) {
+    SampleArgs sa{};
+    sa.logits = h->logits; sa.V = h->cfg.vocab;
+    sa.temperature = h->samp_t; sa.top_k = h->samp_k; sa.top_p = h->samp_p; sa.seed = h->samp_seed;
+    sa.token_out = &h->st->last_token; sa.st = h->st; sa.advance = 1;
+    return sa;
 }
 
 // Enqueue one whole decode step (5L + 1 kernels).  With `ev`, event k is
@@ -239,7 +255,11 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
     la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
     la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
     la.stats_in = st_down;
+    if (h->sampling) {  // the sampler takes the token and advances the state
+        la.token_out = h->samp_scratch; la.st = nullptr; la.advance = 0;
+    }
     if ((e = mark()) != cudaSuccess || (e = launch_lm_head(h->lc, la, h->lm_grid)) != cudaSuccess) return e;
+    if (h->sampling && (e = launch_sample(h->lc, sampler_args(h))) != cudaSuccess) return e;
     return mark();
 }
 
@@ -530,9 +550,13 @@ int prefill_batched(llm_t *h, const int32_t *tokens, int n, int32_t *first_token
     la.eps = c.rms_eps; la.N = c.vocab; la.K = c.hidden; la.x = h->x; la.logits = h->logits;
     la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
     la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
+    if (h->sampling) {
+        la.token_out = h->samp_scratch; la.st = nullptr; la.advance = 0;
+    }
     LaunchCfg lc = h->lc;
     lc.pdl = false;
     if (launch_lm_head(lc, la, h->lm_grid) != cudaSuccess) return LLM_ERR_CUDA;
+    if (h->sampling && launch_sample(lc, sampler_args(h)) != cudaSuccess) return LLM_ERR_CUDA;
     return fetch_token(h, first_token);
 }
 
@@ -616,6 +640,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
               dalloc(&h->part_ml, (size_t)c.n_kv_heads * P_alloc * G * 2) == cudaSuccess &&
               dalloc(&h->stats, (size_t)8 * kStatSlots) == cudaSuccess &&
               dalloc(&h->kv_new, (size_t)2 * c.n_kv_heads * d) == cudaSuccess &&
+              dalloc(&h->samp_scratch, 1) == cudaSuccess &&
               cudaMallocHost(reinterpret_cast<void **>(&h->pinned), 8 * sizeof(int32_t)) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
 
@@ -678,9 +703,21 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph) {
 
 int llm_set_persistent(llm_t *h, int32_t on) {
     if (!h) return LLM_ERR_ARG;
-    if (on && !h->step_ok) return LLM_ERR_ARG;
+    if (on && (!h->step_ok || h->sampling)) return LLM_ERR_ARG;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->persistent = on != 0;
+    return capture(h);
+}
+
+int llm_set_sampling(llm_t *h, float temperature, int32_t top_k, float top_p, uint64_t seed) {
+    if (!h) return LLM_ERR_ARG;
+    const bool on = temperature > 0.f;
+    if (on && (h->persistent || top_k < 1 || top_k > kMaxTopK || top_k > h->cfg.vocab || !(top_p > 0.f) ||
+               top_p > 1.f || !(temperature < INFINITY)))
+        return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->sampling = on;
+    h->samp_t = temperature; h->samp_k = top_k; h->samp_p = top_p; h->samp_seed = seed;
     return capture(h);
 }
 

@@ -101,6 +101,25 @@ struct LmHeadArgs {
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
 };
 
+// Temperature / top-k / top-p sampling of the next token from the logits (in
+// place of the greedy argmax).  One CTA; the token to token_out and, with a
+// state, into it as the next step's input (pos advanced when `advance`); the
+// draw's counter is st->pos (or `counter` without a state).
+constexpr int kMaxTopK = 1024;
+struct SampleArgs {
+    const float *logits;    // [V]
+    int V;
+    float temperature;      // > 0
+    int top_k;              // 1 .. min(V, kMaxTopK)
+    float top_p;            // (0, 1]
+    uint64_t seed;
+    uint64_t counter;       // without a state
+    int *token_out;
+    DevState *st;           // or null
+    int advance;
+};
+cudaError_t launch_sample(const LaunchCfg &lc, const SampleArgs &a);
+
 // Split-K decode attention over the paged cache with the LSE combine.
 struct AttnArgs {
     const float *q;                    // [Hq][d] rotated

@@ -2,6 +2,8 @@
 // launched one at a time on the caller's stream.  Scratch that a kernel needs
 // (attention partials, argmax slots, arrival counters) is stream-ordered
 // (cudaMallocAsync / cudaFreeAsync) and zeroed where it must start at zero.
+#include <cmath>
+
 #include "../../include/llm.h"
 #include "../../include/llm_ops.h"
 #include "kernels.h"
@@ -51,6 +53,18 @@ int llm_op_gemv_int8(const void *w, const float *s, int32_t N, int32_t K, const 
     GemvArgs a{};
     a.mode = 0; a.w = w; a.s = s; a.N = N; a.K = K; a.x = x; a.y = y;
     return status(launch_gemv(op_cfg(stream), kFmtInt8, a));
+}
+
+int llm_op_sample(const float *logits, int32_t V, float temperature, int32_t top_k, float top_p,
+                  uint64_t seed, uint64_t counter, int32_t *token, void *stream) {
+    if (!logits || !token || V < 1 || !(temperature > 0.f) || !(temperature < INFINITY) || top_k < 1 ||
+        top_k > kMaxTopK || top_k > V || !(top_p > 0.f) || top_p > 1.f)
+        return LLM_ERR_ARG;
+    LaunchCfg lc = op_cfg(stream);
+    SampleArgs a{};
+    a.logits = logits; a.V = V; a.temperature = temperature; a.top_k = top_k; a.top_p = top_p;
+    a.seed = seed; a.counter = counter; a.token_out = token; a.st = nullptr; a.advance = 0;
+    return status(launch_sample(lc, a));
 }
 
 int llm_op_lm_head_argmax(const void *w, const float *lm_scale, const void *gamma, float eps,

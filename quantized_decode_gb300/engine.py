@@ -176,6 +176,11 @@ class Engine:
     def set_pdl(self, on):
         L.check(self.lib.llm_set_pdl(self.h, int(bool(on))), "llm_set_pdl")
 
+    def set_sampling(self, temperature, top_k=1, top_p=1.0, seed=0):
+        """temperature <= 0: greedy argmax (default); otherwise top-k / top-p sampling on the GPU."""
+        L.check(self.lib.llm_set_sampling(self.h, float(temperature), int(top_k), float(top_p), int(seed)),
+                "llm_set_sampling")
+
     def set_fused_attention(self, on):
         """True: QKV projection and attention of a layer in one kernel (where the model fits it)."""
         L.check(self.lib.llm_set_fused_attention(self.h, int(bool(on))), "llm_set_fused_attention")
