@@ -52,6 +52,42 @@ def test_op_matches_oracle(lib, V, T, k, p):
     assert compared >= 30
 
 
+def _compare(lib, logits, dev_ptr, V, T, k, p, seed, n_draws, min_compared):
+    compared = 0
+    for counter in range(n_draws):
+        tok = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        assert lib.llm_op_sample(dev_ptr, V, T, k, p, seed, counter, tok.data_ptr(), None) == 0
+        torch.cuda.synchronize()
+        got = int(tok.item())
+        want, kept, margin = smp.sample(logits, T, k, p, seed, counter)
+        assert got in kept, (counter, got)
+        if margin > MARGIN:
+            assert got == want, (counter, got, want, margin)
+            compared += 1
+    assert compared >= min_compared
+
+
+def test_op_one_dense_bin_takes_the_sorting_path(lib):
+    """3000 logits within one 12-bit key bin ([1, 1.0625)): every key is a candidate of the same
+    bin, so the candidates are sorted instead of ranked within their bin."""
+    V = 3000
+    u = synth.normal_f32(V, 11, V, 0.0, 1.0)
+    logits = (1.0 + 0.06 * (0.5 + 0.5 * np.tanh(u))).astype(np.float32)
+    assert logits.min() >= 1.0 and logits.max() < 1.0625
+    dev = to_dev(logits)
+    for T, k, p in ((0.05, 100, 0.9), (0.01, 1000, 1.0), (1.0, 7, 0.5)):
+        _compare(lib, logits, dev.data_ptr(), V, T, k, p, 9, 30, 20)
+
+
+def test_op_unaligned_logits_take_the_word_path(lib):
+    """Logits that do not start on a 16-byte boundary are read a word at a time."""
+    V = 40001
+    logits = synth.normal_f32(V + 1, 13, V + 1, 0.0, 2.0)
+    dev = to_dev(logits)
+    for T, k, p in ((0.6, 20, 0.95), (1.5, 1000, 0.9)):
+        _compare(lib, logits[1:], dev.data_ptr() + 4, V, T, k, p, 4, 30, 20)
+
+
 def test_op_ties_at_the_threshold_keep_the_lowest_indices(lib):
     V = 5000
     logits = np.zeros(V, np.float32)
