@@ -34,11 +34,11 @@ NOMINAL_HBM_GBS = 8000.0
 # stands (profiles/decode_layer_7b_chain_ncu_full.md); keyed by shape and
 # kernel, dropped (None) for any kernel changed since that capture.
 NCU_TRAFFIC = {
-    ("qwen2.5-7b", "gate_up"): 70110208 + 305664,
-    ("qwen2.5-7b", "down"): 35177984,
-    ("qwen2.5-7b", "o_proj"): 6731264,
-    ("qwen2.5-7b", "qkv"): 8602112,
-    ("qwen2.5-7b", "attention"): 8219136,
+    ("qwen2.5-7b", "gate_up"): 70109184 + 318464,
+    ("qwen2.5-7b", "down"): 35177472,
+    ("qwen2.5-7b", "o_proj"): 6730496,
+    ("qwen2.5-7b", "qkv"): 8601344,
+    ("qwen2.5-7b", "attention"): 8219904,
 }
 FALLBACK_HBM_GBS = 6800.0
 
