@@ -45,6 +45,8 @@ extern "C" {
 #define LLM_ERR_TIMEOUT (-5)      /* a bounded device-side wait gave up (sticky error word)   */
 #define LLM_ERR_DEVICE (-6)       /* a device-side check failed (sticky error word)           */
 #define LLM_ERR_STATE (-7)        /* call out of order (e.g. llm_logits before any step)      */
+#define LLM_ERR_FORMAT (-8)       /* not a model file: wrong magic, version, checksum or size  */
+#define LLM_ERR_IO (-9)           /* a model file could not be opened, read or written        */
 
 /* ---- weight formats and packed layouts -------------------------------- */
 /* INT4, symmetric, zero point 0, group 128 along K, one bfloat16 scale per
@@ -267,6 +269,63 @@ int llm_pack_int4_g128(const int8_t *codes, int64_t N, int64_t K, uint32_t *word
 /* Layout LLM_LAYOUT_INT8_ROW keeps codes in natural order: this copies and
  * checks the range [-127, 127].                                              */
 int llm_pack_int8_row(const int8_t *codes, int64_t N, int64_t K, int8_t *out);
+
+/* ---- quantizers (host memory, no GPU needed) --------------------------- */
+
+/* Symmetric INT4, zero point 0, group 128 along K ("How To Construct Your
+ * Personal LLM Runtime From Scratch", §3): for each (row, group) the scale is
+ * absmax / 7 in fp32, stored as bfloat16 (round to nearest even); each code is
+ * the fp32 quotient w / scale (the stored scale) rounded half to even and
+ * clamped to [-8, 7]; an all-zero group gets scale 0 and codes 0.
+ * w: fp32 [N][K] (HOST), K % 128 == 0; codes: int8 [N][K]; scales: bf16 bits
+ * [N][K/128].  Returns LLM_ERR_ARG on a null pointer, a bad shape or a
+ * non-finite weight.  Feed the codes to llm_pack_int4_g128().               */
+int llm_quantize_int4_g128(const float *w, int64_t N, int64_t K, int8_t *codes, uint16_t *scales);
+
+/* Symmetric INT8 with one fp32 scale per output row ("FlashQwen", Stage 8):
+ * scale = absmax / 127 in fp32; code = w / scale rounded half to even,
+ * clamped to [-127, 127]; a zero row gets scale 0 and codes 0.
+ * w: fp32 [N][K] (HOST); codes: int8 [N][K]; scales: fp32 [N].             */
+int llm_quantize_int8_row(const float *w, int64_t N, int64_t K, int8_t *codes, float *scales);
+
+/* ---- model file ---------------------------------------------------------- */
+/* One binary file holds a packed model ("How To Construct Your Personal LLM
+ * Runtime From Scratch", §3-§4: one mmap-able file, a 256-byte header opening
+ * with an 8-byte magic, payloads on 128-byte boundaries, refused on a wrong
+ * magic or layout id before any weight is uploaded):
+ *   bytes 0-7 the magic "QDECODEW"; 8-11 version 1; 12-15 header size 256;
+ *   16-79 the llm_config (16 little-endian 4-byte fields in declaration
+ *   order); 80-87 payload offset 256; 88-95 payload bytes; 96-103 FNV-1a 64
+ *   of bytes 0-95; zeros to byte 256.  Then each tensor on the next 128-byte
+ *   boundary, in this order, with the sizes llm_create() documents: embed,
+ *   final_norm, [lm_head (bf16, INT4 models; int8, INT8 models), [lm_scale
+ *   (INT8 models)]] unless tied_lm_head, then per layer wq sq [bq] wk sk [bk]
+ *   wv sv [bv] wo so wg sg wu su wd sd attn_norm mlp_norm [q_norm k_norm]
+ *   (brackets: only with qkv_bias, resp. qk_norm).  Padding bytes are zero. */
+
+/* Size in bytes of the file for this configuration.  Errors: LLM_ERR_ARG.   */
+int llm_model_file_bytes(const llm_config *cfg, int64_t *bytes);
+
+/* Write the model to `path` (created or truncated).  host_weights: the same
+ * fields as for llm_create() but HOST pointers, in the config's packed layout
+ * (llm_pack_int4_g128 / llm_pack_int8_row output and their scales); read
+ * only during the call.  Errors: LLM_ERR_ARG (null or missing tensor, bad
+ * shape), LLM_ERR_LAYOUT (layout_id does not match weight_format), LLM_ERR_IO. */
+int llm_model_file_write(const char *path, const llm_config *cfg, const llm_weights *host_weights);
+
+/* Read and check a file's header into *cfg_out (no weights are read).
+ * Errors: LLM_ERR_IO (cannot open), LLM_ERR_FORMAT (wrong magic, version or
+ * checksum, impossible shape, size that does not match the configuration or
+ * a truncated file), LLM_ERR_LAYOUT (layout_id does not match the format).  */
+int llm_model_file_read_config(const char *path, llm_config *cfg_out);
+
+/* Check the file as llm_model_file_read_config() does, copy its payload to
+ * one device allocation (read in 64 MB chunks), and llm_create() an engine
+ * on those weights; the handle owns the allocation and llm_destroy() frees
+ * it.  max_context > 0 replaces the file's max_context; 0 keeps it.  On error
+ * *out is NULL and nothing leaks.  Errors: those of
+ * llm_model_file_read_config(), LLM_ERR_CUDA, and those of llm_create().    */
+int llm_create_from_file(const char *path, int32_t max_context, void *cuda_stream, llm_t **out);
 
 #ifdef __cplusplus
 }

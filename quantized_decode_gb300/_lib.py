@@ -17,6 +17,8 @@ LLM_ERR_CUDA = -4
 LLM_ERR_TIMEOUT = -5
 LLM_ERR_DEVICE = -6
 LLM_ERR_STATE = -7
+LLM_ERR_FORMAT = -8
+LLM_ERR_IO = -9
 
 LLM_FMT_INT4_G128 = 1
 LLM_FMT_INT8_ROW = 2
@@ -74,6 +76,12 @@ SIGNATURES = {
     "llm_set_prefill_batched": (i32, [vp, i32]),
     "llm_pack_int4_g128": (i32, [vp, i64, i64, vp]),
     "llm_pack_int8_row": (i32, [vp, i64, i64, vp]),
+    "llm_quantize_int4_g128": (i32, [vp, i64, i64, vp, vp]),
+    "llm_quantize_int8_row": (i32, [vp, i64, i64, vp, vp]),
+    "llm_model_file_bytes": (i32, [ctypes.POINTER(llm_config), ctypes.POINTER(i64)]),
+    "llm_model_file_write": (i32, [ctypes.c_char_p, ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights)]),
+    "llm_model_file_read_config": (i32, [ctypes.c_char_p, ctypes.POINTER(llm_config)]),
+    "llm_create_from_file": (i32, [ctypes.c_char_p, i32, vp, ctypes.POINTER(vp)]),
     "llm_op_gemv_int4": (i32, [vp, vp, vp, i32, i32, vp, vp, vp]),
     "llm_op_gemv_int8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_op_lm_head_argmax": (i32, [vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]),

@@ -28,6 +28,7 @@ using namespace qd;
 
 struct llm_t {
     llm_config cfg;
+    void *weight_buffer = nullptr;  // llm_create_from_file: the weights' device copy, owned
     int fmt = 0;
     std::vector<llm_layer_weights> layers;
     llm_weights w{};
@@ -562,6 +563,11 @@ int prefill_batched(llm_t *h, const int32_t *tokens, int n, int32_t *first_token
 
 }  // namespace
 
+namespace qd {
+// llm_create_from_file hands the handle the weights' device copy (freed by llm_destroy).
+void adopt_weight_buffer(llm_t *h, void *dev) { h->weight_buffer = dev; }
+}  // namespace qd
+
 extern "C" {
 
 const char *llm_status_str(int s) {
@@ -574,6 +580,8 @@ const char *llm_status_str(int s) {
         case LLM_ERR_TIMEOUT: return "device wait timed out";
         case LLM_ERR_DEVICE: return "device-side check failed";
         case LLM_ERR_STATE: return "call out of order";
+        case LLM_ERR_FORMAT: return "not a model file, or a corrupt or truncated one";
+        case LLM_ERR_IO: return "file could not be opened, read or written";
         default: return "unknown status";
     }
 }
@@ -692,6 +700,7 @@ void llm_destroy(llm_t *h) {
     if (!h) return;
     cudaStreamSynchronize(h->stream);
     free_all(h);
+    if (h->weight_buffer) cudaFree(h->weight_buffer);
     delete h;
 }
 

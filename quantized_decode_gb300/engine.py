@@ -48,6 +48,58 @@ def make_config(cfg):
         max_context=cfg.max_context, page_tokens=16)
 
 
+def quantize_int4(w):
+    """fp32 weights [N][K] -> (codes int8 [N][K], bf16 scale bits [N][K/128]) by libllm's
+    absmax/7 group-128 quantizer (llm_quantize_int4_g128)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K), dtype=np.int8)
+    scales = np.empty((N, K // 128), dtype=np.uint16)
+    L.check(L.load().llm_quantize_int4_g128(_np_ptr(w), N, K, _np_ptr(codes), _np_ptr(scales)),
+            "llm_quantize_int4_g128")
+    return codes, scales
+
+
+def quantize_int8(w):
+    """fp32 weights [N][K] -> (codes int8 [N][K], fp32 row scales [N]) (llm_quantize_int8_row)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K), dtype=np.int8)
+    scales = np.empty(N, dtype=np.float32)
+    L.check(L.load().llm_quantize_int8_row(_np_ptr(w), N, K, _np_ptr(codes), _np_ptr(scales)),
+            "llm_quantize_int8_row")
+    return codes, scales
+
+
+def _fill(cfg, get_proj, get_norms, embed, final_norm, lm_head, put):
+    """llm_layer_weights array and llm_weights with every tensor passed through put(array)
+    -> pointer (device upload, or a host array kept alive)."""
+    int4 = int(cfg.weight_format) == L.LLM_FMT_INT4_G128
+    layers = (L.llm_layer_weights * cfg.n_layers)()
+    for l in range(cfg.n_layers):
+        for proj in PROJS:
+            t = get_proj(l, proj)
+            fw, fs, fb = PROJ_FIELDS[proj]
+            w = pack_int4(t["codes"]) if int4 else pack_int8(t["codes"])
+            setattr(layers[l], fw, put(w))
+            setattr(layers[l], fs, put(np.ascontiguousarray(t["scales"])))
+            if fb and t.get("bias") is not None:
+                setattr(layers[l], fb, put(np.ascontiguousarray(t["bias"], dtype=np.uint16)))
+        for k, v in get_norms(l).items():
+            if v is not None:
+                setattr(layers[l], k, put(np.ascontiguousarray(v, dtype=np.uint16)))
+    w = L.llm_weights()
+    w.embed = put(np.ascontiguousarray(embed, dtype=np.uint16))
+    w.final_norm = put(np.ascontiguousarray(final_norm, dtype=np.uint16))
+    if lm_head["kind"] == "bf16":
+        w.lm_head = put(np.ascontiguousarray(lm_head["w"], dtype=np.uint16))
+    elif lm_head["kind"] == "int8":
+        w.lm_head = put(pack_int8(lm_head["codes"]))
+        w.lm_scale = put(np.ascontiguousarray(lm_head["scales"], dtype=np.float32))
+    w.layers = layers
+    return layers, w
+
+
 class DeviceModel:
     """Packed decoder weights resident in device memory (torch tensors) + the ABI structs.
 
@@ -62,7 +114,6 @@ class DeviceModel:
         self.cfg = cfg
         self.device = device
         self._t = []
-        int4 = int(cfg.weight_format) == L.LLM_FMT_INT4_G128
 
         def up(a):
             a = np.ascontiguousarray(a)
@@ -70,33 +121,35 @@ class DeviceModel:
             self._t.append(t)
             return t.data_ptr()
 
-        layers = (L.llm_layer_weights * cfg.n_layers)()
-        for l in range(cfg.n_layers):
-            for proj in PROJS:
-                t = get_proj(l, proj)
-                fw, fs, fb = PROJ_FIELDS[proj]
-                w = pack_int4(t["codes"]) if int4 else pack_int8(t["codes"])
-                setattr(layers[l], fw, up(w))
-                setattr(layers[l], fs, up(np.ascontiguousarray(t["scales"])))
-                if fb and t.get("bias") is not None:
-                    setattr(layers[l], fb, up(np.ascontiguousarray(t["bias"], dtype=np.uint16)))
-            for k, v in get_norms(l).items():
-                if v is not None:
-                    setattr(layers[l], k, up(np.ascontiguousarray(v, dtype=np.uint16)))
-        self.layers = layers
-        w = L.llm_weights()
-        w.embed = up(np.ascontiguousarray(embed, dtype=np.uint16))
-        w.final_norm = up(np.ascontiguousarray(final_norm, dtype=np.uint16))
-        if lm_head["kind"] == "bf16":
-            w.lm_head = up(np.ascontiguousarray(lm_head["w"], dtype=np.uint16))
-        elif lm_head["kind"] == "int8":
-            w.lm_head = up(pack_int8(lm_head["codes"]))
-            w.lm_scale = up(np.ascontiguousarray(lm_head["scales"], dtype=np.float32))
-        w.layers = layers
-        self.weights = w
+        self.layers, self.weights = _fill(cfg, get_proj, get_norms, embed, final_norm, lm_head, up)
 
     def nbytes(self):
         return sum(t.numel() for t in self._t)
+
+
+def write_model_file(path, cfg, get_proj, get_norms, embed, final_norm, lm_head):
+    """Pack a model (same arguments as DeviceModel) and write it as one model file
+    (llm_model_file_write); no GPU needed."""
+    keep = []
+
+    def host(a):
+        a = np.ascontiguousarray(a)
+        keep.append(a)
+        return a.ctypes.data
+
+    layers, w = _fill(cfg, get_proj, get_norms, embed, final_norm, lm_head, host)
+    c = make_config(cfg)
+    L.check(L.load().llm_model_file_write(str(path).encode(), ctypes.byref(c), ctypes.byref(w)),
+            "llm_model_file_write")
+    del layers, keep
+
+
+def read_model_config(path):
+    """The llm_config in a model file's header (checked; no weights read)."""
+    c = L.llm_config()
+    L.check(L.load().llm_model_file_read_config(str(path).encode(), ctypes.byref(c)),
+            "llm_model_file_read_config")
+    return c
 
 
 class Engine:
@@ -112,6 +165,25 @@ class Engine:
         L.check(self.lib.llm_create(ctypes.byref(self.cfg), ctypes.byref(model.weights), s,
                                     ctypes.byref(h)), "llm_create")
         self.h = h
+
+    @classmethod
+    def from_file(cls, path, max_context=0, stream=None):
+        """An engine on a model file's weights (llm_create_from_file; the handle owns their
+        device copy).  max_context > 0 overrides the file's."""
+        self = cls.__new__(cls)
+        self.lib = L.load()
+        self.model = None
+        self.cfg = read_model_config(path)
+        if max_context > 0:
+            self.cfg.max_context = max_context
+        self.vocab = self.cfg.vocab
+        h = ctypes.c_void_p()
+        s = None if stream is None else ctypes.c_void_p(stream)
+        self.h = None
+        L.check(self.lib.llm_create_from_file(str(path).encode(), max_context, s, ctypes.byref(h)),
+                "llm_create_from_file")
+        self.h = h
+        return self
 
     def close(self):
         if self.h:
