@@ -393,8 +393,22 @@ def run_ours(args):
         finally:
             eng_l.close()
 
-    other_ms = no_pdl_ms = fused_ms = eager_ms = sampling_ms = None
+    other_ms = no_pdl_ms = fused_ms = eager_ms = sampling_ms = act8_ms = None
     if not args.no_variants:
+        # ---- graph replay with o_proj, gate/up and down on int8 activations (opt-in, INT4 models)
+        try:
+            eng.set_act_int8(True)
+            enqueue(3)
+            s8, e8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s8.record(stream)
+            enqueue(100)
+            e8.record(stream)
+            torch.cuda.synchronize()
+            act8_ms = round(s8.elapsed_time(e8) / 100, 4)
+            eng.set_act_int8(False)
+        except LLMError:
+            pass
+
         # ---- graph replay with top-k / top-p sampling (Qwen's recommended 0.6 / 20 / 0.95) instead of argmax
         eng.set_sampling(0.6, 20, 0.95, args.seed)
         enqueue(3)
@@ -531,6 +545,7 @@ def run_ours(args):
         "graph_no_pdl_ms_per_token": None if no_pdl_ms is None else round(no_pdl_ms, 4),
         "fused_qkv_attention_ms_per_token": fused_ms,
         "sampling_ms_per_token": sampling_ms,
+        "act_int8_ms_per_token": act8_ms,
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
             None if other_ms is None else round(other_ms, 4),
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,

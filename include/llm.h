@@ -242,6 +242,19 @@ int llm_set_pdl(llm_t *h, int32_t use_pdl);
  * (null handle, or 1 for a model outside the fused kernel), LLM_ERR_CUDA.    */
 int llm_set_fused_attention(llm_t *h, int32_t on);
 
+/* 1: the o_proj, gate/up and down GEMVs of the decode step (INT4 models) run
+ * on activations quantized to int8 per group of 128 inside each GEMV's
+ * staging (scale = absmax / 127, round half to even) with __dp4a products
+ * ("How To Construct Your Personal LLM Runtime From Scratch", §7, Path A;
+ * llm_op_gemv_int4_a8 gives the exact definition).  The QKV projection,
+ * the LM head and the batched prefill keep their activations.  0 (default):
+ * fp16 activations.  The logits change by the activation rounding (within
+ * the acceptance tolerance on the test models).  Not with the persistent
+ * step.  Re-captures the graph; waits for enqueued work first.  Errors:
+ * LLM_ERR_ARG (null handle, INT8 model, persistent step, or shapes outside
+ * the GEMV), LLM_ERR_CUDA.                                                  */
+int llm_set_act_int8(llm_t *h, int32_t on);
+
 /* How each step (and the batched prefill) picks the next token.  temperature
  * <= 0 (default): greedy argmax, lowest index on ties ("FlashQwen", "Stage 5 -
  * GPU argmax for greedy").  Otherwise sampling on the GPU ("FlashQwen" run

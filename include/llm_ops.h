@@ -23,6 +23,18 @@ extern "C" {
  * accumulate the row in FP32).  w: layout LLM_LAYOUT_INT4_VALUESHUFFLE words
  * [N][K/8]; s: bf16 [N][K/128]; bias: bf16 [N] or NULL; x: fp32 [K]; y: fp32 [N].
  * N % 32 == 0, K % 256 == 0.                                               */
+/* The same product on int8 activations ("How To Construct Your Personal LLM
+ * Runtime From Scratch", §7, Path A: activations quantized to INT8 with one
+ * scale per group before the GEMV, __dp4a products, the group scales applied
+ * in the accumulator).  For each group g of 128 along K: sx[g] = max|x| / 127
+ * and q[k] = x[k] / sx[g] rounded half to even (fp32, clamped to +-127; a zero
+ * group has sx 0 and codes 0), and
+ *   y[n] = sum_g scale[n][g] * sx[g] * sum_{k in g} code[n][k] * q[k],
+ * the inner sums exact in int32.  Arguments as llm_op_gemv_int4 (no bias).
+ * N % 32 == 0, K % 256 == 0, K <= 32768.                                    */
+int llm_op_gemv_int4_a8(const void *w, const void *s, int32_t N, int32_t K, const float *x, float *y,
+                        void *stream);
+
 int llm_op_gemv_int4(const void *w, const void *s, const void *bias, int32_t N, int32_t K,
                      const float *x, float *y, void *stream);
 

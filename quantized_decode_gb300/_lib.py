@@ -73,6 +73,8 @@ SIGNATURES = {
     "llm_set_sampling": (i32, [vp, f32, i32, f32, ctypes.c_uint64]),
     "llm_op_sample": (i32, [vp, i32, f32, i32, f32, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
     "llm_set_persistent": (i32, [vp, i32]),
+    "llm_set_act_int8": (i32, [vp, i32]),
+    "llm_op_gemv_int4_a8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_set_prefill_batched": (i32, [vp, i32]),
     "llm_pack_int4_g128": (i32, [vp, i64, i64, vp]),
     "llm_pack_int8_row": (i32, [vp, i64, i64, vp]),

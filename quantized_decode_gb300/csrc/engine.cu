@@ -51,6 +51,7 @@ struct llm_t {
     int P = 1, attn_cs = 8, lm_grid = 1;
     // llm_set_sampling: temperature / top-k / top-p instead of the greedy argmax
     bool sampling = false;
+    bool act_int8 = false;      // llm_set_act_int8: o_proj, gate/up, down on int8 activations
     float samp_t = 0.f, samp_p = 1.f;
     int samp_k = 1;
     uint64_t samp_seed = 0;
@@ -170,6 +171,9 @@ SampleArgs sampler_args(const llm_t *h) {
 
 // Enqueue one whole decode step (5L + 1 kernels).  With `ev`, event k is
 // recorded before kernel k and event 5L+1 after the last one.
+// Format of the o_proj, gate/up and down GEMVs (INT4 models may run them on int8 activations).
+int gemv_fmt(const llm_t *h) { return h->act_int8 ? kFmtInt4A8 : h->fmt; }
+
 cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
     if (h->persistent && !ev) return launch_step(h->sl, h->sp, h->stream);
     const llm_config &c = h->cfg;
@@ -231,20 +235,20 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         GemvArgs o{};
         o.mode = 1; o.w = L.wo; o.s = L.so; o.N = c.hidden; o.K = rq; o.x = h->attn; o.y = h->x;
         o.stats_in = st_attn; o.stats_out = st_o; o.stats_gamma = (const uint16_t *)L.mlp_norm;
-        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, o)) != cudaSuccess) return e;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), o)) != cudaSuccess) return e;
 
         GemvArgs gu{};
         gu.mode = 2; gu.w = L.wg; gu.s = L.sg; gu.w2 = L.wu; gu.s2 = L.su;
         gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
         gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
         gu.stats_in = st_o; gu.stats_out = st_gu;
-        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, gu)) != cudaSuccess) return e;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), gu)) != cudaSuccess) return e;
 
         GemvArgs dn{};
         dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
         dn.stats_in = st_gu; dn.stats_out = st_down;
         dn.stats_gamma = (const uint16_t *)(l + 1 < c.n_layers ? h->layers[l + 1].attn_norm : h->w.final_norm);
-        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, h->fmt, dn)) != cudaSuccess) return e;
+        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), dn)) != cudaSuccess) return e;
     }
     LmHeadArgs la{};
     const bool int8_head = h->fmt == kFmtInt8 && !c.tied_lm_head;
@@ -712,9 +716,21 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph) {
 
 int llm_set_persistent(llm_t *h, int32_t on) {
     if (!h) return LLM_ERR_ARG;
-    if (on && (!h->step_ok || h->sampling)) return LLM_ERR_ARG;
+    if (on && (!h->step_ok || h->sampling || h->act_int8)) return LLM_ERR_ARG;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->persistent = on != 0;
+    return capture(h);
+}
+
+int llm_set_act_int8(llm_t *h, int32_t on) {
+    if (!h) return LLM_ERR_ARG;
+    if (on && (h->fmt != kFmtInt4 || h->persistent)) return LLM_ERR_ARG;
+    if (on && (!gemv_shape_ok(kFmtInt4A8, h->cfg.hidden, h->cfg.n_q_heads * h->cfg.head_dim, 1) ||
+               !gemv_shape_ok(kFmtInt4A8, h->cfg.mlp, h->cfg.hidden, 2) ||
+               !gemv_shape_ok(kFmtInt4A8, h->cfg.hidden, h->cfg.mlp, 1)))
+        return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->act_int8 = on != 0;
     return capture(h);
 }
 

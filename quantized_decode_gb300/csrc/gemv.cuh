@@ -160,6 +160,23 @@ QD_DEV float int4_unit_dot(uint4 q, const uint4 (&x)[4]) {
     const float2 f = __half22float2(__hadd2(a, b));
     return f.x + f.y;
 }
+// INT4 unit against int8 activations (kFmtInt4A8): the word's nibbles n = c + 8
+// as bytes -- (w & 0x0F0F0F0F) ^ 0x08080808 holds n0, n4, n1, n5 and the same of
+// w >> 4 holds n2, n6, n3, n7 -- against activation bytes staged in that order
+// (q0 q4 q1 q5 | q2 q6 q3 q7 per 8 codes); returns sum n q (exact), the caller
+// subtracts 8 sum q.
+QD_DEV int int4_a8_unit_dot(uint4 q, const uint4 (&x)[2]) {
+    int s = 0;
+    s = __dp4a((int)lop3_and_xor(q.x, 0x0F0F0F0Fu, 0x08080808u), (int)x[0].x, s);
+    s = __dp4a((int)lop3_and_xor(q.x >> 4, 0x0F0F0F0Fu, 0x08080808u), (int)x[0].y, s);
+    s = __dp4a((int)lop3_and_xor(q.y, 0x0F0F0F0Fu, 0x08080808u), (int)x[0].z, s);
+    s = __dp4a((int)lop3_and_xor(q.y >> 4, 0x0F0F0F0Fu, 0x08080808u), (int)x[0].w, s);
+    s = __dp4a((int)lop3_and_xor(q.z, 0x0F0F0F0Fu, 0x08080808u), (int)x[1].x, s);
+    s = __dp4a((int)lop3_and_xor(q.z >> 4, 0x0F0F0F0Fu, 0x08080808u), (int)x[1].y, s);
+    s = __dp4a((int)lop3_and_xor(q.w, 0x0F0F0F0Fu, 0x08080808u), (int)x[1].z, s);
+    s = __dp4a((int)lop3_and_xor(q.w >> 4, 0x0F0F0F0Fu, 0x08080808u), (int)x[1].w, s);
+    return s;
+}
 QD_DEV float int8_unit_dot(uint4 q, const uint4 (&x)[2]) {
     half2 a = u32_as_h2(0u), b = u32_as_h2(0u);
     a = int8_word_dot(q.x, x[0].x, x[0].y, a);
@@ -181,8 +198,9 @@ QD_DEV float bf16_unit_dot(uint4 q, const float4 (&x)[2]) {
 template <int FMT, int RT, int D, class Rows, class Epi, class Sync>
 QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int t_first, int t_stride,
                         int n_tiles, int sb_begin, int sb_end, int U, int j, const void *xs, uint4 *ring,
-                        uint32_t *sring) {
+                        uint32_t *sring, const float *a8_sx = nullptr, const int *a8_qs = nullptr) {
     static_assert(D >= 2, "ring depth");
+    constexpr bool W4 = FMT == kFmtInt4 || FMT == kFmtInt4A8;  // INT4 codes and group scales
     constexpr int XC = FMT == kFmtInt4 ? 4 : 2;  // 16-byte activation chunks per unit
     const int lane = threadIdx.x & 31;
     const int n_it = sb_end > sb_begin ? sb_end - sb_begin : 0;
@@ -211,7 +229,7 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
                 for (int i = 0; i < RT; ++i) cp_async16(ring + ((slot * RT + i) * 2 + h) * 32 + lane, lrow[i].w + u);
             }
         }
-        if constexpr (FMT == kFmtInt4) {
+        if constexpr (W4) {
             // lane j < 2 of the slot: word j of the slab's 4 group scales (groups per row: U / 4, even)
             if (j < 2 && 4 * sb + 2 * j < (U >> 2)) {
 #pragma unroll
@@ -244,11 +262,11 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
         // the scale words are shared by the lanes of a row slot: every lane is
         // past its reads of the stage before it is refilled (here), and sees the
         // copying lanes' words once they completed (after the wait)
-        if constexpr (FMT == kFmtInt4) __syncwarp();
+        if constexpr (W4) __syncwarp();
         if (f + D - 1 < F) issue(f + D - 1);
         cp_async_commit();
         cp_async_wait<D - 1>();
-        if constexpr (FMT == kFmtInt4) __syncwarp();
+        if constexpr (W4) __syncwarp();
         const int slot = f % D;
         const int ub = 16 * (sb_begin + ci) + j;
 #pragma unroll
@@ -274,6 +292,11 @@ QD_DEV void gemv_stream(const Rows &rows, const Epi &epi, const Sync &sync, int 
                             const uint32_t sw = sring[((slot * RT + i) * 4 + rslot) * 2 + h];
                             const float sc = __uint_as_float(shi ? (sw & 0xFFFF0000u) : (sw << 16));
                             acc[i] = fmaf(int4_unit_dot(ring[idx], xr), sc, acc[i]);
+                        } else if constexpr (FMT == kFmtInt4A8) {
+                            const uint32_t sw = sring[((slot * RT + i) * 4 + rslot) * 2 + h];
+                            const float sc = __uint_as_float(shi ? (sw & 0xFFFF0000u) : (sw << 16));
+                            const int d = int4_a8_unit_dot(ring[idx], xr) - 8 * a8_qs[u];
+                            acc[i] = fmaf((float)d, sc * a8_sx[u >> 2], acc[i]);
                         } else {
                             acc[i] += int8_unit_dot(ring[idx], xr);
                         }
@@ -325,8 +348,9 @@ QD_DEV bool ksplit_reduce(float (&out)[RT], int ks, int kp, int slot_id, float *
 }
 
 // Units per row for a weight format: 16 bytes hold 32 INT4, 16 INT8 or 8 bf16 values.
+QD_HOST_DEV_INLINE bool int4_weights(int fmt) { return fmt == kFmtInt4 || fmt == kFmtInt4A8; }
 QD_HOST_DEV_INLINE int units_per_row(int fmt, int K) {
-    return fmt == kFmtInt4 ? K / 32 : (fmt == kFmtInt8 ? K / 16 : K / 8);
+    return int4_weights(fmt) ? K / 32 : (fmt == kFmtInt8 ? K / 16 : K / 8);
 }
 
 // Slabs (16 units) per row, the last one possibly partial.
@@ -372,6 +396,10 @@ QD_DEV void write_block_stats(float ss, float mx, float *out, float *red) {
 // is read once; otherwise they are computed here first.
 //   half_out: fp16 pairs of gamma*x*inv_rms*2^-e, max |value| < 1; returns 2^e.
 //   f32_out:  fp32 gamma*x*inv_rms (no prescale); returns 1.
+//   i8_out:   (kFmtInt4A8) the fp32 values gamma*x*inv_rms quantized per group
+//             of 128 to int8: sx_out[g] = absmax / 127, code = value / sx
+//             rounded half to even (fp32), bytes in the order int4_a8_unit_dot
+//             reads; qs_out[u] = the sum of unit u's 32 codes; returns 1.
 // gamma_s: the gain's shared-memory copy from gain_copy_async() (completed by
 // this thread before the call), used from the conversion pass on (or null: the
 // gain is read from global memory).
@@ -401,7 +429,8 @@ QD_DEV void gain_copy_async(const uint16_t *__restrict__ gamma, int K, uint16_t 
 QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__restrict__ src_bf16,
                                const uint16_t *__restrict__ gamma, float eps, int K,
                                const float *__restrict__ stats_in, half2 *half_out, float *f32_out,
-                               float *red, int blk_bytes = 0, const uint16_t *gamma_s = nullptr) {
+                               float *red, int blk_bytes = 0, const uint16_t *gamma_s = nullptr,
+                               uint8_t *i8_out = nullptr, float *sx_out = nullptr, int *qs_out = nullptr) {
     constexpr int kBatch = kStageBatch;
     const int tid = threadIdx.x, NT = blockDim.x;
     auto load4 = [&](int i) -> float4 {
@@ -501,6 +530,41 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int i = base + tid * 4 + b * step;
+            if (i8_out) {
+                // int8 per 128-group: a warp's 128 values of this batch are one group
+                // (K % 128 == 0, so i < K is warp-uniform); lanes 2m, 2m + 1 hold codes
+                // 0-3 and 4-7 of an octet, lanes 8m .. 8m + 7 one 32-code unit
+                const bool in = i < K;
+                float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (in) {
+                    const float4 g = gain4(i);
+                    vv = make_float4(g.x * (v[b].x * pre), g.y * (v[b].y * pre), g.z * (v[b].z * pre),
+                                     g.w * (v[b].w * pre));
+                }
+                const float am = warp_max(fmaxf(fmaxf(fabsf(vv.x), fabsf(vv.y)), fmaxf(fabsf(vv.z), fabsf(vv.w))));
+                const float sx = am / 127.f;
+                auto qz = [&](float t) -> int {
+                    return sx > 0.f ? max(-127, min(127, __float2int_rn(__fdiv_rn(t, sx)))) : 0;
+                };
+                const int q0 = qz(vv.x), q1 = qz(vv.y), q2 = qz(vv.z), q3 = qz(vv.w);
+                const uint32_t p = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
+                                   ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+                const uint32_t po = __shfl_xor_sync(0xffffffffu, p, 1);
+                int qs = q0 + q1 + q2 + q3;
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 4);
+                const int ln = tid & 31;
+                if (in) {
+                    if ((ln & 1) == 0) {  // q0 q4 q1 q5 | q2 q6 q3 q7
+                        const uint2 wv = make_uint2(prmt(p, po, 0x5140u), prmt(p, po, 0x7362u));
+                        *reinterpret_cast<uint2 *>(i8_out + swz_offset((uint32_t)i, blk_bytes)) = wv;
+                    }
+                    if ((ln & 7) == 0) qs_out[i >> 5] = qs;
+                    if (ln == 0) sx_out[i >> 7] = sx;
+                }
+                continue;
+            }
             if (i < K) {
                 const float4 g = gain4(i);
                 if (half_out) {

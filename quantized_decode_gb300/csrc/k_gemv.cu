@@ -20,6 +20,15 @@ constexpr int kDepth = RT >= 4 ? 4 : 5;
 
 QD_DEV float silu(float a) { return a / (1.f + __expf(-a)); }
 
+// Shared memory of the staged activations: fp16 [K], or for kFmtInt4A8 int8 [K]
+// then the group scales fp32 [K/128] and the unit code sums int32 [K/32].
+template <int FMT>
+QD_HOST_DEV_INLINE size_t act_region_bytes(int K) {
+    return FMT == kFmtInt4A8 ? (((size_t)K + 4 * (size_t)(K / 128) + 4 * (size_t)(K / 32) + 15) & ~(size_t)15)
+                             : (((size_t)K * 2 + 15) & ~(size_t)15);
+}
+QD_HOST_DEV_INLINE size_t gain_region_bytes(int K) { return ((size_t)K * 2 + 15) & ~(size_t)15; }
+
 template <int FMT, int RT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     constexpr int LPR = kLanesPerRow;
@@ -34,12 +43,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     const int U = units_per_row(FMT, a.K);
     const int PP = (NP + ks - 1) / ks;
     const int p_begin = kp * PP, p_end = min(NP, p_begin + PP);
-    const size_t rb = FMT == kFmtInt4 ? (size_t)a.K / 2 : (size_t)a.K;
+    const size_t rb = int4_weights(FMT) ? (size_t)a.K / 2 : (size_t)a.K;
     const int G = a.K / kGroup;
     half2 *xs = reinterpret_cast<half2 *>(smem);
-    const size_t xbytes = ((size_t)a.K * 2 + 15) & ~(size_t)15;
+    const size_t xbytes = act_region_bytes<FMT>(a.K);
+    float *a8_sx = FMT == kFmtInt4A8 ? reinterpret_cast<float *>((char *)smem + a.K) : nullptr;
+    int *a8_qs = FMT == kFmtInt4A8 ? reinterpret_cast<int *>(a8_sx + a.K / kGroup) : nullptr;
     uint16_t *gs = reinterpret_cast<uint16_t *>((char *)smem + xbytes);  // the gain (when a.gamma)
-    const size_t gbytes = a.gamma ? xbytes : 0;
+    const size_t gbytes = a.gamma ? gain_region_bytes(a.K) : 0;
     uint4 *ring;
     uint32_t *sring;
     warp_rings<RT, kDepth<RT>>((char *)smem + xbytes + gbytes, NW, warp, ring, sring);
@@ -68,8 +79,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
             }
         }
         pdl_wait();
-        post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, xs, nullptr, red,
-                                 act_blk_bytes<FMT>(), a.gamma ? gs : nullptr);
+        post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, FMT == kFmtInt4A8 ? nullptr : xs,
+                                 nullptr, red, act_blk_bytes<FMT>(), a.gamma ? gs : nullptr,
+                                 FMT == kFmtInt4A8 ? reinterpret_cast<uint8_t *>(xs) : nullptr, a8_sx, a8_qs);
         pdl_launch();
     };
     gain_copy_async(a.gamma, a.K, gs);
@@ -100,7 +112,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
             }
         };
         gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
-                                 sring);
+                                 sring, a8_sx, a8_qs);
     } else {
         const int TR = S * RT;
         auto rows = [&](int t, int i) -> RowRef {
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
             }
         };
         gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
-                                 sring);
+                                 sring, a8_sx, a8_qs);
     }
     if (a.stats_out) write_block_stats(st_ss, st_mx, a.stats_out, red);
 }
@@ -140,7 +152,7 @@ cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
     constexpr int LPR = kLanesPerRow;
     const int rows_per_tile = a.mode == 2 ? (32 / LPR) * (RT / 2) : (32 / LPR) * RT;
     const int tiles = a.N / rows_per_tile;
-    const size_t fixed = (((size_t)a.K * 2 + 15) & ~(size_t)15) * (a.gamma ? 2 : 1);  // activations (+ gain)
+    const size_t fixed = act_region_bytes<FMT>(a.K) + (a.gamma ? gain_region_bytes(a.K) : 0);  // activations (+ gain)
     const size_t per_warp = ring_bytes_per_warp<RT, kDepth<RT>>() + (size_t)32 * RT * 4;
     const int fit = (int)((kMaxSmemOptin - fixed) / per_warp);  // warps whose rings fit in shared memory
     GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots,
@@ -166,7 +178,7 @@ cudaError_t launch_fmt(const LaunchCfg &lc, const GemvArgs &a) {
 }  // namespace
 
 bool gemv_shape_ok(int fmt, int N, int K, int mode) {
-    if (fmt == kFmtInt4 ? (K % 256 != 0) : (K % 128 != 0)) return false;
+    if (int4_weights(fmt) ? (K % 256 != 0) : (K % 128 != 0)) return false;
     const int rows_per_tile = mode == 2 ? 4 * 2 : 4 * 2;
     return N > 0 && N % rows_per_tile == 0 && (size_t)K * 2 <= 64 * 1024;
 }
@@ -174,6 +186,7 @@ bool gemv_shape_ok(int fmt, int N, int K, int mode) {
 cudaError_t launch_gemv(const LaunchCfg &lc, int fmt, const GemvArgs &a) {
     if (fmt == kFmtInt4) return launch_fmt<kFmtInt4>(lc, a);
     if (fmt == kFmtInt8) return launch_fmt<kFmtInt8>(lc, a);
+    if (fmt == kFmtInt4A8) return launch_fmt<kFmtInt4A8>(lc, a);
     return cudaErrorInvalidValue;
 }
 

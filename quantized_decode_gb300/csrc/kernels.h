@@ -16,7 +16,9 @@ constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in 
 // Device-side error word (sticky until the host clears it).
 enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3, kErrTimeout = 16 };
 
-enum WeightFormat : int { kFmtInt4 = 1, kFmtInt8 = 2, kFmtBf16 = 3 };
+// kFmtInt4A8: INT4 g128 weights against activations quantized to int8 per
+// 128-group inside the GEMV (dp4a), an opt-in decode variant.
+enum WeightFormat : int { kFmtInt4 = 1, kFmtInt8 = 2, kFmtBf16 = 3, kFmtInt4A8 = 4 };
 
 // Scalars of the running sequence, resident in device memory so that one
 // captured graph serves every position.

@@ -46,6 +46,15 @@ int llm_op_gemv_int4(const void *w, const void *s, const void *bias, int32_t N, 
     return status(launch_gemv(op_cfg(stream), kFmtInt4, a));
 }
 
+int llm_op_gemv_int4_a8(const void *w, const void *s, int32_t N, int32_t K, const float *x, float *y,
+                        void *stream) {
+    if (!a16(w) || !s || !a16(x) || !y || N <= 0 || K <= 0 || N % 32 || K % 256) return LLM_ERR_ARG;
+    if (!gemv_shape_ok(kFmtInt4A8, N, K, 0)) return LLM_ERR_ARG;
+    GemvArgs a{};
+    a.mode = 0; a.w = w; a.s = s; a.N = N; a.K = K; a.x = x; a.y = y;
+    return status(launch_gemv(op_cfg(stream), kFmtInt4A8, a));
+}
+
 int llm_op_gemv_int8(const void *w, const float *s, int32_t N, int32_t K, const float *x, float *y,
                      void *stream) {
     if (!a16(w) || !s || !a16(x) || !y || N <= 0 || K <= 0 || N % 32 || K % 128) return LLM_ERR_ARG;

@@ -253,6 +253,9 @@ class Engine:
         L.check(self.lib.llm_set_sampling(self.h, float(temperature), int(top_k), float(top_p), int(seed)),
                 "llm_set_sampling")
 
+    def set_act_int8(self, on):
+        L.check(self.lib.llm_set_act_int8(self.h, int(on)), "llm_set_act_int8")
+
     def set_fused_attention(self, on):
         """True: QKV projection and attention of a layer in one kernel (where the model fits it)."""
         L.check(self.lib.llm_set_fused_attention(self.h, int(bool(on))), "llm_set_fused_attention")
