@@ -1,0 +1,49 @@
+"""Host logic of bench.py (CPU): the roofline's algorithmic bytes against the sizes of the
+tensors the packer actually produces, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from synth import model as sm
+
+from .test_model_file import TINY8, _expected_tensors
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    sys.path.insert(0, ROOT)
+    import bench as b
+    return b
+
+
+@pytest.mark.parametrize("cfg", [sm.CONFIGS["tiny"], TINY8], ids=["int4", "int8"])
+def test_algorithmic_bytes_match_the_packed_tensors(bench, cfg):
+    """Per step: every packed tensor once, except the embedding (one row), plus the K/V read at
+    length T and the appended row."""
+    import quantized_decode_gb300 as qd
+    qd.build()
+    sizes = dict((n, len(b)) for n, b in _expected_tensors(cfg, 1))
+    weights = sum(sizes.values()) - sizes["embed"] + cfg.hidden * 2
+    T = 200
+    kv = cfg.n_layers * (2 * cfg.n_kv_heads * cfg.head_dim * 2 * (T + 1))
+    assert bench.algorithmic_bytes(cfg, T) == weights + kv
+
+
+def test_reference_arm_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--ctx", "256", "--cycle", "16", "--steps", "2",
+                          "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = [l for l in out.stdout.splitlines() if l.startswith("{")][-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["unit"] == "ms/token" and d["higher_is_better"] is False
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "ms/token", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
