@@ -70,6 +70,17 @@ def parse():
     return p.parse_args()
 
 
+def max_over_ranks(x, device):
+    """The largest x (one float) over all ranks of the process group; x itself without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -346,10 +357,7 @@ def run_ours(args):
             torch.distributed.barrier()
     eng.sync()
     elapsed_ms = start_ev.elapsed_time(end_ev)
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, "cuda")
     ms_per_token = elapsed_ms / args.steps
     clocks = clk.summary(w0, w1)
 
