@@ -44,7 +44,7 @@
  * always formed in double.  The KV cache stores bfloat16 (round to nearest
  * even) in both variants, as the configuration prescribes.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - RoPE pairs element i with element i + d/2 of a head ("rotate half"),
  *     theta_i = base^(-2i/d), angle = pos * theta_i.
  *   - softmax scale is 1/sqrt(d); the new token attends to itself.
