@@ -125,9 +125,28 @@ def test_null_handles_and_status_strings(lib):
     out = ctypes.c_int32()
     assert lib.llm_decode_step(None, -1, ctypes.byref(out)) == L.LLM_ERR_ARG
     assert lib.llm_reset(None) == L.LLM_ERR_ARG
-    for code in range(0, -8, -1):
-        assert lib.llm_status_str(code)
+    for code in range(0, -10, -1):
+        assert lib.llm_status_str(code) != b"unknown status", code
     assert b"context" in lib.llm_status_str(L.LLM_ERR_CONTEXT_FULL)
+    assert b"model file" in lib.llm_status_str(L.LLM_ERR_FORMAT)
+    assert lib.llm_set_sampling(None, 0.6, 20, 0.95, 1) == L.LLM_ERR_ARG
+    assert lib.llm_set_act_int8(None, 1) == L.LLM_ERR_ARG
+
+
+def test_new_ops_refuse_bad_arguments_before_any_launch(lib):
+    """Argument checks that return before any CUDA call (no GPU here)."""
+    from quantized_decode_gb300 import _lib as L
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16   # 16-byte aligned host address
+    tok = ctypes.c_int32()
+    for V, T, k, top_p in ((0, 1.0, 1, 1.0), (100, 0.0, 5, 0.9), (100, float("inf"), 5, 0.9), (100, 1.0, 0, 0.9),
+                           (100, 1.0, 101, 0.9), (2000, 1.0, 1025, 0.9), (100, 1.0, 5, 0.0), (100, 1.0, 5, 1.5)):
+        assert lib.llm_op_sample(p, V, T, k, top_p, 1, 0, ctypes.byref(tok), None) == L.LLM_ERR_ARG
+    assert lib.llm_op_sample(None, 100, 1.0, 5, 0.9, 1, 0, ctypes.byref(tok), None) == L.LLM_ERR_ARG
+    for N, K in ((32, 128), (30, 256), (32, 65536), (0, 256)):
+        assert lib.llm_op_gemv_int4_a8(p, p, N, K, p, p, None) == L.LLM_ERR_ARG
+    assert lib.llm_op_gemv_int4_a8(p + 4, p, 32, 256, p, p, None) == L.LLM_ERR_ARG   # misaligned codes
+    assert lib.llm_op_gemv_int4_a8(p, None, 32, 256, p, p, None) == L.LLM_ERR_ARG
 
 
 def test_synthetic_scales_give_rms_002():
