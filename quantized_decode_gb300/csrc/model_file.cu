@@ -50,9 +50,14 @@ uint64_t fnv1a64(const unsigned char *p, size_t n) {
     return h;
 }
 
+// Positive and bounded (a header is only trusted after these checks; the
+// bounds are far above any model the engine takes).
 bool shape_ok(const llm_config &c) {
     if (c.n_layers <= 0 || c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 ||
         c.mlp <= 0 || c.vocab <= 0)
+        return false;
+    if (c.n_layers > 1024 || c.hidden > 65536 || c.n_q_heads > 1024 || c.n_kv_heads > 1024 || c.head_dim > 1024 ||
+        c.mlp > 1 << 20 || c.vocab > 1 << 24)
         return false;
     if (c.weight_format != LLM_FMT_INT4_G128 && c.weight_format != LLM_FMT_INT8_ROW) return false;
     if (c.weight_format == LLM_FMT_INT4_G128 &&
@@ -67,9 +72,11 @@ int layout_check(const llm_config &c) {
 }
 
 // Visits every tensor of the model in file order: f(field, bytes), where field
-// is the pointer slot of llm_weights / llm_layer_weights that holds it.
+// is the pointer slot of llm_weights / llm_layer_weights that holds it (with
+// layers == nullptr every layer visits one scratch struct: sizes only).
 template <class F>
 void tensor_map(const llm_config &c, llm_weights &w, llm_layer_weights *layers, F &&f) {
+    llm_layer_weights scratch{};
     const bool int4 = c.weight_format == LLM_FMT_INT4_G128;
     const int64_t h = c.hidden, qd = (int64_t)c.n_q_heads * c.head_dim, kvd = (int64_t)c.n_kv_heads * c.head_dim;
     const int64_t F_ = c.mlp, V = c.vocab, d = c.head_dim;
@@ -86,7 +93,7 @@ void tensor_map(const llm_config &c, llm_weights &w, llm_layer_weights *layers, 
         }
     }
     for (int l = 0; l < c.n_layers; ++l) {
-        llm_layer_weights &L = layers[l];
+        llm_layer_weights &L = layers ? layers[l] : scratch;
         f(L.wq, wb(qd, h)), f(L.sq, sb(qd, h));
         if (c.qkv_bias) f(L.bq, (uint64_t)(qd * 2));
         f(L.wk, wb(kvd, h)), f(L.sk, sb(kvd, h));
@@ -111,9 +118,8 @@ uint64_t align_up(uint64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Total file bytes of a model with this configuration.
 uint64_t file_bytes(const llm_config &c) {
     llm_weights w{};
-    std::vector<llm_layer_weights> layers((size_t)c.n_layers);
     uint64_t off = kHeaderBytes;
-    tensor_map(c, w, layers.data(), [&](const void *&, uint64_t bytes) { off = align_up(off) + bytes; });
+    tensor_map(c, w, nullptr, [&](const void *&, uint64_t bytes) { off = align_up(off) + bytes; });
     return off;
 }
 
@@ -186,7 +192,7 @@ int llm_model_file_bytes(const llm_config *cfg, int64_t *bytes) {
     return LLM_OK;
 }
 
-int llm_model_file_write(const char *path, const llm_config *cfg, const llm_weights *host_weights) {
+static int model_file_write(const char *path, const llm_config *cfg, const llm_weights *host_weights) {
     if (!path || !cfg || !host_weights || !host_weights->layers || !shape_ok(*cfg)) return LLM_ERR_ARG;
     const int lr = layout_check(*cfg);
     if (lr != LLM_OK) return lr;
@@ -232,7 +238,7 @@ int llm_model_file_read_config(const char *path, llm_config *cfg_out) {
     return read_header(f.fd, cfg_out, &pbytes);
 }
 
-int llm_create_from_file(const char *path, int32_t max_context, void *cuda_stream, llm_t **out) {
+static int create_from_file(const char *path, int32_t max_context, void *cuda_stream, llm_t **out) {
     if (!path || !out || max_context < 0) return LLM_ERR_ARG;
     *out = nullptr;
     Fd f;
@@ -245,10 +251,12 @@ int llm_create_from_file(const char *path, int32_t max_context, void *cuda_strea
     if (max_context > 0) cfg.max_context = max_context;
 
     // the payload in one device buffer, read in 64 MB chunks through a host buffer
-    char *dev = nullptr;
-    if (cudaMalloc(&dev, pbytes) != cudaSuccess) return LLM_ERR_CUDA;
+    // (host allocations first: nothing below can throw once the device buffer exists)
     constexpr uint64_t kChunk = 64ull << 20;
     std::vector<char> buf((size_t)(pbytes < kChunk ? pbytes : kChunk));
+    std::vector<llm_layer_weights> layers((size_t)cfg.n_layers);
+    char *dev = nullptr;
+    if (cudaMalloc(&dev, pbytes) != cudaSuccess) return LLM_ERR_CUDA;
     for (uint64_t done = 0; done < pbytes && rc == LLM_OK;) {
         const uint64_t n = pbytes - done < kChunk ? pbytes - done : kChunk;
         if (!read_all(f.fd, buf.data(), n, kHeaderBytes + done)) rc = LLM_ERR_IO;
@@ -260,7 +268,6 @@ int llm_create_from_file(const char *path, int32_t max_context, void *cuda_strea
         return rc;
     }
     llm_weights w{};
-    std::vector<llm_layer_weights> layers((size_t)cfg.n_layers);
     uint64_t off = kHeaderBytes;
     tensor_map(cfg, w, layers.data(), [&](const void *&p, uint64_t bytes) {
         const uint64_t at = align_up(off);
@@ -275,6 +282,24 @@ int llm_create_from_file(const char *path, int32_t max_context, void *cuda_strea
     }
     qd::adopt_weight_buffer(*out, dev);
     return LLM_OK;
+}
+
+// No C++ exception crosses the C ABI (allocation failures become errors).
+int llm_model_file_write(const char *path, const llm_config *cfg, const llm_weights *host_weights) {
+    try {
+        return model_file_write(path, cfg, host_weights);
+    } catch (...) {
+        return LLM_ERR_IO;
+    }
+}
+
+int llm_create_from_file(const char *path, int32_t max_context, void *cuda_stream, llm_t **out) {
+    if (out) *out = nullptr;
+    try {
+        return create_from_file(path, max_context, cuda_stream, out);
+    } catch (...) {
+        return LLM_ERR_IO;
+    }
 }
 
 }  // extern "C"

@@ -217,6 +217,10 @@ def test_file_refusals(qd, tmp_path):
     struct.pack_into("<i", bad, 16 + lid, L.LLM_LAYOUT_INT8_ROW)          # layout id
     struct.pack_into("<Q", bad, 96, _fnv1a64(bytes(bad[:96])))
     assert code_of(bytes(bad)) == L.LLM_ERR_LAYOUT
+    bad = bytearray(good)
+    struct.pack_into("<i", bad, 16, 1 << 30)                              # n_layers: a crafted header
+    struct.pack_into("<Q", bad, 96, _fnv1a64(bytes(bad[:96])))
+    assert code_of(bytes(bad)) == L.LLM_ERR_FORMAT
     with pytest.raises(LLMError) as e:
         qd.read_model_config(tmp_path / "missing.qd")
     assert e.value.code == L.LLM_ERR_IO
