@@ -217,7 +217,10 @@ class OracleModel:
     codes are packed with the oracle's own packer.  Holds its own KV cache.
     """
 
-    def __init__(self, cfg, seed, precision="f32", t_max=None, tensors=None):
+    def __init__(self, cfg, seed, precision="f32", t_max=None, tensors=None, norms=None,
+                 embed=None):
+        """tensors(layer, proj) / norms(layer) / embed [V][h] override the seeded draws
+        (the model-level pins build structured special cases through them)."""
         from synth import model as sm
         self.cfg = cfg
         self.seed = seed
@@ -243,12 +246,12 @@ class OracleModel:
                 setattr(layers[l], fs, self._hold(s))
                 if fb and t["bias"] is not None:
                     setattr(layers[l], fb, self._hold(_c(t["bias"], np.uint16)))
-            norms = sm.layer_norms(cfg, seed, l)
-            for k, v in norms.items():
+            nl = norms(l) if norms else sm.layer_norms(cfg, seed, l)
+            for k, v in nl.items():
                 if v is not None:
                     setattr(layers[l], k, self._hold(_c(v, np.uint16)))
         self.layers = layers
-        self.embed = _c(sm.embedding(cfg, seed), np.uint16)
+        self.embed = _c(sm.embedding(cfg, seed) if embed is None else embed, np.uint16)
         lm = sm.lm_head(cfg, seed)
         w = OrWeights()
         w.embed = self._hold(self.embed)
