@@ -132,17 +132,22 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
  * filling the KV cache, and return the greedy next token in *first_token
  * (HOST).  Blocks until done.  Prompts of 2 or more tokens run as one batch
  * on the tensor cores (llm_set_prefill_batched); the first such call
- * allocates the batch workspace (up to 1024 rows of activations plus one fp16
- * copy of the largest weight matrix, 2 * mlp * hidden * 2 bytes).  Errors:
+ * allocates the batch workspace (up to 1024 rows of residual, GEMM-operand,
+ * QKV and SwiGLU activations; the GEMMs read the packed weight codes and
+ * dequantize them in shared memory, so no weight copy is made).  Errors:
  * LLM_ERR_ARG (n <= 0, token out of range), LLM_ERR_CONTEXT_FULL,
- * LLM_ERR_CUDA, LLM_ERR_DEVICE.                                             */
+ * LLM_ERR_CUDA, LLM_ERR_TIMEOUT (a bounded wait inside a GEMM ran out),
+ * LLM_ERR_DEVICE (a device-side check failed).                              */
 int llm_prefill(llm_t *h, const int32_t *tokens, int32_t n, int32_t *first_token);
 
 /* One decode step by graph replay.  The step consumes `forced_input` when it
  * is >= 0 (teacher forcing), else the token the previous step emitted, writes
  * its K/V at position seq_len, and returns the greedy argmax in *out_token
  * (HOST).  Blocks until done.  Errors: LLM_ERR_ARG, LLM_ERR_CONTEXT_FULL
- * (checked before any launch), LLM_ERR_STATE (no previous token), LLM_ERR_CUDA. */
+ * (checked before any launch), LLM_ERR_STATE (no previous token), LLM_ERR_CUDA,
+ * LLM_ERR_TIMEOUT (a bounded device-side wait ran out: the step's outputs are
+ * undefined and the sticky error word stays set until llm_reset),
+ * LLM_ERR_DEVICE (a device-side check failed, same rule).                    */
 int llm_decode_step(llm_t *h, int32_t forced_input, int32_t *out_token);
 
 /* Enqueue n greedy decode steps (graph replays) on the engine's stream and
@@ -188,6 +193,12 @@ void llm_destroy(llm_t *h);
 /* Static string naming a status code. */
 const char *llm_status_str(int status);
 
+/* Identity of the build: the first 16 hex digits of a SHA-256 over the
+ * library's sources, these headers and its compile flags (no counterpart in
+ * the source pages; the Python package refuses a library whose id does not
+ * match the sources next to it).  Static string, never NULL.                 */
+const char *llm_build_id(void);
+
 /* Test and benchmark hook: DEVICE pointers to the KV pools ([L][pages][Hkv][16][d]
  * bf16) and the page table (int32 [pages], logical page -> physical page,
  * identity after create) so a caller can fill or shuffle them, and the number
@@ -208,6 +219,18 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph);
  * first.  Errors: LLM_ERR_ARG (null handle, or 1 for a model outside the
  * persistent kernel's shapes), LLM_ERR_CUDA.                                */
 int llm_set_persistent(llm_t *h, int32_t on);
+
+/* Test hook of the persistent kernel's failure path: its phase-counter waits
+ * expect `extra_arrivals` (0 or 1) arrivals more than any step delivers and
+ * give up after counter_wait_ns (1 us .. 1 s; default 1 s).  With 1, every
+ * step run as the persistent kernel ends by that bounded wait: the kernel
+ * records the timeout in the sticky error word, stops issuing copies, waits
+ * (with the normal 1 s bound) for the copies it has in flight, and returns;
+ * llm_decode_step then returns LLM_ERR_TIMEOUT, and llm_reset makes the engine
+ * usable again.  No GPU fault or hang is involved.  Re-captures the graph when
+ * the persistent kernel is on.  Errors: LLM_ERR_ARG (null handle, a model
+ * outside the persistent kernel's shapes, values out of range), LLM_ERR_CUDA. */
+int llm_debug_step_wait(llm_t *h, int32_t extra_arrivals, int64_t counter_wait_ns);
 
 /* Prefill mode for prompts of 2 or more tokens.  1 (default where the model's
  * shapes allow it): the prompt runs as a batch -- per layer RMSNorm, weight

@@ -65,14 +65,20 @@ int llm_op_sample(const float *logits, int32_t V, float temperature, int32_t top
  * on NVIDIA H100", "Architectural Blueprint").  For every query head h with
  * group g = h / (Hq/Hkv): out[h] = sum_t softmax_t(q_h . K[g][t] / sqrt(d)) V[g][t]
  * over t < T.  q: fp32 [Hq][d] (already rotated); k_pool, v_pool: bf16
- * [pages][Hkv][16][d]; page_table: int32, logical page -> physical page
- * (entries below (2^31 - 1) / (16 Hkv); one outside [0, that bound) reads page
- * 0 and is an error of the call); n_splits: key-range partitions per KV head
- * (1..256, rounded up to a multiple of 8, the CTAs of one cluster; 0 = the
- * engine's choice); out: fp32 [Hq][d].  d in {64, 128}, Hq/Hkv <= 8, T >= 1.  */
+ * [n_pool_pages][Hkv][16][d], 16-byte aligned, n_pool_pages * Hkv * 16 <= 2^31 - 1
+ * (the pools' extent: the kernel's copies never address past it);
+ * page_table: int32 [ceil(T/16)], logical page -> physical page, every entry
+ * in [0, n_pool_pages); n_splits: key-range partitions per KV head (1..256,
+ * rounded up to a multiple of 8, the CTAs of one cluster; 0 = the engine's
+ * choice); out: fp32 [Hq][d].  d in {64, 128}, Hq/Hkv <= 8, T >= 1.
+ * Blocks until the kernel has finished (it reads the kernel's error word back):
+ * a table entry outside [0, n_pool_pages) is replaced by page 0 on the device
+ * and returns LLM_ERR_DEVICE (out then undefined); a page copy that never
+ * lands within the kernel's 1 s bound returns LLM_ERR_TIMEOUT.  Other errors:
+ * LLM_ERR_ARG (checked before any launch), LLM_ERR_CUDA.                      */
 int llm_op_attention(const float *q, const void *k_pool, const void *v_pool,
-                     const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv, int32_t d,
-                     int32_t n_splits, float *out, void *stream);
+                     const int32_t *page_table, int32_t n_pool_pages, int32_t T, int32_t Hq,
+                     int32_t Hkv, int32_t d, int32_t n_splits, float *out, void *stream);
 
 /* llm_op_attention without any device allocation.  There is no counterpart
  * in the source pages: this serves callers that may not allocate device memory
@@ -89,10 +95,15 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool,
  * first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current, so make it before any
  * stream capture.  All calls on a device share the array: calls that may run
- * concurrently on the GPU (different streams without ordering) race.         */
+ * concurrently on the GPU (different streams without ordering) race.  Like
+ * llm_op_attention it blocks until the kernel has finished and reports a bad
+ * page (LLM_ERR_DEVICE) or a page wait that ran out (LLM_ERR_TIMEOUT).  The
+ * array's address is looked up once per device and kept: do not use the
+ * library across a cudaDeviceReset.                                           */
 int llm_op_attention_noalloc(const float *q, const void *k_pool, const void *v_pool,
-                             const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv,
-                             int32_t d, int32_t n_splits, float *out, void *stream);
+                             const int32_t *page_table, int32_t n_pool_pages, int32_t T,
+                             int32_t Hq, int32_t Hkv, int32_t d, int32_t n_splits, float *out,
+                             void *stream);
 
 /* Weight dequantization for the batched prefill ("Bare-Metal LLM Inference on
  * NVIDIA H100", prefill path: dequantized tiles feed the tensor cores):

@@ -3,6 +3,7 @@
 Each translation unit compiles in its own process so the build stays within a minute or
 two; objects go to quantized_decode_gb300/_build/ and the library next to this file.
 """
+import hashlib
 import os
 import shutil
 import subprocess
@@ -27,22 +28,41 @@ def _nvcc():
     return cand
 
 
-def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files += [os.path.join(HERE, "..", "include", f) for f in ("llm.h", "llm_ops.h")]
-    return max(os.path.getmtime(f) for f in files if os.path.exists(f))
+BASE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fopenmp",
+              "--expt-relaxed-constexpr"]
+ID_FILE = LIB + ".buildid"
+
+
+def source_hash(extra_flags=()):
+    """SHA-256 (first 16 hex digits) of every source, public header and compile flag of the
+    library.  It is compiled into libllm.so (llm_build_id) and checked when the library is
+    loaded, so a binary built from other sources is never used."""
+    h = hashlib.sha256()
+    files = sorted(os.listdir(CSRC))
+    for f in files:
+        h.update(f.encode() + b"\0")
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    for f in ("llm.h", "llm_ops.h"):
+        with open(os.path.join(HERE, "..", "include", f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    h.update(" ".join([*ARCH, *BASE_FLAGS, *extra_flags]).encode())
+    return h.hexdigest()[:16]
 
 
 def build(force=False, verbose=False, extra_flags=()):
-    """Compile every CUDA/C++ source and link libllm.so; returns the library path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps() and not extra_flags:
-        return LIB
+    """Compile every CUDA/C++ source and link libllm.so; returns the library path.  An
+    existing library is reused only if it was built from exactly these sources and flags."""
+    bid = source_hash(extra_flags)
+    if not force and os.path.exists(LIB) and os.path.exists(ID_FILE):
+        with open(ID_FILE) as fh:
+            if fh.read().strip() == bid:
+                return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
-    common = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fopenmp",
-              "--expt-relaxed-constexpr", *extra_flags]
+    common = [*BASE_FLAGS, *extra_flags, f"-DQD_BUILD_ID=\"{bid}\""]
     for src in CU_SOURCES:
         obj = os.path.join(BUILD, src + ".o")
         cmd = [nvcc, *ARCH, *common, "-c", os.path.join(CSRC, src), "-o", obj]
@@ -69,6 +89,9 @@ def build(force=False, verbose=False, extra_flags=()):
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fopenmp"])
     os.replace(tmp, LIB)
+    with open(ID_FILE + ".tmp", "w") as fh:
+        fh.write(bid + "\n")
+    os.replace(ID_FILE + ".tmp", ID_FILE)
     return LIB
 
 

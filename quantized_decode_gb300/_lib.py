@@ -51,6 +51,7 @@ class llm_weights(ctypes.Structure):
 
 # name -> (restype, argtypes)
 SIGNATURES = {
+    "llm_build_id": (ctypes.c_char_p, []),
     "llm_create": (i32, [ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights), vp,
                          ctypes.POINTER(vp)]),
     "llm_prefill": (i32, [vp, ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]),
@@ -73,6 +74,7 @@ SIGNATURES = {
     "llm_set_sampling": (i32, [vp, f32, i32, f32, ctypes.c_uint64]),
     "llm_op_sample": (i32, [vp, i32, f32, i32, f32, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
     "llm_set_persistent": (i32, [vp, i32]),
+    "llm_debug_step_wait": (i32, [vp, i32, i64]),
     "llm_set_act_int8": (i32, [vp, i32]),
     "llm_op_gemv_int4_a8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_set_prefill_batched": (i32, [vp, i32]),
@@ -87,8 +89,8 @@ SIGNATURES = {
     "llm_op_gemv_int4": (i32, [vp, vp, vp, i32, i32, vp, vp, vp]),
     "llm_op_gemv_int8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_op_lm_head_argmax": (i32, [vp, vp, vp, f32, i32, i32, vp, vp, vp, vp]),
-    "llm_op_attention": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
-    "llm_op_attention_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "llm_op_attention": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
+    "llm_op_attention_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "llm_op_dequant_f16": (i32, [i32, vp, vp, i32, i32, vp, vp]),
     "llm_op_gemm_f16": (i32, [vp, vp, i32, i32, i32, vp, vp]),
     "llm_op_gemm_quant": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, vp]),
@@ -112,6 +114,11 @@ def load():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    from . import _build
+    want, got = _build.source_hash(), lib.llm_build_id().decode()
+    if got != want:
+        raise RuntimeError(f"{LIB_PATH} was built from other sources (build id {got}, sources {want}); "
+                           "rebuild it with quantized_decode_gb300.build(force=True)")
     _lib = lib
     return lib
 

@@ -323,6 +323,8 @@ int plan_step(llm_t *h, int n_sm) {
     p.lm_val = h->lm_part_val;
     p.lm_idx = h->lm_part_idx;
     p.wait_ns = 1000000000ull;  // 1 s: a step takes about a millisecond
+    p.counter_wait_ns = p.wait_ns;
+    p.test_extra_arrivals = 0;
     p.inflight = kStepMaxSlots; // ring items in flight: enough bytes to cover the HBM latency
     int max_smem = 0;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
@@ -396,7 +398,7 @@ int fetch_token(llm_t *h, int32_t *out) {
                         cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
         return LLM_ERR_CUDA;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
-    if (h->pinned[3] != kErrNone) return LLM_ERR_DEVICE;
+    if (h->pinned[3] != kErrNone) return h->pinned[3] == kErrTimeout ? LLM_ERR_TIMEOUT : LLM_ERR_DEVICE;
     if (out) *out = h->pinned[2];
     return LLM_OK;
 }
@@ -574,6 +576,11 @@ void adopt_weight_buffer(llm_t *h, void *dev) { h->weight_buffer = dev; }
 
 extern "C" {
 
+#ifndef QD_BUILD_ID
+#define QD_BUILD_ID "unknown"
+#endif
+const char *llm_build_id(void) { return QD_BUILD_ID; }
+
 const char *llm_status_str(int s) {
     switch (s) {
         case LLM_OK: return "ok";
@@ -720,6 +727,16 @@ int llm_set_persistent(llm_t *h, int32_t on) {
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->persistent = on != 0;
     return capture(h);
+}
+
+int llm_debug_step_wait(llm_t *h, int32_t extra_arrivals, int64_t counter_wait_ns) {
+    if (!h || !h->step_ok || extra_arrivals < 0 || extra_arrivals > 1 || counter_wait_ns < 1000 ||
+        counter_wait_ns > 1000000000ll)
+        return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->sp.test_extra_arrivals = extra_arrivals;
+    h->sp.counter_wait_ns = (unsigned long long)counter_wait_ns;
+    return h->persistent ? capture(h) : LLM_OK;
 }
 
 int llm_set_act_int8(llm_t *h, int32_t on) {

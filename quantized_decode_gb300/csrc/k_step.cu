@@ -301,9 +301,12 @@ struct Smem {
     uint4 *stage;      // staged activations (mma B fragments)
     float *corr;       // per-block offset corrections of the staged activations
     float *red;        // 64 floats of reduction scratch
-    int *misc;         // [0] abort, [1..32] finished heads, [33] last-CTA flag
+    int *misc;         // [0] abort, [1..32] finished heads, [33] last-CTA flag,
+                       // [34] producers done, [40 + slot] uses of the slot issued
     StepLayer *layers; // copy of the per-layer pointer table
 };
+constexpr int kMiscProducersDone = 34, kMiscIssued = 40;
+static_assert(kMiscIssued + kStepMaxSlots <= 64, "misc words");
 QD_HOST_DEV_INLINE size_t smem_bytes(int n_slots, int n_layers) {
     return 1024 + (size_t)n_slots * kStepSlotBytes + (size_t)n_slots * 16 + (size_t)kStepResFloats * 4 +
            kStepStageBytes + 64 * 4 + 64 * 4 + (size_t)n_layers * sizeof(StepLayer);
@@ -333,10 +336,11 @@ QD_DEV Smem carve(uint8_t *raw, int n_slots) {
 // false (and records the error) when the wait runs out or another CTA failed.
 QD_DEV bool wait_counter(const StepParams &p, const int *ctr, int target) {
     const uint64_t t0 = gtimer();
+    target += p.test_extra_arrivals;
     for (uint32_t n = 0;; ++n) {
         if (ld_acquire(ctr) >= target) return true;
         if (ld_relaxed(&p.st->err) != kErrNone) return false;
-        if ((n & 15) == 15 && gtimer() - t0 > p.wait_ns) {
+        if ((n & 15) == 15 && gtimer() - t0 > p.counter_wait_ns) {
             atomicCAS(&p.st->err, kErrNone, kErrTimeout);
             return false;
         }
@@ -406,6 +410,7 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int pw) {
             }
             uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
             uint64_t *bar = s.full + rp.slot;
+            atomicAdd(s.misc + kMiscIssued + rp.slot, 1);
             // codes: one box of 4 rows (gate/up: 2 gate rows, then 2 up rows);
             // INT4 scales: the 16-byte cover of the rows' whole scale rows
             const int lo = (local * g.sr) & ~15, hi = ((local + nl) * g.sr + 15) & ~15;
@@ -435,6 +440,7 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int pw) {
             if (!claim()) continue;
             uint8_t *dst = s.ring + (size_t)rp.slot * kStepSlotBytes;
             uint64_t *bar = s.full + rp.slot;
+            atomicAdd(s.misc + kMiscIssued + rp.slot, 1);
             mbar_expect_tx(bar, (uint32_t)(np * 64 * DH));
             for (int k = 0; k < np; ++k) {
                 int phys = __ldg(p.page_table + k0 + k);
@@ -462,15 +468,22 @@ QD_DEV void producer(const StepParams &p, const Smem &s, int pw) {
         gemv_items(Ly, kPhDown);
     }
     if (ok) gemv_items(s.layers[0], kPhLm);
-    // Producer 0 leaves only once the last use of every slot has landed
+    // Producer 0 leaves only once every copy issued into the ring has landed
     // (bounded): consumers that gave up early must not leave copies in flight
-    // into a CTA that has exited.  Every producer walked the same schedule,
-    // so k_item is the CTA's item count.
+    // into a CTA that has exited.  It first waits (bounded) until every
+    // producer has stopped issuing; then, per slot, the last issued use u - 1
+    // is either in flight (the barrier's current phase, waited for) or landed
+    // (the phase just before the current one, which the parity wait returns at
+    // once).  Uses of a slot land in order, so earlier uses have landed too.
+    atomicAdd(s.misc + kMiscProducersDone, 1);
     if (pw == 0) {
         const uint64_t t0 = gtimer();
-        for (int sl = 0; sl < n_slots && sl < k_item; ++sl) {
-            const int last = (k_item - 1 - sl) / n_slots * n_slots + sl;  // last item in slot sl
-            const uint32_t par = (uint32_t)(last / n_slots) & 1u;
+        while (*(volatile int *)(s.misc + kMiscProducersDone) < kStepProducers && gtimer() - t0 < p.wait_ns) {
+        }
+        for (int sl = 0; sl < n_slots; ++sl) {
+            const int u = *(volatile int *)(s.misc + kMiscIssued + sl);
+            if (u == 0) continue;
+            const uint32_t par = (uint32_t)(u - 1) & 1u;
             while (!mbar_try_wait(s.full + sl, par) && gtimer() - t0 < p.wait_ns) {
             }
         }
@@ -1235,6 +1248,8 @@ __global__ void __launch_bounds__((NCW + 4) * 32, 1) k_step(const __grid_constan
             mbar_init(s.empty + i, 1);  // each item is released by the one warp that owns it
         }
         s.misc[0] = 0;
+        s.misc[kMiscProducersDone] = 0;
+        for (int i = 0; i < p.n_slots; ++i) s.misc[kMiscIssued + i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {

@@ -7,17 +7,12 @@
 #include "../../include/llm.h"
 #include "../../include/llm_ops.h"
 #include "kernels.h"
+#include "ops_util.h"
 #include "prefill.h"
 
 using namespace qd;
 
 namespace {
-
-// The pools' extent is not an argument of the ops: pages are bounded only so
-// that every row index (page * Hkv * 16) stays an int32 TMA coordinate; a
-// table entry past the bound is flagged as a bad page.
-inline int op_max_pages(int Hkv) { return (int)(((1u << 31) - 1) / (unsigned)(Hkv * kPageTokens)); }
-
 
 LaunchCfg op_cfg(void *stream) {
     LaunchCfg lc{};
@@ -102,10 +97,11 @@ int llm_op_lm_head_argmax(const void *w, const float *lm_scale, const void *gamm
 }
 
 int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, const int32_t *page_table,
-                     int32_t T, int32_t Hq, int32_t Hkv, int32_t d, int32_t n_splits, float *out,
-                     void *stream) {
+                     int32_t n_pool_pages, int32_t T, int32_t Hq, int32_t Hkv, int32_t d, int32_t n_splits,
+                     float *out, void *stream) {
     if (!q || !a16(k_pool) || !a16(v_pool) || !page_table || !out || T < 1 || Hkv < 1 ||
-        Hq % Hkv || Hq / Hkv > kMaxGqa || (d != 64 && d != 128) || n_splits < 0 || n_splits > 256)
+        Hq % Hkv || Hq / Hkv > kMaxGqa || (d != 64 && d != 128) || n_splits < 0 || n_splits > 256 ||
+        !op_pool_pages_ok(n_pool_pages, Hkv))
         return LLM_ERR_ARG;
     LaunchCfg lc = op_cfg(stream);
     const int n_pg = (T + kPageTokens - 1) / kPageTokens;
@@ -122,7 +118,7 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, con
     if (cudaMemsetAsync(scratch, 0, cnt_bytes, lc.stream) != cudaSuccess) return LLM_ERR_CUDA;
     AttnArgs a{};
     a.q = q; a.k_pool = (const uint16_t *)k_pool; a.v_pool = (const uint16_t *)v_pool;
-    a.page_table = page_table; a.n_pages = op_max_pages(Hkv);
+    a.page_table = page_table; a.n_pages = n_pool_pages;
     a.st = nullptr; a.T_fixed = T;
     a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.P = P;
     a.counter = (int *)scratch;
@@ -131,8 +127,9 @@ int llm_op_attention(const float *q, const void *k_pool, const void *v_pool, con
     a.part_ml = (float *)(scratch + cnt_bytes + o_bytes);
     a.out = out;
     cudaError_t e = launch_attention(lc, a);
+    int rc = e == cudaSuccess ? op_read_err(a.err, lc.stream) : LLM_ERR_CUDA;
     cudaError_t f = cudaFreeAsync(scratch, lc.stream);
-    return status(e != cudaSuccess ? e : f);
+    return rc != LLM_OK ? rc : status(f);
 }
 
 int llm_op_dequant_f16(int32_t fmt, const void *w, const void *s, int32_t N, int32_t K, void *out,

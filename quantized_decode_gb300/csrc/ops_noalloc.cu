@@ -16,22 +16,20 @@
 // current, on the first call made on that device.  That first call should
 // therefore come before any stream capture.  All calls on a device share the one
 // array and it keeps the last call's contents; calls whose executions overlap on
-// the GPU (different streams, no ordering between them) race on it.
+// the GPU (different streams, no ordering between them) race on it.  The cached
+// address is valid for the life of the device's primary context: the library
+// must not be used across a cudaDeviceReset (the module, and with it the array,
+// is loaded again at a new address).
 #include <mutex>
 
 #include "../../include/llm.h"
 #include "../../include/llm_ops.h"
 #include "kernels.h"
+#include "ops_util.h"
 
 using namespace qd;
 
 namespace {
-
-// The pools' extent is not an argument of the ops: pages are bounded only so
-// that every row index (page * Hkv * 16) stays an int32 TMA coordinate; a
-// table entry past the bound is flagged as a bad page.
-inline int op_max_pages(int Hkv) { return (int)(((1u << 31) - 1) / (unsigned)(Hkv * kPageTokens)); }
-
 
 constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB per device
 constexpr size_t kCounterBytes = 256;              // arrival counters + error word, zeroed per call
@@ -60,11 +58,12 @@ int scratch_address(void **out) {
 }  // namespace
 
 extern "C" int llm_op_attention_noalloc(const float *q, const void *k_pool, const void *v_pool,
-                                        const int32_t *page_table, int32_t T, int32_t Hq, int32_t Hkv,
-                                        int32_t d, int32_t n_splits, float *out, void *stream) {
+                                        const int32_t *page_table, int32_t n_pool_pages, int32_t T,
+                                        int32_t Hq, int32_t Hkv, int32_t d, int32_t n_splits, float *out,
+                                        void *stream) {
     if (!q || !k_pool || !v_pool || ((uintptr_t)k_pool & 15) || ((uintptr_t)v_pool & 15) || !page_table ||
         !out || T < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > kMaxGqa || (d != 64 && d != 128) ||
-        n_splits < 0 || n_splits > 256)
+        n_splits < 0 || n_splits > 256 || !op_pool_pages_ok(n_pool_pages, Hkv))
         return LLM_ERR_ARG;
     LaunchCfg lc{};
     lc.stream = (cudaStream_t)stream;
@@ -93,7 +92,7 @@ extern "C" int llm_op_attention_noalloc(const float *q, const void *k_pool, cons
     a.k_pool = (const uint16_t *)k_pool;
     a.v_pool = (const uint16_t *)v_pool;
     a.page_table = page_table;
-    a.n_pages = op_max_pages(Hkv);
+    a.n_pages = n_pool_pages;
     a.st = nullptr;
     a.T_fixed = T;
     a.Hq = Hq;
@@ -105,5 +104,6 @@ extern "C" int llm_op_attention_noalloc(const float *q, const void *k_pool, cons
     a.part_o = (float *)(scratch + kCounterBytes);
     a.part_ml = (float *)(scratch + kCounterBytes + o_bytes);
     a.out = out;
-    return launch_attention(lc, a) == cudaSuccess ? LLM_OK : LLM_ERR_CUDA;
+    if (launch_attention(lc, a) != cudaSuccess) return LLM_ERR_CUDA;
+    return op_read_err(a.err, lc.stream);
 }

@@ -103,6 +103,11 @@ struct StepParams {
     int inflight;                // ring items a CTA may have in flight at once
     unsigned long long *prof;    // null, or 5 L + 2 phase timestamps (CTA 0)
     unsigned long long wait_ns;  // bound on every wait
+    // Test hooks (llm_debug_step_wait): the phase-counter waits expect this many
+    // arrivals more than will come and give up after counter_wait_ns; the
+    // waits that guard copies in flight keep wait_ns.
+    int test_extra_arrivals;
+    unsigned long long counter_wait_ns;
 };
 
 // Host side (k_step.cu).

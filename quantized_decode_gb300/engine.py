@@ -264,6 +264,12 @@ class Engine:
         """True: the step is the persistent whole-step kernel; False: the kernel chain."""
         L.check(self.lib.llm_set_persistent(self.h, int(bool(on))), "llm_set_persistent")
 
+    def debug_step_wait(self, extra_arrivals, counter_wait_ns):
+        """Test hook: the persistent kernel's phase-counter waits expect extra_arrivals (0/1)
+        more arrivals and give up after counter_wait_ns (llm_debug_step_wait)."""
+        L.check(self.lib.llm_debug_step_wait(self.h, int(extra_arrivals), int(counter_wait_ns)),
+                "llm_debug_step_wait")
+
     def set_prefill_batched(self, on):
         """True: prompts run as one batch on the tensor cores; False: token by token."""
         L.check(self.lib.llm_set_prefill_batched(self.h, int(bool(on))), "llm_set_prefill_batched")

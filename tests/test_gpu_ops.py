@@ -178,8 +178,8 @@ def _attention(lib, q, kp, vp, table, T, Hq, Hkv, d, P):
     qd_ = torch.from_numpy(np.ascontiguousarray(q, np.float32)).cuda()
     kd, vd, td = to_dev(kp), to_dev(vp), to_dev(np.ascontiguousarray(table, np.int32))
     out = torch.empty(Hq * d, dtype=torch.float32, device="cuda")
-    rc = lib.llm_op_attention(qd_.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(), T, Hq, Hkv,
-                              d, P, out.data_ptr(), None)
+    rc = lib.llm_op_attention(qd_.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(),
+                              kp.shape[0], T, Hq, Hkv, d, P, out.data_ptr(), None)
     assert rc == 0
     torch.cuda.synchronize()
     return out.cpu().numpy()
@@ -226,3 +226,35 @@ def test_attention_split_count_invariance(lib):
     for P in (2, 16, 125, 200):
         out = _attention(lib, q, kp, vp, ident, T, Hq, Hkv, d, P)
         np.testing.assert_allclose(out, base, rtol=0, atol=1e-5 * np.max(np.abs(base)))
+
+
+def test_attention_reports_a_page_outside_the_pools(lib):
+    """A table entry past the caller's pools is never fetched (page 0 stands in on the
+    device) and the call returns LLM_ERR_DEVICE; the next good call returns LLM_OK."""
+    from quantized_decode_gb300 import _lib as L
+    T, Hq, Hkv, d = 100, 28, 4, 128
+    n_pg = (T + 15) // 16
+    ident = np.arange(n_pg, dtype=np.int32)
+    q = synth.normal_f32(9, 1, Hq * d, 0.0, 1.0)
+    kc = synth.f32_to_bf16(synth.normal_f32(9, 2, T * Hkv * d, 0.0, 1.0)).reshape(T, Hkv, d)
+    vc = synth.f32_to_bf16(synth.normal_f32(9, 3, T * Hkv * d, 0.0, 1.0)).reshape(T, Hkv, d)
+    kp, vp = _paged(kc, vc, n_pg, ident)
+    kd, vd = to_dev(kp), to_dev(vp)
+    qd_ = torch.from_numpy(q).cuda()
+    out = torch.empty(Hq * d, dtype=torch.float32, device="cuda")
+    for bad in (n_pg, -1, 1 << 20):
+        table = ident.copy()
+        table[3] = bad
+        td = to_dev(table)
+        rc = lib.llm_op_attention(qd_.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(), n_pg,
+                                  T, Hq, Hkv, d, 0, out.data_ptr(), None)
+        assert rc == L.LLM_ERR_DEVICE, bad
+    td = to_dev(ident)
+    rc = lib.llm_op_attention(qd_.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(), n_pg, T,
+                              Hq, Hkv, d, 0, out.data_ptr(), None)
+    assert rc == 0
+    # pool extent refused on the host before any launch
+    for n_pool in (0, -5, (1 << 31) // (16 * Hkv) + 1):
+        rc = lib.llm_op_attention(qd_.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(), n_pool,
+                                  T, Hq, Hkv, d, 0, out.data_ptr(), None)
+        assert rc == L.LLM_ERR_ARG, n_pool

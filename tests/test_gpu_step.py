@@ -117,6 +117,7 @@ def test_full_width_two_layers_vs_oracle(name, T0):
         for i in range(3):
             eng.decode_step(tok)
             ref = ref_orc.step(tok, T0 + i)
+            check_logits(eng.logits(), ref, f"{name} chain step {i}")
             scale = float(np.max(np.abs(ref)))
             assert float(np.max(np.abs(eng.logits() - logits[i]))) <= 2e-2 * scale
             tok = int(np.argmax(ref))
@@ -142,3 +143,36 @@ def test_full_width_steps_do_not_stall():
         assert time.perf_counter() - t0 < 0.5
     finally:
         eng.close()
+
+
+def test_counter_wait_that_runs_out_returns_timeout_and_reset_recovers(tiny):
+    """The failure path of a bounded device wait, without any GPU fault: the test hook makes
+    the persistent kernel's phase-counter waits expect one arrival more than will come, with
+    a 2 ms bound.  The step must come back with LLM_ERR_TIMEOUT well within a second (the
+    kernel records the timeout, stops issuing copies, drains the ones in flight and
+    returns), and after llm_reset the engine must reproduce a clean run bit for bit."""
+    import ctypes
+    import time
+    from quantized_decode_gb300 import _lib as L
+    cfg, eng = tiny
+    eng.set_persistent(True)
+    prompt = sm.prompt(cfg, SEED, 12)
+    want = _forced(eng, prompt, [5, 6, 7])
+    eng.reset()
+    eng.prefill(prompt)
+    eng.debug_step_wait(1, 2_000_000)
+    try:
+        out = ctypes.c_int32()
+        for _ in range(2):                 # the sticky word keeps reporting until llm_reset
+            t0 = time.perf_counter()
+            rc = eng.lib.llm_decode_step(eng.h, 5, ctypes.byref(out))
+            dt = time.perf_counter() - t0
+            assert rc == L.LLM_ERR_TIMEOUT, rc
+            assert dt < 0.5, dt
+    finally:
+        eng.debug_step_wait(0, 1_000_000_000)
+    eng.reset()
+    got = _forced(eng, prompt, [5, 6, 7])
+    for x, y in zip(want, got):
+        np.testing.assert_array_equal(x, y)
+    eng.set_persistent(False)

@@ -30,13 +30,13 @@ def _case(seed, T, Hq, Hkv, d):
     kpad[:T], vpad[:T] = kc, vc
     kp[perm[:n_pg]] = kpad.reshape(n_pg, 16, Hkv, d).transpose(0, 2, 1, 3)
     vp[perm[:n_pg]] = vpad.reshape(n_pg, 16, Hkv, d).transpose(0, 2, 1, 3)
-    return (torch.from_numpy(q).cuda(), to_dev(kp), to_dev(vp), to_dev(perm))
+    return (torch.from_numpy(q).cuda(), to_dev(kp), to_dev(vp), to_dev(perm), n_pg + 3)
 
 
 def _run(fn, case, T, Hq, Hkv, d, P):
-    q, kp, vp, pt = case
+    q, kp, vp, pt, n_pool = case
     out = torch.full((Hq * d,), float("nan"), dtype=torch.float32, device="cuda")
-    rc = fn(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), pt.data_ptr(), T, Hq, Hkv, d, P,
+    rc = fn(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), pt.data_ptr(), n_pool, T, Hq, Hkv, d, P,
             out.data_ptr(), None)
     assert rc == 0
     torch.cuda.synchronize()
@@ -62,8 +62,27 @@ def test_noalloc_attention_rejects_requests_beyond_its_array():
     lib = qd.load()
     T, Hq, Hkv, d, P = 64, 64, 8, 128, 256   # 64 * 256 * 130 * 4 bytes > 4 MiB
     case = _case(3, T, 64, Hkv, d)
-    q, kp, vp, pt = case
+    q, kp, vp, pt, n_pool = case
     out = torch.zeros(Hq * d, dtype=torch.float32, device="cuda")
-    rc = lib.llm_op_attention_noalloc(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), pt.data_ptr(), T, Hq,
-                                      Hkv, d, P, out.data_ptr(), None)
+    rc = lib.llm_op_attention_noalloc(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), pt.data_ptr(), n_pool,
+                                      T, Hq, Hkv, d, P, out.data_ptr(), None)
     assert rc == L.LLM_ERR_ARG
+
+
+def test_noalloc_attention_reports_a_page_outside_the_pools():
+    """The shared array carries the error word too: a bad page returns LLM_ERR_DEVICE and
+    the next call (which clears the word) returns LLM_OK with the allocating entry's result."""
+    import quantized_decode_gb300 as qd
+    from quantized_decode_gb300 import _lib as L
+    lib = qd.load()
+    T, Hq, Hkv, d = 200, 28, 4, 128
+    q, kp, vp, pt, n_pool = _case(4, T, Hq, Hkv, d)
+    bad = pt.clone()
+    bad[0:4] = torch.tensor([n_pool, 0, 0, 0], dtype=torch.uint8)   # entry 0 := n_pool (past the pools)
+    out = torch.zeros(Hq * d, dtype=torch.float32, device="cuda")
+    rc = lib.llm_op_attention_noalloc(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), bad.data_ptr(), n_pool,
+                                      T, Hq, Hkv, d, 0, out.data_ptr(), None)
+    assert rc == L.LLM_ERR_DEVICE
+    ref = _run(lib.llm_op_attention, (q, kp, vp, pt, n_pool), T, Hq, Hkv, d, 0)
+    got = _run(lib.llm_op_attention_noalloc, (q, kp, vp, pt, n_pool), T, Hq, Hkv, d, 0)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.max(np.abs(ref)) + 1e-6)
