@@ -10,9 +10,10 @@ HBM before timing, and a KV cache pre-filled with seeded N(0,1) bf16 values thro
 table; timed positions cycle through [ctx - cycle, ctx) so every step attends to ~ctx tokens.
 The 4.7 GB read per step is far larger than L2 (129 MB), so no flush is needed between steps.
 
---impl reference times the CPU oracle instead (a bounded sample of the same workload,
-scaled to ms/token).  Under torchrun every rank runs its own replica (no collective on the
-data path); rank 0 prints one JSON line.
+--impl reference times the CPU oracle instead: the whole 28-layer model with the real
+vocabulary, greedy steps on the same seeded weights and KV fill (no extrapolation; the step
+count is capped by a time budget and the steps actually run are reported).  Under torchrun
+every rank runs its own replica (no collective on the data path); rank 0 prints one JSON line.
 """
 import argparse
 import json
@@ -30,17 +31,27 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode ms/token & HBM GB/s (7B INT4, ctx 4096); TTFT pp512"
 NOMINAL_HBM_GBS = 8000.0
-# DRAM bytes read + written per launch, from one ncu capture of the kernel as it
-# stands (profiles/decode_layer_7b_chain_ncu_full.md); keyed by shape and
-# kernel, dropped (None) for any kernel changed since that capture.
-NCU_TRAFFIC = {
-    ("qwen2.5-7b", "gate_up"): 70109184 + 318464,
-    ("qwen2.5-7b", "down"): 35177472,
-    ("qwen2.5-7b", "o_proj"): 6730496,
-    ("qwen2.5-7b", "qkv"): 8601344,
-    ("qwen2.5-7b", "attention"): 8219904,
-}
+# DRAM bytes read + written per launch come from an ncu capture summarised in
+# profiles/: lines "traffic: build=<id> shape=<name> kernel=<k> bytes=<n>".  A
+# line counts only while the library's build id (a hash of every source) is the
+# one it was measured on, so a changed kernel reports traffic null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic_7b.md")
 FALLBACK_HBM_GBS = 6800.0
+ORACLE_BUDGET_S = 240.0   # bound on the oracle's timed steps (reference arm)
+
+
+def ncu_traffic(build_id, shape, kernel):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if not line.startswith("traffic:"):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                if kv.get("build") == build_id and kv.get("shape") == shape and kv.get("kernel") == kernel:
+                    return int(kv["bytes"])
+    except OSError:
+        pass
+    return None
 
 
 def parse():
@@ -67,6 +78,10 @@ def parse():
     p.add_argument("--profile-steps", type=int, default=4)
     p.add_argument("--step", default="chain", choices=["chain", "persistent"],
                    help="decode step as a kernel chain or as one persistent kernel")
+    p.add_argument("--timeline-steps", type=int, default=16,
+                   help="steps of the in-graph per-kernel timeline (0: skip)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the 1.5B (pp512/tg128) and Qwen3-8B INT8 (inputs 128..4096) lines")
     return p.parse_args()
 
 
@@ -209,59 +224,65 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# ---------------------------------------------------------------- CPU oracle sample
+# ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(cfg, seed, T, n_layer_steps, lm_w):
-    """Oracle ms/token for the full model from a bounded sample: a one-layer model of the
-    same shape at KV length T (timed per step) and the full LM head GEMV (timed once)."""
+def oracle_decode(cfg, seed, T0, n_warm, n_steps, rec=None, budget_s=None):
+    """The oracle (fp32, all host cores) on the whole model: the seeded weights, the KV
+    cache filled with the same seeded values as the GPU run up to T0, then greedy steps at
+    positions T0, T0 + 1, ...  Returns (mean ms/step, sample text, steps timed)."""
     import oracle
     from synth import model as sm
-    one = cfg.with_(n_layers=1, vocab=64, max_context=T + n_layer_steps + 1)
-    orc = oracle.OracleModel(one, seed)
-    k, v = sm.kv_fill(one, seed, 0, T)
-    orc.set_kv(0, k, v)
-    o = oracle.Oracle("f32")
-    x = np.ones(cfg.hidden, np.float32)
-    t0 = time.perf_counter()
-    if lm_w is not None:
-        o.gemv_bf16(lm_w, x)
-    lm_ms = (time.perf_counter() - t0) * 1e3
+    get_proj, get_norms, emb, fin, lm = rec if rec is not None else sm.recipe(cfg, seed)
+    orc = oracle.OracleModel(cfg, seed, t_max=T0 + n_warm + n_steps + 1, tensors=get_proj,
+                             norms=get_norms, embed=emb, lm_head=lm)
+    for l in range(cfg.n_layers):
+        k, v = sm.kv_fill(cfg, seed + 1, l, T0)
+        orc.set_kv(l, k, v)
+    tok, pos = 7, T0
+    for _ in range(n_warm):
+        tok = int(np.argmax(orc.step(tok, pos)))
+        pos += 1
     times = []
-    for i in range(n_layer_steps):
+    t_start = time.perf_counter()
+    for i in range(n_steps):
         t0 = time.perf_counter()
-        orc.step(5, T + i)
+        tok = int(np.argmax(orc.step(tok, pos)))
         times.append((time.perf_counter() - t0) * 1e3)
-    layer_ms = statistics.median(times)
-    total = lm_ms + cfg.n_layers * layer_ms
-    sample = (f"oracle fp32: {n_layer_steps} steps of a 1-layer {cfg.name}-shape model at KV {T} "
-              f"(median {layer_ms:.1f} ms/layer) x {cfg.n_layers} layers + one full LM-head GEMV "
-              f"({lm_ms:.1f} ms)")
-    return total, sample, times
+        pos += 1
+        if budget_s is not None and time.perf_counter() - t_start > budget_s:
+            break
+    mean_ms = statistics.mean(times)
+    sample = (f"oracle fp32, whole {cfg.name}-shape model ({cfg.n_layers} layers, vocab {cfg.vocab}): "
+              f"{len(times)} greedy steps at KV {T0 + n_warm + 1}..{T0 + n_warm + len(times)} after "
+              f"{n_warm} warm-up steps, mean {mean_ms:.1f} ms/token")
+    return mean_ms, sample, len(times)
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    from synth import model as sm
     cfg = model_cfg(args)
-    lm = sm.lm_head(cfg, args.seed)
-    lm_w = lm.get("w")
-    T = args.ctx
-    total, sample, _ = oracle_sample(cfg, args.seed, T, max(args.warmup, 1), lm_w)  # warm-up
-    total, sample, times = oracle_sample(cfg, args.seed, T, args.steps, lm_w)
+    ctx, cycle = args.ctx, min(args.cycle, args.ctx - 1)
+    T0 = ctx - cycle
+    n_warm = args.warmup
+    t0 = time.perf_counter()
+    mean_ms, sample, n_run = oracle_decode(cfg, args.seed, T0, n_warm, args.steps, budget_s=ORACLE_BUDGET_S)
+    wall = time.perf_counter() - t0
     cores = os.cpu_count()
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(total, 3), "unit": "ms/token",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total, 3), "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": f"{cfg.name} INT4 g128 decode, batch 1, KV {T}", "global_batch": 1,
-                   "seq_len": T, "parallelism": "replicas"},
-        "cpu_baseline": {"value": round(total, 3), "unit": "ms/token", "cores": cores,
+        "impl": "reference", "metric": METRIC, "value": round(mean_ms, 3), "unit": "ms/token",
+        "n_gpus": args.gpus, "steps": n_run, "steps_requested": args.steps, "warmup": n_warm,
+        "ms_per_step": round(mean_ms, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded weights and KV fill)",
+        "config": {"workload": f"{cfg.name}-shape INT4 g128 decode, batch 1, greedy, KV {T0 + 1}.."
+                               f"{T0 + n_warm + n_run}, seeded KV", "global_batch": 1, "seq_len": ctx,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(mean_ms, 3), "unit": "ms/token", "cores": cores,
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(total, 3), "unit": "ms/token", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(mean_ms, 3), "unit": "ms/token", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
     }
     print(json.dumps(line), flush=True)
 
@@ -288,7 +309,6 @@ def run_ours(args):
     t_setup = time.perf_counter()
     rec = sm.recipe(cfg, args.seed)
     model = DeviceModel(cfg, *rec)
-    lm_w = rec[4].get("w")
     stream = torch.cuda.Stream()
     eng = Engine(model, stream=stream.cuda_stream)
     if args.step == "persistent":
@@ -317,8 +337,12 @@ def run_ours(args):
         return
 
     # ---- KV filled with seeded values through a shuffled page table
-    from tests._gpu import fill_kv
+    from quantized_decode_gb300.kvfill import write_kv
     import synth
+
+    def fill_kv(e, c, seed, T, page_perm):
+        write_kv(e, c, lambda l: sm.kv_fill(c, seed, l, T), T, page_perm)
+
     n_pages = (ctx + 15) // 16
     fill_kv(eng, cfg, args.seed + 1, T0, page_perm=synth.permutation(args.seed, 3, n_pages))
 
@@ -482,8 +506,35 @@ def run_ours(args):
         eager_ms = s2.elapsed_time(e2) / n_eager
         eng.set_graph_mode(True)
 
-    # ---- per-kernel breakdown (events between serialised launches)
+    # ---- per-kernel share of the step inside graph replay: every launch records the time its
+    # last CTA finished; launch j's share is the time from launch j-1's finish to its own
+    # (the kernels overlap under programmatic dependent launch, so this partition of the step
+    # period is what each kernel adds to the token's latency)
     names = ["qkv", "attention", "o_proj", "gate_up", "down"]
+    kb = kernel_bytes(cfg, mean_T)
+    timeline = None
+    if args.timeline_steps > 1 and args.step == "chain":
+        if eng.seq_len() + args.timeline_steps > ctx:
+            eng.truncate(T0)
+        st = eng.timeline_steps(args.timeline_steps).astype(np.int64)
+        n_per = st.shape[1]
+        prev = np.concatenate([st[:-1, -1:], st[1:, :-1]], axis=1)      # steps 1.. only
+        dur_us = (st[1:] - prev) / 1e3                                    # [steps-1][n_per]
+        kinds = [names[j % 5] for j in range(5 * cfg.n_layers)] + ["lm_head"]
+        kinds += ["sampler"] * (n_per - len(kinds))
+        period_us = float(np.mean((st[1:, -1] - st[:-1, -1]) / 1e3))
+        tl_kern = {}
+        for k in dict.fromkeys(kinds):
+            cols = [j for j, kk in enumerate(kinds) if kk == k]
+            per_launch = dur_us[:, cols]
+            tot = float(np.mean(per_launch.sum(axis=1)))
+            ent = {"avg_us": round(float(np.mean(per_launch)), 2), "share": round(tot / period_us, 4)}
+            if k in kb:
+                ent["gbs"] = round(kb[k] / (float(np.mean(per_launch)) * 1e-6) / 1e9, 1)
+            tl_kern[k] = ent
+        timeline = {"steps": args.timeline_steps - 1, "period_us": round(period_us, 2), "kernels": tl_kern}
+
+    # ---- per-kernel breakdown (events between serialised launches; secondary)
     per = {n: [] for n in names + ["lm_head"]}
     for _ in range(args.profile_steps):
         if eng.seq_len() >= ctx:
@@ -493,17 +544,28 @@ def run_ours(args):
             for j, n in enumerate(names):
                 per[n].append(float(ms[5 * l + j]))
         per["lm_head"].append(float(ms[-1]))
-    kb = kernel_bytes(cfg, mean_T)
     if all(v == 0.0 for v in per["attention"]):  # the fused QKV + attention kernel fills the QKV entry
         per = {("qkv_attention" if n == "qkv" else n): v for n, v in per.items() if n != "attention"}
         kb["qkv_attention"] = kb["qkv"] + kb["attention"]
     totals = {n: sum(v) / args.profile_steps for n, v in per.items()}
-    dom = max(totals, key=totals.get)
-    avg_ms = statistics.mean(per[dom])
+    if timeline is not None:     # the roofline of the kernel with the largest in-graph share
+        dom = max((k for k in timeline["kernels"] if k in kb), key=lambda k: timeline["kernels"][k]["share"])
+        avg_ms = timeline["kernels"][dom]["avg_us"] * 1e-3
+        roof_src = "in-graph timeline (last-CTA finish times, graph replay with PDL)"
+    else:
+        dom = max(totals, key=totals.get)
+        avg_ms = statistics.mean(per[dom])
+        roof_src = "CUDA events between serialised launches"
     achieved = kb[dom] / (avg_ms * 1e-3) / 1e9
     breakdown = {n: {"avg_us": round(1e3 * statistics.mean(v), 2),
                      "share": round(totals[n] / sum(totals.values()), 4),
                      "gbs": round(kb[n] / (statistics.mean(v) * 1e-3) / 1e9, 1)} for n, v in per.items()}
+
+    # ---- the other configurations' own protocols (1.5B pp512 / tg128; Qwen3-8B INT8 inputs
+    # 128 .. 4096 with 128 greedy output tokens), on their own seeded models
+    sweep = None
+    if not args.no_sweep and ws == 1 and args.layers == 0 and args.vocab == 0:
+        sweep = config_sweep(args, stream, peak, peak_kind)
 
     # ---- end to end through the C ABI: host token in (pinned H2D), host token out (D2H)
     toks = sm.prompt(cfg, args.seed, args.e2e_steps, stream=1)
@@ -516,11 +578,11 @@ def run_ours(args):
         eng.decode_step(int(t))
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
 
-    # ---- CPU oracle baseline (rank 0, one GPU only)
+    # ---- CPU oracle baseline (rank 0, one GPU only): the whole model, a few greedy steps
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        total, sample, _ = oracle_sample(cfg, args.seed, ctx, 6, lm_w)
-        cpu = {"value": round(total, 2), "unit": "ms/token", "cores": os.cpu_count(),
+        mean_ms, sample, _ = oracle_decode(cfg, args.seed, T0, 1, 6, rec=rec)
+        cpu = {"value": round(mean_ms, 2), "unit": "ms/token", "cores": os.cpu_count(),
                "kind": "oracle", "sample": sample}
 
     tok_s = 1e3 / ms_per_token
@@ -542,10 +604,11 @@ def run_ours(args):
                           "bytes_per_step": int(step_bytes)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": NCU_TRAFFIC.get((cfg.name, dom)),
+                     "traffic": ncu_traffic(eng.lib.llm_build_id().decode(), cfg.name, dom),
                      "bytes_per_launch": int(kb[dom]), "avg_launch_us": round(avg_ms * 1e3, 2),
-                     "peak_kind": peak_kind},
-        "kernels": breakdown,
+                     "peak_kind": peak_kind, "duration_source": roof_src},
+        "kernels_in_graph": timeline,
+        "kernels_serialised": breakdown,
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
         "kv_sweep_ms_per_token": kv_sweep,
         "long_context_ms_per_token": long_ctx,
@@ -556,6 +619,7 @@ def run_ours(args):
         "act_int8_ms_per_token": act8_ms,
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
             None if other_ms is None else round(other_ms, 4),
+        "config_sweep": sweep,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps * ((4 if "qkv_attention" in per else 5) * cfg.n_layers + 1) + extra,
@@ -569,6 +633,71 @@ def run_ours(args):
     eng.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def config_sweep(args, stream, peak, peak_kind):
+    """TTFT and decode ms/token of the 1.5B (pp512 / tg128) and Qwen3-8B INT8 (inputs
+    128 .. 4096, 128 greedy output tokens each) configurations, graph replay, seeded inputs."""
+    import torch
+    from quantized_decode_gb300 import DeviceModel, Engine
+    from synth import model as sm
+
+    def decode_ms(eng, n):
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        eng.decode_enqueue(n)
+        e0.record(stream)
+        torch.cuda.synchronize()
+        eng.sync()
+        return s0.elapsed_time(e0) / n
+
+    def roof(cfg, T, ms):
+        gbs = algorithmic_bytes(cfg, T) / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "kv_len_mean": T}
+
+    out = {}
+    # Qwen2.5-1.5B shape: 512-token prompt, then 128 greedy tokens
+    cfg = sm.CONFIGS["qwen2.5-1.5b"].with_(max_context=1024)
+    eng = Engine(DeviceModel(cfg, *sm.recipe(cfg, args.seed)), stream=stream.cuda_stream)
+    try:
+        prompt = sm.prompt(cfg, args.seed, 512)
+        eng.prefill(prompt[:8])
+        ttft = []
+        for _ in range(3):
+            eng.reset()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            eng.prefill(prompt)
+            ttft.append((time.perf_counter() - t0) * 1e3)
+        eng.decode_enqueue(3)                       # warm-up
+        eng.sync()
+        eng.truncate(513)
+        ms = decode_ms(eng, 128)
+        out[cfg.name] = {"ttft_pp512_ms": round(float(np.median(ttft)), 2), "tg128_ms_per_token": round(ms, 4),
+                         "tokens_per_s": round(1e3 / ms, 1), "step_roofline": roof(cfg, 512 + 64.5, ms)}
+    finally:
+        eng.close()
+    # Qwen3-8B shape, INT8 per-row weights and LM head: inputs 128 .. 4096, 128 output tokens
+    cfg = sm.CONFIGS["qwen3-8b"]
+    eng = Engine(DeviceModel(cfg, *sm.recipe(cfg, args.seed)), stream=stream.cuda_stream)
+    try:
+        per_input, ttft = {}, {}
+        for n_in in (128, 512, 1024, 2048, 4096):
+            prompt = sm.prompt(cfg, args.seed, n_in)
+            eng.reset()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            eng.prefill(prompt)
+            ttft[str(n_in)] = round((time.perf_counter() - t0) * 1e3, 2)
+            per_input[str(n_in)] = round(decode_ms(eng, 128), 4)
+        out[cfg.name] = {"tpot_ms_by_input": per_input, "ttft_ms_by_input": ttft,
+                         "step_roofline_input_4096": roof(cfg, 4096 + 64.5, per_input["4096"]),
+                         "step_roofline_input_128": roof(cfg, 128 + 64.5, per_input["128"])}
+    finally:
+        eng.close()
+    return out
 
 
 def main():

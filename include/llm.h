@@ -187,6 +187,21 @@ int llm_truncate(llm_t *h, int32_t seq_len);
  * by one with a CUDA event between neighbours.  Blocks until done.          */
 int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels);
 
+/* In-graph timeline of the kernel chain ("How To Construct Your Personal LLM
+ * Runtime From Scratch", §6: where the token's time goes, kernel gaps
+ * included).  Captures n_steps consecutive greedy steps into one graph whose
+ * every launch records, on the device's global timer (ns), the time its last
+ * CTA finished, runs it once (advancing the sequence by n_steps, like
+ * llm_decode_enqueue) and writes stamps[i * n + j] = finish time of launch j
+ * of step i (HOST, capacity cap >= n_steps * (5 * n_layers + 2)); *n_per_step
+ * = n, the launches per step.  The launches overlap exactly as in normal
+ * replay (programmatic dependent launch included), so stamps[i][j] -
+ * stamps[i][j - 1] is launch j's share of the step period and the shares of a
+ * step sum to its period.  Blocks until done.  Errors: LLM_ERR_ARG (persistent
+ * step on, cap too small), LLM_ERR_STATE (no token to feed),
+ * LLM_ERR_CONTEXT_FULL, LLM_ERR_CUDA.                                       */
+int llm_timeline_steps(llm_t *h, int32_t n_steps, uint64_t *stamps, int32_t cap, int32_t *n_per_step);
+
 /* Free everything the handle owns (not the caller's weights).  NULL is a no-op. */
 void llm_destroy(llm_t *h);
 

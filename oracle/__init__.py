@@ -29,7 +29,7 @@ def build(force=False):
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".tmp{os.getpid()}"
         o32, o64 = tmp + ".f32.o", tmp + ".f64.o"
-        common = ["gcc", "-O2", "-fopenmp", "-fPIC", "-ffp-contract=off", "-c", _SRC]
+        common = ["gcc", "-O3", "-fopenmp", "-fPIC", "-ffp-contract=off", "-c", _SRC]
         subprocess.check_call(common + ["-o", o32])
         subprocess.check_call(common + ["-DOR_REAL=double", "-DOR_DOUBLE_BUILD", "-o", o64])
         subprocess.check_call(["gcc", "-shared", "-fopenmp", "-o", tmp, o32, o64, "-lm"])
@@ -89,6 +89,9 @@ def _load():
                 g("step").argtypes = [ctypes.POINTER(OrConfig), ctypes.POINTER(OrWeights), vp, vp,
                                       i64, i32, i64, vp, vp]
                 g("step").restype = ctypes.c_int
+                g("prefill").argtypes = [ctypes.POINTER(OrConfig), ctypes.POINTER(OrWeights), vp, vp,
+                                         i64, vp, i64, i64, vp]
+                g("prefill").restype = ctypes.c_int
                 for n in ("rmsnorm", "rope", "softmax", "silu_mul", "gemv_int4", "gemv_int8",
                           "gemv_bf16", "attention"):
                     g(n).restype = None
@@ -218,9 +221,10 @@ class OracleModel:
     """
 
     def __init__(self, cfg, seed, precision="f32", t_max=None, tensors=None, norms=None,
-                 embed=None):
-        """tensors(layer, proj) / norms(layer) / embed [V][h] override the seeded draws
-        (the model-level pins build structured special cases through them)."""
+                 embed=None, lm_head=None):
+        """tensors(layer, proj) / norms(layer) / embed [V][h] / lm_head (synth.model.lm_head's
+        dict) override the seeded draws (the model-level pins build structured special cases
+        through them; the full-depth tests pass arrays already drawn)."""
         from synth import model as sm
         self.cfg = cfg
         self.seed = seed
@@ -252,7 +256,7 @@ class OracleModel:
                     setattr(layers[l], k, self._hold(_c(v, np.uint16)))
         self.layers = layers
         self.embed = _c(sm.embedding(cfg, seed) if embed is None else embed, np.uint16)
-        lm = sm.lm_head(cfg, seed)
+        lm = sm.lm_head(cfg, seed) if lm_head is None else lm_head
         w = OrWeights()
         w.embed = self._hold(self.embed)
         w.final_norm = self._hold(_c(sm.final_norm(cfg, seed), np.uint16))
@@ -286,6 +290,20 @@ class OracleModel:
         if rc != 0:
             raise ValueError(f"oracle step rejected token={token} pos={pos}")
         return (logits, hidden) if want_hidden else logits
+
+    def prefill(self, tokens, pos0=0):
+        """The step applied to tokens at positions pos0.. (every linear layer evaluated for
+        all rows at once, each output the same sum as the step's); returns the logits of the
+        last token (fp32).  Equals len(tokens) calls of step() bit for bit."""
+        cfg = self.cfg
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        logits = np.empty(cfg.vocab, np.float32)
+        rc = self.oracle._f("prefill")(ctypes.byref(self.c), ctypes.byref(self.w), _p(self.k_cache),
+                                       _p(self.v_cache), self.t_max, _p(toks), toks.size, int(pos0),
+                                       _p(logits))
+        if rc != 0:
+            raise ValueError(f"oracle prefill rejected n={toks.size} pos0={pos0}")
+        return logits
 
     def set_kv(self, layer, k, v, start=0):
         """Write bf16 K/V rows [T][Hkv][d] at positions start.. of one layer."""

@@ -394,3 +394,148 @@ int OR_PREFIX(step)(const or_config *c, const or_weights *W, uint16_t *k_cache, 
     free(ga); free(up); free(u); free(tmp);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Prompt prefill: the step above applied to n tokens at positions      */
+/* pos0 .. pos0 + n - 1, with each linear layer evaluated for all rows  */
+/* at once.  Every output element is the same sum as in the GEMV (k     */
+/* ascending, the same dequantized weight, the same rounding), so the   */
+/* result equals n calls of the step bit for bit; only the loops are    */
+/* interchanged so that each weight row is unpacked once per block of   */
+/* rows instead of once per token.                                      */
+/* ------------------------------------------------------------------ */
+
+/* W[n][k] for one output row n, as the GEMVs form it. */
+static void dequant_row(const or_config *c, const void *w, const void *s, int64_t n, int64_t K, real_t *out) {
+    if (c->weight_format == 1) {
+        const uint32_t *words = (const uint32_t *)w;
+        const uint16_t *scales = (const uint16_t *)s;
+        for (int64_t k = 0; k < K; ++k)
+            out[k] = (real_t)int4_code(words, K, n, k) * (real_t)bf16_to_float(scales[n * (K / 128) + k / 128]);
+    } else {
+        const int8_t *codes = (const int8_t *)w;
+        for (int64_t k = 0; k < K; ++k) out[k] = (real_t)codes[n * K + k] * (real_t)((const float *)s)[n];
+    }
+}
+
+/* Y[m][n] = sum_k W[n][k] X[m][k] (+ b[n]) for the M rows of X [M][K]. */
+static void linear_rows(const or_config *c, const void *w, const void *s, const void *b, int64_t N,
+                        int64_t K, const real_t *X, int64_t M, real_t *Y) {
+    enum { NB = 16 };  /* output rows per block */
+    real_t *XT = malloc(sizeof(real_t) * (size_t)(K * M));   /* X transposed: [K][M] */
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) XT[k * M + m] = X[m * K + k];
+#pragma omp parallel
+    {
+        real_t *wb = malloc(sizeof(real_t) * (size_t)(NB * K));
+        real_t *acc = malloc(sizeof(real_t) * (size_t)(NB * M));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t n0 = 0; n0 < N; n0 += NB) {
+            const int64_t nb = N - n0 < NB ? N - n0 : NB;
+            for (int64_t j = 0; j < nb; ++j) dequant_row(c, w, s, n0 + j, K, wb + j * K);
+            for (int64_t i = 0; i < nb * M; ++i) acc[i] = 0;
+            for (int64_t k = 0; k < K; ++k) {
+                const real_t *xk = XT + k * M;
+                for (int64_t j = 0; j < nb; ++j) {
+                    const real_t wk = wb[j * K + k];
+                    real_t *a = acc + j * M;
+                    for (int64_t m = 0; m < M; ++m) a[m] += wk * xk[m];
+                }
+            }
+            for (int64_t j = 0; j < nb; ++j)
+                for (int64_t m = 0; m < M; ++m) {
+                    real_t v = acc[j * M + m];
+                    if (b) v += (real_t)bf16_to_float(((const uint16_t *)b)[n0 + j]);
+                    Y[m * N + n0 + j] = v;
+                }
+        }
+        free(wb);
+        free(acc);
+    }
+    free(XT);
+}
+
+/*
+ * Prefill: consume tokens[0..n-1] at positions pos0.., append their K/V, and
+ * write the logits of the last token (the distribution of the first generated
+ * token).  Returns 0, or -1 on bad arguments.
+ */
+int OR_PREFIX(prefill)(const or_config *c, const or_weights *W, uint16_t *k_cache, uint16_t *v_cache,
+                       int64_t t_max, const int32_t *tokens, int64_t n_tok, int64_t pos0, float *logits) {
+    const int64_t h = c->hidden, Hq = c->n_q_heads, Hkv = c->n_kv_heads, d = c->head_dim;
+    const int64_t F = c->mlp, V = c->vocab, M = n_tok;
+    if (M < 1 || pos0 < 0 || pos0 + M > t_max || Hq % Hkv != 0 || Hq * d != h) return -1;
+    for (int64_t m = 0; m < M; ++m)
+        if (tokens[m] < 0 || tokens[m] >= V) return -1;
+
+    real_t *x = calloc((size_t)(M * h), sizeof(real_t));
+    real_t *nrm = calloc((size_t)(M * h), sizeof(real_t));
+    real_t *q = calloc((size_t)(M * Hq * d), sizeof(real_t));
+    real_t *k = calloc((size_t)(M * Hkv * d), sizeof(real_t));
+    real_t *v = calloc((size_t)(M * Hkv * d), sizeof(real_t));
+    real_t *o = calloc((size_t)(M * h), sizeof(real_t));
+    real_t *t = calloc((size_t)(M * h), sizeof(real_t));
+    real_t *ga = calloc((size_t)(M * F), sizeof(real_t));
+    real_t *up = calloc((size_t)(M * F), sizeof(real_t));
+    real_t *u = calloc((size_t)(M * F), sizeof(real_t));
+    real_t *tmp = calloc((size_t)(V > d ? V : d), sizeof(real_t));
+
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t i = 0; i < h; ++i) x[m * h + i] = (real_t)bf16_to_float(W->embed[(int64_t)tokens[m] * h + i]);
+
+    for (int64_t l = 0; l < c->n_layers; ++l) {
+        const or_layer *L = &W->layers[l];
+        uint16_t *kc = k_cache + l * t_max * Hkv * d;
+        uint16_t *vc = v_cache + l * t_max * Hkv * d;
+
+        for (int64_t m = 0; m < M; ++m) OR_PREFIX(rmsnorm)(x + m * h, L->attn_norm, h, c->rms_eps, nrm + m * h);
+        linear_rows(c, L->wq, L->sq, c->qkv_bias ? L->bq : NULL, Hq * d, h, nrm, M, q);
+        linear_rows(c, L->wk, L->sk, c->qkv_bias ? L->bk : NULL, Hkv * d, h, nrm, M, k);
+        linear_rows(c, L->wv, L->sv, c->qkv_bias ? L->bv : NULL, Hkv * d, h, nrm, M, v);
+        for (int64_t m = 0; m < M; ++m) {
+            real_t *qm = q + m * Hq * d, *km = k + m * Hkv * d, *vm = v + m * Hkv * d;
+            const int64_t pos = pos0 + m;
+            if (c->qk_norm) {
+                for (int64_t hh = 0; hh < Hq; ++hh) {
+                    OR_PREFIX(rmsnorm)(qm + hh * d, L->q_norm, d, c->rms_eps, tmp);
+                    memcpy(qm + hh * d, tmp, sizeof(real_t) * (size_t)d);
+                }
+                for (int64_t hh = 0; hh < Hkv; ++hh) {
+                    OR_PREFIX(rmsnorm)(km + hh * d, L->k_norm, d, c->rms_eps, tmp);
+                    memcpy(km + hh * d, tmp, sizeof(real_t) * (size_t)d);
+                }
+            }
+            OR_PREFIX(rope)(qm, Hq, d, pos, (double)c->rope_base);
+            OR_PREFIX(rope)(km, Hkv, d, pos, (double)c->rope_base);
+            for (int64_t i = 0; i < Hkv * d; ++i) {
+                kc[pos * Hkv * d + i] = float_to_bf16((float)km[i]);
+                vc[pos * Hkv * d + i] = float_to_bf16((float)vm[i]);
+            }
+        }
+        /* row m attends to positions 0 .. pos0 + m (causal; its own K/V included) */
+        for (int64_t m = 0; m < M; ++m)
+            OR_PREFIX(attention)(q + m * Hq * d, kc, vc, pos0 + m + 1, Hq, Hkv, d, o + m * h);
+
+        linear_rows(c, L->wo, L->so, NULL, h, Hq * d, o, M, t);
+        for (int64_t i = 0; i < M * h; ++i) x[i] += t[i];
+
+        for (int64_t m = 0; m < M; ++m) OR_PREFIX(rmsnorm)(x + m * h, L->mlp_norm, h, c->rms_eps, nrm + m * h);
+        linear_rows(c, L->wg, L->sg, NULL, F, h, nrm, M, ga);
+        linear_rows(c, L->wu, L->su, NULL, F, h, nrm, M, up);
+        OR_PREFIX(silu_mul)(ga, up, M * F, u);
+        linear_rows(c, L->wd, L->sd, NULL, h, F, u, M, t);
+        for (int64_t i = 0; i < M * h; ++i) x[i] += t[i];
+    }
+
+    /* the last row only: its logits are the first generated token's */
+    OR_PREFIX(rmsnorm)(x + (M - 1) * h, W->final_norm, h, c->rms_eps, nrm);
+    if (W->lm_scale)
+        OR_PREFIX(gemv_int8)((const int8_t *)W->lm_head, W->lm_scale, V, h, nrm, tmp, NULL);
+    else
+        OR_PREFIX(gemv_bf16)((const uint16_t *)W->lm_head, V, h, nrm, tmp, NULL);
+    for (int64_t i = 0; i < V; ++i) logits[i] = (float)tmp[i];
+
+    free(x); free(nrm); free(q); free(k); free(v); free(o); free(t);
+    free(ga); free(up); free(u); free(tmp);
+    return 0;
+}

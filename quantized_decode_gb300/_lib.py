@@ -64,6 +64,7 @@ SIGNATURES = {
     "llm_reset": (i32, [vp]),
     "llm_truncate": (i32, [vp, i32]),
     "llm_profile_step": (i32, [vp, vp, i32, ctypes.POINTER(i32)]),
+    "llm_timeline_steps": (i32, [vp, i32, vp, i32, ctypes.POINTER(i32)]),
     "llm_destroy": (None, [vp]),
     "llm_status_str": (ctypes.c_char_p, [i32]),
     "llm_debug_kv": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),

@@ -90,4 +90,20 @@ QD_DEV float slot_sum(float v) {
     return v;
 }
 
+// ---- in-graph timeline (llm_timeline_steps) ---------------------------------
+// When a launch carries a timestamp slot, thread 0 of every CTA raises it to
+// the global timer at the CTA's exit, so the slot ends up holding the time the
+// launch's last CTA finished.  Declared first in a kernel so that every return
+// path records.  A null slot (the normal case) costs one predicated branch.
+struct TimelineMark {
+    unsigned long long *slot;
+    QD_DEV ~TimelineMark() {
+        if (slot && threadIdx.x == 0) {
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            atomicMax(slot, t);
+        }
+    }
+};
+
 }  // namespace qd

@@ -174,12 +174,21 @@ SampleArgs sampler_args(const llm_t *h) {
 // Format of the o_proj, gate/up and down GEMVs (INT4 models may run them on int8 activations).
 int gemv_fmt(const llm_t *h) { return h->act_int8 ? kFmtInt4A8 : h->fmt; }
 
-cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
+// With `tl`, launch i of the step carries timestamp slot tl[i] (TimelineMark);
+// *n_launch receives the number of kernels the step launched.
+cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long *tl = nullptr,
+                         int *n_launch = nullptr) {
     if (h->persistent && !ev) return launch_step(h->sl, h->sp, h->stream);
     const llm_config &c = h->cfg;
     const int d = c.head_dim, rq = c.n_q_heads * d, rkv = c.n_kv_heads * d;
     cudaError_t e;
     int k = 0;
+    int kl = 0;
+    auto slot = [&]() -> unsigned long long * {
+        unsigned long long *p = tl ? tl + kl : nullptr;
+        ++kl;
+        return p;
+    };
     float *st_attn = h->stats, *st_o = h->stats + 2 * kStatSlots;
     float *st_gu = h->stats + 4 * kStatSlots, *st_down = h->stats + 6 * kStatSlots;
     auto mark = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[k++], h->stream) : cudaSuccess; };
@@ -224,10 +233,13 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         LaunchCfg lc = h->lc;
         if (l == 0) lc.pdl = false;
         if (h->fused) {
+            qa.tl = slot();
             if ((e = mark()) != cudaSuccess || (e = launch_qkv_attn(lc, h->fmt, qa, aa)) != cudaSuccess ||
                 (e = mark()) != cudaSuccess)
                 return e;
         } else {
+            qa.tl = slot();
+            aa.tl = slot();
             if ((e = mark()) != cudaSuccess || (e = launch_qkv(lc, h->fmt, qa)) != cudaSuccess) return e;
             if ((e = mark()) != cudaSuccess || (e = launch_attention(h->lc, aa)) != cudaSuccess) return e;
         }
@@ -235,6 +247,7 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         GemvArgs o{};
         o.mode = 1; o.w = L.wo; o.s = L.so; o.N = c.hidden; o.K = rq; o.x = h->attn; o.y = h->x;
         o.stats_in = st_attn; o.stats_out = st_o; o.stats_gamma = (const uint16_t *)L.mlp_norm;
+        o.tl = slot();
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), o)) != cudaSuccess) return e;
 
         GemvArgs gu{};
@@ -242,12 +255,14 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
         gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
         gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
         gu.stats_in = st_o; gu.stats_out = st_gu;
+        gu.tl = slot();
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), gu)) != cudaSuccess) return e;
 
         GemvArgs dn{};
         dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
         dn.stats_in = st_gu; dn.stats_out = st_down;
         dn.stats_gamma = (const uint16_t *)(l + 1 < c.n_layers ? h->layers[l + 1].attn_norm : h->w.final_norm);
+        dn.tl = slot();
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), dn)) != cudaSuccess) return e;
     }
     LmHeadArgs la{};
@@ -263,8 +278,14 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr) {
     if (h->sampling) {  // the sampler takes the token and advances the state
         la.token_out = h->samp_scratch; la.st = nullptr; la.advance = 0;
     }
+    la.tl = slot();
     if ((e = mark()) != cudaSuccess || (e = launch_lm_head(h->lc, la, h->lm_grid)) != cudaSuccess) return e;
-    if (h->sampling && (e = launch_sample(h->lc, sampler_args(h))) != cudaSuccess) return e;
+    if (h->sampling) {
+        SampleArgs sa = sampler_args(h);
+        sa.tl = slot();
+        if ((e = launch_sample(h->lc, sa)) != cudaSuccess) return e;
+    }
+    if (n_launch) *n_launch = kl;
     return mark();
 }
 
@@ -892,6 +913,51 @@ int llm_truncate(llm_t *h, int32_t seq_len) {
     if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
     h->seq_len = seq_len;
     return LLM_OK;
+}
+
+int llm_timeline_steps(llm_t *h, int32_t n_steps, uint64_t *stamps, int32_t cap, int32_t *n_per_step) {
+    if (!h || n_steps < 1 || !stamps || !n_per_step) return LLM_ERR_ARG;
+    if (h->persistent || !h->have_token) return h->persistent ? LLM_ERR_ARG : LLM_ERR_STATE;
+    if ((int64_t)h->seq_len + n_steps > h->cfg.max_context) return LLM_ERR_CONTEXT_FULL;
+    const int per = 5 * h->cfg.n_layers + 2;  // upper bound on launches per step
+    if ((int64_t)cap < (int64_t)n_steps * per) return LLM_ERR_ARG;
+    unsigned long long *tl = nullptr;
+    const size_t bytes = (size_t)n_steps * per * sizeof(unsigned long long);
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess || cudaMalloc((void **)&tl, bytes) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t x = nullptr;
+    int rc = LLM_OK, n = 0;
+    if (cudaMemsetAsync(tl, 0, bytes, h->stream) != cudaSuccess ||
+        cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = LLM_ERR_CUDA;
+    } else {
+        cudaError_t ce = cudaSuccess;
+        for (int i = 0; i < n_steps && ce == cudaSuccess; ++i) ce = enqueue_step(h, nullptr, tl + (size_t)i * per, &n);
+        cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+        if (ce != cudaSuccess || ee != cudaSuccess || cudaGraphInstantiate(&x, g, 0) != cudaSuccess ||
+            cudaGraphLaunch(x, h->stream) != cudaSuccess)
+            rc = LLM_ERR_CUDA;
+    }
+    if (rc == LLM_OK) {
+        rc = fetch_token(h, nullptr);
+        if (rc == LLM_OK) {
+            h->seq_len += n_steps;
+            h->stepped = true;
+            std::vector<unsigned long long> host((size_t)n_steps * per);
+            if (cudaMemcpy(host.data(), tl, bytes, cudaMemcpyDeviceToHost) != cudaSuccess) {
+                rc = LLM_ERR_CUDA;
+            } else {
+                for (int i = 0; i < n_steps; ++i)
+                    for (int j = 0; j < n; ++j) stamps[(size_t)i * n + j] = host[(size_t)i * per + j];
+                *n_per_step = n;
+            }
+        }
+    }
+    if (x) cudaGraphExecDestroy(x);
+    if (g) cudaGraphDestroy(g);
+    cudaFree(tl);
+    return rc;
 }
 
 int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels) {

@@ -38,6 +38,7 @@ using namespace attn;
 
 template <int G, int D, int CS>
 __global__ void __launch_bounds__(kNT, 1) k_attn(const __grid_constant__ AttnArgs a) {
+    TimelineMark timeline_mark{a.tl};
     extern __shared__ __align__(128) uint16_t smem_raw[];
     uint16_t *smem = align_ring(smem_raw);
     const int g = blockIdx.y;

@@ -31,6 +31,7 @@ QD_HOST_DEV_INLINE size_t gain_region_bytes(int K) { return ((size_t)K * 2 + 15)
 
 template <int FMT, int RT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
+    TimelineMark timeline_mark{a.tl};
     constexpr int LPR = kLanesPerRow;
     extern __shared__ uint4 smem[];
     __shared__ float red[64];

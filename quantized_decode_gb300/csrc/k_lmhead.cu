@@ -29,6 +29,7 @@ constexpr int kLPR = kLanesPerRow;
 
 template <int FMT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
+    TimelineMark timeline_mark{a.tl};
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
     __shared__ float s_val[kMaxWarps];

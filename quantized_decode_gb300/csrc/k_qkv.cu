@@ -134,6 +134,7 @@ constexpr int kLPR = kLanesPerRow;
 
 template <int FMT, int DH>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
+    TimelineMark timeline_mark{a.tl};
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
     constexpr int S = 32 / kLPR;

@@ -67,6 +67,7 @@ QD_HOST_DEV_INLINE FusedLayout fused_layout(int G, int K) {
 
 template <int FMT, int G>
 __global__ void __launch_bounds__(kNT, 1) k_qkv_attn(QkvArgs qa, const __grid_constant__ AttnArgs at) {
+    TimelineMark timeline_mark{qa.tl};
     constexpr int D = kD128;
     constexpr int NT = G + 2;  // tiles per CTA
     extern __shared__ __align__(128) uint16_t smem_raw[];

@@ -108,6 +108,7 @@ QD_DEV void bitonic_desc(uint64_t *c, int n2) {
 }
 
 __global__ void __launch_bounds__(kSampleThreads, 1) k_sample(SampleArgs a) {
+    TimelineMark timeline_mark{a.tl};
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t *off = reinterpret_cast<uint32_t *>(smem);                // histogram, then bin offsets
     uint64_t *cand = reinterpret_cast<uint64_t *>(smem + 4096 * 4);

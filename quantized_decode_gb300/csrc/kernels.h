@@ -62,6 +62,7 @@ struct QkvArgs {
     uint16_t *kv_new;       // [2][Hkv][d] bf16 copy of the appended K and V rows
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
     int ks;                 // set by the launcher: warps per tile along K
+    unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
 };
 
 // y = W x with a fused epilogue: mode 0 stores (plus optional bias), mode 1
@@ -80,6 +81,7 @@ struct GemvArgs {
     float *stats_out;       // this kernel's (ss, mx) pairs for y, or null
     const uint16_t *stats_gamma;  // gain of y's consumer norm for mx (null: none)
     int ks;                 // set by the launcher: warps per tile along K
+    unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
 };
 
 // Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
@@ -101,6 +103,7 @@ struct LmHeadArgs {
     DevState *st;           // non-null: last_token/token written, pos advanced
     int advance;
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
+    unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
 };
 
 // Temperature / top-k / top-p sampling of the next token from the logits (in
@@ -119,6 +122,7 @@ struct SampleArgs {
     int *token_out;
     DevState *st;           // or null
     int advance;
+    unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
 };
 cudaError_t launch_sample(const LaunchCfg &lc, const SampleArgs &a);
 
@@ -142,6 +146,7 @@ struct AttnArgs {
                                        // [pages * Hkv * 16][d] for TMA page loads
     float *stats_out;                  // (ss, mx) pairs of out, or null: slot g per KV head, or with
                                        // one 16-CTA cluster per head slot 16 g + rank (others untouched)
+    unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
 };
 
 // Each launcher returns the launch's cudaError_t.

@@ -245,6 +245,16 @@ class Engine:
                 "llm_profile_step")
         return out[:n.value]
 
+    def timeline_steps(self, n_steps):
+        """n_steps greedy steps replayed from one graph whose launches record their last CTA's
+        finish time (llm_timeline_steps) -> uint64 ns array [n_steps][launches per step]."""
+        per = 5 * self.cfg.n_layers + 2
+        out = np.zeros(n_steps * per, dtype=np.uint64)
+        n = ctypes.c_int32()
+        L.check(self.lib.llm_timeline_steps(self.h, int(n_steps), _np_ptr(out), out.size, ctypes.byref(n)),
+                "llm_timeline_steps")
+        return out[:n_steps * n.value].reshape(n_steps, n.value)
+
     def set_pdl(self, on):
         L.check(self.lib.llm_set_pdl(self.h, int(bool(on))), "llm_set_pdl")
 

@@ -390,3 +390,27 @@ def test_composed_step_matches_closed_form_special_case():
     }
     for name, alt in slips.items():
         assert np.max(np.abs(alt - want)) > 1e-3 * np.max(np.abs(want)), name
+
+
+@pytest.mark.parametrize("cfg_name,precision", [("tiny", "f32"), ("tiny", "f64"), ("q3", "f32")])
+def test_prefill_equals_sequential_steps_bitwise(cfg_name, precision):
+    """The multi-row prefill is the step with its loops interchanged: same logits of the last
+    token and the same bf16 K/V rows, bit for bit, including a prompt that continues a cache."""
+    if cfg_name == "q3":
+        cfg = sm.CONFIGS["qwen3-8b"].with_(n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2,
+                                           head_dim=64, mlp=384, vocab=512, max_context=96)
+    else:
+        cfg = TINY.with_(max_context=96)
+    toks = sm.prompt(cfg, SEED, 53)
+    a = oracle.OracleModel(cfg, SEED, precision=precision)
+    b = oracle.OracleModel(cfg, SEED, precision=precision)
+    for pos, t in enumerate(toks[:37]):
+        ra = a.step(int(t), pos)
+    rb = b.prefill(toks[:37])
+    np.testing.assert_array_equal(ra, rb)
+    for pos in range(37, 53):
+        ra = a.step(int(toks[pos]), pos)
+    rb = b.prefill(toks[37:53], pos0=37)
+    np.testing.assert_array_equal(ra, rb)
+    np.testing.assert_array_equal(a.k_cache, b.k_cache)
+    np.testing.assert_array_equal(a.v_cache, b.v_cache)
