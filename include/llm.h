@@ -181,7 +181,8 @@ int llm_truncate(llm_t *h, int32_t seq_len);
  * one step, advancing the sequence like a greedy step, and writes the
  * duration in ms of region i to kernel_ms[i] (HOST, capacity cap).  Order:
  * for each layer {qkv, attention, o_proj, gate_up, down}, then lm_head;
- * *n_kernels = 5 * n_layers + 1.  With the persistent step kernel a region is
+ * *n_kernels = 5 * n_layers + 1 (with a fused kernel, the first of its
+ * regions holds it and the others read 0).  With the persistent step kernel a region is
  * the time between phase starts as seen by CTA 0 (device clock, waits for
  * other CTAs included); with the kernel chain it is one kernel, launched one
  * by one with a CUDA event between neighbours.  Blocks until done.          */
@@ -234,6 +235,48 @@ int llm_set_graph_mode(llm_t *h, int32_t use_graph);
  * first.  Errors: LLM_ERR_ARG (null handle, or 1 for a model outside the
  * persistent kernel's shapes), LLM_ERR_CUDA.                                */
 int llm_set_persistent(llm_t *h, int32_t on);
+
+/* 1: the MLP block of a layer -- RMSNorm, gate/up, SiLU * mul
+ * and down ("从头开始手写一个Qwen的Naive CUDA Kernel推理引擎(一)", "SwiGLU") --
+ * runs as one kernel in which every CTA multiplies its slice of the hidden
+ * units by the matching columns of W_down (repacked by llm_create into an
+ * engine-owned copy, mlp * hidden / 2 bytes per layer for INT4) and adds the
+ * partial sums into a residual buffer with integer reductions in L2 (64-bit
+ * fixed point, 2^-32 units: exact, so results do not depend on the order of
+ * the CTAs; |values| must stay below 2^31).  Shapes: hidden % 256 == 0,
+ * hidden <= 4096, mlp % 128 == 0.  On by default where it fits and hidden <=
+ * 2048 (measured faster there); 0: the block is two GEMV kernels (gate/up,
+ * then down).
+ * With int8 activations (llm_set_act_int8) the two kernels always run.
+ * Re-captures the graph.  Errors: LLM_ERR_ARG (null handle, or 1 for shapes
+ * the kernel does not take), LLM_ERR_CUDA.                                  */
+int llm_set_fused_mlp(llm_t *h, int32_t on);
+
+/* Launch kinds of a decode step, in launch order (the step as last captured):
+ * writes kinds[i] for each launch (HOST, capacity cap) and *n = launches; 0
+ * for the persistent kernel.  Kinds: */
+#define LLM_KIND_QKV 0
+#define LLM_KIND_ATTENTION 1
+#define LLM_KIND_O_PROJ 2
+#define LLM_KIND_GATE_UP 3
+#define LLM_KIND_DOWN 4
+#define LLM_KIND_LM_HEAD 5
+#define LLM_KIND_SAMPLER 6
+#define LLM_KIND_QKV_ATTENTION 7
+#define LLM_KIND_MLP 8
+int llm_step_kinds(llm_t *h, int32_t *kinds, int32_t cap, int32_t *n);
+
+/* L2 staging of weights ahead of the kernel that reads them: kernels of the
+ * chain issue bulk L2 prefetches (cp.async.bulk.prefetch.L2, by the TMA
+ * engine) of a later kernel's weights at their start, so that HBM streams
+ * while the latency-bound kernels of the attention block run.  Flags (OR):
+ * 1 = QKV prefetches the layer's gate/up weights, 2 = gate/up prefetches the
+ * layer's down weights, 4 = down prefetches the next layer's QKV and o_proj
+ * codes, 8 = QKV prefetches the layer's o_proj weights (without 1),
+ * 16 = o_proj prefetches the layer's gate/up weights; 0 = off.  Results are
+ * unchanged (prefetches only move data into L2).  Re-captures the graph.
+ * Errors: LLM_ERR_ARG (null handle, flags outside 0..31), LLM_ERR_CUDA.      */
+int llm_set_l2_prefetch(llm_t *h, int32_t flags);
 
 /* Test hook of the persistent kernel's failure path: its phase-counter waits
  * expect `extra_arrivals` (0 or 1) arrivals more than any step delivers and

@@ -20,6 +20,8 @@ LLM_ERR_STATE = -7
 LLM_ERR_FORMAT = -8
 LLM_ERR_IO = -9
 
+KIND_NAMES = ("qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "sampler", "qkv_attention", "mlp")
+
 LLM_FMT_INT4_G128 = 1
 LLM_FMT_INT8_ROW = 2
 LLM_LAYOUT_INT4_VALUESHUFFLE = 1
@@ -76,6 +78,9 @@ SIGNATURES = {
     "llm_op_sample": (i32, [vp, i32, f32, i32, f32, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
     "llm_set_persistent": (i32, [vp, i32]),
     "llm_debug_step_wait": (i32, [vp, i32, i64]),
+    "llm_set_l2_prefetch": (i32, [vp, i32]),
+    "llm_set_fused_mlp": (i32, [vp, i32]),
+    "llm_step_kinds": (i32, [vp, vp, i32, ctypes.POINTER(i32)]),
     "llm_set_act_int8": (i32, [vp, i32]),
     "llm_op_gemv_int4_a8": (i32, [vp, vp, i32, i32, vp, vp, vp]),
     "llm_set_prefill_batched": (i32, [vp, i32]),

@@ -90,6 +90,35 @@ QD_DEV float slot_sum(float v) {
     return v;
 }
 
+// ---- the MLP's pending contribution to the residual ------------------------------
+// k_mlp's CTAs add their partial sums of the down projection into one vector D.
+// D is kept in 64-bit fixed point (units of 2^-32, |value| < 2^31) so that those
+// additions are exact integer adds: the result does not depend on the order in
+// which the CTAs arrive.  A partial sum is rounded once to the grid (2^-33 at
+// most) and the total once back to fp32 where it is read.
+QD_DEV long long delta_to_fixed(float v) { return __float2ll_rn(v * 4294967296.f); }
+QD_DEV float delta_to_float(long long q) { return __ll2float_rn(q) * 2.3283064365386963e-10f; }
+
+// ---- L2 prefetch for a later kernel -------------------------------------------
+// CTA c of nc prefetches its share of each range into L2 with bulk copies of
+// the TMA engine (no registers, no shared memory, nothing to wait for); the
+// lines are there when a later kernel of the step streams the same bytes.
+QD_DEV void l2_prefetch_share(const L2Range (&r)[kMaxL2Ranges], int c, int nc) {
+    if (threadIdx.x != 0) return;
+    constexpr unsigned long long kChunk = 2048;  // 16-byte units per instruction (32 KB)
+#pragma unroll 1
+    for (int i = 0; i < kMaxL2Ranges; ++i) {
+        const char *base = static_cast<const char *>(r[i].p);
+        if (!base) continue;
+        const unsigned long long n = r[i].bytes / 16, per = (n + nc - 1) / nc;
+        const unsigned long long lo = per * (unsigned long long)c, hi = lo + per < n ? lo + per : n;
+        for (unsigned long long u = lo; u < hi; u += kChunk) {
+            const unsigned sz = (unsigned)((hi - u < kChunk ? hi - u : kChunk) * 16);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + u * 16), "r"(sz) : "memory");
+        }
+    }
+}
+
 // ---- in-graph timeline (llm_timeline_steps) ---------------------------------
 // When a launch carries a timestamp slot, thread 0 of every CTA raises it to
 // the global timer at the CTA's exit, so the slot ends up holding the time the

@@ -26,6 +26,16 @@
 
 using namespace qd;
 
+// llm_set_l2_prefetch flags (see llm.h)
+enum : int {
+    kL2pfQkvMlp = 1,    // QKV prefetches the layer's gate and up weights
+    kL2pfGuDown = 2,    // gate/up prefetches the layer's down weights
+    kL2pfDownNext = 4,  // down prefetches the next layer's QKV and o_proj codes
+    kL2pfQkvO = 8,      // QKV prefetches the layer's o_proj weights (when bit 1 is clear)
+    kL2pfOMlp = 16,     // o_proj prefetches the layer's gate and up weights
+    kL2pfAll = 31
+};
+
 struct llm_t {
     llm_config cfg;
     void *weight_buffer = nullptr;  // llm_create_from_file: the weights' device copy, owned
@@ -56,6 +66,15 @@ struct llm_t {
     int samp_k = 1;
     uint64_t samp_seed = 0;
     int *samp_scratch = nullptr;  // the LM head's unused argmax while sampling
+    int l2pf = 0;               // llm_set_l2_prefetch flags
+    // the MLP block as one kernel (k_mlp.cu): repacked down weights per layer and the
+    // buffer D of the block's pending contribution to the residual
+    bool mlp_ok = false;        // the model's shapes fit it
+    bool mlp_fused = false;     // llm_set_fused_mlp (on by default where it fits)
+    char *mlp_buf = nullptr;    // repacked down codes (+ INT4 scales) of every layer
+    size_t mlp_w_bytes = 0, mlp_s_bytes = 0;  // per layer
+    long long *mlp_d = nullptr;  // fixed point, 2^-32 units
+    std::vector<int32_t> kinds; // kind of every launch of the captured step (llm_step_kinds)
     bool fused_ok = false;      // the model fits the fused QKV + attention kernel
     bool fused = false;         // llm_set_fused_attention
 
@@ -111,7 +130,7 @@ void free_all(llm_t *h) {
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
                     h->d_layers, h->d_maps, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
-                    h->pf_qh, h->pf_ql, h->pf_tok, h->samp_scratch};
+                    h->pf_qh, h->pf_ql, h->pf_tok, h->samp_scratch, h->mlp_buf, h->mlp_d};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -169,6 +188,12 @@ SampleArgs sampler_args(const llm_t *h) {
     return sa;
 }
 
+// Bytes of one packed weight matrix [N][K] and of its scales.
+size_t code_bytes(const llm_t *h, int N, int K) { return h->fmt == kFmtInt4 ? (size_t)N * K / 2 : (size_t)N * K; }
+size_t scale_bytes(const llm_t *h, int N, int K) {
+    return h->fmt == kFmtInt4 ? (size_t)N * (K / kGroup) * 2 : (size_t)N * 4;
+}
+
 // Enqueue one whole decode step (5L + 1 kernels).  With `ev`, event k is
 // recorded before kernel k and event 5L+1 after the last one.
 // Format of the o_proj, gate/up and down GEMVs (INT4 models may run them on int8 activations).
@@ -184,11 +209,15 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
     cudaError_t e;
     int k = 0;
     int kl = 0;
-    auto slot = [&]() -> unsigned long long * {
+    h->kinds.clear();
+    // timestamp slot of the next launch, which is of kind `kind` (LLM_KIND_*)
+    auto slot = [&](int kind) -> unsigned long long * {
         unsigned long long *p = tl ? tl + kl : nullptr;
         ++kl;
+        h->kinds.push_back(kind);
         return p;
     };
+    const bool fmlp = h->mlp_fused && !h->act_int8;  // int8 activations keep the separate GEMVs
     float *st_attn = h->stats, *st_o = h->stats + 2 * kStatSlots;
     float *st_gu = h->stats + 4 * kStatSlots, *st_down = h->stats + 6 * kStatSlots;
     auto mark = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[k++], h->stream) : cudaSuccess; };
@@ -205,6 +234,7 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         qa.rows_q = rq; qa.rows_kv = rkv; qa.K = c.hidden; qa.d = d;
         qa.Hq = c.n_q_heads; qa.Hkv = c.n_kv_heads;
         qa.x = h->x;
+        qa.x2 = fmlp && l > 0 ? h->mlp_d : nullptr;  // the previous layer's MLP output is still in D
         qa.embed = l == 0 ? (const uint16_t *)h->w.embed : nullptr;
         qa.x_init = h->x;
         qa.gamma = (const uint16_t *)L.attn_norm;
@@ -218,7 +248,19 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         qa.v_pool = h->v_pool + (size_t)l * h->layer_kv_elems;
         qa.page_table = h->page_table; qa.n_pages = h->n_pages;
         qa.rope_cs = h->rope_cs; qa.st = h->st;
-        qa.kv_new = h->kv_new; qa.stats_in = l == 0 ? nullptr : st_down;
+        qa.kv_new = h->kv_new; qa.stats_in = l == 0 || fmlp ? nullptr : st_down;
+        {
+            int n = 0;
+            if (h->l2pf & kL2pfQkvMlp) {  // gate and up of this layer, during the attention block
+                qa.pf[n++] = {L.wg, code_bytes(h, c.mlp, c.hidden)};
+                qa.pf[n++] = {L.wu, code_bytes(h, c.mlp, c.hidden)};
+                qa.pf[n++] = {L.sg, scale_bytes(h, c.mlp, c.hidden)};
+                qa.pf[n++] = {L.su, scale_bytes(h, c.mlp, c.hidden)};
+            } else if (h->l2pf & kL2pfQkvO) {
+                qa.pf[n++] = {L.wo, code_bytes(h, c.hidden, rq)};
+                qa.pf[n++] = {L.so, scale_bytes(h, c.hidden, rq)};
+            }
+        }
 
         AttnArgs aa{};
         aa.q = h->q; aa.k_pool = qa.k_pool; aa.v_pool = qa.v_pool;
@@ -233,36 +275,75 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         LaunchCfg lc = h->lc;
         if (l == 0) lc.pdl = false;
         if (h->fused) {
-            qa.tl = slot();
+            qa.tl = slot(LLM_KIND_QKV_ATTENTION);
             if ((e = mark()) != cudaSuccess || (e = launch_qkv_attn(lc, h->fmt, qa, aa)) != cudaSuccess ||
                 (e = mark()) != cudaSuccess)
                 return e;
         } else {
-            qa.tl = slot();
-            aa.tl = slot();
+            qa.tl = slot(LLM_KIND_QKV);
+            aa.tl = slot(LLM_KIND_ATTENTION);
             if ((e = mark()) != cudaSuccess || (e = launch_qkv(lc, h->fmt, qa)) != cudaSuccess) return e;
             if ((e = mark()) != cudaSuccess || (e = launch_attention(h->lc, aa)) != cudaSuccess) return e;
         }
 
         GemvArgs o{};
         o.mode = 1; o.w = L.wo; o.s = L.so; o.N = c.hidden; o.K = rq; o.x = h->attn; o.y = h->x;
+        if (h->l2pf & kL2pfOMlp) {  // gate and up of this layer
+            o.pf[0] = {L.wg, code_bytes(h, c.mlp, c.hidden)};
+            o.pf[1] = {L.wu, code_bytes(h, c.mlp, c.hidden)};
+            o.pf[2] = {L.sg, scale_bytes(h, c.mlp, c.hidden)};
+            o.pf[3] = {L.su, scale_bytes(h, c.mlp, c.hidden)};
+        }
         o.stats_in = st_attn; o.stats_out = st_o; o.stats_gamma = (const uint16_t *)L.mlp_norm;
-        o.tl = slot();
+        if (fmlp) {  // fold the previous layer's D into x (a new step starts from the embedding: zero only)
+            o.fold = h->mlp_d;
+            o.fold_add = l > 0;
+        }
+        o.tl = slot(LLM_KIND_O_PROJ);
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), o)) != cudaSuccess) return e;
+
+        if (fmlp) {
+            MlpArgs m{};
+            m.wg = L.wg; m.sg = L.sg; m.wu = L.wu; m.su = L.su;
+            m.wd = reinterpret_cast<const uint4 *>(h->mlp_buf + (size_t)l * (h->mlp_w_bytes + h->mlp_s_bytes));
+            m.sd = h->fmt == kFmtInt4 ? (const void *)(h->mlp_buf + (size_t)l * (h->mlp_w_bytes + h->mlp_s_bytes) +
+                                                       h->mlp_w_bytes)
+                                      : L.sd;
+            m.F = c.mlp; m.h = c.hidden; m.x = h->x; m.gamma = (const uint16_t *)L.mlp_norm; m.eps = c.rms_eps;
+            m.stats_in = st_o; m.D = h->mlp_d; m.prefetch_down = 1;
+            m.err = &h->st->err; m.wait_ns = 1000000000ull;
+            m.tl = slot(LLM_KIND_MLP);
+            // the gate/up and down regions of llm_profile_step: the kernel, then nothing
+            if ((e = mark()) != cudaSuccess || (e = launch_mlp(h->lc, h->fmt, m)) != cudaSuccess ||
+                (e = mark()) != cudaSuccess)
+                return e;
+            continue;
+        }
 
         GemvArgs gu{};
         gu.mode = 2; gu.w = L.wg; gu.s = L.sg; gu.w2 = L.wu; gu.s2 = L.su;
         gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
         gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
         gu.stats_in = st_o; gu.stats_out = st_gu;
-        gu.tl = slot();
+        gu.tl = slot(LLM_KIND_GATE_UP);
+        if (h->l2pf & kL2pfGuDown) {  // down of this layer
+            gu.pf[0] = {L.wd, code_bytes(h, c.hidden, c.mlp)};
+            gu.pf[1] = {L.sd, scale_bytes(h, c.hidden, c.mlp)};
+        }
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), gu)) != cudaSuccess) return e;
 
         GemvArgs dn{};
         dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
         dn.stats_in = st_gu; dn.stats_out = st_down;
         dn.stats_gamma = (const uint16_t *)(l + 1 < c.n_layers ? h->layers[l + 1].attn_norm : h->w.final_norm);
-        dn.tl = slot();
+        dn.tl = slot(LLM_KIND_DOWN);
+        if ((h->l2pf & kL2pfDownNext) && l + 1 < c.n_layers) {  // the next layer's QKV and o_proj codes
+            const llm_layer_weights &Nx = h->layers[l + 1];
+            dn.pf[0] = {Nx.wq, code_bytes(h, rq, c.hidden)};
+            dn.pf[1] = {Nx.wk, code_bytes(h, rkv, c.hidden)};
+            dn.pf[2] = {Nx.wv, code_bytes(h, rkv, c.hidden)};
+            dn.pf[3] = {Nx.wo, code_bytes(h, c.hidden, rq)};
+        }
         if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), dn)) != cudaSuccess) return e;
     }
     LmHeadArgs la{};
@@ -274,15 +355,16 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
     la.eps = c.rms_eps; la.N = c.vocab; la.K = c.hidden; la.x = h->x; la.logits = h->logits;
     la.part_val = h->lm_part_val; la.part_idx = h->lm_part_idx; la.counter = h->lm_counter;
     la.token_out = &h->st->last_token; la.st = h->st; la.advance = 1;
-    la.stats_in = st_down;
+    la.stats_in = fmlp ? nullptr : st_down;
+    la.x2 = fmlp ? h->mlp_d : nullptr;
     if (h->sampling) {  // the sampler takes the token and advances the state
         la.token_out = h->samp_scratch; la.st = nullptr; la.advance = 0;
     }
-    la.tl = slot();
+    la.tl = slot(LLM_KIND_LM_HEAD);
     if ((e = mark()) != cudaSuccess || (e = launch_lm_head(h->lc, la, h->lm_grid)) != cudaSuccess) return e;
     if (h->sampling) {
         SampleArgs sa = sampler_args(h);
-        sa.tl = slot();
+        sa.tl = slot(LLM_KIND_SAMPLER);
         if ((e = launch_sample(h->lc, sa)) != cudaSuccess) return e;
     }
     if (n_launch) *n_launch = kl;
@@ -712,6 +794,29 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
          cudaStreamSynchronize(h->stream) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
 
+    // The MLP block as one kernel: W_down of every layer repacked unit-major (the
+    // layout k_mlp streams), D zeroed.
+    h->mlp_ok = mlp_shape_ok(h->fmt, c.hidden, c.mlp);
+    if (h->mlp_ok) {
+        h->mlp_w_bytes = (h->fmt == kFmtInt4 ? (size_t)c.hidden * c.mlp / 2 : (size_t)c.hidden * c.mlp);
+        h->mlp_s_bytes = h->fmt == kFmtInt4 ? (((size_t)c.hidden * (c.mlp / kGroup) * 2 + 255) & ~(size_t)255) : 0;
+        const size_t per = h->mlp_w_bytes + h->mlp_s_bytes;
+        ok = cudaMalloc((void **)&h->mlp_buf, per * c.n_layers) == cudaSuccess &&
+             dalloc(&h->mlp_d, c.hidden) == cudaSuccess &&
+             cudaMemsetAsync(h->mlp_d, 0, (size_t)c.hidden * sizeof(long long), h->stream) == cudaSuccess;
+        for (int l = 0; ok && l < c.n_layers; ++l) {
+            char *dst = h->mlp_buf + (size_t)l * per;
+            ok = mlp_repack_down(h->fmt, h->layers[l].wd, h->layers[l].sd, c.hidden, c.mlp, dst,
+                                 h->fmt == kFmtInt4 ? dst + h->mlp_w_bytes : nullptr, h->stream) == cudaSuccess;
+        }
+        if (!ok || cudaStreamSynchronize(h->stream) != cudaSuccess) return fail(LLM_ERR_CUDA);
+        // Default where it measured faster than the two GEMV kernels: narrow models,
+        // whose down GEMV has few row tiles per SM (1.5B shape: 1.018 vs 1.069 ms per
+        // token); on the 7B shape the in-CTA down phase is slower than the separate
+        // kernel (2.07 vs 1.75 ms per token).
+        h->mlp_fused = c.hidden <= 2048;
+    }
+
     if (plan_step(h, n_sm) != LLM_OK) return fail(LLM_ERR_CUDA);
     h->pf_ok = prefill_shapes_ok(c);
 
@@ -747,6 +852,34 @@ int llm_set_persistent(llm_t *h, int32_t on) {
     if (on && (!h->step_ok || h->sampling || h->act_int8)) return LLM_ERR_ARG;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->persistent = on != 0;
+    return capture(h);
+}
+
+int llm_set_fused_mlp(llm_t *h, int32_t on) {
+    if (!h || (on && !h->mlp_ok)) return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->mlp_fused = on != 0;
+    // D may hold a finished step's last-layer output: the next step's first o_proj
+    // zeroes it either way, and the unfused chain never reads it.
+    return capture(h);
+}
+
+int llm_step_kinds(llm_t *h, int32_t *kinds, int32_t cap, int32_t *n) {
+    if (!h || !kinds || !n) return LLM_ERR_ARG;
+    *n = (int32_t)h->kinds.size();
+    if (h->persistent) {
+        *n = 0;
+        return LLM_OK;
+    }
+    if (cap < *n) return LLM_ERR_ARG;
+    for (int i = 0; i < *n; ++i) kinds[i] = h->kinds[i];
+    return LLM_OK;
+}
+
+int llm_set_l2_prefetch(llm_t *h, int32_t flags) {
+    if (!h || flags < 0 || flags > kL2pfAll) return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->l2pf = flags;
     return capture(h);
 }
 

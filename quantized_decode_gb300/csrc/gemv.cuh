@@ -430,16 +430,26 @@ QD_DEV float stage_activations(const float *__restrict__ src, const uint16_t *__
                                const uint16_t *__restrict__ gamma, float eps, int K,
                                const float *__restrict__ stats_in, half2 *half_out, float *f32_out,
                                float *red, int blk_bytes = 0, const uint16_t *gamma_s = nullptr,
-                               uint8_t *i8_out = nullptr, float *sx_out = nullptr, int *qs_out = nullptr) {
+                               uint8_t *i8_out = nullptr, float *sx_out = nullptr, int *qs_out = nullptr,
+                               const long long *__restrict__ src2 = nullptr) {
     constexpr int kBatch = kStageBatch;
     const int tid = threadIdx.x, NT = blockDim.x;
+    // src2 (optional): the MLP's pending contribution D in fixed point (delta_to_float),
+    // added to src element-wise; the statistics must then be computed here (no stats_in)
     auto load4 = [&](int i) -> float4 {
         if (src_bf16) {
             const uint2 b = *reinterpret_cast<const uint2 *>(src_bf16 + i);
             return make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
                                __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
         }
-        return __ldcg(reinterpret_cast<const float4 *>(src + i));
+        float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+        if (src2) {
+            const longlong2 d0 = __ldcg(reinterpret_cast<const longlong2 *>(src2 + i));
+            const longlong2 d1 = __ldcg(reinterpret_cast<const longlong2 *>(src2 + i + 2));
+            v = make_float4(v.x + delta_to_float(d0.x), v.y + delta_to_float(d0.y), v.z + delta_to_float(d1.x),
+                            v.w + delta_to_float(d1.y));
+        }
+        return v;
     };
     bool gs_ok = false;  // the gain's shared-memory copy is visible (after the first barrier)
     auto gain4 = [&](int i) -> float4 {

@@ -32,6 +32,7 @@ QD_HOST_DEV_INLINE size_t gain_region_bytes(int K) { return ((size_t)K * 2 + 15)
 template <int FMT, int RT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     TimelineMark timeline_mark{a.tl};
+    l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);
     constexpr int LPR = kLanesPerRow;
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
@@ -75,7 +76,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
             for (int i = 0; i < RT; ++i) {
                 const int r = t_first * S * RT + slot * RT + i;
                 pre_mul[i] = FMT == kFmtInt8 ? __ldg((const float *)a.s + r) : 1.f;
-                pre_add[i] = a.mode == 1 ? __ldcg(a.y + r) : (a.bias ? bf16_bits_to_float(__ldg(a.bias + r)) : 0.f);
+                // mode 1 with fold: the MLP's pending contribution (written three kernels
+                // earlier, complete by the same argument) joins the residual here
+                pre_add[i] = a.mode == 1
+                                 ? __ldcg(a.y + r) + (a.fold && a.fold_add ? delta_to_float(__ldcg(a.fold + r)) : 0.f)
+                                 : (a.bias ? bf16_bits_to_float(__ldg(a.bias + r)) : 0.f);
                 pre_g[i] = a.stats_gamma ? bf16_bits_to_float(__ldg(a.stats_gamma + r)) : 1.f;
             }
         }
@@ -132,11 +137,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                 if (first) {
                     v += pre_add[i];
                 } else if (a.mode == 1) {
-                    v += __ldcg(a.y + r);
+                    v += __ldcg(a.y + r) + (a.fold && a.fold_add ? delta_to_float(__ldcg(a.fold + r)) : 0.f);
                 } else if (a.bias) {
                     v += bf16_bits_to_float(__ldg(a.bias + r));
                 }
                 a.y[r] = v;
+                if (a.mode == 1 && a.fold) a.fold[r] = 0;
                 st_ss += v * v;
                 const float gn = first ? pre_g[i] : (a.stats_gamma ? bf16_bits_to_float(__ldg(a.stats_gamma + r)) : 1.f);
                 st_mx = fmaxf(st_mx, fabsf(v * gn));

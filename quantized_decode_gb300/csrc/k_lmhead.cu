@@ -56,10 +56,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_lm_head(LmHeadArgs a) {
         pdl_wait();
         if constexpr (FMT == kFmtBf16)
             post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, nullptr,
-                                     reinterpret_cast<float *>(smem), red, act_blk_bytes<FMT>(), gs);
+                                     reinterpret_cast<float *>(smem), red, act_blk_bytes<FMT>(), gs, nullptr,
+                                     nullptr, nullptr, a.x2);
         else
             post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in,
-                                     reinterpret_cast<half2 *>(smem), nullptr, red, act_blk_bytes<FMT>(), gs);
+                                     reinterpret_cast<half2 *>(smem), nullptr, red, act_blk_bytes<FMT>(), gs,
+                                     nullptr, nullptr, nullptr, a.x2);
         pdl_launch();
     };
     auto rows = [&](int t, int i) -> RowRef {

@@ -135,6 +135,7 @@ constexpr int kLPR = kLanesPerRow;
 template <int FMT, int DH>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
     TimelineMark timeline_mark{a.tl};
+    l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);
     extern __shared__ uint4 smem[];
     __shared__ float red[64];
     constexpr int S = 32 / kLPR;
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_qkv(QkvArgs a) {
         if (erow && blockIdx.x == 0)
             for (int i = threadIdx.x; i < a.K; i += blockDim.x) a.x_init[i] = bf16_bits_to_float(erow[i]);
         post = stage_activations(a.x, erow, a.gamma, a.eps, a.K, erow ? nullptr : a.stats_in, xs, nullptr, red,
-                                 act_blk_bytes<FMT>(), gs);
+                                 act_blk_bytes<FMT>(), gs, nullptr, nullptr, nullptr, erow ? nullptr : a.x2);
         phys = __ldg(a.page_table + pos / kPageTokens);  // used by the k/v tiles' epilogues
         pdl_launch();
     };

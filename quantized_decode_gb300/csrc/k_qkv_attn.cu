@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kNT, 1) k_qkv_attn(QkvArgs qa, const __grid_co
             if (erow && g == 0 && rank == 0)
                 for (int i = threadIdx.x; i < qa.K; i += blockDim.x) qa.x_init[i] = bf16_bits_to_float(erow[i]);
             post = stage_activations(qa.x, erow, qa.gamma, qa.eps, qa.K, erow ? nullptr : qa.stats_in, xs, nullptr,
-                                     red, act_blk_bytes<FMT>());  // its barriers publish the constants
+                                     red, act_blk_bytes<FMT>(), nullptr, nullptr, nullptr, nullptr,
+                                     erow ? nullptr : qa.x2);  // its barriers publish the constants
             pdl_launch();
         };
         auto epi = [&](int t, float(&out)[kQRT]) {

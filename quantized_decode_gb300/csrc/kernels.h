@@ -13,6 +13,15 @@ constexpr int kMaxGqa = 8;        // query heads per KV head supported by the at
 constexpr int kStatSlots = 256;   // (sum of squares, max) pairs per producer: one per CTA, >= grid
 constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in to (sm_103a)
 
+// Byte ranges a kernel prefetches into L2 for a later kernel of the step
+// (llm_set_l2_prefetch): every CTA issues bulk prefetches of its share of each
+// range at its start, before its dependency wait.  Null ranges are skipped.
+struct L2Range {
+    const void *p;              // 16-byte aligned
+    unsigned long long bytes;
+};
+constexpr int kMaxL2Ranges = 4;
+
 // Device-side error word (sticky until the host clears it).
 enum : int { kErrNone = 0, kErrBadPage = 1, kErrBadToken = 2, kErrBadPos = 3, kErrTimeout = 16 };
 
@@ -46,6 +55,7 @@ struct QkvArgs {
     int K;                  // hidden
     int d, Hq, Hkv;
     const float *x;         // residual [K] (ignored when embed != null)
+    const long long *x2;    // the MLP's pending contribution (fixed point) added to x, or null; then no stats_in
     const uint16_t *embed;  // layer 0: bf16 embedding table [V][K]
     float *x_init;          // layer 0: residual initialised from the embedding row
     const uint16_t *gamma;  // attn_norm
@@ -63,6 +73,7 @@ struct QkvArgs {
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
     int ks;                 // set by the launcher: warps per tile along K
     unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
+    L2Range pf[kMaxL2Ranges];  // L2 prefetch for a later kernel, or all null
 };
 
 // y = W x with a fused epilogue: mode 0 stores (plus optional bias), mode 1
@@ -77,12 +88,39 @@ struct GemvArgs {
     const uint16_t *gamma;  // RMSNorm gain applied to x first, or null
     float eps;
     float *y;               // output [N]
+    long long *fold;        // mode 1: y += fold (fixed point) and fold = 0 (fold_add), or fold = 0 only; or null
+    int fold_add;
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
     float *stats_out;       // this kernel's (ss, mx) pairs for y, or null
     const uint16_t *stats_gamma;  // gain of y's consumer norm for mx (null: none)
     int ks;                 // set by the launcher: warps per tile along K
     unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
+    L2Range pf[kMaxL2Ranges];  // L2 prefetch for a later kernel, or all null
 };
+
+// The MLP block as one kernel (k_mlp.cu): RMSNorm -> gate/up -> SiLU * mul ->
+// down, each CTA on a slice of the hidden units, D += its down partial sums.
+struct MlpArgs {
+    const void *wg, *sg, *wu, *su;  // gate / up codes and scales [F][h] (INT4: bf16 [F][h/128]; INT8: fp32 [F])
+    const uint4 *wd;                // down codes, unit-major [F / C][h][16 B] (mlp_repack_down)
+    const void *sd;                 // INT4: bf16 [F / 128][h] (repacked); INT8: fp32 [h] row scales
+    int F, h;
+    const float *x;                 // residual after the attention block [h]
+    const uint16_t *gamma;          // mlp_norm
+    float eps;
+    const float *stats_in;          // o_proj's (ss, mx) pairs for x
+    long long *D;                   // [h]: zero on entry; receives the block's output (fixed point, 2^-32)
+    int prefetch_down;              // prefetch the CTA's down block into L2 at its start
+    int *err;                       // device error word (kErrTimeout when a bounded copy wait runs out)
+    unsigned long long wait_ns;     // bound on every wait of the kernel
+    unsigned long long *tl;         // timeline slot of this launch, or null (TimelineMark)
+};
+bool mlp_shape_ok(int fmt, int h, int F);
+cudaError_t launch_mlp(const LaunchCfg &lc, int fmt, const MlpArgs &a);
+// Repack W_down [h][F] into the unit-major layout k_mlp reads (w_out: h * F / 2
+// bytes INT4, h * F INT8; s_out: INT4 scales [F/128][h], unused for INT8).
+cudaError_t mlp_repack_down(int fmt, const void *w, const void *s, int h, int F, void *w_out, void *s_out,
+                            cudaStream_t stream);
 
 // Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
 // ties).  The last CTA reduces the per-CTA maxima, writes the token into the
@@ -95,6 +133,7 @@ struct LmHeadArgs {
     float eps;
     int N, K;
     const float *x;
+    const long long *x2;    // the MLP's pending contribution (fixed point) added to x, or null; then no stats_in
     float *logits;          // [N]
     float *part_val;        // [grid] per-CTA maxima
     int *part_idx;          // [grid]

@@ -280,6 +280,21 @@ class Engine:
         L.check(self.lib.llm_debug_step_wait(self.h, int(extra_arrivals), int(counter_wait_ns)),
                 "llm_debug_step_wait")
 
+    def set_fused_mlp(self, on):
+        """True (default where it fits): the MLP block as one kernel; False: gate/up + down."""
+        L.check(self.lib.llm_set_fused_mlp(self.h, int(bool(on))), "llm_set_fused_mlp")
+
+    def step_kinds(self):
+        """Names of the launches of one decode step, in order (empty for the persistent kernel)."""
+        out = np.zeros(5 * self.cfg.n_layers + 2, dtype=np.int32)
+        n = ctypes.c_int32()
+        L.check(self.lib.llm_step_kinds(self.h, _np_ptr(out), out.size, ctypes.byref(n)), "llm_step_kinds")
+        return [L.KIND_NAMES[k] for k in out[:n.value]]
+
+    def set_l2_prefetch(self, flags):
+        """Bulk L2 prefetch of later kernels' weights (llm_set_l2_prefetch flags; 0 = off)."""
+        L.check(self.lib.llm_set_l2_prefetch(self.h, int(flags)), "llm_set_l2_prefetch")
+
     def set_prefill_batched(self, on):
         """True: prompts run as one batch on the tensor cores; False: token by token."""
         L.check(self.lib.llm_set_prefill_batched(self.h, int(bool(on))), "llm_set_prefill_batched")
