@@ -149,6 +149,7 @@ def kernel_bytes(cfg, T):
         "o_proj": w(h, rq) + rq * 4 + h * 4 * 2,
         "gate_up": 2 * w(F, h) + h * 4 + F * 4,
         "down": w(h, F) + F * 4 + h * 4 * 2,
+        "mlp": 3 * w(F, h) + h * 4 + h * 8,
         "lm_head": V * h * 2 + h * 4 + V * 4,
     }
 
@@ -506,6 +507,7 @@ def run_ours(args):
         eager_ms = s2.elapsed_time(e2) / n_eager
         eng.set_graph_mode(True)
 
+    step_kinds = eng.step_kinds() or ["step"]   # the launches of one step (persistent: one kernel)
     # ---- per-kernel share of the step inside graph replay: every launch records the time its
     # last CTA finished; launch j's share is the time from launch j-1's finish to its own
     # (the kernels overlap under programmatic dependent launch, so this partition of the step
@@ -517,11 +519,9 @@ def run_ours(args):
         if eng.seq_len() + args.timeline_steps > ctx:
             eng.truncate(T0)
         st = eng.timeline_steps(args.timeline_steps).astype(np.int64)
-        n_per = st.shape[1]
         prev = np.concatenate([st[:-1, -1:], st[1:, :-1]], axis=1)      # steps 1.. only
-        dur_us = (st[1:] - prev) / 1e3                                    # [steps-1][n_per]
-        kinds = [names[j % 5] for j in range(5 * cfg.n_layers)] + ["lm_head"]
-        kinds += ["sampler"] * (n_per - len(kinds))
+        dur_us = (st[1:] - prev) / 1e3                                    # [steps-1][launches]
+        kinds = eng.step_kinds()
         period_us = float(np.mean((st[1:, -1] - st[:-1, -1]) / 1e3))
         tl_kern = {}
         for k in dict.fromkeys(kinds):
@@ -622,7 +622,7 @@ def run_ours(args):
         "config_sweep": sweep,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 8},
-        "gpu_launches": args.steps * ((4 if "qkv_attention" in per else 5) * cfg.n_layers + 1) + extra,
+        "gpu_launches": args.steps * len(step_kinds) + extra,
         "clocks": clocks,
         "setup_s": round(setup_s, 1),
     }
