@@ -203,6 +203,61 @@ int llm_profile_step(llm_t *h, float *kernel_ms, int32_t cap, int32_t *n_kernels
  * LLM_ERR_CONTEXT_FULL, LLM_ERR_CUDA.                                       */
 int llm_timeline_steps(llm_t *h, int32_t n_steps, uint64_t *stamps, int32_t cap, int32_t *n_per_step);
 
+/* ---- Multi-sequence decode ------------------------------------------------
+ * Up to 8 sequences decoding together on one GPU ("Systems Foundations for
+ * LLMs", PagedAttention and its block manager): one K/V pool of 16-token pages
+ * shared by all sequences, a page table per sequence filled on demand from a
+ * free list (page 0 is reserved), and steps in which every weight is read once
+ * for all the sequences taking part (their linear layers run as skinny GEMMs on
+ * the tensor cores, mma.sync with bf16 operands and fp32 accumulation; attention
+ * runs per sequence through its own page table).  Each step is one CUDA graph
+ * replay.  Weights: as for llm_create (borrowed, same layouts). */
+typedef struct llm_batch_t llm_batch_t; /* opaque; owned by the library */
+
+/* max_seqs: sequence slots (1..8); n_pages: pages in the shared pool including
+ * the reserved one (0 = max_seqs * ceil(max_context / 16) + 1).  Validation and
+ * errors as for llm_create. */
+int llm_batch_create(const llm_config *cfg, const llm_weights *weights, int32_t max_seqs, int32_t n_pages,
+                     void *cuda_stream, llm_batch_t **out);
+void llm_batch_destroy(llm_batch_t *h);
+
+/* A new, empty sequence in a free slot -> *seq.  LLM_ERR_STATE: all slots hold one. */
+int llm_batch_add(llm_batch_t *h, int32_t *seq);
+
+/* End a sequence: its pages go back to the free list, its slot becomes free.  */
+int llm_batch_release(llm_batch_t *h, int32_t seq);
+
+/* One decode step for the n sequences seqs[0..n-1] (distinct, live): each
+ * consumes inputs[i] when inputs is non-NULL and inputs[i] >= 0, else the token
+ * its previous step emitted; each writes its K/V at its current length (a new
+ * page is taken from the free list whenever the length crosses a page
+ * boundary) and emits its greedy argmax into out_tokens[i] (HOST; may be NULL).
+ * The other slots keep their caches and lengths.  Blocks until done.  Errors:
+ * LLM_ERR_ARG, LLM_ERR_STATE (a sequence with nothing to feed),
+ * LLM_ERR_CONTEXT_FULL (a sequence at max_context, or the free list cannot
+ * cover the step: checked before any work), LLM_ERR_CUDA, LLM_ERR_DEVICE /
+ * LLM_ERR_TIMEOUT (a device-side check of a sequence in the step).          */
+int llm_batch_step(llm_batch_t *h, const int32_t *seqs, const int32_t *inputs, int32_t n, int32_t *out_tokens);
+
+/* Feed a prompt to one sequence, token by token through the batched step (the
+ * other sequences do not move); *first_token = the greedy token after it.    */
+int llm_batch_prefill(llm_batch_t *h, int32_t seq, const int32_t *tokens, int32_t n, int32_t *first_token);
+
+/* fp32 logits [vocab] of the sequence's last step (HOST).                    */
+int llm_batch_logits(llm_batch_t *h, int32_t seq, float *host_out, int32_t vocab);
+
+/* A sequence's length, its physical pages in logical order (HOST, capacity
+ * cap; may be NULL), their count, and the pages left on the free list.       */
+int llm_batch_seq_info(llm_batch_t *h, int32_t seq, int32_t *len, int32_t *pages, int32_t cap,
+                       int32_t *n_pages, int32_t *free_pages);
+
+/* Test hook: the order in which the free list hands out pages 1..n_pages-1
+ * (order[0] first); only while no slot holds a sequence.                     */
+int llm_batch_set_page_order(llm_batch_t *h, const int32_t *order, int32_t n);
+
+/* Test hook: the K and V pools ([L][n_pages][Hkv][16][d] bf16, device).       */
+int llm_batch_debug_kv(llm_batch_t *h, void **k_pool, void **v_pool, int32_t *n_pages);
+
 /* Free everything the handle owns (not the caller's weights).  NULL is a no-op. */
 void llm_destroy(llm_t *h);
 

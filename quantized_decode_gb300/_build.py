@@ -16,7 +16,7 @@ LIB = os.path.join(HERE, "libllm.so")
 
 CU_SOURCES = ["engine.cu", "ops.cu", "ops_noalloc.cu", "k_qkv.cu", "k_gemv.cu", "k_lmhead.cu",
               "k_attn.cu", "k_qkv_attn.cu", "k_sample.cu", "k_step.cu", "k_tcgemm.cu", "k_prefill.cu",
-              "model_file.cu", "k_mlp.cu"]
+              "model_file.cu", "k_mlp.cu", "k_batch.cu", "batch.cu"]
 CPP_SOURCES = ["pack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -54,6 +54,18 @@ class llm_weights(ctypes.Structure):
 # name -> (restype, argtypes)
 SIGNATURES = {
     "llm_build_id": (ctypes.c_char_p, []),
+    "llm_batch_create": (i32, [ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights), i32, i32, vp,
+                               ctypes.POINTER(vp)]),
+    "llm_batch_destroy": (None, [vp]),
+    "llm_batch_add": (i32, [vp, ctypes.POINTER(i32)]),
+    "llm_batch_release": (i32, [vp, i32]),
+    "llm_batch_step": (i32, [vp, vp, vp, i32, vp]),
+    "llm_batch_prefill": (i32, [vp, i32, vp, i32, ctypes.POINTER(i32)]),
+    "llm_batch_logits": (i32, [vp, i32, vp, i32]),
+    "llm_batch_seq_info": (i32, [vp, i32, ctypes.POINTER(i32), vp, i32, ctypes.POINTER(i32),
+                                 ctypes.POINTER(i32)]),
+    "llm_batch_set_page_order": (i32, [vp, vp, i32]),
+    "llm_batch_debug_kv": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i32)]),
     "llm_create": (i32, [ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights), vp,
                          ctypes.POINTER(vp)]),
     "llm_prefill": (i32, [vp, ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]),

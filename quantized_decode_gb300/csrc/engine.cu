@@ -178,6 +178,14 @@ int validate(const llm_config *c, const llm_weights *w) {
     return LLM_OK;
 }
 
+}  // namespace
+
+// The single-sequence engine's checks of a configuration and its weights, shared
+// with the multi-sequence engine (batch.cu).
+int engine_validate(const llm_config *c, const llm_weights *w) { return validate(c, w); }
+
+namespace {
+
 // The sampler after the LM head: the token into the state (the next step's
 // input), the position advanced; the draw's counter is the sampled position.
 SampleArgs sampler_args(const llm_t *h) {

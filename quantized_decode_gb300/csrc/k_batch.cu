@@ -1,0 +1,465 @@
+// k_batch.cu - kernels of the multi-sequence decode step (batch.cu): up to 8
+// sequences decode together, each through its own page table, and every weight
+// is read once per step for all of them ("Systems Foundations for LLMs",
+// PagedAttention: per-sequence block tables over one shared pool of 16-token
+// blocks).
+//
+// The linear layers become skinny GEMMs, Y[b][n] = sum_k W[n][k] X[b][k] for
+// b < B <= 8, run on the tensor cores with mma.sync m16n8k16 (bf16 operands,
+// fp32 accumulation): A = 16 weight rows, their INT4 / INT8 codes turned into
+// exact bf16 integers in registers (bf16 weights as they are); B = the 8
+// sequences' activations, staged in shared memory as bf16 after the RMSNorm;
+// the column n of the mma is the sequence.  INT4 group scales are applied to
+// the fp32 partial sum of each 128-code group, INT8 row scales at the end.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "launch_util.cuh"
+
+namespace qd {
+
+namespace {
+
+constexpr int kNW = 8;        // warps per CTA
+constexpr int kKC = 4096;     // K values staged in shared memory at a time
+constexpr int kTPW = 8;       // row tiles per warp at most (fp32 accumulators)
+constexpr int kUB = 4;        // 64-byte row blocks loaded ahead per warp
+
+QD_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                     uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16x2 (x - 136, y - 136): exact for the integers 128 .. 143 the INT4 unpack forms.
+QD_DEV uint32_t bf2_minus136(uint32_t v) {
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    const __nv_bfloat162 k = __floats2bfloat162_rn(136.f, 136.f);
+    a = __hsub2(a, k);
+    return *reinterpret_cast<uint32_t *>(&a);
+}
+
+// INT4 ValueShuffle word -> the bf16 pairs (c0,c1), (c2,c3), (c4,c5), (c6,c7).
+// A pair's nibbles sit at bits (4j, 16 + 4j); nibble ^ 8 = c + 8 under the bf16
+// exponent of 128 (0x4300) is 136 + c, and subtracting 136 is exact.
+QD_DEV void int4_word_bf16(uint32_t w, uint32_t (&p)[4]) {
+    p[0] = bf2_minus136(lop3_and_xor(w, 0x000F000Fu, 0x43084308u));
+    p[1] = bf2_minus136(lop3_and_xor(w >> 4, 0x000F000Fu, 0x43084308u));
+    p[2] = bf2_minus136(lop3_and_xor(w >> 8, 0x000F000Fu, 0x43084308u));
+    p[3] = bf2_minus136(lop3_and_xor(w >> 12, 0x000F000Fu, 0x43084308u));
+}
+
+// INT8 word (natural byte order) -> bf16 pairs (b0,b1), (b2,b3): each byte goes
+// under the fp32 exponent of 2^23 ((b ^ 0x80) = c + 128), 2^23 + 128 is
+// subtracted exactly and the pair is rounded to bf16 (exact: |c| <= 127).
+QD_DEV void int8_word_bf16(uint32_t w, uint32_t (&p)[2]) {
+    const uint32_t t = w ^ 0x80808080u;
+    const float k = 8388736.f;  // 2^23 + 128
+    const float c0 = __uint_as_float(prmt(t, 0x4B000000u, 0x7650u)) - k;
+    const float c1 = __uint_as_float(prmt(t, 0x4B000000u, 0x7651u)) - k;
+    const float c2 = __uint_as_float(prmt(t, 0x4B000000u, 0x7652u)) - k;
+    const float c3 = __uint_as_float(prmt(t, 0x4B000000u, 0x7653u)) - k;
+    __nv_bfloat162 a = __floats2bfloat162_rn(c0, c1), b = __floats2bfloat162_rn(c2, c3);
+    p[0] = *reinterpret_cast<uint32_t *>(&a);
+    p[1] = *reinterpret_cast<uint32_t *>(&b);
+}
+
+// Codes of one 16-byte lane chunk per 64-byte row block.
+template <int FMT>
+constexpr int codes_per_lane() { return FMT == kFmtInt4 ? 32 : (FMT == kFmtInt8 ? 16 : 8); }
+
+// Staged activations: k-chunk c (8 values) of sequence b at 16-byte entry
+// c * 8 + (b ^ ((c >> 2) & 7)) (the swizzle spreads a warp's reads over the banks).
+QD_DEV int act_entry(int c, int b) { return c * 8 + (b ^ ((c >> 2) & 7)); }
+
+template <int FMT>
+__global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
+    constexpr int CPL = codes_per_lane<FMT>();
+    constexpr int NM = CPL / 4;            // mma per 64-byte block
+    constexpr int BLK = 4 * CPL;           // K values per 64-byte row block
+    extern __shared__ uint4 sx[];          // [kKC / 8][8] 16-byte entries of bf16
+    __shared__ float s_inv[8];
+    __shared__ float red[kNW][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int tiles = a.mode == 2 ? a.N / 8 : a.N / 16;
+    const int gw = blockIdx.x * kNW + warp, nwarps = gridDim.x * kNW;
+    const int B = a.B;
+
+    // ---- per-sequence RMSNorm factors (over the whole K)
+    if (threadIdx.x < 8) s_inv[threadIdx.x] = 1.f;
+    if (a.gamma) {
+        float ss[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+        for (int k = threadIdx.x * 4; k < a.K; k += blockDim.x * 4) {
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+                if (b < B) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.ldx + k));
+                    ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const float v = warp_sum(ss[b]);
+            if (lane == 0) red[warp][b] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < 8) {
+            float v = 0.f;
+            for (int w = 0; w < kNW; ++w) v += red[w][threadIdx.x];
+            s_inv[threadIdx.x] = rsqrtf(v / (float)a.K + a.eps);
+        }
+    }
+    __syncthreads();
+
+    float acc[kTPW][4];
+#pragma unroll
+    for (int i = 0; i < kTPW; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    // the row pair (g, g + 8) of tile ti: pointers into the weight rows and scales
+    auto row_ptrs = [&](int ti, const uint4 *&r0, const uint4 *&r1, const void *&s0, const void *&s1, int &rr0,
+                        int &rr1) {
+        const size_t rb = FMT == kFmtInt4 ? (size_t)a.K / 2 : (FMT == kFmtInt8 ? (size_t)a.K : (size_t)a.K * 2);
+        if (a.mode == 2) {  // 8 gate rows then the same 8 up rows
+            const int f = ti * 8 + g;
+            r0 = reinterpret_cast<const uint4 *>((const char *)a.w[0] + (size_t)f * rb);
+            r1 = reinterpret_cast<const uint4 *>((const char *)a.w2 + (size_t)f * rb);
+            s0 = a.s[0];
+            s1 = a.s2;
+            rr0 = rr1 = f;
+            return;
+        }
+        int r = ti * 16 + g, seg = 0;
+        while (seg + 1 < a.n_seg && r >= a.seg_rows[seg]) r -= a.seg_rows[seg++];
+        r0 = reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)r * rb);
+        r1 = reinterpret_cast<const uint4 *>((const char *)a.w[seg] + (size_t)(r + 8) * rb);
+        s0 = s1 = a.s[seg];
+        rr0 = r;
+        rr1 = r + 8;
+    };
+
+#pragma unroll 1
+    for (int k0 = 0; k0 < a.K; k0 += kKC) {
+        const int kc = a.K - k0 < kKC ? a.K - k0 : kKC;
+        // ---- stage X[b][k0 .. k0 + kc) as bf16 (normalized), zeros for b >= B
+        __syncthreads();
+        for (int e = threadIdx.x; e < (kc / 8) * 8; e += blockDim.x) {
+            const int c = e >> 3, b = e & 7;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (b < B) {
+                const float *src = a.x + (size_t)b * a.ldx + k0 + c * 8;
+                const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src));
+                const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                const float inv = s_inv[b];
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float x0 = f[2 * i] * inv, x1 = f[2 * i + 1] * inv;
+                    if (a.gamma) {
+                        const uint32_t gg = __ldg(reinterpret_cast<const uint32_t *>(a.gamma + k0 + c * 8) + i);
+                        x0 *= __uint_as_float(gg << 16);
+                        x1 *= __uint_as_float(gg & 0xFFFF0000u);
+                    }
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                    o[i] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            sx[act_entry(c, b)] = out;
+        }
+        __syncthreads();
+
+        const int nblk = kc / BLK;
+#pragma unroll
+        for (int i = 0; i < kTPW; ++i) {
+            const int ti = gw + i * nwarps;
+            if (ti >= tiles) break;
+            const uint4 *r0, *r1;
+            const void *s0, *s1;
+            int rr0, rr1;
+            row_ptrs(ti, r0, r1, s0, s1, rr0, rr1);
+            const int ub0 = k0 / BLK;  // first block of the chunk in the row (64-byte units)
+#pragma unroll 1
+            for (int bk = 0; bk < nblk; bk += kUB) {
+                uint4 w0[kUB], w1[kUB];
+                float sc0[kUB], sc1[kUB];
+#pragma unroll
+                for (int u = 0; u < kUB; ++u) {
+                    if (bk + u < nblk) {
+                        const int blk = ub0 + bk + u;
+                        w0[u] = ld_stream(r0 + (size_t)blk * 4 + t);
+                        w1[u] = ld_stream(r1 + (size_t)blk * 4 + t);
+                        if constexpr (FMT == kFmtInt4) {
+                            const int G = a.K / kGroup;
+                            sc0[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s0) + (size_t)rr0 * G + blk));
+                            sc1[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s1) + (size_t)rr1 * G + blk));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUB; ++u) {
+                    if (bk + u >= nblk) break;
+                    const int cbase = ((bk + u) * BLK + t * CPL) / 8;  // staged k-chunk of this lane's codes
+                    // A pairs of the two rows
+                    uint32_t pa[2][CPL / 2];
+                    const uint4 wv[2] = {w0[u], w1[u]};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+                        if constexpr (FMT == kFmtInt4) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t p[4];
+                                int4_word_bf16(ww[j], p);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) pa[r][4 * j + q] = p[q];
+                            }
+                        } else if constexpr (FMT == kFmtInt8) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t p[2];
+                                int8_word_bf16(ww[j], p);
+                                pa[r][2 * j] = p[0];
+                                pa[r][2 * j + 1] = p[1];
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) pa[r][j] = ww[j];
+                        }
+                    }
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < NM; ++m) {
+                        // B: this lane's sequence g, k values t*CPL + 4m .. + 3 of the block
+                        const uint4 xb = sx[act_entry(cbase + (4 * m) / 8, g)];
+                        const uint32_t b0 = (m & 1) ? xb.z : xb.x, b1 = (m & 1) ? xb.w : xb.y;
+                        mma_bf16(d, pa[0][2 * m], pa[1][2 * m], pa[0][2 * m + 1], pa[1][2 * m + 1], b0, b1);
+                    }
+                    if constexpr (FMT == kFmtInt4) {
+                        acc[i][0] = fmaf(d[0], sc0[u], acc[i][0]);
+                        acc[i][1] = fmaf(d[1], sc0[u], acc[i][1]);
+                        acc[i][2] = fmaf(d[2], sc1[u], acc[i][2]);
+                        acc[i][3] = fmaf(d[3], sc1[u], acc[i][3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][j] += d[j];
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- epilogue: lane (g, t) holds rows (g, g + 8) x sequences (2t, 2t + 1)
+#pragma unroll
+    for (int i = 0; i < kTPW; ++i) {
+        const int ti = gw + i * nwarps;
+        if (ti >= tiles) break;
+        const uint4 *r0, *r1;
+        const void *s0, *s1;
+        int rr0, rr1;
+        row_ptrs(ti, r0, r1, s0, s1, rr0, rr1);
+        float v[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
+        if constexpr (FMT == kFmtInt8) {
+            const float sa = __ldg(static_cast<const float *>(s0) + rr0), sb = __ldg(static_cast<const float *>(s1) + rr1);
+            v[0] *= sa;
+            v[1] *= sa;
+            v[2] *= sb;
+            v[3] *= sb;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int b = 2 * t + c;
+            if (b >= B) continue;
+            if (a.mode == 2) {
+                const float gt = v[c], up = v[2 + c];
+                a.y[(size_t)b * a.ldy + ti * 8 + g] = gt / (1.f + __expf(-gt)) * up;
+                continue;
+            }
+            const int row0 = ti * 16 + g, row1 = row0 + 8;
+            float y0 = v[c], y1 = v[2 + c];
+            if (a.mode == 0) {
+                int seg = 0, r = row0;
+                while (seg + 1 < a.n_seg && r >= a.seg_rows[seg]) r -= a.seg_rows[seg++];
+                if (a.bias[seg]) {
+                    y0 += bf16_bits_to_float(__ldg(a.bias[seg] + r));
+                    y1 += bf16_bits_to_float(__ldg(a.bias[seg] + r + 8));
+                }
+            }
+            float *yb = a.y + (size_t)b * a.ldy;
+            if (a.mode == 1) {
+                yb[row0] += y0;
+                yb[row1] += y1;
+            } else {
+                yb[row0] = y0;
+                yb[row1] = y1;
+            }
+        }
+    }
+}
+
+// ---- small per-sequence kernels ---------------------------------------------
+
+// x[b] = embedding row of token st[b].token.
+__global__ void k_bembed(const uint16_t *embed, const DevState *st, int B, int h, float *x) {
+    const int b = blockIdx.x;
+    const int tok = st[b].token;
+    for (int i = threadIdx.x; i < h; i += blockDim.x)
+        x[(size_t)b * h + i] = bf16_bits_to_float(embed[(size_t)tok * h + i]);
+}
+
+// Per (sequence, head) of the raw QKV rows: optional RMSNorm of q and k heads,
+// RoPE at the sequence's position, q into q_out, K and V rounded to bf16 and
+// written at slot pos % 16 of the sequence's page table[pos / 16].
+__global__ void k_bqkv_post(BQkvPostArgs a) {
+    const int b = blockIdx.y, head = blockIdx.x, lane = threadIdx.x;
+    if (a.part && !a.part[b]) return;
+    const int H = a.Hq + 2 * a.Hkv, d = a.d, half = d / 2;
+    const int pos = a.st[b].pos;
+    const float *raw = a.raw + (size_t)b * H * d + (size_t)head * d;
+    const bool is_q = head < a.Hq, is_k = !is_q && head < a.Hq + a.Hkv;
+    float v[4];  // lane holds elements lane + 32 m (d <= 128)
+    const int M = d / 32;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) v[m] = m < M ? raw[lane + 32 * m] : 0.f;
+    if ((is_q || is_k) && a.q_gain) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss += v[m] * v[m];
+        ss = warp_sum(ss);
+        const float inv = rsqrtf(ss / (float)d + a.eps);
+        const uint16_t *gm = is_q ? a.q_gain : a.k_gain;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if (m < M) v[m] = bf16_bits_to_float(gm[lane + 32 * m]) * (v[m] * inv);
+    }
+    if (is_q || is_k) {  // rotate pairs (i, i + d/2) by pos * theta_i
+        const float2 *cs = a.rope_cs + (size_t)pos * half;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            if (m >= M / 2) break;
+            const float2 c = cs[lane + 32 * m];
+            const float x0 = v[m], x1 = v[m + M / 2];
+            v[m] = x0 * c.x - x1 * c.y;
+            v[m + M / 2] = x1 * c.x + x0 * c.y;
+        }
+    }
+    if (is_q) {
+        float *q = a.q_out + (size_t)b * a.Hq * d + (size_t)head * d;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if (m < M) q[lane + 32 * m] = v[m];
+        return;
+    }
+    const int gk = is_k ? head - a.Hq : head - a.Hq - a.Hkv;
+    int phys = a.page_table[(size_t)b * a.max_pages + pos / kPageTokens];
+    if (phys < 0 || phys >= a.n_pages) {
+        if (lane == 0) atomicCAS(&a.st[b].err, kErrNone, kErrBadPage);
+        return;
+    }
+    uint16_t *dst = (is_k ? a.k_pool : a.v_pool) + ((((size_t)phys * a.Hkv + gk) * kPageTokens) + pos % kPageTokens) * d;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        if (m < M) dst[lane + 32 * m] = float_to_bf16_bits(v[m]);
+}
+
+// Per sequence: greedy argmax of its logits (lowest index on ties); for the
+// sequences taking part in the step the token becomes the next input and the
+// position moves on.
+__global__ void k_bargmax(const float *logits, int V, DevState *st, const int *part) {
+    const int b = blockIdx.x;
+    const int advance = part ? part[b] : 1;
+    const float *lg = logits + (size_t)b * V;
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) {
+        const float v = lg[i];
+        if (v > best || (v == best && i < bi)) {
+            best = v;
+            bi = i;
+        }
+    }
+    __shared__ float sv[32];
+    __shared__ int si[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) {
+            best = ov;
+            bi = oi;
+        }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        sv[warp] = best;
+        si[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            if (sv[w] > best || (sv[w] == best && si[w] < bi)) {
+                best = sv[w];
+                bi = si[w];
+            }
+        st[b].last_token = bi;
+        if (advance) {
+            st[b].token = bi;
+            st[b].pos += 1;
+        }
+    }
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const LaunchCfg &lc, const BGemvArgs &a, int grid) {
+    return launch_k(lc, k_bgemv<FMT>, dim3(grid), dim3(kNW * 32), (size_t)kKC * 16, a);
+}
+
+}  // namespace
+
+bool bgemv_shape_ok(int fmt, int N, int K, int mode) {
+    const int blk = fmt == kFmtInt4 ? 128 : (fmt == kFmtInt8 ? 64 : 32);
+    return K > 0 && K % blk == 0 && K % 8 == 0 && N > 0 && N % (mode == 2 ? 8 : 16) == 0;
+}
+
+int bgemv_grid(const LaunchCfg &lc, int N, int mode) {
+    const int tiles = mode == 2 ? N / 8 : N / 16;
+    int g = (tiles + kNW - 1) / kNW;
+    if (g > lc.n_sm) g = lc.n_sm;
+    while ((long long)g * kNW * kTPW < tiles) ++g;  // at most kTPW tiles per warp
+    return g;
+}
+
+cudaError_t launch_bgemv(const LaunchCfg &lc, int fmt, const BGemvArgs &a) {
+    if (a.B < 1 || a.B > 8 || !bgemv_shape_ok(fmt, a.N, a.K, a.mode)) return cudaErrorInvalidValue;
+    const int grid = bgemv_grid(lc, a.N, a.mode);
+    if (fmt == kFmtInt4) return launch_fmt<kFmtInt4>(lc, a, grid);
+    if (fmt == kFmtInt8) return launch_fmt<kFmtInt8>(lc, a, grid);
+    if (fmt == kFmtBf16) return launch_fmt<kFmtBf16>(lc, a, grid);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bembed(cudaStream_t s, const uint16_t *embed, const DevState *st, int B, int h, float *x) {
+    k_bembed<<<B, 256, 0, s>>>(embed, st, B, h, x);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bqkv_post(cudaStream_t s, const BQkvPostArgs &a, int B) {
+    if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
+    k_bqkv_post<<<dim3(a.Hq + 2 * a.Hkv, B), 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part) {
+    k_bargmax<<<B, 1024, 0, s>>>(logits, V, st, part);
+    return cudaGetLastError();
+}
+
+}  // namespace qd

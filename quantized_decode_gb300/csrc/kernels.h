@@ -122,6 +122,46 @@ cudaError_t launch_mlp(const LaunchCfg &lc, int fmt, const MlpArgs &a);
 cudaError_t mlp_repack_down(int fmt, const void *w, const void *s, int h, int F, void *w_out, void *s_out,
                             cudaStream_t stream);
 
+// ---- multi-sequence decode (k_batch.cu) ----------------------------------------
+// Y[b][n] = sum_k W[n][k] X[b][k] for b < B <= 8 sequences on the tensor cores
+// (mma.sync, bf16 operands, fp32 accumulation), each weight read once.
+struct BGemvArgs {
+    int mode;                   // 0 store (+ bias), 1 add into y, 2 SiLU(gate) * up (w[0] gate, w2 up), 3 store
+    int n_seg;                  // modes 0/1/3: stacked matrices w[0..n_seg) of seg_rows[i] rows (multiples of 16)
+    const void *w[3], *s[3];    // codes (INT4 words / INT8 / bf16) and scales (INT4 bf16 [N][K/128], INT8 fp32 [N])
+    const uint16_t *bias[3];    // mode 0: bf16 bias per segment, or null
+    int seg_rows[3];
+    const void *w2, *s2;        // mode 2: up codes and scales
+    int N, K, B;                // N output rows (mode 2: hidden units), B sequences
+    const float *x;             // [B][ldx] inputs
+    int ldx;
+    const uint16_t *gamma;      // RMSNorm gain applied to every input row first, or null
+    float eps;
+    float *y;                   // [B][ldy]
+    int ldy;
+};
+// Per (sequence, head): q/k RMSNorm, RoPE at the sequence's position, q out,
+// K/V to slot pos % 16 of the sequence's page table[pos / 16]; sequences whose
+// `part` flag is 0 are skipped.
+struct BQkvPostArgs {
+    const float *raw;           // [B][(Hq + 2 Hkv) d]
+    int Hq, Hkv, d;
+    const uint16_t *q_gain, *k_gain;
+    float eps;
+    const float2 *rope_cs;
+    float *q_out;               // [B][Hq d]
+    uint16_t *k_pool, *v_pool;  // this layer [pages][Hkv][16][d]
+    const int *page_table;      // [B][max_pages]
+    int max_pages, n_pages;
+    DevState *st;               // [B]
+    const int *part;            // [B] 1: the sequence takes part in this step
+};
+bool bgemv_shape_ok(int fmt, int N, int K, int mode);
+cudaError_t launch_bgemv(const LaunchCfg &lc, int fmt, const BGemvArgs &a);
+cudaError_t launch_bembed(cudaStream_t s, const uint16_t *embed, const DevState *st, int B, int h, float *x);
+cudaError_t launch_bqkv_post(cudaStream_t s, const BQkvPostArgs &a, int B);
+cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part);
+
 // Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
 // ties).  The last CTA reduces the per-CTA maxima, writes the token into the
 // state (as the next step's input) and advances the position when `advance`.

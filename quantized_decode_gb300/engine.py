@@ -308,3 +308,78 @@ class Engine:
         L.check(self.lib.llm_debug_kv(self.h, ctypes.byref(k), ctypes.byref(v), ctypes.byref(pt),
                                       ctypes.byref(n), int(set_len)), "llm_debug_kv")
         return k.value, v.value, pt.value, n.value
+
+
+class BatchEngine:
+    """Up to 8 sequences decoding together over one paged K/V pool (llm_batch_t handle)."""
+
+    def __init__(self, model, max_seqs, n_pages=0, stream=None, config=None):
+        self.lib = L.load()
+        self.model = model
+        self.cfg = config if config is not None else make_config(model.cfg)
+        self.vocab = self.cfg.vocab
+        h = ctypes.c_void_p()
+        s = None if stream is None else ctypes.c_void_p(stream)
+        L.check(self.lib.llm_batch_create(ctypes.byref(self.cfg), ctypes.byref(model.weights), int(max_seqs),
+                                          int(n_pages), s, ctypes.byref(h)), "llm_batch_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            self.lib.llm_batch_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self):
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_batch_add(self.h, ctypes.byref(out)), "llm_batch_add")
+        return out.value
+
+    def release(self, seq):
+        L.check(self.lib.llm_batch_release(self.h, int(seq)), "llm_batch_release")
+
+    def step(self, seqs, inputs=None):
+        """One step for the sequences seqs; inputs (same length; -1 = the previous token) or None."""
+        sq = np.ascontiguousarray(seqs, dtype=np.int32)
+        inp = None if inputs is None else np.ascontiguousarray(inputs, dtype=np.int32)
+        out = np.empty(sq.size, dtype=np.int32)
+        L.check(self.lib.llm_batch_step(self.h, _np_ptr(sq), None if inp is None else _np_ptr(inp), sq.size,
+                                        _np_ptr(out)), "llm_batch_step")
+        return out
+
+    def prefill(self, seq, tokens):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_batch_prefill(self.h, int(seq), _np_ptr(toks), toks.size, ctypes.byref(out)),
+                "llm_batch_prefill")
+        return out.value
+
+    def logits(self, seq):
+        out = np.empty(self.vocab, dtype=np.float32)
+        L.check(self.lib.llm_batch_logits(self.h, int(seq), _np_ptr(out), self.vocab), "llm_batch_logits")
+        return out
+
+    def seq_info(self, seq):
+        """-> (length, physical pages in logical order, free pages left)."""
+        n, np_, free = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        L.check(self.lib.llm_batch_seq_info(self.h, int(seq), ctypes.byref(n), None, 0, ctypes.byref(np_),
+                                            ctypes.byref(free)), "llm_batch_seq_info")
+        pages = np.empty(max(np_.value, 1), dtype=np.int32)
+        L.check(self.lib.llm_batch_seq_info(self.h, int(seq), None, _np_ptr(pages), pages.size, None, None),
+                "llm_batch_seq_info")
+        return n.value, pages[:np_.value], free.value
+
+    def set_page_order(self, order):
+        o = np.ascontiguousarray(order, dtype=np.int32)
+        L.check(self.lib.llm_batch_set_page_order(self.h, _np_ptr(o), o.size), "llm_batch_set_page_order")
+
+    def debug_kv(self):
+        k, v, n = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int32()
+        L.check(self.lib.llm_batch_debug_kv(self.h, ctypes.byref(k), ctypes.byref(v), ctypes.byref(n)),
+                "llm_batch_debug_kv")
+        return k.value, v.value, n.value
