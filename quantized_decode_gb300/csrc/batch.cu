@@ -41,8 +41,12 @@ struct llm_batch_t {
     int *part = nullptr;          // [S]
     float2 *rope_cs = nullptr;
     float *x = nullptr, *raw = nullptr, *q = nullptr, *attn = nullptr, *u = nullptr, *logits = nullptr;
-    float *part_o = nullptr, *part_ml = nullptr;
-    int *attn_cnt = nullptr;
+    float *part_o = nullptr, *part_ml = nullptr;  // per slot: attention split partials
+    int *attn_cnt = nullptr;                      // per slot: arrival counters
+    float *arg_v = nullptr;                       // split argmax scratch [S][32]
+    int *arg_i = nullptr;
+    std::vector<cudaStream_t> side;               // per slot: the attention branch of the graph
+    std::vector<cudaEvent_t> ev;                  // fork event, then one join event per slot
     int P = 8, cs = 8;
     int32_t *pinned = nullptr;    // host staging: part [S] | state in [S] | state out [S] | page table [S][max_pages]
     cudaGraph_t graph = nullptr;
@@ -74,10 +78,14 @@ void free_all(llm_batch_t *h) {
     if (h->exec) cudaGraphExecDestroy(h->exec);
     if (h->graph) cudaGraphDestroy(h->graph);
     void *bufs[] = {h->k_pool, h->v_pool, h->page_table, h->st, h->part, h->rope_cs, h->x, h->raw, h->q,
-                    h->attn, h->u, h->logits, h->part_o, h->part_ml, h->attn_cnt};
+                    h->attn, h->u, h->logits, h->part_o, h->part_ml, h->attn_cnt, h->arg_v, h->arg_i};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
+    for (cudaStream_t x : h->side)
+        if (x) cudaStreamDestroy(x);
+    for (cudaEvent_t e : h->ev)
+        if (e) cudaEventDestroy(e);
     if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
 }
 
@@ -112,17 +120,29 @@ cudaError_t enqueue_batch_step(llm_batch_t *h) {
         pa.st = h->st; pa.part = h->part;
         if ((e = launch_bqkv_post(h->stream, pa, S)) != cudaSuccess) return e;
 
-        for (int b = 0; b < S; ++b) {  // attention per sequence, through its own table and length
+        // attention per sequence, through its own table and length: one graph branch
+        // per sequence (its own stream while capturing), so they run side by side
+        const int G = c.n_q_heads / c.n_kv_heads;
+        if ((e = cudaEventRecord(h->ev[0], h->stream)) != cudaSuccess) return e;
+        for (int b = 0; b < S; ++b) {
+            if ((e = cudaStreamWaitEvent(h->side[b], h->ev[0], 0)) != cudaSuccess) return e;
+            LaunchCfg lb = h->lc;
+            lb.stream = h->side[b];
             AttnArgs aa{};
             aa.q = h->q + (size_t)b * rq;
             aa.k_pool = kp; aa.v_pool = vp;
             aa.page_table = h->page_table + (size_t)b * h->max_pages; aa.n_pages = h->n_pages;
             aa.st = h->st + b; aa.T_fixed = -1;
             aa.Hq = c.n_q_heads; aa.Hkv = c.n_kv_heads; aa.d = d; aa.P = h->P; aa.cs = h->cs;
-            aa.part_o = h->part_o; aa.part_ml = h->part_ml; aa.counter = h->attn_cnt;
+            aa.part_o = h->part_o + (size_t)b * c.n_kv_heads * h->P * G * d;
+            aa.part_ml = h->part_ml + (size_t)b * c.n_kv_heads * h->P * G * 2;
+            aa.counter = h->attn_cnt + (size_t)b * c.n_kv_heads;
             aa.out = h->attn + (size_t)b * rq; aa.err = &h->st[b].err;
-            if ((e = launch_attention(h->lc, aa)) != cudaSuccess) return e;
+            if ((e = launch_attention(lb, aa)) != cudaSuccess) return e;
+            if ((e = cudaEventRecord(h->ev[1 + b], h->side[b])) != cudaSuccess) return e;
         }
+        for (int b = 0; b < S; ++b)
+            if ((e = cudaStreamWaitEvent(h->stream, h->ev[1 + b], 0)) != cudaSuccess) return e;
 
         BGemvArgs o{};
         o.mode = 1; o.n_seg = 1; o.w[0] = L.wo; o.s[0] = L.so; o.seg_rows[0] = c.hidden;
@@ -149,7 +169,7 @@ cudaError_t enqueue_batch_step(llm_batch_t *h) {
     lm.N = c.vocab; lm.K = c.hidden; lm.B = S; lm.x = h->x; lm.ldx = c.hidden;
     lm.gamma = (const uint16_t *)h->w.final_norm; lm.eps = c.rms_eps; lm.y = h->logits; lm.ldy = c.vocab;
     if ((e = launch_bgemv(h->lc, int8_head ? kFmtInt8 : kFmtBf16, lm)) != cudaSuccess) return e;
-    return launch_bargmax(h->stream, h->logits, c.vocab, h->st, S, h->part);
+    return launch_bargmax(h->stream, h->logits, c.vocab, h->st, S, h->part, h->arg_v, h->arg_i);
 }
 
 int capture(llm_batch_t *h) {
@@ -234,16 +254,22 @@ int llm_batch_create(const llm_config *cfg, const llm_weights *w, int32_t max_se
               dalloc(&h->x, (size_t)S * c.hidden) == cudaSuccess && dalloc(&h->raw, (size_t)S * nq) == cudaSuccess &&
               dalloc(&h->q, (size_t)S * rq) == cudaSuccess && dalloc(&h->attn, (size_t)S * rq) == cudaSuccess &&
               dalloc(&h->u, (size_t)S * c.mlp) == cudaSuccess && dalloc(&h->logits, (size_t)S * c.vocab) == cudaSuccess &&
-              dalloc(&h->part_o, (size_t)c.n_kv_heads * h->P * G * d) == cudaSuccess &&
-              dalloc(&h->part_ml, (size_t)c.n_kv_heads * h->P * G * 2) == cudaSuccess &&
-              dalloc(&h->attn_cnt, c.n_kv_heads) == cudaSuccess &&
+              dalloc(&h->part_o, (size_t)S * c.n_kv_heads * h->P * G * d) == cudaSuccess &&
+              dalloc(&h->part_ml, (size_t)S * c.n_kv_heads * h->P * G * 2) == cudaSuccess &&
+              dalloc(&h->attn_cnt, (size_t)S * c.n_kv_heads) == cudaSuccess &&
+              dalloc(&h->arg_v, (size_t)S * 32) == cudaSuccess && dalloc(&h->arg_i, (size_t)S * 32) == cudaSuccess &&
               cudaMallocHost((void **)&h->pinned, sizeof(int32_t) * ((size_t)S * 9 + (size_t)S * h->max_pages)) ==
                   cudaSuccess;
+    h->side.assign(S, nullptr);
+    h->ev.assign(S + 1, nullptr);
+    for (int b = 0; ok && b < S; ++b)
+        ok = cudaStreamCreateWithFlags(&h->side[b], cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i <= S; ++i) ok = cudaEventCreateWithFlags(&h->ev[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) return fail(LLM_ERR_CUDA);
     ok = cudaMemsetAsync(h->page_table, 0, sizeof(int) * (size_t)S * h->max_pages, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->st, 0, sizeof(DevState) * S, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->part, 0, sizeof(int) * S, h->stream) == cudaSuccess &&
-         cudaMemsetAsync(h->attn_cnt, 0, sizeof(int) * c.n_kv_heads, h->stream) == cudaSuccess &&
+         cudaMemsetAsync(h->attn_cnt, 0, sizeof(int) * (size_t)S * c.n_kv_heads, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->x, 0, sizeof(float) * (size_t)S * c.hidden, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->attn, 0, sizeof(float) * (size_t)S * rq, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->u, 0, sizeof(float) * (size_t)S * c.mlp, h->stream) == cudaSuccess;

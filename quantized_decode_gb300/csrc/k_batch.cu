@@ -21,9 +21,10 @@ namespace qd {
 namespace {
 
 constexpr int kNW = 8;        // warps per CTA
-constexpr int kKC = 4096;     // K values staged in shared memory at a time
+constexpr int kKC = 12288;    // K values staged in shared memory at a time (192 KB for 8 sequences)
 constexpr int kTPW = 8;       // row tiles per warp at most (fp32 accumulators)
-constexpr int kUB = 4;        // 64-byte row blocks loaded ahead per warp
+constexpr int kUB = 4;        // 64-byte row blocks per load group (two groups in flight per warp)
+constexpr int kNormK = 4096;  // RMSNorm'd inputs: K at most this (their fp32 rows sit in shared memory)
 
 QD_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                      uint32_t b1) {
@@ -86,21 +87,42 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int tiles = a.mode == 2 ? a.N / 8 : a.N / 16;
-    const int gw = blockIdx.x * kNW + warp, nwarps = gridDim.x * kNW;
+    // ks warps share a tile, each over its own part of K (their sums meet in
+    // shared memory at the end); the CTA holds kNW / ks tile slots
+    const int ks = a.ks, kp = warp % ks, tslots = kNW / ks;
+    const int gw = blockIdx.x * tslots + warp / ks, nwarps = gridDim.x * tslots;
     const int B = a.B;
 
-    // ---- per-sequence RMSNorm factors (over the whole K)
+    // ---- with an RMSNorm (K <= kNormK): the B input rows are read once, their fp32
+    // values kept in shared memory behind the staging area while the sums of squares
+    // are formed, then normalized from there
+    float *xf = reinterpret_cast<float *>(sx + (a.K < kKC ? a.K : kKC));  // [8][K] fp32 (gamma only)
     if (threadIdx.x < 8) s_inv[threadIdx.x] = 1.f;
     if (a.gamma) {
         float ss[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) ss[b] = 0.f;
-        for (int k = threadIdx.x * 4; k < a.K; k += blockDim.x * 4) {
+        constexpr int kB = 4;  // float4 loads per sequence in flight per thread
+        for (int k = threadIdx.x * 4; k < a.K; k += blockDim.x * 4 * kB) {
+            float4 v[8][kB];
 #pragma unroll
             for (int b = 0; b < 8; ++b)
-                if (b < B) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.ldx + k));
-                    ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    const int kk = k + j * blockDim.x * 4;
+                    v[b][j] = b < B && kk < a.K ? __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.ldx + kk))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    const int kk = k + j * blockDim.x * 4;
+                    if (kk < a.K) {
+                        ss[b] += v[b][j].x * v[b][j].x + v[b][j].y * v[b][j].y + v[b][j].z * v[b][j].z +
+                                 v[b][j].w * v[b][j].w;
+                        *reinterpret_cast<float4 *>(xf + (size_t)b * a.K + kk) = v[b][j];
+                    }
                 }
         }
 #pragma unroll
@@ -145,19 +167,38 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
         rr1 = r + 8;
     };
 
+    // grid.y parts of K (large-K projections): this CTA's range of 64-byte blocks
+    const int nb_all = a.K / BLK;
+    const int kbeg = (int)((long long)nb_all * blockIdx.y / gridDim.y) * BLK;
+    const int kend = (int)((long long)nb_all * (blockIdx.y + 1) / gridDim.y) * BLK;
 #pragma unroll 1
-    for (int k0 = 0; k0 < a.K; k0 += kKC) {
-        const int kc = a.K - k0 < kKC ? a.K - k0 : kKC;
-        // ---- stage X[b][k0 .. k0 + kc) as bf16 (normalized), zeros for b >= B
+    for (int k0 = kbeg; k0 < kend; k0 += kKC) {
+        const int kc = kend - k0 < kKC ? kend - k0 : kKC;
+        // ---- stage X[b][k0 .. k0 + kc) as bf16 (normalized), zeros for b >= B; the
+        // inputs come from the fp32 copy (RMSNorm) or from global memory, several
+        // entries' loads in flight per thread
         __syncthreads();
-        for (int e = threadIdx.x; e < (kc / 8) * 8; e += blockDim.x) {
-            const int c = e >> 3, b = e & 7;
+        constexpr int kE = 4;
+        for (int e0 = threadIdx.x; e0 < (kc / 8) * 8; e0 += blockDim.x * kE) {
+            float4 v0[kE], v1[kE];
+#pragma unroll
+            for (int j = 0; j < kE; ++j) {
+                const int e = e0 + j * blockDim.x, c = e >> 3, b = e & 7;
+                v0[j] = v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e < (kc / 8) * 8 && b < B) {
+                    const float *src = a.gamma ? xf + (size_t)b * a.K + k0 + c * 8 : a.x + (size_t)b * a.ldx + k0 + c * 8;
+                    v0[j] = a.gamma ? *reinterpret_cast<const float4 *>(src) : __ldcg(reinterpret_cast<const float4 *>(src));
+                    v1[j] = a.gamma ? *reinterpret_cast<const float4 *>(src + 4)
+                                    : __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kE; ++j) {
+            const int e = e0 + j * blockDim.x, c = e >> 3, b = e & 7;
+            if (e >= (kc / 8) * 8) break;
             uint4 out = make_uint4(0u, 0u, 0u, 0u);
             if (b < B) {
-                const float *src = a.x + (size_t)b * a.ldx + k0 + c * 8;
-                const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
-                float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                float f[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w, v1[j].x, v1[j].y, v1[j].z, v1[j].w};
                 const float inv = s_inv[b];
                 uint32_t o[4];
 #pragma unroll
@@ -174,10 +215,13 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
                 out = make_uint4(o[0], o[1], o[2], o[3]);
             }
             sx[act_entry(c, b)] = out;
+            }
         }
         __syncthreads();
 
-        const int nblk = kc / BLK;
+        const int nblk_all = kc / BLK;
+        const int kb0 = nblk_all * kp / ks, kb1 = nblk_all * (kp + 1) / ks;  // this warp's blocks of the chunk
+        const int nblk = kb1 - kb0;
 #pragma unroll
         for (int i = 0; i < kTPW; ++i) {
             const int ti = gw + i * nwarps;
@@ -186,31 +230,34 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
             const void *s0, *s1;
             int rr0, rr1;
             row_ptrs(ti, r0, r1, s0, s1, rr0, rr1);
-            const int ub0 = k0 / BLK;  // first block of the chunk in the row (64-byte units)
-#pragma unroll 1
-            for (int bk = 0; bk < nblk; bk += kUB) {
+            const int ub0 = k0 / BLK + kb0;  // first block of this warp's part in the row (64-byte units)
+            struct Group {
                 uint4 w0[kUB], w1[kUB];
                 float sc0[kUB], sc1[kUB];
+            };
+            auto load = [&](Group &q, int bk) {
 #pragma unroll
                 for (int u = 0; u < kUB; ++u) {
                     if (bk + u < nblk) {
                         const int blk = ub0 + bk + u;
-                        w0[u] = ld_stream(r0 + (size_t)blk * 4 + t);
-                        w1[u] = ld_stream(r1 + (size_t)blk * 4 + t);
+                        q.w0[u] = ld_stream(r0 + (size_t)blk * 4 + t);
+                        q.w1[u] = ld_stream(r1 + (size_t)blk * 4 + t);
                         if constexpr (FMT == kFmtInt4) {
                             const int G = a.K / kGroup;
-                            sc0[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s0) + (size_t)rr0 * G + blk));
-                            sc1[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s1) + (size_t)rr1 * G + blk));
+                            q.sc0[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s0) + (size_t)rr0 * G + blk));
+                            q.sc1[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s1) + (size_t)rr1 * G + blk));
                         }
                     }
                 }
+            };
+            auto compute = [&](const Group &q, int bk) {
 #pragma unroll
                 for (int u = 0; u < kUB; ++u) {
                     if (bk + u >= nblk) break;
-                    const int cbase = ((bk + u) * BLK + t * CPL) / 8;  // staged k-chunk of this lane's codes
+                    const int cbase = ((kb0 + bk + u) * BLK + t * CPL) / 8;  // staged k-chunk of this lane's codes
                     // A pairs of the two rows
                     uint32_t pa[2][CPL / 2];
-                    const uint4 wv[2] = {w0[u], w1[u]};
+                    const uint4 wv[2] = {q.w0[u], q.w1[u]};
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
@@ -220,7 +267,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
                                 uint32_t p[4];
                                 int4_word_bf16(ww[j], p);
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) pa[r][4 * j + q] = p[q];
+                                for (int z = 0; z < 4; ++z) pa[r][4 * j + z] = p[z];
                             }
                         } else if constexpr (FMT == kFmtInt8) {
 #pragma unroll
@@ -244,18 +291,47 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
                         mma_bf16(d, pa[0][2 * m], pa[1][2 * m], pa[0][2 * m + 1], pa[1][2 * m + 1], b0, b1);
                     }
                     if constexpr (FMT == kFmtInt4) {
-                        acc[i][0] = fmaf(d[0], sc0[u], acc[i][0]);
-                        acc[i][1] = fmaf(d[1], sc0[u], acc[i][1]);
-                        acc[i][2] = fmaf(d[2], sc1[u], acc[i][2]);
-                        acc[i][3] = fmaf(d[3], sc1[u], acc[i][3]);
+                        acc[i][0] = fmaf(d[0], q.sc0[u], acc[i][0]);
+                        acc[i][1] = fmaf(d[1], q.sc0[u], acc[i][1]);
+                        acc[i][2] = fmaf(d[2], q.sc1[u], acc[i][2]);
+                        acc[i][3] = fmaf(d[3], q.sc1[u], acc[i][3]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) acc[i][j] += d[j];
                     }
                 }
+            };
+            // two load groups in flight: the next group's loads go out before this one's math
+            Group ga, gb;
+            if (nblk > 0) load(ga, 0);
+#pragma unroll 1
+            for (int bk = 0; bk < nblk; bk += 2 * kUB) {
+                if (bk + kUB < nblk) load(gb, bk + kUB);
+                compute(ga, bk);
+                if (bk + 2 * kUB < nblk) load(ga, bk + 2 * kUB);
+                if (bk + kUB < nblk) compute(gb, bk + kUB);
             }
         }
     }
+
+    // ---- the K parts of a tile meet in shared memory (the staging area is free now)
+    if (ks > 1) {
+        __syncthreads();
+        float *red2 = reinterpret_cast<float *>(sx);  // [kNW][kTPW][4][32]
+#pragma unroll
+        for (int i = 0; i < kTPW; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) red2[((warp * kTPW + i) * 4 + j) * 32 + lane] = acc[i][j];
+        __syncthreads();
+        if (kp == 0) {
+#pragma unroll
+            for (int i = 0; i < kTPW; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    for (int q = 1; q < ks; ++q) acc[i][j] += red2[(((warp + q) * kTPW + i) * 4 + j) * 32 + lane];
+        }
+    }
+    if (kp != 0) return;
 
     // ---- epilogue: lane (g, t) holds rows (g, g + 8) x sequences (2t, 2t + 1)
 #pragma unroll
@@ -294,7 +370,10 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
                 }
             }
             float *yb = a.y + (size_t)b * a.ldy;
-            if (a.mode == 1) {
+            if (a.mode == 1 && gridDim.y > 1) {  // the K parts of other CTAs add into the same rows
+                atomicAdd(yb + row0, y0);
+                atomicAdd(yb + row1, y1);
+            } else if (a.mode == 1) {
                 yb[row0] += y0;
                 yb[row1] += y1;
             } else {
@@ -370,24 +449,24 @@ __global__ void k_bqkv_post(BQkvPostArgs a) {
         if (m < M) dst[lane + 32 * m] = float_to_bf16_bits(v[m]);
 }
 
-// Per sequence: greedy argmax of its logits (lowest index on ties); for the
-// sequences taking part in the step the token becomes the next input and the
-// position moves on.
-__global__ void k_bargmax(const float *logits, int V, DevState *st, const int *part) {
-    const int b = blockIdx.x;
-    const int advance = part ? part[b] : 1;
+// Greedy argmax per sequence (lowest index on ties) in two steps: CTA (x, b)
+// reduces its slice of sequence b's logits to one (value, index) pair; then one
+// warp per sequence reduces the pairs and, for the sequences taking part in the
+// step, makes the token the next input and moves the position on.
+constexpr int kArgSplits = 32;
+__global__ void k_bargmax_part(const float *logits, int V, float *pv, int *pi) {
+    const int b = blockIdx.y, sp = blockIdx.x;
+    const int lo = (int)((long long)V * sp / kArgSplits), hi = (int)((long long)V * (sp + 1) / kArgSplits);
     const float *lg = logits + (size_t)b * V;
     float best = -INFINITY;
     int bi = 0x7fffffff;
-    for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         const float v = lg[i];
         if (v > best || (v == best && i < bi)) {
             best = v;
             bi = i;
         }
     }
-    __shared__ float sv[32];
-    __shared__ int si[32];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, best, o);
@@ -397,6 +476,8 @@ __global__ void k_bargmax(const float *logits, int V, DevState *st, const int *p
             bi = oi;
         }
     }
+    __shared__ float sv[32];
+    __shared__ int si[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
         sv[warp] = best;
@@ -409,8 +490,27 @@ __global__ void k_bargmax(const float *logits, int V, DevState *st, const int *p
                 best = sv[w];
                 bi = si[w];
             }
+        pv[b * kArgSplits + sp] = best;
+        pi[b * kArgSplits + sp] = bi;
+    }
+}
+
+__global__ void k_bargmax_final(const float *pv, const int *pi, DevState *st, const int *part) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    float best = pv[b * kArgSplits + lane];
+    int bi = pi[b * kArgSplits + lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) {
+            best = ov;
+            bi = oi;
+        }
+    }
+    if (lane == 0) {
         st[b].last_token = bi;
-        if (advance) {
+        if (!part || part[b]) {
             st[b].token = bi;
             st[b].pos += 1;
         }
@@ -418,8 +518,14 @@ __global__ void k_bargmax(const float *logits, int V, DevState *st, const int *p
 }
 
 template <int FMT>
-cudaError_t launch_fmt(const LaunchCfg &lc, const BGemvArgs &a, int grid) {
-    return launch_k(lc, k_bgemv<FMT>, dim3(grid), dim3(kNW * 32), (size_t)kKC * 16, a);
+cudaError_t launch_fmt(const LaunchCfg &lc, const BGemvArgs &a, int grid, int gks) {
+    // staging for min(K part, kKC) values of 8 sequences; it also holds the K-part sums
+    const int kpart = (a.K + gks - 1) / gks + 128;
+    size_t smem = (size_t)(kpart < kKC ? kpart : kKC) * 16;
+    const size_t red = (size_t)kNW * kTPW * 4 * 32 * 4;
+    if (smem < red) smem = red;
+    if (a.gamma) smem += (size_t)8 * a.K * 4;  // the fp32 input rows
+    return launch_k(lc, k_bgemv<FMT>, dim3(grid, gks), dim3(kNW * 32), smem, a);
 }
 
 }  // namespace
@@ -429,20 +535,37 @@ bool bgemv_shape_ok(int fmt, int N, int K, int mode) {
     return K > 0 && K % blk == 0 && K % 8 == 0 && N > 0 && N % (mode == 2 ? 8 : 16) == 0;
 }
 
-int bgemv_grid(const LaunchCfg &lc, int N, int mode) {
+// K split: as many warps per tile (1..8) as it takes for the tiles to give every
+// warp of the grid work; then the grid, at most kTPW tiles per tile slot.
+// Large-K projections that add into y (the down projection) also split K over
+// grid.y CTAs of about 2048 values each, so that a CTA stages only its part of the
+// inputs; their partial sums meet in y through atomic adds.
+void bgemv_plan(const LaunchCfg &lc, int N, int K, int mode, int &ks, int &grid, int &gks) {
     const int tiles = mode == 2 ? N / 8 : N / 16;
-    int g = (tiles + kNW - 1) / kNW;
-    if (g > lc.n_sm) g = lc.n_sm;
-    while ((long long)g * kNW * kTPW < tiles) ++g;  // at most kTPW tiles per warp
-    return g;
+    gks = 1;
+    if (mode == 1 && K > kNormK) {
+        gks = K / 2048;
+        if (gks > 8) gks = 8;
+    }
+    const int n_sm = lc.n_sm / gks > 0 ? lc.n_sm / gks : 1;  // SMs per K part
+    ks = 1;
+    while (ks < kNW && (long long)tiles * ks < (long long)kNW * n_sm) ks *= 2;
+    const int tslots = kNW / ks;
+    grid = (tiles + tslots - 1) / tslots;
+    if (grid > n_sm) grid = n_sm;
+    while ((long long)grid * tslots * kTPW < tiles) ++grid;
 }
 
-cudaError_t launch_bgemv(const LaunchCfg &lc, int fmt, const BGemvArgs &a) {
-    if (a.B < 1 || a.B > 8 || !bgemv_shape_ok(fmt, a.N, a.K, a.mode)) return cudaErrorInvalidValue;
-    const int grid = bgemv_grid(lc, a.N, a.mode);
-    if (fmt == kFmtInt4) return launch_fmt<kFmtInt4>(lc, a, grid);
-    if (fmt == kFmtInt8) return launch_fmt<kFmtInt8>(lc, a, grid);
-    if (fmt == kFmtBf16) return launch_fmt<kFmtBf16>(lc, a, grid);
+cudaError_t launch_bgemv(const LaunchCfg &lc, int fmt, const BGemvArgs &args) {
+    if (args.B < 1 || args.B > 8 || !bgemv_shape_ok(fmt, args.N, args.K, args.mode) ||
+        (args.gamma && args.K > kNormK))
+        return cudaErrorInvalidValue;
+    BGemvArgs a = args;
+    int grid = 0, gks = 1;
+    bgemv_plan(lc, a.N, a.K, a.mode, a.ks, grid, gks);
+    if (fmt == kFmtInt4) return launch_fmt<kFmtInt4>(lc, a, grid, gks);
+    if (fmt == kFmtInt8) return launch_fmt<kFmtInt8>(lc, a, grid, gks);
+    if (fmt == kFmtBf16) return launch_fmt<kFmtBf16>(lc, a, grid, gks);
     return cudaErrorInvalidValue;
 }
 
@@ -457,8 +580,11 @@ cudaError_t launch_bqkv_post(cudaStream_t s, const BQkvPostArgs &a, int B) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part) {
-    k_bargmax<<<B, 1024, 0, s>>>(logits, V, st, part);
+cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part,
+                           float *pv, int *pi) {
+    static_assert(kArgSplits == 32, "one lane per split in the final step");
+    k_bargmax_part<<<dim3(kArgSplits, B), 256, 0, s>>>(logits, V, pv, pi);
+    k_bargmax_final<<<B, 32, 0, s>>>(pv, pi, st, part);
     return cudaGetLastError();
 }
 

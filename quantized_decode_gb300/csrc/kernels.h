@@ -139,6 +139,7 @@ struct BGemvArgs {
     float eps;
     float *y;                   // [B][ldy]
     int ldy;
+    int ks;                     // set by the launcher: warps per tile along K
 };
 // Per (sequence, head): q/k RMSNorm, RoPE at the sequence's position, q out,
 // K/V to slot pos % 16 of the sequence's page table[pos / 16]; sequences whose
@@ -160,7 +161,9 @@ bool bgemv_shape_ok(int fmt, int N, int K, int mode);
 cudaError_t launch_bgemv(const LaunchCfg &lc, int fmt, const BGemvArgs &a);
 cudaError_t launch_bembed(cudaStream_t s, const uint16_t *embed, const DevState *st, int B, int h, float *x);
 cudaError_t launch_bqkv_post(cudaStream_t s, const BQkvPostArgs &a, int B);
-cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part);
+// pv, pi: [B][32] scratch of the split argmax.
+cudaError_t launch_bargmax(cudaStream_t s, const float *logits, int V, DevState *st, int B, const int *part,
+                           float *pv, int *pi);
 
 // Final RMSNorm -> LM head GEMV -> logits + greedy argmax (lowest index on
 // ties).  The last CTA reduces the per-CTA maxima, writes the token into the
