@@ -80,6 +80,7 @@ def parse():
                    help="decode step as a kernel chain or as one persistent kernel")
     p.add_argument("--timeline-steps", type=int, default=16,
                    help="steps of the in-graph per-kernel timeline (0: skip)")
+    p.add_argument("--no-batch", action="store_true", help="skip the 8-sequence decode line")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the 1.5B (pp512/tg128) and Qwen3-8B INT8 (inputs 128..4096) lines")
     return p.parse_args()
@@ -567,6 +568,12 @@ def run_ours(args):
     if not args.no_sweep and ws == 1 and args.layers == 0 and args.vocab == 0:
         sweep = config_sweep(args, stream, peak, peak_kind)
 
+    # ---- multi-sequence decode: 8 sequences of the same model over one paged pool, each step
+    # reading the weights once for all of them
+    batch8 = None
+    if not args.no_batch and ws == 1:
+        batch8 = batch_decode(args, model, cfg, stream, peak, peak_kind)
+
     # ---- end to end through the C ABI: host token in (pinned H2D), host token out (D2H)
     toks = sm.prompt(cfg, args.seed, args.e2e_steps, stream=1)
     if eng.seq_len() + args.e2e_steps > ctx:
@@ -620,6 +627,7 @@ def run_ours(args):
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):
             None if other_ms is None else round(other_ms, 4),
         "config_sweep": sweep,
+        "batch_decode": batch8,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/token", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps * len(step_kinds) + extra,
@@ -633,6 +641,41 @@ def run_ours(args):
     eng.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def batch_bytes(cfg, lengths):
+    """Bytes one multi-sequence step must move: every weight once, plus each sequence's K/V
+    read at its length and its appended row."""
+    rkv = cfg.n_kv_heads * cfg.head_dim
+    one = algorithmic_bytes(cfg, 0) - cfg.n_layers * 2 * rkv * 2   # weights (+ embedding row)
+    return one + sum(cfg.n_layers * (2 * rkv * 2 * (T + 1)) for T in lengths)
+
+
+def batch_decode(args, model, cfg, stream, peak, peak_kind, B=8, prompt_len=64, n=64):
+    """tok/s of B sequences decoding together (llm_batch_step), after a prompt each."""
+    from quantized_decode_gb300 import BatchEngine
+    from synth import model as sm
+    eng = BatchEngine(model, B, stream=stream.cuda_stream, config=None)
+    try:
+        seqs = [eng.add() for _ in range(B)]
+        for s in seqs:
+            eng.prefill(s, sm.prompt(cfg, args.seed + 100 + s, prompt_len, stream=100 + s))
+        for _ in range(3):
+            eng.step(seqs)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            eng.step(seqs)
+        dt = (time.perf_counter() - t0) / n
+        lengths = [prompt_len + 3 + n / 2] * B
+        gbs = batch_bytes(cfg, lengths) / dt / 1e9
+        return {"sequences": B, "ms_per_step": round(dt * 1e3, 3), "tokens_per_s": round(B / dt, 1),
+                "step_roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                                  "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+                "timing": "wall clock around llm_batch_step (host page allocation and copies included)",
+                "kv_len_mean": prompt_len + 3 + n / 2}
+    finally:
+        eng.close()
 
 
 def config_sweep(args, stream, peak, peak_kind):

@@ -47,3 +47,14 @@ def test_reference_arm_json_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "ms/token", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("cfg", [sm.CONFIGS["tiny"], TINY8], ids=["int4", "int8"])
+def test_batch_bytes_reads_weights_once(bench, cfg):
+    """One sequence costs what the single-sequence step does; each further sequence adds only
+    its own K/V (read at its length, plus the appended row)."""
+    T = 300
+    assert bench.batch_bytes(cfg, [T]) == bench.algorithmic_bytes(cfg, T)
+    rkv = cfg.n_kv_heads * cfg.head_dim
+    kv = lambda t: cfg.n_layers * 2 * rkv * 2 * (t + 1)  # noqa: E731
+    assert bench.batch_bytes(cfg, [T, 17, 40]) == bench.algorithmic_bytes(cfg, T) + kv(17) + kv(40)
