@@ -546,9 +546,9 @@ int prefill_alloc(llm_t *h) {
     // rows past a chunk's end are read by the GEMMs (their outputs are dropped): keep them finite
     ok = cudaMemsetAsync(h->pf_a, 0, (size_t)R * arow * 2, h->stream) == cudaSuccess &&
          cudaMemsetAsync(h->pf_u, 0, (size_t)R * c.mlp * 2, h->stream) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_ah, h->pf_a, R, c.hidden) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_aq, h->pf_a, R, rq) == cudaSuccess &&
-         tc_operand_map(&h->pf_map_u, h->pf_u, R, c.mlp) == cudaSuccess;
+         tc_act_map(&h->pf_map_ah, h->pf_a, R, c.hidden) == cudaSuccess &&
+         tc_act_map(&h->pf_map_aq, h->pf_a, R, rq) == cudaSuccess &&
+         tc_act_map(&h->pf_map_u, h->pf_u, R, c.mlp) == cudaSuccess;
     if (!ok) return LLM_ERR_CUDA;
     // code-tile maps of every weight matrix (the GEMMs dequantize in shared memory)
     const int rkv = c.n_kv_heads * d;

@@ -160,7 +160,7 @@ int llm_op_gemm_quant(int32_t fmt, const void *A, const void *w, const void *s, 
     if (fmt != LLM_FMT_INT4_G128 && fmt != LLM_FMT_INT8_ROW) return LLM_ERR_ARG;
     const int f = fmt == LLM_FMT_INT4_G128 ? kFmtInt4 : kFmtInt8;
     CUtensorMap am, wm[3];
-    if (tc_operand_map(&am, A, (uint64_t)M, (uint64_t)K) != cudaSuccess ||
+    if (tc_act_map(&am, A, (uint64_t)M, (uint64_t)K) != cudaSuccess ||
         tc_weight_map(&wm[0], w, f, (uint64_t)N, (uint64_t)K, kTcBN) != cudaSuccess)
         return LLM_ERR_CUDA;
     wm[1] = wm[2] = wm[0];

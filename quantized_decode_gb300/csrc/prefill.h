@@ -45,6 +45,10 @@ cudaError_t launch_tc_gemm(cudaStream_t stream, const CUtensorMap &a_map, const 
 // B = the weight codes: up to three stacked matrices (QKV: seg_rows = q, k, v
 // rows, each a multiple of 128), or (interleave) a gate/up pair of seg_rows[0]
 // rows each, whose 128-row tiles hold 64 gate rows then the matching 64 up rows.
+// The kernel computes 128 weight rows x 256 prompt rows per CTA with the
+// dequantized weights in tensor memory; when that leaves most SMs idle it
+// splits K over a cluster of 2 or 4 CTAs and adds their partial sums in a
+// fixed order (results do not depend on the run).
 struct TcQuantB {
     int fmt;                 // kFmtInt4 (bf16 group scales) / kFmtInt8 (fp32 row scales)
     int interleave;
@@ -55,8 +59,15 @@ struct TcQuantB {
 // Tensor map of a code matrix [rows][K] (INT4: K/2 bytes a row) for tiles of
 // box_rows (128, or 64 for an interleaved pair) x 64 codes.
 cudaError_t tc_weight_map(CUtensorMap *map, const void *codes, int fmt, uint64_t rows, uint64_t K, int box_rows);
+// Tensor map of the activations A [rows][cols] fp16 of the quantized GEMM
+// (tiles of 256 rows x 64 columns, 128-byte swizzle; rows past `rows` read as
+// zero).  cols % 64 == 0, base 16-byte aligned.
+cudaError_t tc_act_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols);
+// a_map from tc_act_map, w_maps from tc_weight_map.  kEpiSwiGlu needs interleave.
 cudaError_t launch_tc_gemm_q(cudaStream_t stream, const CUtensorMap &a_map, const CUtensorMap (&w_maps)[3],
                              const TcQuantB &b, const TcGemmArgs &a);
+// K split of a launch (1, 2 or 4) on a device with n_sm SMs.
+int tc_gemm_q_split(int M, int N, int K, int mode, int n_sm);
 
 // ---- weight dequantization to fp16 rows ----------------------------------------
 // out[r][k] = code[src(r)][k] * scale (INT4: bf16 group scale; INT8: fp32 row

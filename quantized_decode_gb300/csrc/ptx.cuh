@@ -1,7 +1,7 @@
 // ptx.cuh - asynchronous-proxy helpers for the prefill kernels (sm_103a):
-// mbarriers with bounded waits, TMA tile loads, and the tcgen05 tensor-core
-// path (TMEM allocation, UMMA shared-memory/instruction descriptors, MMA
-// issue and commit, TMEM loads).
+// mbarriers with bounded waits, TMA tile loads, the tcgen05 tensor-core path
+// (TMEM allocation, UMMA shared-memory/instruction descriptors, MMA issue and
+// commit, TMEM loads and stores) and thread-block cluster primitives.
 #pragma once
 
 #include <cuda.h>
@@ -61,6 +61,25 @@ QD_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+// 2-D tile store (or element-wise fp32 add) of shared memory `src` into the
+// tensor of `map` at (x, y); elements outside the tensor are not written.
+// Tracked by the bulk async-group of the issuing thread.
+QD_DEV void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+QD_DEV void tma_reduce_add_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     map),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+// Close this thread's bulk async-group and wait until its operations are complete.
+QD_DEV void bulk_commit_wait_all() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 QD_DEV void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -122,6 +141,75 @@ QD_DEV void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t i
 QD_DEV void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: the A operand (M = 128 rows, one per TMEM
+// lane; a 16-wide K step is 8 columns, each holding the fp16 pair (2j, 2j + 1)
+// low half first) is read from tensor memory, B through its descriptor.
+QD_DEV void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of the warp's 32 TMEM lanes from registers,
+// then wait until this thread's stores have landed.
+QD_DEV void tmem_st16_wait(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- thread-block clusters ---------------------------------------------------
+QD_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives, then waits for all.
+QD_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+QD_DEV uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+QD_DEV void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster; this thread's earlier
+// writes are visible to whoever then sees the phase complete.
+QD_DEV void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// mbar_wait with cluster-scope acquire (arrivals released from other CTAs).
+QD_DEV bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    auto test = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    if (test()) return true;
+    const uint64_t t0 = gtimer();
+    while (!test())
+        if (gtimer() - t0 > limit_ns) return false;
+    return true;
 }
 
 // 32 consecutive fp32 columns of the warp's 32 TMEM lanes (lane i of the

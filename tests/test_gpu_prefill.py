@@ -86,7 +86,8 @@ def test_gemm_f16_vs_float64(lib, M, N, K):
 
 
 @pytest.mark.parametrize("fmt,M,N,K", [(1, 1, 128, 128), (1, 130, 256, 384), (1, 512, 4608, 3584),
-                                       (1, 77, 3584, 18944), (2, 200, 384, 4096), (2, 64, 256, 12288)])
+                                       (1, 77, 3584, 18944), (2, 200, 384, 4096), (2, 64, 256, 12288),
+                                       (1, 600, 384, 512), (1, 1024, 4608, 1024), (2, 300, 1024, 1024)])
 def test_gemm_quant_vs_float64(lib, fmt, M, N, K):
     """In-kernel dequantization: C against a float64 matmul of A and the oracle's dequantized
     weights (INT4: the exact products; INT8: the weights as fp16 after one rounding)."""
