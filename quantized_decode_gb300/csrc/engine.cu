@@ -585,7 +585,7 @@ cudaError_t prefill_chunk(llm_t *h, int m, int pos0) {
         TcGemmArgs g{};
         g.M = m; g.N = N; g.K = K; g.mode = mode; g.c = cc; g.ldc = ldc; g.h = hh; g.ldh = ldh;
         g.err = err; g.wait_ns = 1000000000ull;
-        return launch_tc_gemm_q(st, am, wm, qb, g);
+        return launch_tc_gemm_q(st, am, wm, qb, g, true);
     };
     auto one = [](const void *scale, int rows) {
         TcQuantB q{};

@@ -79,26 +79,48 @@ __global__ void __launch_bounds__(256) k_embed(const uint16_t *embed, const int 
     for (int k = threadIdx.x; k < h; k += blockDim.x) x[(size_t)i * h + k] = bf16_bits_to_float(__ldg(src + k));
 }
 
-__global__ void __launch_bounds__(256) k_rmsnorm(const float *x, const uint16_t *gamma, float eps, int h,
-                                                 uint16_t *out) {
-    __shared__ float red[8];
-    const float *row = x + (size_t)blockIdx.x * h;
+// One CTA per row: float4 loads kept in registers (rows up to 4096 wide),
+// one block reduction, 8-byte stores of four fp16 outputs.
+constexpr int kNormThreads = 128, kNormVec = 8;
+__global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float *x, const uint16_t *gamma, float eps, int h,
+                                                          uint16_t *out) {
+    __shared__ float red[kNormThreads / 32];
+    pdl_launch();  // the GEMM after this kernel may start its weight loads
+    const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)blockIdx.x * h);
+    const int n4 = h >> 2;
+    float4 v[kNormVec];
     float ss = 0.f;
-    for (int k = threadIdx.x; k < h; k += blockDim.x) {
-        const float v = row[k];
-        ss += v * v;
+    auto sq = [](const float4 &t) { return t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w; };
+#pragma unroll
+    for (int j = 0; j < kNormVec; ++j) {
+        const int i = (int)threadIdx.x + j * kNormThreads;
+        v[j] = i < n4 ? row[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += sq(v[j]);
     }
+    for (int i = (int)threadIdx.x + kNormVec * kNormThreads; i < n4; i += kNormThreads) ss += sq(row[i]);
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
     float t = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) t += red[w];
     const float inv = rsqrtf(t / (float)h + eps);
-    uint16_t *o = out + (size_t)blockIdx.x * h;
-    for (int k = threadIdx.x; k < h; k += blockDim.x) {
-        const __half v = __float2half_rn(bf16_bits_to_float(__ldg(gamma + k)) * (row[k] * inv));
-        o[k] = *reinterpret_cast<const uint16_t *>(&v);
+    const uint2 *g = reinterpret_cast<const uint2 *>(gamma);
+    uint2 *o = reinterpret_cast<uint2 *>(out + (size_t)blockIdx.x * h);
+    auto put = [&](int i, const float4 &a) {
+        const uint2 gw = __ldg(g + i);
+        const __half2 lo = __floats2half2_rn(bf16_bits_to_float((uint16_t)(gw.x & 0xFFFFu)) * (a.x * inv),
+                                             bf16_bits_to_float((uint16_t)(gw.x >> 16)) * (a.y * inv));
+        const __half2 hi = __floats2half2_rn(bf16_bits_to_float((uint16_t)(gw.y & 0xFFFFu)) * (a.z * inv),
+                                             bf16_bits_to_float((uint16_t)(gw.y >> 16)) * (a.w * inv));
+        o[i] = make_uint2(h2_as_u32(lo), h2_as_u32(hi));
+    };
+#pragma unroll
+    for (int j = 0; j < kNormVec; ++j) {
+        const int i = (int)threadIdx.x + j * kNormThreads;
+        if (i < n4) put(i, v[j]);
     }
+    for (int i = (int)threadIdx.x + kNormVec * kNormThreads; i < n4; i += kNormThreads) put(i, row[i]);
 }
 
 // One warp per (row, head): heads [0, Hq) queries, then Hkv keys, Hkv values.
@@ -217,6 +239,7 @@ __global__ void __launch_bounds__(128) k_attn_rows(AttnRowsArgs a) {
     constexpr int NT = D / 8;            // n-tiles over d (output)
     extern __shared__ uint4 smem[];
     uint16_t *kv = reinterpret_cast<uint16_t *>(smem);  // [2 buffers][K, V][64 keys][D]
+    pdl_launch();  // the o_proj GEMM after this kernel may start its weight loads
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
     const int h = blockIdx.y, g = h / (a.Hq / a.Hkv);
     const int q0 = blockIdx.x * kAttnRows;
@@ -415,8 +438,9 @@ cudaError_t launch_embed_rows(cudaStream_t stream, const uint16_t *embed, const 
 
 cudaError_t launch_rmsnorm_rows(cudaStream_t stream, const float *x, const uint16_t *gamma, float eps, int n,
                                 int h, uint16_t *out) {
-    if (n <= 0) return cudaErrorInvalidValue;
-    k_rmsnorm<<<n, 256, 0, stream>>>(x, gamma, eps, h, out);
+    if (n <= 0 || h <= 0 || h % 4 || ((uintptr_t)x & 15) || ((uintptr_t)gamma & 7) || ((uintptr_t)out & 7))
+        return cudaErrorInvalidValue;
+    k_rmsnorm<<<n, kNormThreads, 0, stream>>>(x, gamma, eps, h, out);
     return cudaGetLastError();
 }
 

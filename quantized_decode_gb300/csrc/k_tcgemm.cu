@@ -309,7 +309,26 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            int i = 0;
+            pdl_launch();
+            auto load_codes = [&](int s, int kb) {
+                const int x = kb * code_row;
+                if (qb.interleave) {
+                    tma_load_2d(stage_c(s), &P.w[0], x, n0 / 2, &b->full[s]);
+                    tma_load_2d(stage_c(s) + (kTcBN / 2) * code_row, &P.w[1], x, n0 / 2, &b->full[s]);
+                } else {
+                    tma_load_2d(stage_c(s), &P.w[seg], x, seg_row, &b->full[s]);
+                }
+            };
+            // The first stages' weight codes depend on no earlier kernel: they go out before
+            // the dependency wait (programmatic dependent launch), the activations after it.
+            const int pre = nkb < kWStages ? nkb : kWStages;
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(&b->full[i], (uint32_t)(kWActBytes + kTcBN * code_row));
+                load_codes(i, kb0 + i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) tma_load_2d(stage_a(i), &P.a, (kb0 + i) * kTcBK, m0, &b->full[i]);
+            int i = pre;
             for (; i < nkb && !*abort; ++i) {
                 const int s = i % kWStages, kb = kb0 + i;
                 const uint32_t use = (uint32_t)(i / kWStages);
@@ -319,13 +338,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                 }
                 mbar_expect_tx(&b->full[s], (uint32_t)(kWActBytes + kTcBN * code_row));
                 tma_load_2d(stage_a(s), &P.a, kb * kTcBK, m0, &b->full[s]);
-                const int x = kb * code_row;
-                if (qb.interleave) {
-                    tma_load_2d(stage_c(s), &P.w[0], x, n0 / 2, &b->full[s]);
-                    tma_load_2d(stage_c(s) + (kTcBN / 2) * code_row, &P.w[1], x, n0 / 2, &b->full[s]);
-                } else {
-                    tma_load_2d(stage_c(s), &P.w[seg], x, seg_row, &b->full[s]);
-                }
+                load_codes(s, kb);
             }
             b->issued = i;
         }
@@ -464,7 +477,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
             epi_sync();
             if (issuer && live) {
                 tma_store_2d(&P.out, hs, n0 / 2, m0);
-                bulk_commit_wait_all();
+                bulk_commit_wait_read();
             }
         } else if (C == 1) {
             float *cs = reinterpret_cast<float *>(base);  // [T][128]
@@ -482,7 +495,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
             if (issuer && live) {
                 if (a.mode == kEpiAdd) tma_reduce_add_2d(&P.out, cs, n0, m0);
                 else tma_store_2d(&P.out, cs, n0, m0);
-                bulk_commit_wait_all();
+                bulk_commit_wait_read();
             }
         } else {
             // split K: CTA r owns prompt columns [r W, r W + W), W = T / C; warp half ch takes
@@ -557,7 +570,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
             if (issuer && ok) {
                 if (a.mode == kEpiAdd) tma_reduce_add_2d(&P.out, os, n0, m0 + rank * W);
                 else tma_store_2d(&P.out, os, n0, m0 + rank * W);
-                bulk_commit_wait_all();
+                bulk_commit_wait_read();
             }
         }
     }
@@ -683,7 +696,7 @@ int tc_gemm_q_split(int M, int N, int K, int mode, int n_sm) {
 }
 
 cudaError_t launch_tc_gemm_q(cudaStream_t stream, const CUtensorMap &a_map, const CUtensorMap (&w_maps)[3],
-                             const TcQuantB &b, const TcGemmArgs &a) {
+                             const TcQuantB &b, const TcGemmArgs &a, bool pdl) {
     if (a.M < 1 || a.N < kTcBN || a.N % kTcBN || a.K < kTcBK || a.K % kTcBK) return cudaErrorInvalidValue;
     if (b.fmt != kFmtInt4 && b.fmt != kFmtInt8) return cudaErrorInvalidValue;
     if (b.fmt == kFmtInt4 && a.K % kGroup) return cudaErrorInvalidValue;
@@ -718,7 +731,7 @@ cudaError_t launch_tc_gemm_q(cudaStream_t stream, const CUtensorMap &a_map, cons
     if ((e = tc_out_map(&p.out, a, kWT / p.ksplit)) != cudaSuccess) return e;
     LaunchCfg lc{};
     lc.stream = stream;
-    lc.pdl = false;
+    lc.pdl = pdl;
     const dim3 grid((unsigned)p.ksplit, (unsigned)((a.M + kWT - 1) / kWT), (unsigned)(a.N / kTcBN));
     return launch_kc(lc, k_tc_gemm_q, grid, dim3(kWThreads), kWSmemBytes, p.ksplit, p);
 }

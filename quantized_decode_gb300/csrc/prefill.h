@@ -64,8 +64,10 @@ cudaError_t tc_weight_map(CUtensorMap *map, const void *codes, int fmt, uint64_t
 // zero).  cols % 64 == 0, base 16-byte aligned.
 cudaError_t tc_act_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols);
 // a_map from tc_act_map, w_maps from tc_weight_map.  kEpiSwiGlu needs interleave.
+// With pdl the launch may overlap the previous kernel of the stream: only the
+// weight codes are read before the kernel waits for it.
 cudaError_t launch_tc_gemm_q(cudaStream_t stream, const CUtensorMap &a_map, const CUtensorMap (&w_maps)[3],
-                             const TcQuantB &b, const TcGemmArgs &a);
+                             const TcQuantB &b, const TcGemmArgs &a, bool pdl = false);
 // K split of a launch (1, 2 or 4) on a device with n_sm SMs.
 int tc_gemm_q_split(int M, int N, int K, int mode, int n_sm);
 

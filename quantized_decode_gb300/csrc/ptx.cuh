@@ -76,10 +76,12 @@ QD_DEV void tma_reduce_add_2d(const CUtensorMap *map, const void *src, int x, in
                  "r"(x), "r"(y), "r"(smem_u32(src))
                  : "memory");
 }
-// Close this thread's bulk async-group and wait until its operations are complete.
-QD_DEV void bulk_commit_wait_all() {
+// Close this thread's bulk async-group and wait until its operations have read
+// their shared-memory sources (the writes to global memory complete on their own
+// and are visible to later kernels of the stream).
+QD_DEV void bulk_commit_wait_read() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 QD_DEV void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
