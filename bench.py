@@ -37,6 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 # one it was measured on, so a changed kernel reports traffic null.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic_7b.md")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 ORACLE_BUDGET_S = 240.0   # bound on the oracle's timed steps (reference arm)
 
 
@@ -226,6 +227,83 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s burst (fp16 has the same dense rate): the peak of a GEMM timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_gemm_shapes(cfg):
+    """(name, N, K) of the four GEMMs of a prefill layer (gate and up as one 2F-row GEMM)."""
+    d = cfg.head_dim
+    return [("qkv", (cfg.n_q_heads + 2 * cfg.n_kv_heads) * d, cfg.hidden), ("o_proj", cfg.hidden, cfg.n_q_heads * d),
+            ("gate_up", 2 * cfg.mlp, cfg.hidden), ("down", cfg.hidden, cfg.mlp)]
+
+
+def prefill_gemms(cfg, M=512, reps=5, batch=10):
+    """The prefill GEMM (llm_op_gemm_quant: weight codes dequantized inside the tcgen05 kernel)
+    at the shapes of one layer of an M-row prompt: batches of `batch` back-to-back launches timed
+    with CUDA events (median over reps batches), cycling through copies of the weights and
+    activations that together exceed L2, so every launch reads its operands from HBM.  Seeded
+    codes, unit scales: the timing does not depend on the values.  gate/up is timed with the
+    plain store epilogue (the engine's SwiGLU epilogue writes half the bytes)."""
+    import torch
+    from quantized_decode_gb300 import _lib
+    from synth import model as sm
+    lib = _lib.load()
+    peak, peak_kind = measured_tensor_peak()
+    int4 = cfg.weight_format == sm.FMT_INT4_G128
+    fmt = 1 if int4 else 2
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    out = {}
+    for name, N, K in prefill_gemm_shapes(cfg):
+        per = N * K // (2 if int4 else 1) + M * K * 2
+        copies = max(2, -(-300_000_000 // per))
+        bufs = []
+        for _ in range(copies):
+            A = (torch.randn(M, K, device="cuda", generator=g) * 0.5).half()
+            if int4:
+                w = torch.randint(-2**31, 2**31 - 1, (N * K // 8,), dtype=torch.int32, device="cuda", generator=g)
+                s_ = torch.full((N * K // 128,), 0x3C00, dtype=torch.int16, device="cuda")
+            else:
+                w = torch.randint(-127, 128, (N * K,), dtype=torch.int8, device="cuda", generator=g)
+                s_ = torch.full((N,), 1.0 / 64, dtype=torch.float32, device="cuda")
+            bufs.append((A, w, s_))
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        it = [0]
+
+        def run():
+            A, w, s_ = bufs[it[0] % copies]
+            it[0] += 1
+            rc = lib.llm_op_gemm_quant(fmt, A.data_ptr(), w.data_ptr(), s_.data_ptr(), M, N, K, C.data_ptr(), None)
+            if rc != 0:
+                raise RuntimeError(f"llm_op_gemm_quant {name}: {rc}")
+        for _ in range(3):
+            run()
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(batch):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / batch)
+        us = float(np.median(ts))
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        out[name] = {"M": M, "N": N, "K": K, "us": round(us, 2), "tflops": round(tf, 1), "frac": round(tf / peak, 3)}
+        del bufs, C
+        torch.cuda.empty_cache()
+    out["peak_tflops"] = peak
+    out["peak_kind"] = peak_kind
+    return out
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def oracle_decode(cfg, seed, T0, n_warm, n_steps, rec=None, budget_s=None):
@@ -332,9 +410,12 @@ def run_ours(args):
             runs.append((time.perf_counter() - t0) * 1e3)
         ttft_ms = float(np.median(runs))
         eng.reset()
+    pf_gemms = None
+    if not args.no_ttft and rank == 0:
+        pf_gemms = prefill_gemms(cfg)
     if args.ttft_only:
         if rank == 0:
-            print(json.dumps({"ttft_ms": None if ttft_ms is None else round(ttft_ms, 2)}))
+            print(json.dumps({"ttft_ms": None if ttft_ms is None else round(ttft_ms, 2), "prefill_gemms": pf_gemms}))
         eng.close()
         return
 
@@ -617,6 +698,7 @@ def run_ours(args):
         "kernels_in_graph": timeline,
         "kernels_serialised": breakdown,
         "ttft_ms": None if ttft_ms is None else round(ttft_ms, 2),
+        "prefill_gemms": pf_gemms,
         "kv_sweep_ms_per_token": kv_sweep,
         "long_context_ms_per_token": long_ctx,
         "eager_ms_per_token": None if eager_ms is None else round(eager_ms, 4),

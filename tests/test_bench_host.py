@@ -58,3 +58,16 @@ def test_batch_bytes_reads_weights_once(bench, cfg):
     rkv = cfg.n_kv_heads * cfg.head_dim
     kv = lambda t: cfg.n_layers * 2 * rkv * 2 * (t + 1)  # noqa: E731
     assert bench.batch_bytes(cfg, [T, 17, 40]) == bench.algorithmic_bytes(cfg, T) + kv(17) + kv(40)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen2.5-7b", "qwen3-8b"])
+def test_prefill_gemm_shapes_cover_every_linear_weight(bench, name):
+    """The four prefill GEMMs of a layer (QKV stacked, gate and up as one) multiply every linear
+    weight of the layer exactly once."""
+    cfg = sm.CONFIGS[name]
+    q, kv = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    weights = cfg.hidden * (q + 2 * kv) + q * cfg.hidden + 3 * cfg.mlp * cfg.hidden
+    shapes = bench.prefill_gemm_shapes(cfg)
+    assert [s[0] for s in shapes] == ["qkv", "o_proj", "gate_up", "down"]
+    assert sum(n * k for _, n, k in shapes) == weights
+    assert all(n % 128 == 0 and k % 128 == 0 for _, n, k in shapes)
