@@ -127,9 +127,12 @@ int llm_op_gemm_f16(const void *A, const void *B, int32_t M, int32_t N, int32_t 
  * weights dequantized inside the kernel (the prefill GEMM as the engine runs
  * it): W is fmt 1 = INT4 group-128 (w: LLM_LAYOUT_INT4_VALUESHUFFLE words
  * [N][K/8], s: bf16 [N][K/128]) or fmt 2 = INT8 per row (w: int8 [N][K],
- * s: fp32 [N]); each code tile is converted to fp16 in shared memory (exact
- * for INT4, one rounding for INT8) and never written back.  A: fp16 [M][K],
- * C: fp32 [M][N], 16-byte aligned.  M >= 1, N % 128 == 0, K % 128 == 0.      */
+ * s: fp32 [N]); each code tile is converted to fp16 in tensor memory and
+ * never written back (INT4: code x group scale, exact; INT8: the code, exact,
+ * with the fp32 row scale applied to the fp32 sum).  A: fp16 [M][K],
+ * C: fp32 [M][N], 16-byte aligned.  M >= 1, N % 128 == 0, K % 128 == 0.  The
+ * result does not depend on the run (partial sums of a split K are added in a
+ * fixed order).                                                              */
 int llm_op_gemm_quant(int32_t fmt, const void *A, const void *w, const void *s, int32_t M, int32_t N,
                       int32_t K, float *C, void *stream);
 

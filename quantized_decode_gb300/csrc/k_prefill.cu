@@ -7,7 +7,8 @@
 //
 // fp16 holds every INT4 weight exactly: a code has at most 3 significant bits
 // and a bf16 scale 8, and 11 fit fp16's significand (scales above 2^-14 stay
-// normal).  INT8 weights (7 + 24 bits) round to fp16.
+// normal).  INT8 weights dequantized to fp16 (7 + 24 bits) round once; the
+// prefill GEMM instead keeps INT8 codes exact and scales each row's fp32 sum.
 #include "common.cuh"
 #include "launch_util.cuh"
 #include "prefill.h"

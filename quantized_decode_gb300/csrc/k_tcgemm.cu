@@ -375,8 +375,6 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
         const int G = a.K / kGroup;
         const uint16_t *srow = int4 && have_row ? reinterpret_cast<const uint16_t *>(qb.scale[wseg]) + (size_t)wrow * G
                                                 : nullptr;
-        float sc8 = 0.f;
-        if (!int4 && have_row) sc8 = __ldg(reinterpret_cast<const float *>(qb.scale[wseg]) + wrow);
         // INT4 group scales four groups ahead in a register ring (group g in sc[g & 3])
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         const int g0 = kb0 >> 1;
@@ -412,18 +410,19 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                 }
                 if ((kb & 1) && srow && g + 4 < G) sc[g & 3] = bf16_bits_to_float(__ldg(srow + g + 4));
             } else {
+                // INT8: the codes themselves (exact in fp16: b ^ 0x80 = c + 128 under the exponent
+                // of 1024, minus 1152); the row's fp32 scale multiplies the accumulator instead
                 const uint8_t *src = stage_c(s) + (size_t)t * code_row + 32 * half;
+                const __half2 k1152 = __floats2half2_rn(1152.f, 1152.f);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint4 w = *reinterpret_cast<const uint4 *>(src + 16 * j);
                     const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const uint32_t x = wd[e];
-                        r[8 * j + 2 * e] = h2_as_u32(
-                            __floats2half2_rn((float)(int8_t)(x & 0xFF) * sc8, (float)(int8_t)((x >> 8) & 0xFF) * sc8));
-                        r[8 * j + 2 * e + 1] = h2_as_u32(
-                            __floats2half2_rn((float)(int8_t)((x >> 16) & 0xFF) * sc8, (float)(int8_t)(x >> 24) * sc8));
+                        const uint32_t x = wd[e] ^ 0x80808080u;
+                        r[8 * j + 2 * e] = h2_as_u32(__hsub2(u32_as_h2(prmt(x, 0x64646464u, 0x4140u)), k1152));
+                        r[8 * j + 2 * e + 1] = h2_as_u32(__hsub2(u32_as_h2(prmt(x, 0x64646464u, 0x4342u)), k1152));
                     }
                 }
             }
@@ -441,6 +440,16 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
     if (warp >= 2) {
         const int q = warp & 3, ch = (warp - 2) >> 2, row = 32 * q + lane;
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        // INT8: the fp32 scale of this lane's weight row multiplies its accumulator
+        float rs = 1.f;
+        if (!int4) {
+            int es = seg, er = seg_row + row;
+            if (qb.interleave) {
+                es = row < kTcBN / 2 ? 0 : 1;
+                er = n0 / 2 + (row & (kTcBN / 2 - 1));
+            }
+            rs = __ldg(reinterpret_cast<const float *>(qb.scale[es]) + er);
+        }
         const bool issuer = warp == 2 && lane == 0;
         auto epi_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kWEpiThreads) : "memory"); };
         const bool have = mbar_wait(&b->done, 0, a.wait_ns);
@@ -459,7 +468,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                     float v[32];
                     tmem_ld32(trow + c, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) xu[(c + i) * 64 + j] = v[i];
+                    for (int i = 0; i < 32; ++i) xu[(c + i) * 64 + j] = v[i] * rs;
                 }
             }
             epi_sync();
@@ -470,7 +479,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                     tmem_ld32(trow + c, g);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        hs[(c + i) * 64 + j] = __half_as_ushort(__float2half_rn(silu_f(g[i]) * xu[(c + i) * 64 + j]));
+                        hs[(c + i) * 64 + j] = __half_as_ushort(__float2half_rn(silu_f(g[i] * rs) * xu[(c + i) * 64 + j]));
                 }
             }
             fence_proxy_async_smem();
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                     float v[32];
                     tmem_ld32(trow + c, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) cs[(c + i) * kTcBN + row] = v[i];
+                    for (int i = 0; i < 32; ++i) cs[(c + i) * kTcBN + row] = v[i] * rs;
                 }
             }
             fence_proxy_async_smem();
@@ -562,7 +571,7 @@ __global__ void __launch_bounds__(kWThreads, 1) k_tc_gemm_q(const __grid_constan
                         for (int i = 0; i < 32; ++i) v[i] = r == 0 ? p[(size_t)i * kTcBN] : v[i] + p[(size_t)i * kTcBN];
                     }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) os[(c + i) * kTcBN + row] = v[i];
+                    for (int i = 0; i < 32; ++i) os[(c + i) * kTcBN + row] = v[i] * rs;
                 }
             }
             fence_proxy_async_smem();

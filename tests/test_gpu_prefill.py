@@ -89,8 +89,9 @@ def test_gemm_f16_vs_float64(lib, M, N, K):
                                        (1, 77, 3584, 18944), (2, 200, 384, 4096), (2, 64, 256, 12288),
                                        (1, 600, 384, 512), (1, 1024, 4608, 1024), (2, 300, 1024, 1024)])
 def test_gemm_quant_vs_float64(lib, fmt, M, N, K):
-    """In-kernel dequantization: C against a float64 matmul of A and the oracle's dequantized
-    weights (INT4: the exact products; INT8: the weights as fp16 after one rounding)."""
+    """In-kernel dequantization: C against a float64 matmul of A and the exactly dequantized
+    weights (INT4: the oracle's unpacking x the bf16 group scale; INT8: code x fp32 row scale, the
+    kernel multiplying the row's fp32 sum of code x activation by the scale)."""
     import quantized_decode_gb300 as qd
     a = _f16(41, M * 7 + K, M, K, 1.0)
     if fmt == 1:
@@ -101,7 +102,7 @@ def test_gemm_quant_vs_float64(lib, fmt, M, N, K):
     else:
         codes, scales = sm.quantized_tensor(sm.FMT_INT8_ROW, 43, N + K, N, K)
         w = to_dev(np.ascontiguousarray(codes, np.int8))
-        wref = (codes.astype(np.float32) * scales.astype(np.float32)[:, None]).astype(np.float16).astype(np.float64)
+        wref = codes.astype(np.float64) * scales.astype(np.float32).astype(np.float64)[:, None]
     s = to_dev(scales)
     ad = to_dev(a)
     c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
