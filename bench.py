@@ -508,7 +508,7 @@ def run_ours(args):
         finally:
             eng_l.close()
 
-    other_ms = no_pdl_ms = fused_ms = eager_ms = sampling_ms = act8_ms = None
+    other_ms = no_pdl_ms = fused_ms = eager_ms = sampling_ms = act8_ms = ofold_ms = None
     if not args.no_variants:
         # ---- graph replay with o_proj, gate/up and down on int8 activations (opt-in, INT4 models)
         try:
@@ -573,6 +573,22 @@ def run_ours(args):
             torch.cuda.synchronize()
             fused_ms = round(s6.elapsed_time(e6) / n_pdl, 4)
             eng.set_fused_attention(False)
+        except LLMError:
+            pass
+
+        # ---- graph replay with o_proj folded into the attention clusters (the other setting of
+        # llm_set_o_fold, where the attention plan allows it)
+        try:
+            fold_default = eng.o_fold()
+            eng.set_o_fold(not fold_default)
+            enqueue(3)
+            s9, e9 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s9.record(stream)
+            enqueue(n_pdl)
+            e9.record(stream)
+            torch.cuda.synchronize()
+            ofold_ms = {"o_fold": not fold_default, "ms_per_token": round(s9.elapsed_time(e9) / n_pdl, 4)}
+            eng.set_o_fold(fold_default)
         except LLMError:
             pass
 
@@ -704,6 +720,7 @@ def run_ours(args):
         "eager_ms_per_token": None if eager_ms is None else round(eager_ms, 4),
         "graph_no_pdl_ms_per_token": None if no_pdl_ms is None else round(no_pdl_ms, 4),
         "fused_qkv_attention_ms_per_token": fused_ms,
+        "o_fold_other_setting": ofold_ms,
         "sampling_ms_per_token": sampling_ms,
         "act_int8_ms_per_token": act8_ms,
         ("chain_ms_per_token" if args.step == "persistent" else "persistent_ms_per_token"):

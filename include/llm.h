@@ -307,6 +307,23 @@ int llm_set_persistent(llm_t *h, int32_t on);
  * the kernel does not take), LLM_ERR_CUDA.                                  */
 int llm_set_fused_mlp(llm_t *h, int32_t on);
 
+/* o_proj folded into the decode attention: where the attention runs as one
+ * cluster per KV head (INT4 weights, head_dim 128), that cluster multiplies
+ * its heads' outputs by its columns of W_o (copied into shared memory while
+ * the cluster merges its split-K partials) and adds each row's partial sum
+ * into an engine-owned buffer with 64-bit fixed-point reductions in L2
+ * (2^-32 units, exact, independent of the order of the CTAs); the gate/up
+ * GEMV adds that buffer to the residual before its RMSNorm and the down GEMV
+ * folds it into the residual and zeroes it.  The o_proj kernel is then not
+ * launched.  1: on; 0 (default): o_proj as its own GEMV.  Not with the fused
+ * MLP block, the fused QKV + attention kernel or int8 activations (those
+ * steps keep the o_proj GEMV).  Re-captures the graph.  Errors: LLM_ERR_ARG
+ * (null handle, or 1 where the attention plan or shapes do not allow it),
+ * LLM_ERR_CUDA.                                                             */
+int llm_set_o_fold(llm_t *h, int32_t on);
+/* The current llm_set_o_fold setting in *on (1 or 0).  LLM_ERR_ARG on null.  */
+int llm_get_o_fold(llm_t *h, int32_t *on);
+
 /* Launch kinds of a decode step, in launch order (the step as last captured):
  * writes kinds[i] for each launch (HOST, capacity cap) and *n = launches; 0
  * for the persistent kernel.  Kinds: */

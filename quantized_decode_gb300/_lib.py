@@ -92,6 +92,8 @@ SIGNATURES = {
     "llm_debug_step_wait": (i32, [vp, i32, i64]),
     "llm_set_l2_prefetch": (i32, [vp, i32]),
     "llm_set_fused_mlp": (i32, [vp, i32]),
+    "llm_set_o_fold": (i32, [vp, i32]),
+    "llm_get_o_fold": (i32, [vp, ctypes.POINTER(ctypes.c_int32)]),
     "llm_step_kinds": (i32, [vp, vp, i32, ctypes.POINTER(i32)]),
     "llm_set_act_int8": (i32, [vp, i32]),
     "llm_op_gemv_int4_a8": (i32, [vp, vp, i32, i32, vp, vp, vp]),

@@ -6,6 +6,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "gemv.cuh"
 #include "ptx.cuh"
 
 namespace qd {
@@ -87,7 +88,8 @@ struct AttnInputs {
 // earlier kernel).  The CTA's first page copies go out before the hook, or
 // (LATE) when the hook calls issue_pages() -- the hook may use the page ring's
 // shared memory until then.  smem: ring_bytes<D>() of dynamic shared memory.
-template <int G, int D, int CS, bool QS, bool LATE, class Hook>
+// FOLD: the o_proj fold of a.fold is compiled in (the kernel without it has none of its code).
+template <int G, int D, int CS, bool QS, bool LATE, class Hook, bool FOLD = false>
 QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
     constexpr int CH = D / 8;      // 16-byte chunks per row
     constexpr int PAGE = 16 * D;   // bf16 elements of one K (or V) page slice
@@ -99,6 +101,7 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
     __shared__ float s_fw[8][32], s_fl[8][32];
     __shared__ float s_st[2][kWarps];
     __shared__ int s_last;
+    __shared__ uint64_t s_wbar;  // o_proj fold: the W_o slice has landed
     __shared__ uint64_t s_pbar[kWarps][kWRing];  // page slot arrivals (TMA transaction bytes)
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -299,7 +302,38 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
             s_cl[h] = den;
         }
     }
+    const bool fold = FOLD && C == 1 && a.out != nullptr && a.fold != nullptr;
+    const int fold_rows = fold ? a.fold->hidden / CS : 0;
+    constexpr int kFoldRowBytes = G * D / 2;  // one W_o row's INT4 codes for this KV head's columns
+    if constexpr (FOLD) {
+        if (fold) ptx::fence_proxy_async_smem();  // the warp merge's writes come before the copies' writes
+    }
     cluster.sync();
+    // o_proj fold: this CTA's rows of W_o (its KV head's columns) into the free page ring,
+    // landing while the cluster merges
+    // ring layout of the fold: W_o rows | outputs fp16 | outputs fp32 | group scales | this CTA's
+    // merged outputs (read by the other CTAs of the cluster; the same offset in every CTA)
+    constexpr int kFoldGroups = G * D / kGroup;  // scale groups of a row in this KV head's columns
+    uint16_t *fold_sc = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(smem) + (size_t)fold_rows * kFoldRowBytes +
+                                                     (size_t)G * D * 6);
+    float *s_vec = reinterpret_cast<float *>(
+        reinterpret_cast<char *>(smem) +
+        (((size_t)fold_rows * kFoldRowBytes + (size_t)G * D * 6 + (size_t)fold_rows * kFoldGroups * 2 + 15) & ~(size_t)15));
+    if constexpr (FOLD) {
+    if (fold && tid == 0) {
+        ptx::mbar_init(&s_wbar, 1);
+        ptx::mbar_fence_init();
+        ptx::mbar_expect_tx(&s_wbar, (uint32_t)(fold_rows * kFoldRowBytes));
+        ptx::tma_load_2d(smem, &a.fold->wo_map, g * (kFoldRowBytes / 4), rank * fold_rows, &s_wbar);
+    }
+    if constexpr (kFoldGroups > 0) {
+        if (fold) {  // this CTA's rows' scales (static weights), read once, in flight during the merge
+            const int groups = a.Hq * D / kGroup, r0 = rank * fold_rows;
+            for (int u = tid; u < fold_rows * kFoldGroups; u += kNT)
+                fold_sc[u] = __ldg(a.fold->so + (size_t)(r0 + u / kFoldGroups) * groups + g * kFoldGroups + u % kFoldGroups);
+        }
+    }
+    }
 
     // ---- merge the CS CTAs of the cluster through distributed shared memory;
     // rank r merges an equal slice of the G*D outputs into the cluster's partial,
@@ -325,6 +359,12 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
             }
             if (direct) {  // den > 0: the cluster holds every token
                 const float v = num * (1.f / den);
+                if constexpr (FOLD) {
+                    if (fold) {
+                        s_vec[idx - lo] = v;
+                        continue;
+                    }
+                }
                 a.out[(size_t)(g * G) * D + idx] = v;
                 st_ss += v * v;
                 st_mx = fmaxf(st_mx, fabsf(v));
@@ -337,6 +377,70 @@ QD_DEV void attn_cta(const AttnArgs &a, uint16_t *smem, Hook &&hook) {
                 a.part_ml[(slot * G + h) * 2 + 1] = den;
             }
         }
+    }
+    if constexpr (FOLD) {
+    if (fold) {
+        // every CTA's merged slice is in its s_vec; the merge's reads of s_co are done
+        cluster.sync();
+        const int per = (G * D + CS - 1) / CS;
+        // the cluster's G*D outputs as fp16 scaled by 2^-e (|x| <= 1) after the W_o slice
+        __half *xh = reinterpret_cast<__half *>(reinterpret_cast<char *>(smem) + (size_t)fold_rows * kFoldRowBytes);
+        float *xf = reinterpret_cast<float *>(xh + G * D);  // fp32 copy of the gathered vector
+        float mx = 0.f;
+        for (int idx = tid; idx < G * D; idx += kNT) {
+            const float v = cluster.map_shared_rank(s_vec, (unsigned)(idx / per))[idx % per];
+            xf[idx] = v;
+            mx = fmaxf(mx, fabsf(v));
+        }
+        // this CTA's reads of its peers' shared memory are done; leave only after all peers' are
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        mx = warp_max(mx);
+        if (lane == 0) s_st[1][warp] = mx;
+        __syncthreads();
+        float gmx = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) gmx = fmaxf(gmx, s_st[1][w]);
+        int e = 0;
+        if (gmx > 0.f) frexpf(gmx, &e);  // gmx < 2^e
+        const float down = ldexpf(1.f, -e), up = ldexpf(1.f, e);
+        for (int idx = tid; idx < G * D; idx += kNT) xh[idx] = __float2half_rn(xf[idx] * down);
+        __syncthreads();
+        const bool landed = ptx::mbar_wait(&s_wbar, 0, kPageWaitNs);
+        if (!landed && tid == 0) atomicCAS(a.err, kErrNone, kErrTimeout);
+        // warp w: rows [w R, w R + R) of the CTA's slice; lane l < G*D/32: codes 32 l .. 32 l + 31
+        constexpr int kUnits = G * D / 32;
+        const int R = fold_rows / kWarps, r0 = rank * fold_rows;
+        const uint4 *wq = reinterpret_cast<const uint4 *>(smem);
+        const uint4 *xq = reinterpret_cast<const uint4 *>(xh);
+        const int ul = lane < kUnits ? lane : 0;
+        const uint4 x[4] = {xq[4 * ul], xq[4 * ul + 1], xq[4 * ul + 2], xq[4 * ul + 3]};
+        // four rows at a time: independent dot products and reductions in flight together
+        for (int i0 = warp * R; landed && i0 < warp * R + R; i0 += 4) {
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k;
+                v[k] = 0.f;
+                if (i < warp * R + R && lane < kUnits)
+                    v[k] = int4_unit_dot(wq[(size_t)i * kUnits + lane], x) *
+                           bf16_bits_to_float(fold_sc[i * kFoldGroups + lane / 4]);
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o2);
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (i0 + k < warp * R + R)
+                        atomicAdd(reinterpret_cast<unsigned long long *>(a.fold->out + r0 + i0 + k),
+                                  (unsigned long long)delta_to_fixed(v[k] * up));
+            }
+        }
+        if (!landed) ptx::mbar_wait(&s_wbar, 0, kPageWaitNs);  // copies still in flight land first
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        return;
+    }
     }
     if (direct) {
         // this CTA's reads of its peers' shared memory are done: arrive now and

@@ -74,6 +74,10 @@ struct llm_t {
     char *mlp_buf = nullptr;    // repacked down codes (+ INT4 scales) of every layer
     size_t mlp_w_bytes = 0, mlp_s_bytes = 0;  // per layer
     long long *mlp_d = nullptr;  // fixed point, 2^-32 units
+    long long *o_d = nullptr;    // o_proj folded into the attention: its pending output (fixed point)
+    AttnFold *o_fold_args = nullptr;  // per layer, device memory
+    bool o_fold_ok = false;      // the attention plan and shapes allow the fold
+    bool o_fold = false;         // llm_set_o_fold
     std::vector<int32_t> kinds; // kind of every launch of the captured step (llm_step_kinds)
     bool fused_ok = false;      // the model fits the fused QKV + attention kernel
     bool fused = false;         // llm_set_fused_attention
@@ -130,7 +134,8 @@ void free_all(llm_t *h) {
                     h->attn, h->u, h->logits, h->head_cnt, h->attn_cnt, h->lm_counter,
                     h->lm_part_idx, h->part_o, h->part_ml, h->lm_part_val, h->stats, h->kv_new,
                     h->d_layers, h->d_maps, h->step_sync, h->prof, h->pf_x, h->pf_raw, h->pf_a, h->pf_u,
-                    h->pf_qh, h->pf_ql, h->pf_tok, h->samp_scratch, h->mlp_buf, h->mlp_d};
+                    h->pf_qh, h->pf_ql, h->pf_tok, h->samp_scratch, h->mlp_buf, h->mlp_d, h->o_d,
+                    h->o_fold_args};
     for (void *b : bufs)
         if (b) cudaFree(b);
     if (h->pinned) cudaFreeHost(h->pinned);
@@ -226,6 +231,9 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         return p;
     };
     const bool fmlp = h->mlp_fused && !h->act_int8;  // int8 activations keep the separate GEMVs
+    // o_proj inside the attention clusters: its rows land in o_d, which gate/up adds to x
+    // (computing its RMSNorm statistics itself) and down folds into the residual and zeroes
+    const bool ofold = h->o_fold && !fmlp && !h->fused && !h->act_int8;
     float *st_attn = h->stats, *st_o = h->stats + 2 * kStatSlots;
     float *st_gu = h->stats + 4 * kStatSlots, *st_down = h->stats + 6 * kStatSlots;
     auto mark = [&]() -> cudaError_t { return ev ? cudaEventRecord(ev[k++], h->stream) : cudaSuccess; };
@@ -278,6 +286,10 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         aa.part_o = h->part_o; aa.part_ml = h->part_ml; aa.counter = h->attn_cnt;
         aa.out = h->attn; aa.err = &h->st->err;
         aa.kv_new = h->kv_new; aa.stats_out = st_attn;
+        if (ofold) {
+            aa.fold = h->o_fold_args + l;
+            aa.stats_out = nullptr;
+        }
         // The step's first kernel reads the position before its dependency wait,
         // so it starts only after the previous step has ended (no early launch).
         LaunchCfg lc = h->lc;
@@ -307,8 +319,12 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
             o.fold = h->mlp_d;
             o.fold_add = l > 0;
         }
-        o.tl = slot(LLM_KIND_O_PROJ);
-        if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), o)) != cudaSuccess) return e;
+        if (ofold) {
+            if ((e = mark()) != cudaSuccess) return e;  // the o_proj region of llm_profile_step: empty
+        } else {
+            o.tl = slot(LLM_KIND_O_PROJ);
+            if ((e = mark()) != cudaSuccess || (e = launch_gemv(h->lc, gemv_fmt(h), o)) != cudaSuccess) return e;
+        }
 
         if (fmlp) {
             MlpArgs m{};
@@ -332,7 +348,8 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         gu.mode = 2; gu.w = L.wg; gu.s = L.sg; gu.w2 = L.wu; gu.s2 = L.su;
         gu.N = c.mlp; gu.K = c.hidden; gu.x = h->x;
         gu.gamma = (const uint16_t *)L.mlp_norm; gu.eps = c.rms_eps; gu.y = h->u;
-        gu.stats_in = st_o; gu.stats_out = st_gu;
+        gu.stats_in = ofold ? nullptr : st_o; gu.stats_out = st_gu;
+        gu.x2 = ofold ? h->o_d : nullptr;
         gu.tl = slot(LLM_KIND_GATE_UP);
         if (h->l2pf & kL2pfGuDown) {  // down of this layer
             gu.pf[0] = {L.wd, code_bytes(h, c.hidden, c.mlp)};
@@ -343,6 +360,10 @@ cudaError_t enqueue_step(llm_t *h, cudaEvent_t *ev = nullptr, unsigned long long
         GemvArgs dn{};
         dn.mode = 1; dn.w = L.wd; dn.s = L.sd; dn.N = c.hidden; dn.K = c.mlp; dn.x = h->u; dn.y = h->x;
         dn.stats_in = st_gu; dn.stats_out = st_down;
+        if (ofold) {
+            dn.fold = h->o_d;
+            dn.fold_add = 1;
+        }
         dn.stats_gamma = (const uint16_t *)(l + 1 < c.n_layers ? h->layers[l + 1].attn_norm : h->w.final_norm);
         dn.tl = slot(LLM_KIND_DOWN);
         if ((h->l2pf & kL2pfDownNext) && l + 1 < c.n_layers) {  // the next layer's QKV and o_proj codes
@@ -750,6 +771,7 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
     h->attn_cs = ap.cs;
     h->fused_ok = qkv_attn_fusable(h->fmt, c.n_q_heads, c.n_kv_heads, d, c.hidden, c.qk_norm != 0, ap);
     h->fused = false;  // measured slower than the separate kernels at 7B (1.83 vs 1.69 ms/token)
+    h->o_fold_ok = attn_fold_ok(h->fmt, c.n_q_heads, c.n_kv_heads, d, c.hidden, ap);
     h->lm_grid = lm_head_grid(h->lc, c.vocab);
     const int P_alloc = h->P > n_sm / c.n_kv_heads ? h->P : n_sm / c.n_kv_heads + 1;
     const int lm_alloc = h->lm_grid > n_sm ? h->lm_grid : n_sm;
@@ -825,6 +847,25 @@ int llm_create(const llm_config *cfg, const llm_weights *weights, void *cuda_str
         h->mlp_fused = c.hidden <= 2048;
     }
 
+    // o_proj folded into the attention: its pending output, zero between steps
+    if (h->o_fold_ok) {
+        std::vector<AttnFold> fa((size_t)c.n_layers);
+        const AttnPlan ap{h->P, h->attn_cs};
+        if (dalloc(&h->o_d, c.hidden) != cudaSuccess ||
+            cudaMemsetAsync(h->o_d, 0, (size_t)c.hidden * sizeof(long long), h->stream) != cudaSuccess ||
+            cudaMalloc((void **)&h->o_fold_args, fa.size() * sizeof(AttnFold)) != cudaSuccess)
+            return fail(LLM_ERR_CUDA);
+        for (int l = 0; l < c.n_layers; ++l)
+            if (attn_fold_args(fa[l], h->layers[l].wo, (const uint16_t *)h->layers[l].so, h->o_d, c.n_q_heads,
+                               c.n_kv_heads, d, c.hidden, ap) != cudaSuccess)
+                return fail(LLM_ERR_CUDA);
+        if (cudaMemcpyAsync(h->o_fold_args, fa.data(), fa.size() * sizeof(AttnFold), cudaMemcpyHostToDevice,
+                            h->stream) != cudaSuccess ||
+            cudaStreamSynchronize(h->stream) != cudaSuccess)
+            return fail(LLM_ERR_CUDA);
+        h->o_fold = false;
+    }
+
     if (plan_step(h, n_sm) != LLM_OK) return fail(LLM_ERR_CUDA);
     h->pf_ok = prefill_shapes_ok(c);
 
@@ -861,6 +902,20 @@ int llm_set_persistent(llm_t *h, int32_t on) {
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->persistent = on != 0;
     return capture(h);
+}
+
+int llm_set_o_fold(llm_t *h, int32_t on) {
+    if (!h || (on && !h->o_fold_ok)) return LLM_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
+    h->o_fold = on != 0;
+    // o_d is zero between completed steps either way: each layer's down zeroes it
+    return capture(h);
+}
+
+int llm_get_o_fold(llm_t *h, int32_t *on) {
+    if (!h || !on) return LLM_ERR_ARG;
+    *on = h->o_fold ? 1 : 0;
+    return LLM_OK;
 }
 
 int llm_set_fused_mlp(llm_t *h, int32_t on) {
@@ -1040,6 +1095,9 @@ int llm_reset(llm_t *h) {
     // a step that failed part-way leaves its counters raised
     if (h->step_sync && cudaMemsetAsync(h->step_sync, 0, ((size_t)h->cfg.n_layers * kSyncStride + 1) * sizeof(int),
                                         h->stream) != cudaSuccess)
+        return LLM_ERR_CUDA;
+    // ... and a part-way o_proj fold output
+    if (h->o_d && cudaMemsetAsync(h->o_d, 0, (size_t)h->cfg.hidden * sizeof(long long), h->stream) != cudaSuccess)
         return LLM_ERR_CUDA;
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return LLM_ERR_CUDA;
     h->seq_len = 0;

@@ -36,18 +36,19 @@ namespace {
 
 using namespace attn;
 
-template <int G, int D, int CS>
+template <int G, int D, int CS, bool FOLD = false>
 __global__ void __launch_bounds__(kNT, 1) k_attn(const __grid_constant__ AttnArgs a) {
     TimelineMark timeline_mark{a.tl};
     extern __shared__ __align__(128) uint16_t smem_raw[];
     uint16_t *smem = align_ring(smem_raw);
     const int g = blockIdx.y;
-    attn_cta<G, D, CS, false, false>(a, smem, [&](auto &&) {
+    auto hook = [&](auto &&) {
         pdl_wait();
         pdl_launch();
         return AttnInputs{a.q + (size_t)g * G * D, a.kv_new ? a.kv_new + (size_t)g * D : nullptr,
                           a.kv_new ? a.kv_new + (size_t)(a.Hkv + g) * D : nullptr};
-    });
+    };
+    attn_cta<G, D, CS, false, false, decltype(hook) &, FOLD>(a, smem, hook);
 }
 
 
@@ -55,9 +56,18 @@ template <int G>
 cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
     const dim3 grid(a.P, a.Hkv);
     if (a.cs == kCSWide && a.d == 128) {
+        if (a.fold) {
+            if constexpr (G * 128 % kGroup == 0) {
+                if (!allow_wide(k_attn<G, 128, kCSWide, true>)) return cudaErrorInvalidValue;
+                return launch_kc(lc, k_attn<G, 128, kCSWide, true>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCSWide,
+                                 a);
+            }
+            return cudaErrorInvalidValue;
+        }
         if (!allow_wide(k_attn<G, 128, kCSWide>)) return cudaErrorInvalidValue;
         return launch_kc(lc, k_attn<G, 128, kCSWide>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCSWide, a);
     }
+    if (a.fold) return cudaErrorInvalidValue;  // the fold needs one 16-CTA cluster per KV head
     if (a.cs != 0 && a.cs != kCS) return cudaErrorInvalidValue;
     if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCS>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCS, a);
     if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCS>, grid, dim3(kNT), ring_alloc_bytes<64>(), kCS, a);
@@ -145,10 +155,12 @@ AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages) {
     return {default_splits(n_sm, Hq, Hkv, d, max_pages), kCS};
 }
 
-cudaError_t attention_pool_maps(AttnArgs &a) {
-    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// cuTensorMapEncodeTiled through the runtime's driver entry point (null if unavailable)
+EncodeFn tensor_map_encoder() {
     static EncodeFn enc = []() -> EncodeFn {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q{};
@@ -158,6 +170,12 @@ cudaError_t attention_pool_maps(AttnArgs &a) {
             return reinterpret_cast<EncodeFn>(p);
         return nullptr;
     }();
+    return enc;
+}
+}  // namespace
+
+cudaError_t attention_pool_maps(AttnArgs &a) {
+    EncodeFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     if (!a.k_pool || !a.v_pool || ((uintptr_t)a.k_pool & 15) || ((uintptr_t)a.v_pool & 15) || a.n_pages < 1 ||
         a.Hkv < 1 || (a.d != 64 && a.d != 128))
@@ -177,9 +195,41 @@ cudaError_t attention_pool_maps(AttnArgs &a) {
     return cudaSuccess;
 }
 
+bool attn_fold_ok(int fmt, int Hq, int Hkv, int d, int hidden, const AttnPlan &ap) {
+    if (fmt != kFmtInt4 || d != 128 || Hkv < 1 || Hq % Hkv || ap.P != ap.cs || hidden <= 0) return false;
+    const int G = Hq / Hkv;
+    if (G > 8 || (G * d) % kGroup || hidden % (ap.cs * kWarps) || hidden / ap.cs > 256) return false;
+    // the CTA's W_o rows (its KV head's columns), the gathered outputs as fp16 and fp32, the rows'
+    // scales, the CTA's merged outputs
+    const size_t need = (((size_t)(hidden / ap.cs) * (G * d / 2 + G * d / kGroup * 2) + (size_t)G * d * 6 + 15) & ~(size_t)15) +
+                        (size_t)(G * d + ap.cs - 1) / ap.cs * 4;
+    return need <= ring_bytes<128>();
+}
+
+cudaError_t attn_fold_args(AttnFold &f, const void *wo, const uint16_t *so, long long *out, int Hq, int Hkv, int d,
+                           int hidden, const AttnPlan &ap) {
+    if (!wo || ((uintptr_t)wo & 15) || !so || !out || !attn_fold_ok(kFmtInt4, Hq, Hkv, d, hidden, ap))
+        return cudaErrorInvalidValue;
+    EncodeFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)Hq * d / 8, (cuuint64_t)hidden};
+    const cuuint64_t strides[1] = {(cuuint64_t)Hq * d / 2};
+    const cuuint32_t box[2] = {(cuuint32_t)(Hq / Hkv * d / 8), (cuuint32_t)(hidden / ap.cs)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&f.wo_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(wo), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    f.so = so;
+    f.out = out;
+    f.hidden = hidden;
+    return cudaSuccess;
+}
+
 cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &args) {
     const int cs = args.cs == kCSWide ? kCSWide : kCS;
     if (args.P < cs || args.P > 256 || args.P % cs || args.Hkv < 1 || args.Hq % args.Hkv) return cudaErrorInvalidValue;
+    if (args.fold && !args.out) return cudaErrorInvalidValue;  // the fold's shapes: attn_fold_args
     AttnArgs a = args;
     const cudaError_t me = attention_pool_maps(a);
     if (me != cudaSuccess) return me;

@@ -29,7 +29,9 @@ QD_HOST_DEV_INLINE size_t act_region_bytes(int K) {
 }
 QD_HOST_DEV_INLINE size_t gain_region_bytes(int K) { return ((size_t)K * 2 + 15) & ~(size_t)15; }
 
-template <int FMT, int RT>
+// X2: the staged input is x + a.x2 (fixed point), a separate instantiation so that the
+// common one keeps a compile-time null second source
+template <int FMT, int RT, bool X2>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     TimelineMark timeline_mark{a.tl};
     l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);
@@ -87,7 +89,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
         pdl_wait();
         post = stage_activations(a.x, nullptr, a.gamma, a.eps, a.K, a.stats_in, FMT == kFmtInt4A8 ? nullptr : xs,
                                  nullptr, red, act_blk_bytes<FMT>(), a.gamma ? gs : nullptr,
-                                 FMT == kFmtInt4A8 ? reinterpret_cast<uint8_t *>(xs) : nullptr, a8_sx, a8_qs);
+                                 FMT == kFmtInt4A8 ? reinterpret_cast<uint8_t *>(xs) : nullptr, a8_sx, a8_qs,
+                                 X2 ? a.x2 : nullptr);
         pdl_launch();
     };
     gain_copy_async(a.gamma, a.K, gs);
@@ -166,7 +169,14 @@ cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
                             (fit < kMaxWarps ? fit : kMaxWarps) / ks * ks);
     a.ks = ks;
     const size_t smem = fixed + (size_t)pl.nw * per_warp;
-    return launch_k(lc, k_gemv<FMT, RT>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
+    if (a.x2) {
+        if constexpr (RT == 4) {
+            if (a.mode != 2 || a.stats_in) return cudaErrorInvalidValue;
+            return launch_k(lc, k_gemv<FMT, RT, true>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
+        }
+        return cudaErrorInvalidValue;
+    }
+    return launch_k(lc, k_gemv<FMT, RT, false>, dim3(pl.grid), dim3(pl.nw * 32), smem, a);
 }
 
 // Shape choices: K split over warps for short row counts (o_proj, down), so

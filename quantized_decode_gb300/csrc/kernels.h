@@ -90,6 +90,8 @@ struct GemvArgs {
     float *y;               // output [N]
     long long *fold;        // mode 1: y += fold (fixed point) and fold = 0 (fold_add), or fold = 0 only; or null
     int fold_add;
+    const long long *x2;    // mode 2: a pending contribution (fixed point) added to x first, or null;
+                            // then stats_in must be null (the statistics are computed here)
     const float *stats_in;  // producer (ss, mx) pairs for x, or null (computed here)
     float *stats_out;       // this kernel's (ss, mx) pairs for y, or null
     const uint16_t *stats_gamma;  // gain of y's consumer norm for mx (null: none)
@@ -229,7 +231,22 @@ struct AttnArgs {
     float *stats_out;                  // (ss, mx) pairs of out, or null: slot g per KV head, or with
                                        // one 16-CTA cluster per head slot 16 g + rank (others untouched)
     unsigned long long *tl; // timeline slot of this launch, or null (TimelineMark)
+    // o_proj folded in (one cluster per KV head only, INT4 W_o, d = 128; see AttnFold), in
+    // device memory; out is then not written.  Null: no fold.
+    const struct AttnFold *fold;
 };
+
+// The o_proj fold of one layer: the cluster of KV head g multiplies its G*d outputs by
+// W_o's columns [g G d, (g + 1) G d) and adds the rows to out (fixed point, 2^-32), CTA r
+// of the cluster taking rows [r hidden / cs, (r + 1) hidden / cs).
+struct alignas(64) AttnFold {
+    CUtensorMap wo_map;                // W_o as 32-bit words [hidden][Hq d / 8], boxes of G d / 8 words
+                                       // x hidden / cs rows
+    const uint16_t *so;                // bf16 scales [hidden][Hq d / 128]
+    long long *out;                    // [hidden]
+    int hidden;
+};
+
 
 // Each launcher returns the launch's cudaError_t.
 cudaError_t launch_qkv(const LaunchCfg &lc, int fmt, const QkvArgs &a);
@@ -249,6 +266,12 @@ struct AttnPlan {
     int P, cs;
 };
 AttnPlan plan_attention(int n_sm, int Hq, int Hkv, int d, int max_pages);
+// Whether attention with plan `ap` can fold o_proj in (shapes and shared memory).
+bool attn_fold_ok(int fmt, int Hq, int Hkv, int d, int hidden, const AttnPlan &ap);
+// The fold of one layer (host copy, to be copied to device memory): W_o codes (16-byte
+// aligned) and scales, the output buffer.
+cudaError_t attn_fold_args(AttnFold &f, const void *wo, const uint16_t *so, long long *out, int Hq, int Hkv, int d,
+                           int hidden, const AttnPlan &ap);
 
 // QKV projection + attention of a layer in one kernel (one 16-CTA cluster per
 // KV head; models without q/k norms, d = 128).  `at` as for launch_attention

@@ -280,6 +280,16 @@ class Engine:
         L.check(self.lib.llm_debug_step_wait(self.h, int(extra_arrivals), int(counter_wait_ns)),
                 "llm_debug_step_wait")
 
+    def set_o_fold(self, on):
+        """True: o_proj inside the decode attention clusters; False (default): its own GEMV."""
+        L.check(self.lib.llm_set_o_fold(self.h, int(bool(on))), "llm_set_o_fold")
+
+    def o_fold(self):
+        """The current set_o_fold setting."""
+        out = ctypes.c_int32()
+        L.check(self.lib.llm_get_o_fold(self.h, ctypes.byref(out)), "llm_get_o_fold")
+        return bool(out.value)
+
     def set_fused_mlp(self, on):
         """True (default where it fits): the MLP block as one kernel; False: gate/up + down."""
         L.check(self.lib.llm_set_fused_mlp(self.h, int(bool(on))), "llm_set_fused_mlp")
