@@ -87,7 +87,8 @@ def test_gemm_f16_vs_float64(lib, M, N, K):
 
 @pytest.mark.parametrize("fmt,M,N,K", [(1, 1, 128, 128), (1, 130, 256, 384), (1, 512, 4608, 3584),
                                        (1, 77, 3584, 18944), (2, 200, 384, 4096), (2, 64, 256, 12288),
-                                       (1, 600, 384, 512), (1, 1024, 4608, 1024), (2, 300, 1024, 1024)])
+                                       (1, 600, 384, 512), (1, 1024, 4608, 1024), (2, 300, 1024, 1024),
+                                       (1, 512, 37888, 3584)])
 def test_gemm_quant_vs_float64(lib, fmt, M, N, K):
     """In-kernel dequantization: C against a float64 matmul of A and the exactly dequantized
     weights (INT4: the oracle's unpacking x the bf16 group scale; INT8: code x fp32 row scale, the
