@@ -226,3 +226,26 @@ def test_full_width_prefill_two_layers_vs_oracle(name, n):
         check_logits(eng.logits(), orc.step(tok, n), f"{name} first decode step")
     finally:
         eng.close()
+
+
+def test_prompt_longer_than_one_chunk_two_layers_vs_oracle():
+    """1100 prompt rows: two prefill chunks (1024 + 76 rows, the second at position 1024 over the
+    first chunk's cache), then a decode step; 1.5B widths, 2 layers, against the oracle's own
+    prefill (bitwise the same as 1100 oracle steps)."""
+    from quantized_decode_gb300 import Engine
+    cfg = sm.CONFIGS["qwen2.5-1.5b"].with_(n_layers=2)
+    n = 1100
+    eng = Engine(device_model(cfg, SEED))
+    try:
+        prompt = sm.prompt(cfg, SEED + 5, n)
+        first = eng.prefill(prompt)
+        orc = oracle.OracleModel(cfg, SEED, t_max=n + 4)
+        ref = orc.prefill(prompt)
+        check_logits(eng.logits(), ref, "1100-row prefill")
+        assert first == int(np.argmax(eng.logits()))
+        assert eng.seq_len() == n
+        tok = int(np.argmax(ref))
+        eng.decode_step(tok)
+        check_logits(eng.logits(), orc.step(tok, n), "decode after the 1100-row prefill")
+    finally:
+        eng.close()
