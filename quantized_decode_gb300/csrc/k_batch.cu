@@ -8,9 +8,11 @@
 // b < B <= 8, run on the tensor cores with mma.sync m16n8k16 (bf16 operands,
 // fp32 accumulation): A = 16 weight rows, their INT4 / INT8 codes turned into
 // exact bf16 integers in registers (bf16 weights as they are); B = the 8
-// sequences' activations, staged in shared memory as bf16 after the RMSNorm;
-// the column n of the mma is the sequence.  INT4 group scales are applied to
-// the fp32 partial sum of each 128-code group, INT8 row scales at the end.
+// sequences' activations, staged in shared memory as bf16
+// after the RMSNorm; the column n of the mma is the sequence.  INT4 group
+// scales are applied to the fp32 partial sum of each 128-code group, INT8 row
+// scales at the end.  Each warp streams its rows' 64-byte blocks through a
+// cp.async ring in shared memory, kRD - 1 blocks ahead of the arithmetic.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -23,7 +25,9 @@ namespace {
 constexpr int kNW = 8;        // warps per CTA
 constexpr int kKC = 12288;    // K values staged in shared memory at a time (192 KB for 8 sequences)
 constexpr int kTPW = 8;       // row tiles per warp at most (fp32 accumulators)
-constexpr int kUB = 4;        // 64-byte row blocks per load group (two groups in flight per warp)
+constexpr int kRD = 12;       // weight ring stages per warp (64-byte blocks of its two rows, cp.async)
+constexpr int kRingWarpBytes = kRD * 2 * 32 * (16 + 4);  // codes + INT4 scale words, per warp
+constexpr int kRedEntries = kNW * kTPW * 4 * 32 * 4 / 16;  // 16-byte entries of the K-part sums
 constexpr int kNormK = 4096;  // RMSNorm'd inputs: K at most this (their fp32 rows sit in shared memory)
 
 QD_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -97,6 +101,14 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
     // values kept in shared memory behind the staging area while the sums of squares
     // are formed, then normalized from there
     float *xf = reinterpret_cast<float *>(sx + (a.K < kKC ? a.K : kKC));  // [8][K] fp32 (gamma only)
+    // each warp's weight ring after the staging area (over the fp32 input rows, which the
+    // staging has consumed by the time the ring fills)
+    int stage_entries = (a.K + (int)gridDim.y - 1) / (int)gridDim.y + 128;
+    if (stage_entries > kKC) stage_entries = kKC;
+    if (stage_entries < kRedEntries) stage_entries = kRedEntries;
+    char *ring_base = reinterpret_cast<char *>(sx + stage_entries) + (size_t)warp * kRingWarpBytes;
+    uint4 *rc = reinterpret_cast<uint4 *>(ring_base);                    // [kRD][2 rows][32 lanes]
+    uint32_t *rs = reinterpret_cast<uint32_t *>(ring_base + kRD * 2 * 32 * 16);  // [kRD][2][32]
     if (threadIdx.x < 8) s_inv[threadIdx.x] = 1.f;
     if (a.gamma) {
         float ss[8];
@@ -222,96 +234,123 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
         const int nblk_all = kc / BLK;
         const int kb0 = nblk_all * kp / ks, kb1 = nblk_all * (kp + 1) / ks;  // this warp's blocks of the chunk
         const int nblk = kb1 - kb0;
-#pragma unroll
-        for (int i = 0; i < kTPW; ++i) {
-            const int ti = gw + i * nwarps;
-            if (ti >= tiles) break;
-            const uint4 *r0, *r1;
+        int nt = 0;  // this warp's tiles
+        while (nt < kTPW && gw + nt * nwarps < tiles) ++nt;
+        const int F = nblk > 0 ? nt * nblk : 0;
+        const int ub0 = k0 / BLK + kb0;  // first block of this warp's part in the row (64-byte units)
+        // Weight stream: stage f (tile f / nblk, block f % nblk) holds lane t's 16 bytes of the
+        // tile's two rows (and, INT4, the word holding each row's group scale) in ring slot
+        // f % kRD; kRD - 1 stages are in flight while one is multiplied.
+        // issue cursor: tile li, block lb, ring slot ls; the tile's row pointers are found once
+        int li = 0, lb = 0, ls = 0;
+        const uint4 *lr0 = nullptr, *lr1 = nullptr;
+        const uint32_t *lsc0 = nullptr, *lsc1 = nullptr;
+        auto tile_rows = [&](int i) {
             const void *s0, *s1;
             int rr0, rr1;
-            row_ptrs(ti, r0, r1, s0, s1, rr0, rr1);
-            const int ub0 = k0 / BLK + kb0;  // first block of this warp's part in the row (64-byte units)
-            struct Group {
-                uint4 w0[kUB], w1[kUB];
-                float sc0[kUB], sc1[kUB];
-            };
-            auto load = [&](Group &q, int bk) {
-#pragma unroll
-                for (int u = 0; u < kUB; ++u) {
-                    if (bk + u < nblk) {
-                        const int blk = ub0 + bk + u;
-                        q.w0[u] = ld_stream(r0 + (size_t)blk * 4 + t);
-                        q.w1[u] = ld_stream(r1 + (size_t)blk * 4 + t);
-                        if constexpr (FMT == kFmtInt4) {
-                            const int G = a.K / kGroup;
-                            q.sc0[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s0) + (size_t)rr0 * G + blk));
-                            q.sc1[u] = bf16_bits_to_float(__ldg(static_cast<const uint16_t *>(s1) + (size_t)rr1 * G + blk));
-                        }
-                    }
-                }
-            };
-            auto compute = [&](const Group &q, int bk) {
-#pragma unroll
-                for (int u = 0; u < kUB; ++u) {
-                    if (bk + u >= nblk) break;
-                    const int cbase = ((kb0 + bk + u) * BLK + t * CPL) / 8;  // staged k-chunk of this lane's codes
-                    // A pairs of the two rows
-                    uint32_t pa[2][CPL / 2];
-                    const uint4 wv[2] = {q.w0[u], q.w1[u]};
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
-                        if constexpr (FMT == kFmtInt4) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                uint32_t p[4];
-                                int4_word_bf16(ww[j], p);
-#pragma unroll
-                                for (int z = 0; z < 4; ++z) pa[r][4 * j + z] = p[z];
-                            }
-                        } else if constexpr (FMT == kFmtInt8) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                uint32_t p[2];
-                                int8_word_bf16(ww[j], p);
-                                pa[r][2 * j] = p[0];
-                                pa[r][2 * j + 1] = p[1];
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) pa[r][j] = ww[j];
-                        }
-                    }
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int m = 0; m < NM; ++m) {
-                        // B: this lane's sequence g, k values t*CPL + 4m .. + 3 of the block
-                        const uint4 xb = sx[act_entry(cbase + (4 * m) / 8, g)];
-                        const uint32_t b0 = (m & 1) ? xb.z : xb.x, b1 = (m & 1) ? xb.w : xb.y;
-                        mma_bf16(d, pa[0][2 * m], pa[1][2 * m], pa[0][2 * m + 1], pa[1][2 * m + 1], b0, b1);
-                    }
-                    if constexpr (FMT == kFmtInt4) {
-                        acc[i][0] = fmaf(d[0], q.sc0[u], acc[i][0]);
-                        acc[i][1] = fmaf(d[1], q.sc0[u], acc[i][1]);
-                        acc[i][2] = fmaf(d[2], q.sc1[u], acc[i][2]);
-                        acc[i][3] = fmaf(d[3], q.sc1[u], acc[i][3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[i][j] += d[j];
-                    }
-                }
-            };
-            // two load groups in flight: the next group's loads go out before this one's math
-            Group ga, gb;
-            if (nblk > 0) load(ga, 0);
+            row_ptrs(gw + i * nwarps, lr0, lr1, s0, s1, rr0, rr1);
+            lr0 += (size_t)ub0 * 4 + t;
+            lr1 += (size_t)ub0 * 4 + t;
+            if constexpr (FMT == kFmtInt4) {  // scale words: G even (K % 256 == 0), a block's parity picks the half
+                const size_t G = (size_t)a.K / kGroup;
+                lsc0 = static_cast<const uint32_t *>(s0) + (((size_t)rr0 * G + ub0) >> 1);
+                lsc1 = static_cast<const uint32_t *>(s1) + (((size_t)rr1 * G + ub0) >> 1);
+            }
+        };
+        auto issue = [&]() {
+            cp_async16(rc + (ls * 2 + 0) * 32 + lane, lr0 + (size_t)lb * 4);
+            cp_async16(rc + (ls * 2 + 1) * 32 + lane, lr1 + (size_t)lb * 4);
+            if constexpr (FMT == kFmtInt4) {
+                const int hw = ((ub0 & 1) + lb) >> 1;  // scale word of block ub0 + lb, from the tile's first
+                cp_async4(rs + (ls * 2 + 0) * 32 + lane, lsc0 + hw);
+                cp_async4(rs + (ls * 2 + 1) * 32 + lane, lsc1 + hw);
+            }
+            if (++ls == kRD) ls = 0;
+            if (++lb == nblk) {
+                lb = 0;
+                if (++li < nt) tile_rows(li);
+            }
+        };
+        if (F > 0) tile_rows(0);
+        for (int f = 0; f < kRD - 1; ++f) {
+            if (f < F) issue();
+            cp_async_commit();
+        }
+        float cur[4] = {0.f, 0.f, 0.f, 0.f};
+        int i = 0, bk = 0, slot = 0;  // compute cursor
 #pragma unroll 1
-            for (int bk = 0; bk < nblk; bk += 2 * kUB) {
-                if (bk + kUB < nblk) load(gb, bk + kUB);
-                compute(ga, bk);
-                if (bk + 2 * kUB < nblk) load(ga, bk + 2 * kUB);
-                if (bk + kUB < nblk) compute(gb, bk + kUB);
+        for (int f = 0; f < F; ++f) {
+            if (f + kRD - 1 < F) issue();
+            cp_async_commit();
+            cp_async_wait<kRD - 1>();
+            const int cbase = ((kb0 + bk) * BLK + t * CPL) / 8;  // staged k-chunk of this lane's codes
+            // A pairs of the two rows
+            uint32_t pa[2][CPL / 2];
+            const uint4 wv[2] = {rc[(slot * 2 + 0) * 32 + lane], rc[(slot * 2 + 1) * 32 + lane]};
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+                if constexpr (FMT == kFmtInt4) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t p[4];
+                        int4_word_bf16(ww[j], p);
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) pa[r][4 * j + z] = p[z];
+                    }
+                } else if constexpr (FMT == kFmtInt8) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t p[2];
+                        int8_word_bf16(ww[j], p);
+                        pa[r][2 * j] = p[0];
+                        pa[r][2 * j + 1] = p[1];
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) pa[r][j] = ww[j];
+                }
+            }
+            // two accumulator chains (even and odd k-steps) halve the mma dependency chain
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+                // B: this lane's sequence g, k values t*CPL + 4m .. + 3 of the block
+                const uint4 xb = sx[act_entry(cbase + (4 * m) / 8, g)];
+                const uint32_t b0 = (m & 1) ? xb.z : xb.x, b1 = (m & 1) ? xb.w : xb.y;
+                if (m & 1) mma_bf16(e, pa[0][2 * m], pa[1][2 * m], pa[0][2 * m + 1], pa[1][2 * m + 1], b0, b1);
+                else mma_bf16(d, pa[0][2 * m], pa[1][2 * m], pa[0][2 * m + 1], pa[1][2 * m + 1], b0, b1);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[j] += e[j];
+            if constexpr (FMT == kFmtInt4) {
+                const bool hi = ((ub0 + bk) & 1) != 0;
+                const uint32_t w0 = rs[(slot * 2 + 0) * 32 + lane], w1 = rs[(slot * 2 + 1) * 32 + lane];
+                const float sc0 = __uint_as_float(hi ? (w0 & 0xFFFF0000u) : (w0 << 16));
+                const float sc1 = __uint_as_float(hi ? (w1 & 0xFFFF0000u) : (w1 << 16));
+                cur[0] = fmaf(d[0], sc0, cur[0]);
+                cur[1] = fmaf(d[1], sc0, cur[1]);
+                cur[2] = fmaf(d[2], sc1, cur[2]);
+                cur[3] = fmaf(d[3], sc1, cur[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cur[j] += d[j];
+            }
+            if (++slot == kRD) slot = 0;
+            if (++bk == nblk) {  // the tile's part is done: into its accumulators
+#pragma unroll
+                for (int ii = 0; ii < kTPW; ++ii)
+                    if (ii == i) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[ii][j] += cur[j];
+                    }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cur[j] = 0.f;
+                bk = 0;
+                ++i;
             }
         }
+        cp_async_wait<0>();
     }
 
     // ---- the K parts of a tile meet in shared memory (the staging area is free now)
@@ -519,19 +558,25 @@ __global__ void k_bargmax_final(const float *pv, const int *pi, DevState *st, co
 
 template <int FMT>
 cudaError_t launch_fmt(const LaunchCfg &lc, const BGemvArgs &a, int grid, int gks) {
-    // staging for min(K part, kKC) values of 8 sequences; it also holds the K-part sums
-    const int kpart = (a.K + gks - 1) / gks + 128;
-    size_t smem = (size_t)(kpart < kKC ? kpart : kKC) * 16;
-    const size_t red = (size_t)kNW * kTPW * 4 * 32 * 4;
-    if (smem < red) smem = red;
-    if (a.gamma) smem += (size_t)8 * a.K * 4;  // the fp32 input rows
+    // staging for min(K part, kKC) values of 8 sequences (it also holds the K-part sums), then
+    // the warps' weight rings; with an RMSNorm the fp32 input rows sit after min(K, kKC) entries
+    int stage_entries = (a.K + gks - 1) / gks + 128;
+    if (stage_entries > kKC) stage_entries = kKC;
+    if (stage_entries < kRedEntries) stage_entries = kRedEntries;
+    size_t smem = (size_t)stage_entries * 16 + (size_t)kNW * kRingWarpBytes;
+    if (a.gamma) {
+        const size_t xf_end = (size_t)(a.K < kKC ? a.K : kKC) * 16 + (size_t)8 * a.K * 4;
+        if (smem < xf_end) smem = xf_end;
+    }
+    if (smem > (size_t)kMaxSmemOptin) return cudaErrorInvalidValue;
     return launch_k(lc, k_bgemv<FMT>, dim3(grid, gks), dim3(kNW * 32), smem, a);
 }
 
 }  // namespace
 
 bool bgemv_shape_ok(int fmt, int N, int K, int mode) {
-    const int blk = fmt == kFmtInt4 ? 128 : (fmt == kFmtInt8 ? 64 : 32);
+    // INT4: K % 256 (an even number of groups per row: a block's parity picks its scale's half)
+    const int blk = fmt == kFmtInt4 ? 256 : (fmt == kFmtInt8 ? 64 : 32);
     return K > 0 && K % blk == 0 && K % 8 == 0 && N > 0 && N % (mode == 2 ? 8 : 16) == 0;
 }
 

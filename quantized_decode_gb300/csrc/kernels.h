@@ -239,7 +239,7 @@ struct AttnArgs {
 // The o_proj fold of one layer: the cluster of KV head g multiplies its G*d outputs by
 // W_o's columns [g G d, (g + 1) G d) and adds the rows to out (fixed point, 2^-32), CTA r
 // of the cluster taking rows [r hidden / cs, (r + 1) hidden / cs).
-struct alignas(64) AttnFold {
+struct AttnFold {
     CUtensorMap wo_map;                // W_o as 32-bit words [hidden][Hq d / 8], boxes of G d / 8 words
                                        // x hidden / cs rows
     const uint16_t *so;                // bf16 scales [hidden][Hq d / 128]
