@@ -17,6 +17,7 @@ namespace attn {
 
 constexpr int kCS = 8;        // CTAs per cluster (portable size)
 constexpr int kCSWide = 16;   // one cluster per KV head (non-portable size)
+constexpr int kCSSmall = 4;   // several sequences at once (multi-sequence decode)
 constexpr int kWarps = 8;
 constexpr int kNT = kWarps * 32;
 constexpr int kWRing = 2;     // page slots per warp

@@ -234,14 +234,20 @@ int llm_batch_create(const llm_config *cfg, const llm_weights *w, int32_t max_se
         h->own_stream = true;
     }
     h->lc.stream = h->stream;
-    h->lc.pdl = false;
+    h->lc.pdl = true;  // the GEMMs and the attention wait for their predecessor before touching activations
     h->lc.n_sm = n_sm;
     const llm_config &c = h->cfg;
     h->max_pages = (c.max_context + kPageTokens - 1) / kPageTokens;
     h->n_pages = n_pages > 0 ? n_pages : max_seqs * h->max_pages + 1;
     if (h->n_pages < 2 || (int64_t)h->n_pages * c.n_kv_heads * kPageTokens > INT32_MAX) return fail(LLM_ERR_ARG);
     h->layer_kv = (size_t)h->n_pages * c.n_kv_heads * kPageTokens * d;
-    const AttnPlan ap = plan_attention(n_sm, c.n_q_heads, c.n_kv_heads, d, h->max_pages);
+    AttnPlan ap = plan_attention(n_sm, c.n_q_heads, c.n_kv_heads, d, h->max_pages);
+    // the sequences' attention kernels run side by side: narrower clusters, one cluster per KV
+    // head and sequence, once max_seqs of the single-sequence plan would take more than the SMs
+    if ((long long)max_seqs * c.n_kv_heads * ap.P > n_sm) {
+        const int cs = (long long)max_seqs * c.n_kv_heads * 8 <= n_sm ? 8 : 4;
+        ap = AttnPlan{cs, cs};
+    }
     h->P = ap.P;
     h->cs = ap.cs;
     const int G = c.n_q_heads / c.n_kv_heads;

@@ -68,6 +68,11 @@ cudaError_t launch_g(const LaunchCfg &lc, const AttnArgs &a) {
         return launch_kc(lc, k_attn<G, 128, kCSWide>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCSWide, a);
     }
     if (a.fold) return cudaErrorInvalidValue;  // the fold needs one 16-CTA cluster per KV head
+    if (a.cs == kCSSmall) {  // several sequences side by side: fewer CTAs per KV head
+        if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCSSmall>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCSSmall, a);
+        if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCSSmall>, grid, dim3(kNT), ring_alloc_bytes<64>(), kCSSmall, a);
+        return cudaErrorInvalidValue;
+    }
     if (a.cs != 0 && a.cs != kCS) return cudaErrorInvalidValue;
     if (a.d == 128) return launch_kc(lc, k_attn<G, 128, kCS>, grid, dim3(kNT), ring_alloc_bytes<128>(), kCS, a);
     if (a.d == 64) return launch_kc(lc, k_attn<G, 64, kCS>, grid, dim3(kNT), ring_alloc_bytes<64>(), kCS, a);
@@ -227,7 +232,7 @@ cudaError_t attn_fold_args(AttnFold &f, const void *wo, const uint16_t *so, long
 }
 
 cudaError_t launch_attention(const LaunchCfg &lc, const AttnArgs &args) {
-    const int cs = args.cs == kCSWide ? kCSWide : kCS;
+    const int cs = args.cs == kCSWide ? kCSWide : (args.cs == kCSSmall ? kCSSmall : kCS);
     if (args.P < cs || args.P > 256 || args.P % cs || args.Hkv < 1 || args.Hq % args.Hkv) return cudaErrorInvalidValue;
     if (args.fold && !args.out) return cudaErrorInvalidValue;  // the fold's shapes: attn_fold_args
     AttnArgs a = args;

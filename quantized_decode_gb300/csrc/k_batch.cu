@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
     const int ks = a.ks, kp = warp % ks, tslots = kNW / ks;
     const int gw = blockIdx.x * tslots + warp / ks, nwarps = gridDim.x * tslots;
     const int B = a.B;
+    // programmatic dependent launch: everything below reads or writes activations
+    pdl_wait();
+    pdl_launch();
 
     // ---- with an RMSNorm (K <= kNormK): the B input rows are read once, their fp32
     // values kept in shared memory behind the staging area while the sums of squares

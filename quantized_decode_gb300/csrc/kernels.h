@@ -225,7 +225,7 @@ struct AttnArgs {
     float *out;                        // [Hq][d]
     int *err;
     const uint16_t *kv_new;            // [2][Hkv][d] appended K/V row, or null (all rows in pages)
-    int cs;                            // CTAs per cluster: 8 (0 = 8) or 16 (d = 128 only)
+    int cs;                            // CTAs per cluster: 8 (0 = 8), 16 (d = 128 only) or 4
     CUtensorMap k_map, v_map;          // set by the launcher: the pools as 2-D tensors
                                        // [pages * Hkv * 16][d] for TMA page loads
     float *stats_out;                  // (ss, mx) pairs of out, or null: slot g per KV head, or with
