@@ -583,7 +583,7 @@ bool bgemv_shape_ok(int fmt, int N, int K, int mode) {
     return K > 0 && K % blk == 0 && K % 8 == 0 && N > 0 && N % (mode == 2 ? 8 : 16) == 0;
 }
 
-// K split: as many warps per tile (1..8) as it takes for the tiles to give every
+// K split: as many warps per tile (a divisor of kNW) as it takes for the tiles to give every
 // warp of the grid work; then the grid, at most kTPW tiles per tile slot.
 // Large-K projections that add into y (the down projection) also split K over
 // grid.y CTAs of about 2048 values each, so that a CTA stages only its part of the
@@ -596,8 +596,13 @@ void bgemv_plan(const LaunchCfg &lc, int N, int K, int mode, int &ks, int &grid,
         if (gks > 8) gks = 8;
     }
     const int n_sm = lc.n_sm / gks > 0 ? lc.n_sm / gks : 1;  // SMs per K part
+    // the smallest divisor of kNW that gives every warp of the grid work, else the largest
     ks = 1;
-    while (ks < kNW && (long long)tiles * ks < (long long)kNW * n_sm) ks *= 2;
+    for (int d = 1; d <= kNW; ++d) {
+        if (kNW % d) continue;
+        ks = d;
+        if ((long long)tiles * d >= (long long)kNW * n_sm) break;
+    }
     const int tslots = kNW / ks;
     grid = (tiles + tslots - 1) / tslots;
     if (grid > n_sm) grid = n_sm;
