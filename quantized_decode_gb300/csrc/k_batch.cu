@@ -28,7 +28,7 @@ constexpr int kTPW = 8;       // row tiles per warp at most (fp32 accumulators)
 constexpr int kRD = 12;       // weight ring stages per warp (64-byte blocks of its two rows, cp.async)
 constexpr int kRingWarpBytes = kRD * 2 * 32 * (16 + 4);  // codes + INT4 scale words, per warp
 constexpr int kRedEntries = kNW * kTPW * 4 * 32 * 4 / 16;  // 16-byte entries of the K-part sums
-constexpr int kNormK = 4096;  // RMSNorm'd inputs: K at most this (their fp32 rows sit in shared memory)
+constexpr int kNormK = 4096;  // RMSNorm'd inputs: K at most this
 
 QD_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                      uint32_t b1) {
@@ -96,63 +96,14 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
     const int ks = a.ks, kp = warp % ks, tslots = kNW / ks;
     const int gw = blockIdx.x * tslots + warp / ks, nwarps = gridDim.x * tslots;
     const int B = a.B;
-    // programmatic dependent launch: everything below reads or writes activations
-    pdl_wait();
-    pdl_launch();
-
-    // ---- with an RMSNorm (K <= kNormK): the B input rows are read once, their fp32
-    // values kept in shared memory behind the staging area while the sums of squares
-    // are formed, then normalized from there
-    float *xf = reinterpret_cast<float *>(sx + (a.K < kKC ? a.K : kKC));  // [8][K] fp32 (gamma only)
-    // each warp's weight ring after the staging area (over the fp32 input rows, which the
-    // staging has consumed by the time the ring fills)
+    // shared memory: the staging area for min(K part, kKC) values of 8 sequences (it also
+    // holds the K-part sums at the end), then each warp's weight ring
     int stage_entries = (a.K + (int)gridDim.y - 1) / (int)gridDim.y + 128;
     if (stage_entries > kKC) stage_entries = kKC;
     if (stage_entries < kRedEntries) stage_entries = kRedEntries;
     char *ring_base = reinterpret_cast<char *>(sx + stage_entries) + (size_t)warp * kRingWarpBytes;
     uint4 *rc = reinterpret_cast<uint4 *>(ring_base);                    // [kRD][2 rows][32 lanes]
     uint32_t *rs = reinterpret_cast<uint32_t *>(ring_base + kRD * 2 * 32 * 16);  // [kRD][2][32]
-    if (threadIdx.x < 8) s_inv[threadIdx.x] = 1.f;
-    if (a.gamma) {
-        float ss[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) ss[b] = 0.f;
-        constexpr int kB = 4;  // float4 loads per sequence in flight per thread
-        for (int k = threadIdx.x * 4; k < a.K; k += blockDim.x * 4 * kB) {
-            float4 v[8][kB];
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-#pragma unroll
-                for (int j = 0; j < kB; ++j) {
-                    const int kk = k + j * blockDim.x * 4;
-                    v[b][j] = b < B && kk < a.K ? __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.ldx + kk))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-#pragma unroll
-                for (int j = 0; j < kB; ++j) {
-                    const int kk = k + j * blockDim.x * 4;
-                    if (kk < a.K) {
-                        ss[b] += v[b][j].x * v[b][j].x + v[b][j].y * v[b][j].y + v[b][j].z * v[b][j].z +
-                                 v[b][j].w * v[b][j].w;
-                        *reinterpret_cast<float4 *>(xf + (size_t)b * a.K + kk) = v[b][j];
-                    }
-                }
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const float v = warp_sum(ss[b]);
-            if (lane == 0) red[warp][b] = v;
-        }
-        __syncthreads();
-        if (threadIdx.x < 8) {
-            float v = 0.f;
-            for (int w = 0; w < kNW; ++w) v += red[w][threadIdx.x];
-            s_inv[threadIdx.x] = rsqrtf(v / (float)a.K + a.eps);
-        }
-    }
-    __syncthreads();
 
     float acc[kTPW][4];
 #pragma unroll
@@ -186,11 +137,110 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
     const int nb_all = a.K / BLK;
     const int kbeg = (int)((long long)nb_all * blockIdx.y / gridDim.y) * BLK;
     const int kend = (int)((long long)nb_all * (blockIdx.y + 1) / gridDim.y) * BLK;
+
+    // Weight stream of a chunk of K: stage f (tile f / nblk, block f % nblk) holds lane t's
+    // 16 bytes of the tile's two rows (and, INT4, the word holding each row's group scale)
+    // in ring slot f % kRD; kRD - 1 stages are in flight while one is multiplied.
+    // issue cursor: tile li, block lb, ring slot ls; the tile's row pointers are found once
+    int kb0 = 0, nblk = 0, nt = 0, F = 0, ub0 = 0;
+    int li = 0, lb = 0, ls = 0;
+    const uint4 *lr0 = nullptr, *lr1 = nullptr;
+    const uint32_t *lsc0 = nullptr, *lsc1 = nullptr;
+    auto tile_rows = [&](int i) {
+        const void *s0, *s1;
+        int rr0, rr1;
+        row_ptrs(gw + i * nwarps, lr0, lr1, s0, s1, rr0, rr1);
+        lr0 += (size_t)ub0 * 4 + t;
+        lr1 += (size_t)ub0 * 4 + t;
+        if constexpr (FMT == kFmtInt4) {  // scale words: G even (K % 256 == 0), a block's parity picks the half
+            const size_t G = (size_t)a.K / kGroup;
+            lsc0 = static_cast<const uint32_t *>(s0) + (((size_t)rr0 * G + ub0) >> 1);
+            lsc1 = static_cast<const uint32_t *>(s1) + (((size_t)rr1 * G + ub0) >> 1);
+        }
+    };
+    auto issue = [&]() {
+        cp_async16(rc + (ls * 2 + 0) * 32 + lane, lr0 + (size_t)lb * 4);
+        cp_async16(rc + (ls * 2 + 1) * 32 + lane, lr1 + (size_t)lb * 4);
+        if constexpr (FMT == kFmtInt4) {
+            const int hw = ((ub0 & 1) + lb) >> 1;  // scale word of block ub0 + lb, from the tile's first
+            cp_async4(rs + (ls * 2 + 0) * 32 + lane, lsc0 + hw);
+            cp_async4(rs + (ls * 2 + 1) * 32 + lane, lsc1 + hw);
+        }
+        if (++ls == kRD) ls = 0;
+        if (++lb == nblk) {
+            lb = 0;
+            if (++li < nt) tile_rows(li);
+        }
+    };
+    // the chunk [k0, k0 + kc): this warp's blocks and tiles, and its first kRD - 1 stages
+    auto start_chunk = [&](int k0, int kc) {
+        const int nblk_all = kc / BLK;
+        kb0 = nblk_all * kp / ks;
+        const int kb1 = nblk_all * (kp + 1) / ks;  // this warp's blocks of the chunk
+        nblk = kb1 - kb0;
+        nt = 0;
+        while (nt < kTPW && gw + nt * nwarps < tiles) ++nt;
+        F = nblk > 0 ? nt * nblk : 0;
+        ub0 = k0 / BLK + kb0;  // first block of this warp's part in the row (64-byte units)
+        li = lb = ls = 0;
+        if (F > 0) tile_rows(0);
+        for (int f = 0; f < kRD - 1; ++f) {
+            if (f < F) issue();
+            cp_async_commit();
+        }
+    };
+    // the first chunk's weights go out before the dependency wait: nothing an earlier
+    // kernel writes is read by them, and the ring lies outside the staging area
+    start_chunk(kbeg, kend - kbeg < kKC ? kend - kbeg : kKC);
+
+    // programmatic dependent launch: everything below reads or writes activations
+    pdl_wait();
+    pdl_launch();
+
+    // ---- with an RMSNorm (K <= kNormK): the sums of squares of the B input rows (one pass
+    // over them in L2); the staging below reads them again and normalizes
+    if (threadIdx.x < 8) s_inv[threadIdx.x] = 1.f;
+    if (a.gamma) {
+        float ss[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+        constexpr int kB = 4;  // float4 loads per sequence in flight per thread
+        for (int k = threadIdx.x * 4; k < a.K; k += blockDim.x * 4 * kB) {
+            float4 v[8][kB];
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    const int kk = k + j * blockDim.x * 4;
+                    v[b][j] = b < B && kk < a.K ? __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.ldx + kk))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+#pragma unroll
+                for (int j = 0; j < kB; ++j)
+                    ss[b] += v[b][j].x * v[b][j].x + v[b][j].y * v[b][j].y + v[b][j].z * v[b][j].z +
+                             v[b][j].w * v[b][j].w;
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const float v = warp_sum(ss[b]);
+            if (lane == 0) red[warp][b] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < 8) {
+            float v = 0.f;
+            for (int w = 0; w < kNW; ++w) v += red[w][threadIdx.x];
+            s_inv[threadIdx.x] = rsqrtf(v / (float)a.K + a.eps);
+        }
+    }
+    __syncthreads();
+
 #pragma unroll 1
     for (int k0 = kbeg; k0 < kend; k0 += kKC) {
         const int kc = kend - k0 < kKC ? kend - k0 : kKC;
-        // ---- stage X[b][k0 .. k0 + kc) as bf16 (normalized), zeros for b >= B; the
-        // inputs come from the fp32 copy (RMSNorm) or from global memory, several
+        if (k0 != kbeg) start_chunk(k0, kc);  // the previous chunk's ring is drained
+        // ---- stage X[b][k0 .. k0 + kc) as bf16 (normalized), zeros for b >= B, several
         // entries' loads in flight per thread
         __syncthreads();
         constexpr int kE = 4;
@@ -201,10 +251,9 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
                 const int e = e0 + j * blockDim.x, c = e >> 3, b = e & 7;
                 v0[j] = v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (e < (kc / 8) * 8 && b < B) {
-                    const float *src = a.gamma ? xf + (size_t)b * a.K + k0 + c * 8 : a.x + (size_t)b * a.ldx + k0 + c * 8;
-                    v0[j] = a.gamma ? *reinterpret_cast<const float4 *>(src) : __ldcg(reinterpret_cast<const float4 *>(src));
-                    v1[j] = a.gamma ? *reinterpret_cast<const float4 *>(src + 4)
-                                    : __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                    const float *src = a.x + (size_t)b * a.ldx + k0 + c * 8;
+                    v0[j] = __ldcg(reinterpret_cast<const float4 *>(src));
+                    v1[j] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
                 }
             }
 #pragma unroll
@@ -234,51 +283,6 @@ __global__ void __launch_bounds__(kNW * 32, 1) k_bgemv(BGemvArgs a) {
         }
         __syncthreads();
 
-        const int nblk_all = kc / BLK;
-        const int kb0 = nblk_all * kp / ks, kb1 = nblk_all * (kp + 1) / ks;  // this warp's blocks of the chunk
-        const int nblk = kb1 - kb0;
-        int nt = 0;  // this warp's tiles
-        while (nt < kTPW && gw + nt * nwarps < tiles) ++nt;
-        const int F = nblk > 0 ? nt * nblk : 0;
-        const int ub0 = k0 / BLK + kb0;  // first block of this warp's part in the row (64-byte units)
-        // Weight stream: stage f (tile f / nblk, block f % nblk) holds lane t's 16 bytes of the
-        // tile's two rows (and, INT4, the word holding each row's group scale) in ring slot
-        // f % kRD; kRD - 1 stages are in flight while one is multiplied.
-        // issue cursor: tile li, block lb, ring slot ls; the tile's row pointers are found once
-        int li = 0, lb = 0, ls = 0;
-        const uint4 *lr0 = nullptr, *lr1 = nullptr;
-        const uint32_t *lsc0 = nullptr, *lsc1 = nullptr;
-        auto tile_rows = [&](int i) {
-            const void *s0, *s1;
-            int rr0, rr1;
-            row_ptrs(gw + i * nwarps, lr0, lr1, s0, s1, rr0, rr1);
-            lr0 += (size_t)ub0 * 4 + t;
-            lr1 += (size_t)ub0 * 4 + t;
-            if constexpr (FMT == kFmtInt4) {  // scale words: G even (K % 256 == 0), a block's parity picks the half
-                const size_t G = (size_t)a.K / kGroup;
-                lsc0 = static_cast<const uint32_t *>(s0) + (((size_t)rr0 * G + ub0) >> 1);
-                lsc1 = static_cast<const uint32_t *>(s1) + (((size_t)rr1 * G + ub0) >> 1);
-            }
-        };
-        auto issue = [&]() {
-            cp_async16(rc + (ls * 2 + 0) * 32 + lane, lr0 + (size_t)lb * 4);
-            cp_async16(rc + (ls * 2 + 1) * 32 + lane, lr1 + (size_t)lb * 4);
-            if constexpr (FMT == kFmtInt4) {
-                const int hw = ((ub0 & 1) + lb) >> 1;  // scale word of block ub0 + lb, from the tile's first
-                cp_async4(rs + (ls * 2 + 0) * 32 + lane, lsc0 + hw);
-                cp_async4(rs + (ls * 2 + 1) * 32 + lane, lsc1 + hw);
-            }
-            if (++ls == kRD) ls = 0;
-            if (++lb == nblk) {
-                lb = 0;
-                if (++li < nt) tile_rows(li);
-            }
-        };
-        if (F > 0) tile_rows(0);
-        for (int f = 0; f < kRD - 1; ++f) {
-            if (f < F) issue();
-            cp_async_commit();
-        }
         float cur[4] = {0.f, 0.f, 0.f, 0.f};
         int i = 0, bk = 0, slot = 0;  // compute cursor
 #pragma unroll 1
@@ -562,15 +566,11 @@ __global__ void k_bargmax_final(const float *pv, const int *pi, DevState *st, co
 template <int FMT>
 cudaError_t launch_fmt(const LaunchCfg &lc, const BGemvArgs &a, int grid, int gks) {
     // staging for min(K part, kKC) values of 8 sequences (it also holds the K-part sums), then
-    // the warps' weight rings; with an RMSNorm the fp32 input rows sit after min(K, kKC) entries
+    // the warps' weight rings
     int stage_entries = (a.K + gks - 1) / gks + 128;
     if (stage_entries > kKC) stage_entries = kKC;
     if (stage_entries < kRedEntries) stage_entries = kRedEntries;
-    size_t smem = (size_t)stage_entries * 16 + (size_t)kNW * kRingWarpBytes;
-    if (a.gamma) {
-        const size_t xf_end = (size_t)(a.K < kKC ? a.K : kKC) * 16 + (size_t)8 * a.K * 4;
-        if (smem < xf_end) smem = xf_end;
-    }
+    const size_t smem = (size_t)stage_entries * 16 + (size_t)kNW * kRingWarpBytes;
     if (smem > (size_t)kMaxSmemOptin) return cudaErrorInvalidValue;
     return launch_k(lc, k_bgemv<FMT>, dim3(grid, gks), dim3(kNW * 32), smem, a);
 }
