@@ -68,6 +68,8 @@ def parse():
     p.add_argument("--vocab", type=int, default=0, help="override vocab (profiling cases)")
     p.add_argument("--seed", type=int, default=4242)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-oracle-timings", action="store_true",
+                   help="skip the oracle's prefill and one-thread figures beside its baseline")
     p.add_argument("--no-ttft", action="store_true")
     p.add_argument("--ttft-only", action="store_true",
                    help="time the pp512 prefill only and print {'ttft_ms': ...} (profiling case)")
@@ -338,6 +340,53 @@ def oracle_decode(cfg, seed, T0, n_warm, n_steps, rec=None, budget_s=None):
     return mean_ms, sample, len(times)
 
 
+def oracle_timings(cfg7, rec7, seed):
+    """The oracle's own prefill and per-thread figures, beside its decode baseline: pp512 of
+    the tiny and 1.5B configurations, pp64 of the 7B shape, and one decode step of the tiny
+    and 7B shapes on a single host thread (the oracle's results do not depend on the thread
+    count).  Seeded prompts, fresh caches."""
+    import oracle
+    from synth import model as sm
+    threads = oracle.threads()
+    out = {"threads": threads}
+
+    def timed_prefill(cfg, n, rec=None):
+        get_proj, get_norms, emb, fin, lm = rec if rec is not None else sm.recipe(cfg, seed)
+        orc = oracle.OracleModel(cfg, seed, t_max=n + 24, tensors=get_proj, norms=get_norms,
+                                 embed=emb, lm_head=lm)
+        toks = sm.prompt(cfg, seed + 7, n, stream=1)
+        t0 = time.perf_counter()
+        logits = orc.prefill(toks)
+        ms = (time.perf_counter() - t0) * 1e3
+        return orc, int(np.argmax(logits)), ms
+
+    def one_thread_step(orc, tok, pos):
+        oracle.set_threads(1)
+        try:
+            t0 = time.perf_counter()
+            orc.step(tok, pos)
+            return (time.perf_counter() - t0) * 1e3
+        finally:
+            oracle.set_threads(threads)
+
+    tiny = sm.CONFIGS["tiny"].with_(max_context=1024)
+    orc, tok, ms = timed_prefill(tiny, 512)
+    t0 = time.perf_counter()
+    for i in range(16):
+        tok = int(np.argmax(orc.step(tok, 512 + i)))
+    out["tiny"] = {"pp512_ms": round(ms, 1), "decode_ms_per_token": round((time.perf_counter() - t0) * 1e3 / 16, 2),
+                   "decode_ms_per_token_1_thread": round(one_thread_step(orc, tok, 528), 2)}
+    del orc
+    b15 = sm.CONFIGS["qwen2.5-1.5b"]
+    orc, _, ms = timed_prefill(b15, 512)
+    out["qwen2.5-1.5b"] = {"pp512_ms": round(ms, 1)}
+    del orc
+    orc, tok, ms = timed_prefill(cfg7, 64, rec7)
+    out[cfg7.name] = {"pp64_ms": round(ms, 1), "decode_ms_per_token_1_thread": round(one_thread_step(orc, tok, 64), 1)}
+    del orc
+    return out
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -349,7 +398,8 @@ def run_reference(args):
     t0 = time.perf_counter()
     mean_ms, sample, n_run = oracle_decode(cfg, args.seed, T0, n_warm, args.steps, budget_s=ORACLE_BUDGET_S)
     wall = time.perf_counter() - t0
-    cores = os.cpu_count()
+    import oracle
+    cores = oracle.threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(mean_ms, 3), "unit": "ms/token",
         "n_gpus": args.gpus, "steps": n_run, "steps_requested": args.steps, "warmup": n_warm,
@@ -685,9 +735,12 @@ def run_ours(args):
     # ---- CPU oracle baseline (rank 0, one GPU only): the whole model, a few greedy steps
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
         mean_ms, sample, _ = oracle_decode(cfg, args.seed, T0, 1, 6, rec=rec)
-        cpu = {"value": round(mean_ms, 2), "unit": "ms/token", "cores": os.cpu_count(),
+        cpu = {"value": round(mean_ms, 2), "unit": "ms/token", "cores": oracle.threads(),
                "kind": "oracle", "sample": sample}
+        if not args.no_oracle_timings:
+            cpu["more"] = oracle_timings(cfg, rec, args.seed)
 
     tok_s = 1e3 / ms_per_token
     line = {

@@ -76,6 +76,10 @@ def _load():
             lib.or_bf16_round.restype = ctypes.c_uint16
             lib.or_argmax.argtypes = [vp, i64]
             lib.or_argmax.restype = i64
+            lib.or_threads.argtypes = []
+            lib.or_threads.restype = ctypes.c_int
+            lib.or_set_threads.argtypes = [ctypes.c_int]
+            lib.or_set_threads.restype = None
             for p in ("f32", "f64"):
                 g = lambda n: getattr(lib, f"or_{p}_{n}")  # noqa: E731
                 g("rmsnorm").argtypes = [vp, vp, i64, f32, vp]
@@ -97,6 +101,16 @@ def _load():
                     g(n).restype = None
             _lib = lib
     return _lib
+
+
+def threads():
+    """Host threads the oracle's parallel loops use."""
+    return int(_load().or_threads())
+
+
+def set_threads(n):
+    """Set the oracle's host threads (timing only: its results do not depend on them)."""
+    _load().or_set_threads(int(n))
 
 
 def _p(a):

@@ -52,6 +52,7 @@
  *   - argmax ties resolve to the lowest index.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -131,6 +132,10 @@ int64_t or_argmax(const float *v, int64_t n) {
         if (v[i] > v[best]) best = i;
     return best;
 }
+
+/* Host threads of the parallel loops (timing only: results do not depend on it). */
+int or_threads(void) { return omp_get_max_threads(); }
+void or_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 
 #endif /* !OR_DOUBLE_BUILD */
 

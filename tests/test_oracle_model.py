@@ -39,6 +39,26 @@ def test_step_is_deterministic_and_finite():
         np.testing.assert_array_equal(x, y)
 
 
+def test_results_do_not_depend_on_host_threads():
+    # the timed baseline runs on every host thread, its single-thread figure on one
+    n = oracle.threads()
+    toks = sm.prompt(TINY, SEED, 7)
+    try:
+        oracle.set_threads(1)
+        assert oracle.threads() == 1
+        one = _run(oracle.OracleModel(TINY, SEED), toks)
+        one_pf = oracle.OracleModel(TINY, SEED).prefill(toks)
+        oracle.set_threads(max(n, 3))
+        many = _run(oracle.OracleModel(TINY, SEED), toks)
+        many_pf = oracle.OracleModel(TINY, SEED).prefill(toks)
+    finally:
+        oracle.set_threads(n)
+    for x, y in zip(one, many):
+        np.testing.assert_array_equal(x, y)
+    np.testing.assert_array_equal(one_pf, many_pf)
+    np.testing.assert_array_equal(one_pf, one[-1])
+
+
 def test_gqa_equals_replicated_kv_heads_model():
     """Hkv=2 model == Hkv=4 model whose k/v rows repeat each KV head twice (same Hq)."""
     cfg2 = TINY
