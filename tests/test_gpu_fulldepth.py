@@ -9,7 +9,7 @@ vocabularies, directly against the CPU oracle -- never through another GPU path:
     16 decode steps;
   * Qwen3-8B INT8 (per-row scales, q/k norms, INT8 LM head): a 128-token prompt, and a
     seeded 4096-token cache, 4 decode steps each.
-Acceptance per step ("north star" criterion of the workload): max |GPU - oracle| <= 2e-2 *
+Acceptance per step (the workload's parity criterion): max |GPU - oracle| <= 2e-2 *
 max |oracle|, and the argmax equal wherever the oracle's top-1/top-2 margin exceeds 5e-2.
 The worst relative error per configuration is printed (pytest -s / -rP shows it).
 """
