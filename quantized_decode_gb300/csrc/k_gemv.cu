@@ -13,10 +13,16 @@ namespace qd {
 namespace {
 
 constexpr int kMaxWarps = 16;  // 512 threads at <= 128 registers
-// Ring depth: copies D - 1 steps ahead of the arithmetic.  Deeper rings keep
-// more weight bytes in flight per SM (HBM latency under load is ~2-3 us).
-template <int RT>
-constexpr int kDepth = RT >= 4 ? 4 : 5;
+// Ring depth: copies D - 1 steps ahead of the arithmetic.  Measured on the 7B
+// INT4 decode step (in-graph times): shallow rings win -- o_proj / down at D = 2
+// (down 12.1 us against 13.5 at D = 5), gate/up at D = 3 (17.0 against 17.9 at
+// D = 4; D = 2 starves it, 26.7).  The fewer weight copies a kernel issues
+// before its dependency wait, the sooner the input staging after the wait
+// gets its round trip.  A step of INT8 (or bf16) rows covers half (a quarter)
+// of the K values of an INT4 step; those keep the deeper rings (Qwen3-8B INT8
+// decode was 3 % slower at the INT4 depths).
+template <int FMT, int RT>
+constexpr int kDepth = (FMT == kFmtInt4 || FMT == kFmtInt4A8) ? (RT >= 4 ? 3 : 2) : (RT >= 4 ? 4 : 5);
 
 QD_DEV float silu(float a) { return a / (1.f + __expf(-a)); }
 
@@ -57,9 +63,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     const size_t gbytes = a.gamma ? gain_region_bytes(a.K) : 0;
     uint4 *ring;
     uint32_t *sring;
-    warp_rings<RT, kDepth<RT>>((char *)smem + xbytes + gbytes, NW, warp, ring, sring);
+    warp_rings<RT, kDepth<FMT, RT>>((char *)smem + xbytes + gbytes, NW, warp, ring, sring);
     float *kred = reinterpret_cast<float *>((char *)smem + xbytes + gbytes +
-                                            (size_t)NW * ring_bytes_per_warp<RT, kDepth<RT>>()) +
+                                            (size_t)NW * ring_bytes_per_warp<RT, kDepth<FMT, RT>>()) +
                   (size_t)tslot * ks * 32 * RT;
     float post = 1.f;
     float st_ss = 0.f, st_mx = 0.f;  // statistics of what this thread writes
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
     // after its own wait, i.e. after its predecessor completed).
     float pre_mul[RT], pre_add[RT], pre_g[RT];
     auto sync = [&]() {
-        cp_async_wait<kDepth<RT> - 1>();  // the gain (the ring's first steps stay in flight)
+        cp_async_wait<kDepth<FMT, RT> - 1>();  // the gain (the ring's first steps stay in flight)
         if (a.mode != 2 && j == 0 && kp == 0 && t_first < a.N / (S * RT)) {
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                 st_mx = fmaxf(st_mx, fabsf(yv));
             }
         };
-        gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
+        gemv_stream<FMT, RT, kDepth<FMT, RT>>(rows, epi, sync, t_first, t_stride, a.N / TU, p_begin, p_end, U, j, xs, ring,
                                  sring, a8_sx, a8_qs);
     } else {
         const int TR = S * RT;
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_gemv(GemvArgs a) {
                 st_mx = fmaxf(st_mx, fabsf(v * gn));
             }
         };
-        gemv_stream<FMT, RT, kDepth<RT>>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
+        gemv_stream<FMT, RT, kDepth<FMT, RT>>(rows, epi, sync, t_first, t_stride, a.N / TR, p_begin, p_end, U, j, xs, ring,
                                  sring, a8_sx, a8_qs);
     }
     if (a.stats_out) write_block_stats(st_ss, st_mx, a.stats_out, red);
@@ -163,7 +169,7 @@ cudaError_t launch_shape(const LaunchCfg &lc, GemvArgs a, int ks) {
     const int rows_per_tile = a.mode == 2 ? (32 / LPR) * (RT / 2) : (32 / LPR) * RT;
     const int tiles = a.N / rows_per_tile;
     const size_t fixed = act_region_bytes<FMT>(a.K) + (a.gamma ? gain_region_bytes(a.K) : 0);  // activations (+ gain)
-    const size_t per_warp = ring_bytes_per_warp<RT, kDepth<RT>>() + (size_t)32 * RT * 4;
+    const size_t per_warp = ring_bytes_per_warp<RT, kDepth<FMT, RT>>() + (size_t)32 * RT * 4;
     const int fit = (int)((kMaxSmemOptin - fixed) / per_warp);  // warps whose rings fit in shared memory
     GemvPlan pl = plan_gemv(tiles, ks, lc.n_sm < kStatSlots ? lc.n_sm : kStatSlots,
                             (fit < kMaxWarps ? fit : kMaxWarps) / ks * ks);

@@ -14,12 +14,12 @@ namespace qd {
 
 namespace {
 
-// 7 warps of 6-stage rings (168 KB of weights in flight per SM): measured against
-// 16 x 3, 12 x 4, 9 x 5, 8 x 6, 6 x 8 and 5 x 9 on the 7B head (152064 x 3584 bf16),
-// 7 x 6 and 7 x 7 were fastest by 4-40 %
+// 7 warps of 4-stage rings: measured against 16 x 3, 12 x 4, 9 x 5, 8 x 6, 6 x 8 and
+// 5 x 9 on the 7B head (152064 x 3584 bf16), 7 warps were fastest by 4-40 %, and 7 x 4
+// beat 7 x 6 and 7 x 7 by 2 us
 constexpr int kMaxWarps = 7;
 constexpr int kRT = 4;  // rows per lane
-constexpr int kD = 6;   // ring depth (copies 5 steps ahead)
+constexpr int kD = 4;   // ring depth (copies 3 steps ahead)
 
 QD_DEV void better(float &v, int &i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) {
