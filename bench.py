@@ -413,6 +413,9 @@ def run_reference(args):
         "e2e": {"value": round(mean_ms, 3), "unit": "ms/token", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 1),
+        # every requested step ran inside the oracle's time bound (so the driver's clock
+        # around this run covers the region the value claims)
+        "fits_in_driver_run": n_run == args.steps,
     }
     print(json.dumps(line), flush=True)
 

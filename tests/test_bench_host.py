@@ -43,6 +43,7 @@ def test_reference_arm_json_line():
     d = json.loads(line)
     assert d["impl"] == "reference" and d["unit"] == "ms/token" and d["higher_is_better"] is False
     assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 0
+    assert d["fits_in_driver_run"] is True and d["steps_requested"] == 2
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "ms/token", "h2d_bytes_per_step": 0,
